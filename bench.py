@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""WKV7 forward + checkpointed backward throughput on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole path on one batch of the 36M "debug" training
+shape (B=12, T=1024, H=6, D=64, bf16 inputs, fp32 state, chunk 32): wkv7_forward
+(y, checkpoints, hT) then wkv7_backward (dr, dw, dk, dv, da, db, dh0).  Inputs are
+seeded synthetic draws (wkv7_inputs.py).  Under torchrun each rank runs its own
+independent batch (weak scaling, no collective on the data path); rank 0 prints
+one JSON line.
+
+--impl reference times the fp64 CPU oracle on this host's cores instead, on a
+bounded sample of the same workload, in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import wkv7_inputs as gen  # noqa: E402
+
+METRIC = "WKV7 fwd+bwd tokens/s at B12 T1024 H6 D64; % of FP32/HBM roofline"
+WORKLOAD = "debug_b12_t1024_h6"
+N_SETS = 4  # input/output sets rotated between steps so a step never finds its inputs in L2
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------ workload math
+
+def byte_counts(wl, in_bytes: int):
+    """Minimum HBM bytes the method must move (forward, backward), per step."""
+    N = wl.B * wl.T * wl.H * wl.D
+    C = math.ceil(wl.T / wl.chunk)
+    S = wl.B * wl.H * wl.D * wl.D * 4
+    h0 = S if wl.h0_std else 0
+    dhT = S if wl.dhT_std else 0
+    fwd = 6 * N * in_bytes + h0 + 4 * N + C * S + S
+    bwd = 6 * N * in_bytes + 4 * N + (C - 1) * S + h0 + dhT + 6 * 4 * N + S
+    return fwd, bwd
+
+
+def literal_flops(wl):
+    return 8 * wl.D * wl.D * wl.B * wl.T * wl.H
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def kernel_source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", "wkv7_device.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel: str, workload: str, src_sha: str):
+    """DRAM bytes per launch from profiles/dram_traffic.md, only if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[3] == src_sha:
+            try:
+                return float(cells[2])
+            except ValueError:
+                return None
+    return None
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                   "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                   "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                   "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.uuid:
+                cmd[1:1] = ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sms.append(float(c[1]))
+                mx = float(c[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, c[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------------------ oracle (CPU)
+
+def oracle_pass(wl, heads, xs_by_b):
+    """fp64 oracle forward + checkpointed backward over the given (b, h) heads."""
+    import oracle
+    for b, h in heads:
+        x, dy = xs_by_b[b]
+        sl = {n: x[n][None, :, h:h + 1] for n in "rwkvab"}
+        _, ck, _ = oracle.forward(*(sl[n] for n in "rwkvab"), None, chunk=wl.chunk)
+        oracle.backward(*(sl[n] for n in "rwkvab"), None, ck, dy[None, :, h:h + 1], None,
+                        chunk=wl.chunk, mode="ckpt")
+
+
+def cpu_baseline(wl, seconds: float):
+    xs = {b: (gen.token_inputs(wl, b), gen.dy_init(wl, b)) for b in range(wl.B)}
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    oracle_pass(wl, heads[:1], xs)  # build + warm
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(wl, heads, xs)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done * wl.B * wl.T / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"all {len(heads)} heads of {wl.name} (B{wl.B} T{wl.T} H{wl.H} D{wl.D}), fp64 "
+                      f"forward + checkpoint-recompute backward, {done} pass(es), single-threaded C"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = gen.WORKLOADS[WORKLOAD]
+    xs = {b: (gen.token_inputs(wl, b), gen.dy_init(wl, b)) for b in range(wl.B)}
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)][:12]  # bounded sample: 12 of 72 heads
+    frac = len(heads) / (wl.B * wl.H)
+    for _ in range(args.warmup):
+        oracle_pass(wl, heads, xs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(wl, heads, xs)
+    el = time.perf_counter() - t0
+    value = args.steps * frac * wl.B * wl.T / el
+    sample = (f"{len(heads)} of {wl.B * wl.H} heads of {wl.name} per step (fp64 forward + checkpoint-recompute "
+              f"backward, single-threaded C); value scaled to whole-batch tokens/s")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, wkv7_inputs.py)",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "D": wl.D, "chunk": wl.chunk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import linear_rnn_lm_wkv7_b300 as wkv7
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS[WORKLOAD]
+    B, T, H, D = wl.B, wl.T, wl.H, wl.D
+    C = wkv7.num_chunks(T, wl.chunk)
+
+    x = gen.full(wl)   # same seeded batch on every rank (each rank owns an independent replica)
+    host_in = {n: torch.from_numpy(x[n]).to(torch.bfloat16) for n in "rwkvab"}
+    host_dy = torch.from_numpy(x["dy"])
+
+    def make_set():
+        s = {n: host_in[n].to(dev) for n in "rwkvab"}
+        s["dy"] = host_dy.to(dev)
+        s["y"] = torch.empty((B, T, H, D), device=dev)
+        s["ck"] = torch.empty((B, H, C, D, D), device=dev)
+        s["hT"] = torch.empty((B, H, D, D), device=dev)
+        s["g"] = [torch.empty((B, T, H, D), device=dev) for _ in range(6)] + [torch.empty((B, H, D, D), device=dev)]
+        return s
+
+    sets = [make_set() for _ in range(N_SETS)]
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev=None):
+        ins = [s[n] for n in "rwkvab"]
+        if ev is not None:
+            ev[0].record(stream)
+        wkv7.forward(*ins, None, chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"]))
+        if ev is not None:
+            ev[1].record(stream)
+        wkv7.backward(*ins, None, s["ck"], s["dy"], None, chunk=wl.chunk, out=s["g"])
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(max(3, args.warmup)):
+        step(sets[i % N_SETS])
+    torch.cuda.synchronize()
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % N_SETS], evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+    clocks = clk.summary()
+    elapsed_ms = start.elapsed_time(stop)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    tokens_per_s = world * B * T * args.steps / (elapsed_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        pin_in = {n: host_in[n].pin_memory() for n in "rwkvab"}
+        pin_dy = host_dy.pin_memory()
+        pin_y = torch.empty((B, T, H, D), pin_memory=True)
+        pin_g = [torch.empty((B, T, H, D), pin_memory=True) for _ in range(6)] + \
+                [torch.empty((B, H, D, D), pin_memory=True)]
+        s = sets[0]
+        h2d = sum(t.numel() * t.element_size() for t in pin_in.values()) + pin_dy.numel() * 4
+        d2h = pin_y.numel() * 4 + sum(t.numel() * 4 for t in pin_g)
+
+        def e2e_step():
+            for n in "rwkvab":
+                s[n].copy_(pin_in[n], non_blocking=True)
+            s["dy"].copy_(pin_dy, non_blocking=True)
+            step(s)
+            pin_y.copy_(s["y"], non_blocking=True)
+            for hg, dg in zip(pin_g, s["g"]):
+                hg.copy_(dg, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([ems], device=dev)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * B * T * args.e2e_steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+
+    fwd_b, bwd_b = byte_counts(wl, 2)
+    hbm, peak_kind, peaks = measured_peaks()
+    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dom = ("wkv7_bwd", bwd_b, b_ms, "wkv7_bwd.cu") if b_ms >= f_ms else ("wkv7_fwd", fwd_b, f_ms, "wkv7_fwd.cu")
+    achieved = dom[1] / (dom[2] / 1e3) / 1e9
+    sha = kernel_source_sha(dom[3])
+    traffic = profiled_traffic(dom[0], wl.name, sha)
+    step_s = elapsed_ms / 1e3 / args.steps
+    roof_s = max((fwd_b + bwd_b) / (hbm * 1e9), literal_flops(wl) / (fp32_peak_tflops(peaks) * 1e12))
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, wkv7_inputs.py)",
+        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": "bf16",
+                   "state": "fp32", "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "l2": f"{N_SETS} rotating input/output sets "
+                         f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "algorithmic_bytes": dom[1], "avg_launch_ms": dom[2]},
+        "roofline_step": {"definition": "max(HBM bytes / peak BW, 8*D^2 FLOP per head-token / FP32 peak) / step time",
+                          "bytes": fwd_b + bwd_b, "roofline_ms": roof_s * 1e3, "frac": roof_s / step_s},
+        "kernels_ms": {"wkv7_fwd": f_ms, "wkv7_bwd": b_ms},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def fp32_peak_tflops(peaks: dict) -> float:
+    """FP32 CUDA-core peak: 148 SMs x 128 FMA lanes x 2 FLOP x max SM clock."""
+    mhz = float(peaks.get("sm_max_mhz", 2032.0)) if peaks else 2032.0
+    return 148 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,127 @@
+/*
+ * wkv7.h -- C ABI of the B300 (sm_103a) WKV7 state-recurrence library.
+ *
+ * The operation (per batch row b and head h, state S of D x D fp32 values,
+ * row i = value index, column j = key index), for each token t in order:
+ *
+ *     sa_i  = sum_j S_ij a_j                    (state before the update)
+ *     S_ij <- S_ij w_j + v_i k_j + sa_i b_j
+ *     y_i   = sum_j S_ij r_j                    (state after the update)
+ *
+ * Source: "RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel
+ * architecture": the Forward listing (the update above, and a copy of the
+ * state kept after every chunk of 32 tokens), the Backward listing (chunks
+ * walked in reverse from those exact copies, the VJP giving dr, dw, dk, dv,
+ * da, db, the previous state rebuilt as (h - v k - sa b) / w), and the note
+ * that dividing by w amplifies rounding by (1/w)^N, which is why the copies
+ * are kept every 32 tokens.  The listing leaves `sa` undefined; this library
+ * reads it as the state times a, before the update.  The single-token decode
+ * is the same update for T = 1 applied to a resident state ("RWKV-7 最新、最全
+ * 的动态": the 7B model updates 32 x 64 heads of 64 x 64 state values per
+ * token; "RWKV LM": an RNN continues from a passed state).
+ *
+ * Common conventions
+ *   - Layouts are row-major and dense.  Per-token tensors are (B, T, H, D):
+ *     element (b, t, h, j) at ((b*T + t)*H + h)*D + j.  States are (B, H, D, D):
+ *     element (b, h, i, j) at ((b*H + h)*D + i)*D + j.  Checkpoints are
+ *     (B, H, C, D, D) with C = wkv7_num_chunks(T, chunk).
+ *   - r, w, k, v, a, b have dtype `in_dtype` (WKV7_F32 or WKV7_BF16).  All
+ *     states, y and every gradient are fp32.  w is the decay multiplier, not its
+ *     log, and must be > 0 where the backward divides by it.
+ *   - Every pointer is a DEVICE pointer on the current CUDA device (memory the
+ *     caller owns; the library allocates, frees and keeps nothing), 16-byte
+ *     aligned.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and is asynchronous: no call synchronises the device.
+ *   - D must be 64.  1 <= chunk <= 32.  B, H >= 1, T >= 0.
+ *   - Outputs are fully overwritten (never accumulated into).  Outputs must not
+ *     alias inputs or each other, except the in-place decode state.
+ *   - Errors: every argument is checked on the host before anything is
+ *     enqueued; a non-zero wkv7_status is returned and nothing runs.  A launch
+ *     failure returns WKV7_ERR_CUDA (the CUDA error text is available from
+ *     wkv7_last_cuda_error()).  Nothing aborts the process.
+ */
+#ifndef WKV7_H
+#define WKV7_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { WKV7_F32 = 0, WKV7_BF16 = 1 } wkv7_dtype;
+
+typedef enum {
+    WKV7_OK = 0,
+    WKV7_ERR_ARG = 1,      /* a required pointer is NULL, or a size is negative */
+    WKV7_ERR_SHAPE = 2,    /* D != 64, chunk outside [1, 32], or sizes overflow the index range */
+    WKV7_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned */
+    WKV7_ERR_DTYPE = 4,    /* in_dtype is not WKV7_F32 / WKV7_BF16 */
+    WKV7_ERR_CUDA = 5,     /* the CUDA runtime reported an error at launch */
+    WKV7_ERR_TIMEOUT = 6   /* a bounded device-side wait gave up (reserved) */
+} wkv7_status;
+
+/* Number of checkpoints the forward writes: ceil(T / chunk); 0 for T == 0. */
+int wkv7_num_chunks(int T, int chunk);
+
+/*
+ * Forward over T tokens.
+ *   h0      (B,H,D,D) initial state, or NULL for zeros.
+ *   y       (B,T,H,D) fp32 output, required.
+ *   h_ckpt  (B,H,C,D,D) fp32 output or NULL (then no checkpoints are written --
+ *           an inference prefill).  Entry c is the state after token
+ *           min(T, (c+1)*chunk) - 1, so the last entry equals hT (T % chunk
+ *           may be non-zero: the last chunk is then shorter).
+ *   hT      (B,H,D,D) fp32 final state, or NULL.
+ * Source: Forward listing of "Metal kernel architecture" (see top of file).
+ */
+int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
+                 const void *r, const void *w, const void *k,
+                 const void *v, const void *a, const void *b,
+                 const float *h0, float *y, float *h_ckpt, float *hT, void *stream);
+
+/*
+ * Checkpointed backward (vector-Jacobian product of wkv7_forward).
+ *   h0      the forward's initial state, or NULL for zeros.
+ *   h_ckpt  the forward's checkpoints (B,H,C,D,D), required when T > 0; the same
+ *           chunk value must be passed.
+ *   dy      (B,T,H,D) fp32 gradient of the loss w.r.t. y, required.
+ *   dhT     (B,H,D,D) fp32 gradient w.r.t. hT, or NULL for zeros.
+ *   dr, dw, dk, dv, da, db  (B,T,H,D) fp32 outputs, required.
+ *   dh0     (B,H,D,D) fp32 gradient w.r.t. h0, or NULL (not written).
+ * Each chunk is recomputed forward from its start checkpoint (h0 for the first)
+ * to obtain sa, then walked in reverse from its end checkpoint, the earlier
+ * states rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).
+ * Source: Backward listing of "Metal kernel architecture" (see top of file).
+ */
+int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
+                  const void *r, const void *w, const void *k,
+                  const void *v, const void *a, const void *b,
+                  const float *h0, const float *h_ckpt, const float *dy, const float *dhT,
+                  float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                  float *dh0, void *stream);
+
+/*
+ * One decode token for B sequences of H heads, state updated in place.
+ *   state   (B,H,D,D) fp32, read and overwritten; same layout as h0 / hT.
+ *   r..b    (B,H,D) in in_dtype (the (B,T,H,D) layout with T = 1).
+ *   y       (B,H,D) fp32 output, required.
+ * Equal to wkv7_forward with T = 1, h0 = state, hT = state.
+ */
+int wkv7_decode(int B, int H, int D, int in_dtype, float *state,
+                const void *r, const void *w, const void *k,
+                const void *v, const void *a, const void *b,
+                float *y, void *stream);
+
+/* Static text for a wkv7_status value. */
+const char *wkv7_strerror(int status);
+
+/* Text of the last CUDA error seen by this library on the calling thread ("" if none). */
+const char *wkv7_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int wkv7_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV7_H */

@@ -1,0 +1,191 @@
+"""ctypes binding of libwkv7.so (the C ABI declared in include/wkv7.h).
+
+Argument marshalling only: shapes, dtypes and devices of torch tensors are
+checked, outputs are allocated with torch when the caller passes none, and the
+raw device pointers plus the current CUDA stream go to the C entry points.
+Every step of the recurrence runs in the library's kernels; there is no other
+implementation behind these functions.  If libwkv7.so is missing the import
+fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(PKG, "libwkv7.so")
+
+F32 = 0
+BF16 = 1
+D_HEAD = 64
+MAX_CHUNK = 32
+
+STATUS = {0: "WKV7_OK", 1: "WKV7_ERR_ARG", 2: "WKV7_ERR_SHAPE", 3: "WKV7_ERR_ALIGN",
+          4: "WKV7_ERR_DTYPE", 5: "WKV7_ERR_CUDA", 6: "WKV7_ERR_TIMEOUT"}
+
+# every function the header declares, with (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "wkv7_num_chunks": (_I, [_I, _I]),
+    "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P]),
+    "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P] * 7 + [_P]),
+    "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
+    "wkv7_strerror": (ctypes.c_char_p, [_I]),
+    "wkv7_last_cuda_error": (ctypes.c_char_p, []),
+    "wkv7_version": (_I, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIBRARY_PATH):
+        raise ImportError(f"{LIBRARY_PATH} is not built: run `python -m linear_rnn_lm_wkv7_b300.build`")
+    lib = ctypes.CDLL(LIBRARY_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class WKV7Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib.wkv7_strerror(status).decode()
+        if status == 5:
+            msg += f" ({lib.wkv7_last_cuda_error().decode()})"
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise WKV7Error(status, where)
+
+
+def num_chunks(T: int, chunk: int) -> int:
+    return lib.wkv7_num_chunks(T, chunk)
+
+
+def version() -> int:
+    return lib.wkv7_version()
+
+
+# ------------------------------------------------------------------------------ torch API
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _in_dtype(x):
+    torch = _torch()
+    if x.dtype == torch.float32:
+        return F32
+    if x.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"inputs must be float32 or bfloat16, got {x.dtype}")
+
+
+def _check_inputs(tensors, shape, where):
+    dt = tensors[0].dtype
+    dev = tensors[0].device
+    for t in tensors:
+        if t.device.type != "cuda" or t.device != dev:
+            raise ValueError(f"{where}: every tensor must be on the same CUDA device")
+        if t.dtype != dt:
+            raise TypeError(f"{where}: r, w, k, v, a, b must share one dtype")
+        if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+            raise ValueError(f"{where}: expected contiguous {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check_f32(t, shape, name, where, dev):
+    if t is None:
+        return
+    torch = _torch()
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or t.device != dev:
+        raise ValueError(f"{where}: {name} must be a contiguous float32 {tuple(shape)} tensor on {dev}")
+
+
+def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True, final_state: bool = True,
+            out=None, stream=None):
+    """WKV7 forward.  r..b: (B, T, H, 64) float32/bfloat16 CUDA tensors; h0: (B, H, 64, 64) float32 or None.
+
+    Returns (y, h_ckpt, hT): y (B,T,H,64) fp32; h_ckpt (B,H,C,64,64) fp32 (None when
+    checkpoints=False); hT (B,H,64,64) fp32 (None when final_state=False).  `out` may give
+    preallocated (y, h_ckpt, hT).
+    """
+    torch = _torch()
+    B, T, H, D = r.shape
+    _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.forward")
+    C = num_chunks(T, chunk)
+    dev = r.device
+    if out is not None:
+        y, ck, hT = out
+    else:
+        y = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
+        ck = torch.empty((B, H, C, D, D), dtype=torch.float32, device=dev) if checkpoints else None
+        hT = torch.empty((B, H, D, D), dtype=torch.float32, device=dev) if final_state else None
+    _check_f32(h0, (B, H, D, D), "h0", "wkv7.forward", dev)
+    _check_f32(y, (B, T, H, D), "y", "wkv7.forward", dev)
+    _check_f32(ck, (B, H, C, D, D), "h_ckpt", "wkv7.forward", dev)
+    _check_f32(hT, (B, H, D, D), "hT", "wkv7.forward", dev)
+    st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT)),
+                          _stream(stream))
+    _check(st, "wkv7_forward")
+    return y, ck, hT
+
+
+def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_dh0: bool = True,
+             out=None, stream=None):
+    """Checkpointed WKV7 backward.  Returns (dr, dw, dk, dv, da, db, dh0), all fp32 (dh0 None when
+    need_dh0=False).  h_ckpt must come from `forward` with the same chunk."""
+    torch = _torch()
+    B, T, H, D = r.shape
+    _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.backward")
+    C = num_chunks(T, chunk)
+    dev = r.device
+    _check_f32(h0, (B, H, D, D), "h0", "wkv7.backward", dev)
+    _check_f32(h_ckpt, (B, H, C, D, D), "h_ckpt", "wkv7.backward", dev)
+    _check_f32(dy, (B, T, H, D), "dy", "wkv7.backward", dev)
+    _check_f32(dhT, (B, H, D, D), "dhT", "wkv7.backward", dev)
+    if out is not None:
+        grads = list(out)
+    else:
+        grads = [torch.empty((B, T, H, D), dtype=torch.float32, device=dev) for _ in range(6)]
+        grads.append(torch.empty((B, H, D, D), dtype=torch.float32, device=dev) if need_dh0 else None)
+    for name, g in zip(("dr", "dw", "dk", "dv", "da", "db"), grads[:6]):
+        _check_f32(g, (B, T, H, D), name, "wkv7.backward", dev)
+    _check_f32(grads[6], (B, H, D, D), "dh0", "wkv7.backward", dev)
+    st = lib.wkv7_backward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, dy, dhT)),
+                           *map(_ptr, grads), _stream(stream))
+    _check(st, "wkv7_backward")
+    return tuple(grads)
+
+
+def decode(state, r, w, k, v, a, b, y=None, stream=None):
+    """One decode token, state (B, H, 64, 64) fp32 updated in place; r..b (B, H, 64).  Returns y (B, H, 64) fp32."""
+    torch = _torch()
+    B, H, D = r.shape
+    _check_inputs((r, w, k, v, a, b), (B, H, D), "wkv7.decode")
+    dev = r.device
+    _check_f32(state, (B, H, D, D), "state", "wkv7.decode", dev)
+    if y is None:
+        y = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    _check_f32(y, (B, H, D), "y", "wkv7.decode", dev)
+    st = lib.wkv7_decode(B, H, D, _in_dtype(r), _ptr(state), *map(_ptr, (r, w, k, v, a, b)), _ptr(y),
+                         _stream(stream))
+    _check(st, "wkv7_decode")
+    return y

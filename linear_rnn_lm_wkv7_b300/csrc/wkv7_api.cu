@@ -1,0 +1,136 @@
+// extern "C" entry points of libwkv7: argument checks on the host, then one launch on
+// the caller's stream.  Declared (with layouts, ownership and errors) in include/wkv7.h.
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <climits>
+#include <initializer_list>
+
+#include "wkv7.h"
+#include "wkv7_launch.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxChunk = 32;
+constexpr int kHeadSize = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int record_cuda(cudaError_t err) {
+  if (err == cudaSuccess) return WKV7_OK;
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(err),
+           cudaGetErrorString(err));
+  return WKV7_ERR_CUDA;
+}
+
+int check_dtype(int in_dtype) {
+  return (in_dtype == WKV7_F32 || in_dtype == WKV7_BF16) ? WKV7_OK : WKV7_ERR_DTYPE;
+}
+
+// sizes shared by forward and backward; element counts must stay inside the index range
+int check_sizes(int B, int T, int H, int D, int chunk) {
+  if (B < 1 || H < 1 || T < 0) return WKV7_ERR_ARG;
+  if (D != kHeadSize) return WKV7_ERR_SHAPE;
+  if (chunk < 1 || chunk > kMaxChunk) return WKV7_ERR_SHAPE;
+  const unsigned long long bh = (unsigned long long)B * (unsigned long long)H;
+  if (bh * 4ull > (unsigned long long)INT_MAX) return WKV7_ERR_SHAPE;
+  const unsigned long long elems = bh * (unsigned long long)(T > 0 ? T : 1) * 64ull;
+  if (elems > (1ull << 40)) return WKV7_ERR_SHAPE;
+  return WKV7_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+  for (const void* p : required)
+    if (p == nullptr) return WKV7_ERR_ARG;
+  for (const void* p : required)
+    if (!aligned16(p)) return WKV7_ERR_ALIGN;
+  for (const void* p : optional)
+    if (p != nullptr && !aligned16(p)) return WKV7_ERR_ALIGN;
+  return WKV7_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wkv7_version(void) { return kVersion; }
+
+int wkv7_num_chunks(int T, int chunk) {
+  if (T <= 0 || chunk <= 0) return 0;
+  return (T + chunk - 1) / chunk;
+}
+
+const char* wkv7_strerror(int status) {
+  switch (status) {
+    case WKV7_OK: return "ok";
+    case WKV7_ERR_ARG: return "invalid argument: a required pointer is NULL or a size is out of range";
+    case WKV7_ERR_SHAPE: return "unsupported shape: D must be 64, chunk in [1, 32], sizes within the index range";
+    case WKV7_ERR_ALIGN: return "misaligned pointer: every buffer must be 16-byte aligned";
+    case WKV7_ERR_DTYPE: return "unsupported input dtype: use WKV7_F32 or WKV7_BF16";
+    case WKV7_ERR_CUDA: return "CUDA error at launch (see wkv7_last_cuda_error)";
+    case WKV7_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    default: return "unknown wkv7 status";
+  }
+}
+
+const char* wkv7_last_cuda_error(void) { return g_last_cuda_error; }
+
+int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                 const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
+                 float* h_ckpt, float* hT, void* stream) {
+  int st = check_sizes(B, T, H, D, chunk);
+  if (st) return st;
+  if ((st = check_dtype(in_dtype))) return st;
+  if (T > 0) {
+    if ((st = check_ptrs({r, w, k, v, a, b, y}, {h0, h_ckpt, hT}))) return st;
+  } else if ((st = check_ptrs({}, {h0, hT}))) {
+    return st;
+  }
+  wkv7::FwdArgs p;
+  p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
+  p.bf16 = in_dtype == WKV7_BF16;
+  p.in = {r, w, k, v, a, b};
+  p.h0 = h0; p.y = y; p.h_ckpt = h_ckpt; p.hT = hT;
+  return record_cuda(wkv7::launch_forward(p, static_cast<cudaStream_t>(stream)));
+}
+
+int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                  const void* k, const void* v, const void* a, const void* b, const float* h0,
+                  const float* h_ckpt, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
+                  float* dv, float* da, float* db, float* dh0, void* stream) {
+  int st = check_sizes(B, T, H, D, chunk);
+  if (st) return st;
+  if ((st = check_dtype(in_dtype))) return st;
+  if (T > 0) {
+    if ((st = check_ptrs({r, w, k, v, a, b, h_ckpt, dy, dr, dw, dk, dv, da, db}, {h0, dhT, dh0}))) return st;
+  } else if ((st = check_ptrs({}, {h0, dhT, dh0}))) {
+    return st;
+  }
+  wkv7::BwdArgs p;
+  p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
+  p.bf16 = in_dtype == WKV7_BF16;
+  p.in = {r, w, k, v, a, b};
+  p.h0 = h0; p.h_ckpt = h_ckpt; p.dy = dy; p.dhT = dhT;
+  p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
+  return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
+}
+
+int wkv7_decode(int B, int H, int D, int in_dtype, float* state, const void* r, const void* w, const void* k,
+                const void* v, const void* a, const void* b, float* y, void* stream) {
+  int st = check_sizes(B, 1, H, D, 1);
+  if (st) return st;
+  if ((st = check_dtype(in_dtype))) return st;
+  if ((st = check_ptrs({state, r, w, k, v, a, b, y}, {}))) return st;
+  wkv7::DecodeArgs p;
+  p.B = B; p.H = H;
+  p.bf16 = in_dtype == WKV7_BF16;
+  p.in = {r, w, k, v, a, b};
+  p.state = state; p.y = y;
+  return record_cuda(wkv7::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

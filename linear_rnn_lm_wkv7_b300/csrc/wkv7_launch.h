@@ -1,0 +1,53 @@
+// Internal launchers of the WKV7 kernels (host side).  The extern "C" entry points in
+// wkv7_api.cu validate arguments and call these; nothing here checks arguments again.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace wkv7 {
+
+struct TokenInputs {
+  const void* r;
+  const void* w;
+  const void* k;
+  const void* v;
+  const void* a;
+  const void* b;
+};
+
+struct FwdArgs {
+  int B, T, H, chunk, nchunks;
+  bool bf16;
+  TokenInputs in;
+  const float* h0;
+  float* y;
+  float* h_ckpt;
+  float* hT;
+};
+
+struct BwdArgs {
+  int B, T, H, chunk, nchunks;
+  bool bf16;
+  TokenInputs in;
+  const float* h0;
+  const float* h_ckpt;
+  const float* dy;
+  const float* dhT;
+  float *dr, *dw, *dk, *dv, *da, *db;
+  float* dh0;
+};
+
+struct DecodeArgs {
+  int B, H;
+  bool bf16;
+  TokenInputs in;
+  float* state;
+  float* y;
+};
+
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace wkv7

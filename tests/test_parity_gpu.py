@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs.
+
+Tolerances (relative L2 over the whole tensor, ||x - ref|| / ||ref||): y, hT and checkpoints
+<= 1e-4; every gradient <= 2e-3.  Layout and index mapping of the decode state are checked
+bit for bit with one-hot probes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import wkv7_inputs as gen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL_FWD = 1e-4
+TOL_BWD = 2e-3
+
+
+@pytest.fixture(scope="module")
+def wkv7():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_rnn_lm_wkv7_b300 as m
+    return m
+
+
+def rel(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    n = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / (n if n > 0 else 1.0))
+
+
+def dev(x, dtype):
+    if x is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    return t.cuda()
+
+
+def dev32(x):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+
+
+def host(t):
+    return None if t is None else t.detach().double().cpu().numpy()
+
+
+def run_gpu(wkv7, x, dtype, chunk=32):
+    ins = [dev(x[n], dtype) for n in "rwkvab"]
+    h0 = dev32(x.get("h0"))
+    y, ck, hT = wkv7.forward(*ins, h0, chunk=chunk)
+    grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk)
+    torch.cuda.synchronize()
+    return host(y), host(ck), host(hT), [host(g) for g in grads]
+
+
+def check(x, gpu, chunk, heads=None):
+    """Compare against the oracle; `heads` = list of (b, h) to restrict the oracle to."""
+    y, ck, hT, grads = gpu
+    names = ("dr", "dw", "dk", "dv", "da", "db")
+    if heads is None:
+        sel = [(slice(None), slice(None))]
+    else:
+        sel = [(slice(b, b + 1), slice(h, h + 1)) for b, h in heads]
+    for sb, sh in sel:
+        xs = {n: x[n][sb, :, sh] for n in "rwkvab"}
+        h0 = None if x.get("h0") is None else x["h0"][sb, sh]
+        dhT = None if x.get("dhT") is None else x["dhT"][sb, sh]
+        yo, cko, hTo = oracle.forward(*(xs[n] for n in "rwkvab"), h0, chunk=chunk)
+        assert rel(y[sb, :, sh], yo) <= TOL_FWD, ("y", rel(y[sb, :, sh], yo))
+        assert rel(hT[sb, sh], hTo) <= TOL_FWD, ("hT", rel(hT[sb, sh], hTo))
+        assert rel(ck[sb, sh], cko) <= TOL_FWD, ("h_ckpt", rel(ck[sb, sh], cko))
+        go = oracle.backward(*(xs[n] for n in "rwkvab"), h0, cko, x["dy"][sb, :, sh], dhT, chunk=chunk, mode="ckpt")
+        for name, g, ref in zip(names, grads[:6], go[:6]):
+            assert rel(g[sb, :, sh], ref) <= TOL_BWD, (name, rel(g[sb, :, sh], ref))
+        assert rel(grads[6][sb, sh], go[6]) <= TOL_BWD, ("dh0", rel(grads[6][sb, sh], go[6]))
+    # the last checkpoint is the final state, bit for bit
+    assert np.array_equal(ck[:, :, -1], hT)
+
+
+@pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
+def test_workload_parity_full(wkv7, name):
+    wl = gen.WORKLOADS[name]
+    x = gen.full(wl)
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk), wl.chunk)
+
+
+def test_workload_parity_wide7b_sampled_heads(wkv7):
+    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
+    x = gen.full(wl)
+    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk)
+    check(x, gpu, wl.chunk, heads=[(0, 0), (1, 37), (0, 63)])
+    # every head: properties that hold at any size
+    y, ck, hT, grads = gpu
+    assert all(np.isfinite(g).all() for g in grads[:6]) and np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,T,H,chunk", [
+    (1, 1, 1, 32), (1, 31, 1, 32), (2, 33, 3, 32), (1, 100, 2, 32), (3, 45, 1, 7), (1, 64, 5, 1),
+    (2, 96, 1, 16), (1, 32, 1, 32), (5, 70, 3, 32),
+])
+def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
+    x = gen.random_small(B * 100 + T + H, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    check(x, run_gpu(wkv7, x, dtype, chunk), chunk)
+
+
+def test_no_h0_no_dhT_no_dh0(wkv7):
+    x = gen.random_small(3, B=2, T=64, H=2, D=64)
+    ins = [dev(x[n], "f32") for n in "rwkvab"]
+    y, ck, hT = wkv7.forward(*ins, None)
+    grads = wkv7.backward(*ins, None, ck, dev32(x["dy"]), None, need_dh0=False)
+    assert grads[6] is None
+    yo, cko, _ = oracle.forward(*(x[n] for n in "rwkvab"), None)
+    go = oracle.backward(*(x[n] for n in "rwkvab"), None, cko, x["dy"], None)
+    assert rel(host(y), yo) <= TOL_FWD
+    for g, ref in zip(grads[:6], go[:6]):
+        assert rel(host(g), ref) <= TOL_BWD
+
+
+def test_decay_exactly_one(wkv7):
+    """w == 1 everywhere (bf16 rounding can produce it): the divisions by w are exact."""
+    x = gen.random_small(4, B=1, T=96, H=2, D=64, h0_std=0.1, dhT_std=1.0)
+    x["w"] = np.ones_like(x["w"])
+    check(x, run_gpu(wkv7, x, "f32", 32), 32)
+
+
+def test_prefill_without_checkpoints_and_state_passing(wkv7):
+    """forward(T1) then forward(T2, h0 = hT) equals forward(T1 + T2) bit for bit; h_ckpt may be skipped."""
+    x = gen.random_small(5, B=2, T=96, H=3, D=64, h0_std=0.1)
+    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    h0 = dev32(x["h0"])
+    y, _, hT = wkv7.forward(*ins, h0, checkpoints=False)
+    cut = 40
+    y1, _, h1 = wkv7.forward(*(t[:, :cut].contiguous() for t in ins), h0, checkpoints=False)
+    y2, _, h2 = wkv7.forward(*(t[:, cut:].contiguous() for t in ins), h1, checkpoints=False)
+    assert torch.equal(torch.cat([y1, y2], dim=1), y)
+    assert torch.equal(h2, hT)
+
+
+def test_zero_tokens(wkv7):
+    """T = 0: hT = h0 and dh0 = dhT; nothing else is touched."""
+    B, H = 2, 3
+    h0 = torch.randn(B, H, 64, 64, device="cuda")
+    dhT = torch.randn(B, H, 64, 64, device="cuda")
+    e = torch.empty(B, 0, H, 64, device="cuda")
+    y, ck, hT = wkv7.forward(e, e, e, e, e, e, h0)
+    assert torch.equal(hT, h0) and ck.numel() == 0
+    grads = wkv7.backward(e, e, e, e, e, e, h0, ck, e, dhT)
+    assert torch.equal(grads[6], dhT)
+
+
+# ---------------------------------------------------------------------------------- decode
+
+
+def decode_inputs(wl, b_list):
+    rows = [gen.token_inputs(wl, b) for b in b_list]
+    ins = {n: np.stack([rw[n][0] for rw in rows]) for n in "rwkvab"}   # (B', H, D)
+    st = np.stack([gen.state_init(wl, b, "state") for b in b_list])
+    return ins, st
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_small(wkv7, dtype):
+    x = gen.random_small(6, B=3, T=1, H=5, D=64, h0_std=0.1, dtype=dtype)
+    ins = {n: x[n][:, 0] for n in "rwkvab"}
+    state = dev32(x["h0"])
+    y = wkv7.decode(state, *(dev(ins[n], dtype) for n in "rwkvab"))
+    yo, so = oracle.decode(x["h0"], *(ins[n] for n in "rwkvab"))
+    assert rel(host(y), yo) <= TOL_FWD and rel(host(state), so) <= TOL_FWD
+    # decode == forward with T = 1
+    yf, _, hf = wkv7.forward(*(dev(x[n], dtype) for n in "rwkvab"), dev32(x["h0"]))
+    assert rel(host(state), host(hf)) <= 1e-6 and rel(host(y), host(yf)[:, 0]) <= 1e-6
+
+
+def test_decode_layout_probes(wkv7):
+    """Bit-exact index mapping: state (b,h,i,j) at ((b*H+h)*D+i)*D+j, the same as h0/hT."""
+    B, H, D = 2, 3, 64
+    rng = np.random.default_rng(0)
+    for _ in range(6):
+        b, h, i, j = (int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(D)), int(rng.integers(D)))
+        st = np.zeros((B, H, D, D), np.float32)
+        st[b, h, i, j] = 1.0
+        z = np.zeros((B, H, D), np.float32)
+        w1 = np.ones((B, H, D), np.float32)
+        r = np.zeros((B, H, D), np.float32)
+        r[b, h, j] = 1.0
+        state = dev32(st)
+        y = host(wkv7.decode(state, dev32(r), dev32(w1), dev32(z), dev32(z), dev32(z), dev32(z)))
+        want = np.zeros((B, H, D))
+        want[b, h, i] = 1.0
+        assert np.array_equal(y, want)
+        assert np.array_equal(host(state), st)
+        # from a zero state, v = e_i and k = e_j write exactly 1.0 at (b, h, i, j)
+        state = dev32(np.zeros((B, H, D, D), np.float32))
+        v = np.zeros((B, H, D), np.float32)
+        k = np.zeros((B, H, D), np.float32)
+        v[b, h, i] = 1.0
+        k[b, h, j] = 1.0
+        wkv7.decode(state, dev32(r), dev32(w1), dev32(k), dev32(v), dev32(z), dev32(z))
+        assert np.array_equal(host(state), st)
+
+
+def test_decode7b_full_size_sampled(wkv7):
+    """7B decode step at full size (256 sequences x 2048 heads x 64 x 64 fp32 state, 8.6 GB);
+    the oracle checks sampled sequences, and every sequence must stay finite."""
+    wl = gen.WORKLOADS["decode7b_b256_h2048"]
+    B, H, D = wl.B, wl.H, wl.D
+    state = torch.empty((B, H, D, D), dtype=torch.float32, device="cuda")
+    ins = {n: torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda") for n in "rwkvab"}
+    for b in range(B):
+        row = gen.token_inputs(wl, b)
+        for n in "rwkvab":
+            ins[n][b].copy_(torch.from_numpy(row[n][0]).to(torch.bfloat16))
+        state[b].copy_(torch.from_numpy(gen.state_init(wl, b, "state")))
+    y = wkv7.decode(state, *(ins[n] for n in "rwkvab"))
+    torch.cuda.synchronize()
+    sample = [0, 77, 255]
+    xi, st0 = decode_inputs(wl, sample)
+    yo, so = oracle.decode(st0, *(xi[n] for n in "rwkvab"))
+    for s, b in enumerate(sample):
+        assert rel(host(y[b]), yo[s]) <= TOL_FWD
+        assert rel(host(state[b]), so[s]) <= TOL_FWD
+    assert torch.isfinite(y).all()
