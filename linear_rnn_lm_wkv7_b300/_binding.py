@@ -39,7 +39,7 @@ SIGNATURES = {
 
 def _load():
     if not os.path.exists(LIBRARY_PATH):
-        raise ImportError(f"{LIBRARY_PATH} is not built: run `python -m linear_rnn_lm_wkv7_b300.build`")
+        raise ImportError(f"{LIBRARY_PATH} is not built: run `python linear_rnn_lm_wkv7_b300/build.py`")
     lib = ctypes.CDLL(LIBRARY_PATH)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)

@@ -1,6 +1,8 @@
 """Build libwkv7.so in-tree with nvcc for sm_103a (B300).
 
-    python -m linear_rnn_lm_wkv7_b300.build [--force]
+    python linear_rnn_lm_wkv7_b300/build.py [--force] [-v]
+
+(Run it by path: importing the package itself loads libwkv7.so, which this script makes.)
 
 nvcc cross-compiles without a GPU.  The shared library links the CUDA runtime
 dynamically so that it shares one runtime instance with PyTorch.

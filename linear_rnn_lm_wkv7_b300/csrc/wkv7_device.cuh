@@ -43,4 +43,79 @@ __device__ __forceinline__ void store8(float* p, const float (&o)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 
+// ---- cp.async (16-byte pieces, global -> shared, bypassing L1)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// 8 values already in shared memory (16-byte aligned, input dtype) -> fp32
+__device__ __forceinline__ void raw8(const float* p, float (&o)[8]) {
+  const float4 x = reinterpret_cast<const float4*>(p)[0];
+  const float4 y = reinterpret_cast<const float4*>(p)[1];
+  o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void raw8(const __nv_bfloat16* p, float (&o)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
+  o[4] = bf16_lo(u.z); o[5] = bf16_hi(u.z); o[6] = bf16_lo(u.w); o[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ float2 lo2(float4 x) { return make_float2(x.x, x.y); }
+__device__ __forceinline__ float2 hi2(float4 x) { return make_float2(x.z, x.w); }
+
+// ---- row sums over the 16 lanes of a row group, each lane holding partials of 4 rows.
+// Reduce-scatter: after 5 shuffles lane l (l16 = lane % 16) holds the full sum of row
+// rs_row(l16) = 2*bit3 + bit2.  all_gather4 then hands every lane all four sums.
+__device__ __forceinline__ int rs_row(int l16) { return ((l16 >> 3) & 1) * 2 + ((l16 >> 2) & 1); }
+
+__device__ __forceinline__ float reduce_scatter4(const float (&x)[4], int l16) {
+  const bool b3 = (l16 & 8) != 0, b2 = (l16 & 4) != 0;
+  float k0 = b3 ? x[2] : x[0], k1 = b3 ? x[3] : x[1];
+  const float s0 = b3 ? x[0] : x[2], s1 = b3 ? x[1] : x[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+  float k = b2 ? k1 : k0;
+  const float s = b2 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, s, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+__device__ __forceinline__ void all_gather4(float z, int l16, float (&out)[4]) {
+  const int q = rs_row(l16);
+  const float o = __shfl_xor_sync(0xffffffffu, z, 4);
+  const float e0 = (q & 1) ? o : z;
+  const float e1 = (q & 1) ? z : o;
+  const float f0 = __shfl_xor_sync(0xffffffffu, e0, 8);
+  const float f1 = __shfl_xor_sync(0xffffffffu, e1, 8);
+  const bool hi = (q & 2) != 0;
+  out[0] = hi ? f0 : e0;
+  out[1] = hi ? f1 : e1;
+  out[2] = hi ? e0 : f0;
+  out[3] = hi ? e1 : f1;
+}
+
+// all-reduce of 4 rows over 16 lanes as a 4-level butterfly: more shuffles than
+// reduce-scatter + all-gather but only 4 dependent steps (used on serial chains)
+__device__ __forceinline__ void butterfly4(float (&x)[4]) {
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], m);
+}
+
+// 4-wide dot products of 4 state rows with one float4 (two packed fp32x2 FMAs each)
+__device__ __forceinline__ void dot4x4(const float2 (&S)[4][2], float4 c, float (&out)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p2 = __ffma2_rn(S[i][1], hi2(c), __fmul2_rn(S[i][0], lo2(c)));
+    out[i] = p2.x + p2.y;
+  }
+}
+
 }  // namespace wkv7

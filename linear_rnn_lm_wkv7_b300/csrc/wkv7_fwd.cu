@@ -6,164 +6,285 @@
 // with a copy of S written after every `chunk` tokens.
 //
 // Mapping.  Rows of a head never interact in the forward, so a head is split into
-// 64/ROWS row blocks, one CTA each (grid = B*H*64/ROWS).  Inside a CTA a row is held
-// by L = 64/COLS consecutive lanes, COLS fp32 state values each, in registers for the
-// whole sequence.  The two row sums per token (sa and y) are L-lane butterflies.
-// The per-token column vectors w, k, a, b, r are shared by every row of the head: a
-// tile of 32 tokens is staged into shared memory as fp32 (bf16 widened once per CTA),
-// read back as broadcast float4s.  y goes through shared memory so it leaves as
-// ROWS-float runs; checkpoints and hT leave straight from registers as float4s.
+// 64/ROWS row blocks, one CTA each.  Thread = 4 rows x 4 columns of the state, in
+// registers for the whole sequence; the 16 lanes of a row group own column blocks 4g
+// (g = lane % 16), so a half-warp reads one contiguous 256-byte row of each per-token
+// vector without bank conflicts, and every value a lane loads feeds four rows.  (A
+// 128-bit shared load whose lanes hit distinct addresses costs 4 wavefronts; loads
+// feeding one row per lane made the shared-memory pipe the limit.)
+//
+// One-token lookahead.  The serial chain of the recurrence is sa_t -> S_t -> sa_{t+1}.
+// Since S_t = S_{t-1} diag(w_t) + v_t k_t^T + sa_t b_t^T,
+//     sa_{t+1} = S_{t-1} (w_t o a_{t+1}) + v_t (k_t . a_{t+1}) + sa_t (b_t . a_{t+1}),
+// so the row sum that produces sa_{t+1} reads the state *before* token t and runs in
+// parallel with token t's update.  c_t = w_t o a_{t+1} and the scalars k_t . a_{t+1},
+// b_t . a_{t+1} do not depend on the state; they are formed once per CTA per tile.
+// That row sum is a 4-level butterfly (shortest dependent chain); y, off the chain,
+// uses the cheaper 5-shuffle reduce-scatter.
+//
+// Staging.  Tiles of 32 tokens of w, k, a, b, r (+ one token of a ahead) and the CTA's
+// slice of v are copied to shared memory with cp.async, double-buffered so the copy of
+// tile i+1 overlaps the recurrence over tile i, then widened to fp32 once per CTA.  y
+// leaves through shared memory as ROWS-float runs; checkpoints and hT leave from
+// registers as float4s.
 #include "wkv7_device.cuh"
 #include "wkv7_launch.h"
 
 namespace wkv7 {
 namespace {
 
-constexpr int kTile = 32;  // tokens staged per shared-memory tile
+constexpr int kTile = 32;          // tokens per staged tile
+constexpr int kTileA = kTile + 1;  // rows of a per tile (one token of lookahead)
 
-template <int ROWS>
-constexpr size_t fwd_smem_bytes() {
-  return sizeof(float) * (5 * kTile * kD + 2 * kTile * ROWS);
+template <typename Tin, int ROWS>
+struct FwdLayout {
+  // raw (input dtype) buffer, double-buffered: W, K, B, R [kTile][64], A [kTileA][64], V [kTile][ROWS]
+  static constexpr int kRawElems = 4 * kTile * kD + kTileA * kD + kTile * ROWS;
+  static constexpr size_t kRawBytes = ((kRawElems * sizeof(Tin)) + 15) / 16 * 16;
+  // fp32 tiles: W, K, B, R, C [kTile][64]; KA, BA [kTile]; V, Y [kTile][ROWS]
+  static constexpr int kF32 = 5 * kTile * kD + 2 * kTile + 2 * kTile * ROWS;
+  static constexpr size_t kBytes = 2 * kRawBytes + sizeof(float) * kF32;
+};
+
+// Issue the cp.async copies of tile [t0, t0 + nt): W K B R rows, A rows t0 .. t0+na-1, V slice.
+template <typename Tin, int ROWS, int NT>
+__device__ __forceinline__ void issue_tile(Tin* raw, int t0, int nt, int na, size_t base, size_t tstride,
+                                           int vcol, const Tin* __restrict__ w, const Tin* __restrict__ k,
+                                           const Tin* __restrict__ b, const Tin* __restrict__ r,
+                                           const Tin* __restrict__ a, const Tin* __restrict__ v) {
+  constexpr int CPR = kD * (int)sizeof(Tin) / 16;  // 16-byte pieces per 64-wide row
+  constexpr int EPC = 16 / (int)sizeof(Tin);       // elements per piece
+  const Tin* srcs[4] = {w, k, b, r};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    Tin* dst = raw + q * kTile * kD;
+    for (int e = threadIdx.x; e < nt * CPR; e += NT) {
+      const int tt = e / CPR, pc = e % CPR;
+      cp_async16(dst + tt * kD + pc * EPC, srcs[q] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+    }
+  }
+  {
+    Tin* dst = raw + 4 * kTile * kD;
+    for (int e = threadIdx.x; e < na * CPR; e += NT) {
+      const int tt = e / CPR, pc = e % CPR;
+      cp_async16(dst + tt * kD + pc * EPC, a + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+    }
+  }
+  {
+    constexpr int VPR = ROWS * (int)sizeof(Tin) / 16;  // pieces per token of the CTA's v slice
+    Tin* dst = raw + 4 * kTile * kD + kTileA * kD;
+    for (int e = threadIdx.x; e < nt * VPR; e += NT) {
+      const int tt = e / VPR, pc = e % VPR;
+      cp_async16(dst + tt * ROWS + pc * EPC, v + base + (size_t)(t0 + tt) * tstride + vcol + pc * EPC);
+    }
+  }
 }
 
-template <typename Tin, int COLS, int ROWS>
-__global__ void __launch_bounds__(ROWS*(kD / COLS))
+template <typename Tin, int ROWS>
+__global__ void __launch_bounds__(ROWS * 4, 1)
 fwd_kernel(int T, int H, int chunk, int nchunks,
            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
            const float* __restrict__ h0, float* __restrict__ y, float* __restrict__ h_ckpt,
            float* __restrict__ hT) {
-  constexpr int L = kD / COLS;   // lanes per row
-  constexpr int NT = ROWS * L;   // threads per CTA
-  constexpr int NRB = kD / ROWS; // row blocks per head
-  static_assert(NT % 32 == 0 && 32 % L == 0, "a row group must sit inside one warp");
+  constexpr int NT = ROWS * 4;
+  constexpr int NW = NT / 32;
+  constexpr int NRB = kD / ROWS;
+  using Lay = FwdLayout<Tin, ROWS>;
+  static_assert(ROWS * (int)sizeof(Tin) % 16 == 0, "v slice must be whole 16-byte pieces");
+  static_assert(ROWS % 8 == 0, "a warp holds 8 rows");
 
   extern __shared__ float4 smem4[];
-  float* s_vec = reinterpret_cast<float*>(smem4);  // [5][kTile][kD]: w, k, a, b, r
-  float* s_v = s_vec + 5 * kTile * kD;              // [kTile][ROWS]
-  float* s_y = s_v + kTile * ROWS;                  // [kTile][ROWS]
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+  Tin* raw0 = reinterpret_cast<Tin*>(sm);
+  Tin* raw1 = reinterpret_cast<Tin*>(sm + Lay::kRawBytes);
+  float* fW = reinterpret_cast<float*>(sm + 2 * Lay::kRawBytes);
+  float* fK = fW + kTile * kD;
+  float* fB = fK + kTile * kD;
+  float* fR = fB + kTile * kD;
+  float* fC = fR + kTile * kD;
+  float* fKA = fC + kTile * kD;
+  float* fBA = fKA + kTile;
+  float* fV = fBA + kTile;
+  float* fY = fV + kTile * ROWS;
 
   const int bh = blockIdx.x / NRB;
   const int rb = blockIdx.x - bh * NRB;
   const int bi = bh / H;
   const int hi = bh - bi * H;
   const int tid = threadIdx.x;
-  const int g = tid % L;
-  const int rl = tid / L;
-  const int row = rb * ROWS + rl;
-  const int c0 = g * COLS;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int l16 = tid & 15;
+  const int rloc = 4 * (tid >> 4);    // first local row of this thread
+  const int row0 = rb * ROWS + rloc;  // first row within the head
+  const int j0 = 4 * l16;             // first column
+  const int qrow = rs_row(l16);       // row whose y this lane ends up holding
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
   const size_t sbase = (size_t)bh * kD * kD;
+  const int ntiles = (T + kTile - 1) / kTile;
 
-  float S[COLS];
+  // state: S[i] = row row0+i, columns j0..j0+3 as two float2
+  float2 S[4][2];
   if (h0 != nullptr) {
-    const float4* p = reinterpret_cast<const float4*>(h0 + sbase + (size_t)row * kD + c0);
 #pragma unroll
-    for (int q = 0; q < COLS / 4; ++q) {
-      const float4 x = __ldg(p + q);
-      S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(h0 + sbase + (size_t)(row0 + i) * kD + j0));
+      S[i][0] = lo2(x);
+      S[i][1] = hi2(x);
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < COLS; ++c) S[c] = 0.f;
+    for (int i = 0; i < 4; ++i) S[i][0] = S[i][1] = make_float2(0.f, 0.f);
   }
 
-  int to_ckpt = chunk;  // tokens left until the next checkpoint
-  for (int t0 = 0; t0 < T; t0 += kTile) {
+  if (ntiles > 0) {
+    issue_tile<Tin, ROWS, NT>(raw0, 0, min(kTile, T), min(kTileA, T), base, tstride, rb * ROWS, w, k, b, r, a, v);
+    cp_async_commit();
+  }
+
+  // sa for token 0 (the state before it is h0)
+  float sa[4] = {0.f, 0.f, 0.f, 0.f};
+  if (T > 0) {
+    dot4x4(S, load4(a + base + j0), sa);
+    butterfly4(sa);
+  }
+
+  int to_ckpt = chunk;
+  for (int it = 0; it < ntiles; ++it) {
+    const int t0 = it * kTile;
     const int nt = min(kTile, T - t0);
-    __syncthreads();  // the previous tile's shared data is no longer read
-    for (int e = tid; e < 5 * nt * 8; e += NT) {
-      const int q = e / (nt * 8);
-      const int rem = e - q * nt * 8;
-      const int tt = rem >> 3;
-      const int c8 = rem & 7;
-      const Tin* src = q == 0 ? w : q == 1 ? k : q == 2 ? a : q == 3 ? b : r;
-      float o[8];
-      load8(src + base + (size_t)(t0 + tt) * tstride + c8 * 8, o);
-      store8(s_vec + (q * kTile + tt) * kD + c8 * 8, o);
+    Tin* raw = (it & 1) ? raw1 : raw0;
+    if (it + 1 < ntiles) {
+      const int t1 = t0 + kTile;
+      issue_tile<Tin, ROWS, NT>((it & 1) ? raw0 : raw1, t1, min(kTile, T - t1), min(kTileA, T - t1), base,
+                                tstride, rb * ROWS, w, k, b, r, a, v);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    for (int e = tid; e < nt * ROWS; e += NT) {
-      const int tt = e / ROWS;
-      const int rr = e - tt * ROWS;
-      s_v[tt * ROWS + rr] = to_f32(v[base + (size_t)(t0 + tt) * tstride + rb * ROWS + rr]);
+    __syncthreads();  // tile `it` is in shared memory; the previous tile's fp32 data is consumed
+
+    // ---- widen to fp32 and form the lookahead terms: 4 tokens per warp pass, 8 lanes per token
+    {
+      const Tin* rW = raw;
+      const Tin* rK = raw + kTile * kD;
+      const Tin* rB = raw + 2 * kTile * kD;
+      const Tin* rR = raw + 3 * kTile * kD;
+      const Tin* rA = raw + 4 * kTile * kD;
+      for (int tg = warp * 4; tg < nt; tg += NW * 4) {
+        const int tt = tg + (lane >> 3);
+        const int c8 = (lane & 7) * 8;
+        float ka = 0.f, ba = 0.f;
+        if (tt < nt) {
+          float ww[8], kk[8], bb[8], rr[8], an[8];
+          raw8(rW + tt * kD + c8, ww);
+          raw8(rK + tt * kD + c8, kk);
+          raw8(rB + tt * kD + c8, bb);
+          raw8(rR + tt * kD + c8, rr);
+          if (t0 + tt + 1 < T) {
+            raw8(rA + (tt + 1) * kD + c8, an);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) an[u] = 0.f;
+          }
+          float cc[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            cc[u] = ww[u] * an[u];
+            ka = fmaf(kk[u], an[u], ka);
+            ba = fmaf(bb[u], an[u], ba);
+          }
+          store8(fW + tt * kD + c8, ww);
+          store8(fK + tt * kD + c8, kk);
+          store8(fB + tt * kD + c8, bb);
+          store8(fR + tt * kD + c8, rr);
+          store8(fC + tt * kD + c8, cc);
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+          ka += __shfl_xor_sync(0xffffffffu, ka, m);
+          ba += __shfl_xor_sync(0xffffffffu, ba, m);
+        }
+        if (tt < nt && (lane & 7) == 0) {
+          fKA[tt] = ka;
+          fBA[tt] = ba;
+        }
+      }
+      const Tin* rV = raw + 4 * kTile * kD + kTileA * kD;
+      for (int e = tid; e < nt * ROWS; e += NT) fV[e] = to_f32(rV[e]);
     }
     __syncthreads();
 
+    // ---- the recurrence over the tile (unrolled so consecutive tokens' shuffle chains overlap)
+#pragma unroll 2
     for (int tt = 0; tt < nt; ++tt) {
-      const float4* pw = reinterpret_cast<const float4*>(s_vec + (0 * kTile + tt) * kD + c0);
-      const float4* pk = reinterpret_cast<const float4*>(s_vec + (1 * kTile + tt) * kD + c0);
-      const float4* pa = reinterpret_cast<const float4*>(s_vec + (2 * kTile + tt) * kD + c0);
-      const float4* pb = reinterpret_cast<const float4*>(s_vec + (3 * kTile + tt) * kD + c0);
-      const float4* pr = reinterpret_cast<const float4*>(s_vec + (4 * kTile + tt) * kD + c0);
+      const float4 c4 = *reinterpret_cast<const float4*>(fC + tt * kD + j0);
+      const float4 w4 = *reinterpret_cast<const float4*>(fW + tt * kD + j0);
+      const float4 k4 = *reinterpret_cast<const float4*>(fK + tt * kD + j0);
+      const float4 b4 = *reinterpret_cast<const float4*>(fB + tt * kD + j0);
+      const float4 r4 = *reinterpret_cast<const float4*>(fR + tt * kD + j0);
+      const float4 v4 = *reinterpret_cast<const float4*>(fV + tt * ROWS + rloc);
+      const float ka = fKA[tt], ba = fBA[tt];
+      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 
-      // sa = S a (this thread's columns, then the L-lane butterfly)
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q = 0; q < COLS / 4; ++q) {
-        const float4 av = pa[q];
-        part[0] = fmaf(S[4 * q], av.x, part[0]);
-        part[1] = fmaf(S[4 * q + 1], av.y, part[1]);
-        part[2] = fmaf(S[4 * q + 2], av.z, part[2]);
-        part[3] = fmaf(S[4 * q + 3], av.w, part[3]);
-      }
-      float sa = (part[0] + part[1]) + (part[2] + part[3]);
-#pragma unroll
-      for (int m = 1; m < L; m <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, m);
+      // lookahead row sums on the state before this token
+      float P[4];
+      dot4x4(S, c4, P);
+      butterfly4(P);
 
-      const float vi = s_v[tt * ROWS + rl];
-      float yp[4] = {0.f, 0.f, 0.f, 0.f};
+      // S <- S w + v k + sa b
 #pragma unroll
-      for (int q = 0; q < COLS / 4; ++q) {
-        const float4 wv = pw[q], kv = pk[q], bv = pb[q], rv = pr[q];
-        S[4 * q] = fmaf(S[4 * q], wv.x, fmaf(vi, kv.x, sa * bv.x));
-        S[4 * q + 1] = fmaf(S[4 * q + 1], wv.y, fmaf(vi, kv.y, sa * bv.y));
-        S[4 * q + 2] = fmaf(S[4 * q + 2], wv.z, fmaf(vi, kv.z, sa * bv.z));
-        S[4 * q + 3] = fmaf(S[4 * q + 3], wv.w, fmaf(vi, kv.w, sa * bv.w));
-        yp[0] = fmaf(S[4 * q], rv.x, yp[0]);
-        yp[1] = fmaf(S[4 * q + 1], rv.y, yp[1]);
-        yp[2] = fmaf(S[4 * q + 2], rv.z, yp[2]);
-        yp[3] = fmaf(S[4 * q + 3], rv.w, yp[3]);
+      for (int i = 0; i < 4; ++i) {
+        const float2 s2 = make_float2(sa[i], sa[i]);
+        const float2 v2 = make_float2(vv[i], vv[i]);
+        const float2 u0 = __ffma2_rn(v2, lo2(k4), __fmul2_rn(s2, lo2(b4)));
+        const float2 u1 = __ffma2_rn(v2, hi2(k4), __fmul2_rn(s2, hi2(b4)));
+        S[i][0] = __ffma2_rn(S[i][0], lo2(w4), u0);
+        S[i][1] = __ffma2_rn(S[i][1], hi2(w4), u1);
       }
-      float yi = (yp[0] + yp[1]) + (yp[2] + yp[3]);
+      // y = S r
+      float yp[4];
+      dot4x4(S, r4, yp);
+      const float yq = reduce_scatter4(yp, l16);
+      if ((l16 & 3) == 0) fY[tt * ROWS + rloc + qrow] = yq;
 #pragma unroll
-      for (int m = 1; m < L; m <<= 1) yi += __shfl_xor_sync(0xffffffffu, yi, m);
-      if (g == 0) s_y[tt * ROWS + rl] = yi;
+      for (int i = 0; i < 4; ++i) sa[i] = fmaf(sa[i], ba, fmaf(vv[i], ka, P[i]));
 
       const int t = t0 + tt;
       if (--to_ckpt == 0 || t == T - 1) {
         to_ckpt = chunk;
         if (h_ckpt != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(
-              h_ckpt + ((size_t)bh * nchunks + t / chunk) * kD * kD + (size_t)row * kD + c0);
+          float* dst = h_ckpt + ((size_t)bh * nchunks + t / chunk) * kD * kD + (size_t)row0 * kD + j0;
 #pragma unroll
-          for (int q = 0; q < COLS / 4; ++q)
-            dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(dst + i * kD) = make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
         }
       }
     }
     __syncthreads();
     for (int e = tid; e < nt * ROWS; e += NT) {
       const int tt = e / ROWS;
-      const int rr = e - tt * ROWS;
-      y[base + (size_t)(t0 + tt) * tstride + rb * ROWS + rr] = s_y[tt * ROWS + rr];
+      const int rr = e % ROWS;
+      y[base + (size_t)(t0 + tt) * tstride + rb * ROWS + rr] = fY[e];
     }
   }
 
   if (hT != nullptr) {
-    float4* dst = reinterpret_cast<float4*>(hT + sbase + (size_t)row * kD + c0);
 #pragma unroll
-    for (int q = 0; q < COLS / 4; ++q)
-      dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(hT + sbase + (size_t)(row0 + i) * kD + j0) =
+          make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
   }
 }
 
-template <typename Tin>
-cudaError_t launch_fwd_t(const FwdArgs& p, cudaStream_t stream) {
-  constexpr int COLS = 16, ROWS = 16;
-  constexpr int NT = ROWS * (kD / COLS);
-  const size_t smem = fwd_smem_bytes<ROWS>();
-  auto kern = fwd_kernel<Tin, COLS, ROWS>;
+template <typename Tin, int ROWS>
+cudaError_t launch_fwd_cfg(const FwdArgs& p, cudaStream_t stream) {
+  constexpr int NT = ROWS * 4;
+  const size_t smem = FwdLayout<Tin, ROWS>::kBytes;
+  auto kern = fwd_kernel<Tin, ROWS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * p.H * (kD / ROWS);
@@ -176,7 +297,7 @@ cudaError_t launch_fwd_t(const FwdArgs& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& p, cudaStream_t stream) {
-  return p.bf16 ? launch_fwd_t<__nv_bfloat16>(p, stream) : launch_fwd_t<float>(p, stream);
+  return p.bf16 ? launch_fwd_cfg<__nv_bfloat16, 32>(p, stream) : launch_fwd_cfg<float, 32>(p, stream);
 }
 
 }  // namespace wkv7

@@ -130,7 +130,10 @@ def test_decay_exactly_one(wkv7):
 
 
 def test_prefill_without_checkpoints_and_state_passing(wkv7):
-    """forward(T1) then forward(T2, h0 = hT) equals forward(T1 + T2) bit for bit; h_ckpt may be skipped."""
+    """forward(T1) then forward(T2, h0 = hT) equals forward(T1 + T2) to fp32 rounding; h_ckpt may be skipped.
+
+    Not bit for bit: inside one call sa_t is formed by the one-token lookahead (a different, equal
+    expression), while the first token of a call forms it directly from h0."""
     x = gen.random_small(5, B=2, T=96, H=3, D=64, h0_std=0.1)
     ins = [dev(x[n], "bf16") for n in "rwkvab"]
     h0 = dev32(x["h0"])
@@ -138,8 +141,8 @@ def test_prefill_without_checkpoints_and_state_passing(wkv7):
     cut = 40
     y1, _, h1 = wkv7.forward(*(t[:, :cut].contiguous() for t in ins), h0, checkpoints=False)
     y2, _, h2 = wkv7.forward(*(t[:, cut:].contiguous() for t in ins), h1, checkpoints=False)
-    assert torch.equal(torch.cat([y1, y2], dim=1), y)
-    assert torch.equal(h2, hT)
+    assert rel(host(torch.cat([y1, y2], dim=1)), host(y)) <= 1e-6
+    assert rel(host(h2), host(hT)) <= 1e-6
 
 
 def test_zero_tokens(wkv7):
