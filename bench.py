@@ -236,6 +236,7 @@ def run_ours(args, rank, world, local_rank):
         s["y"] = torch.empty((B, T, H, D), device=dev)
         s["ck"] = torch.empty((B, H, C, D, D), device=dev)
         s["hT"] = torch.empty((B, H, D, D), device=dev)
+        s["sa"] = torch.empty((B, T, H, D), device=dev)
         s["g"] = [torch.empty((B, T, H, D), device=dev) for _ in range(6)] + [torch.empty((B, H, D, D), device=dev)]
         return s
 
@@ -246,10 +247,10 @@ def run_ours(args, rank, world, local_rank):
         ins = [s[n] for n in "rwkvab"]
         if ev is not None:
             ev[0].record(stream)
-        wkv7.forward(*ins, None, chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"]))
+        wkv7.forward(*ins, None, chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"]))
         if ev is not None:
             ev[1].record(stream)
-        wkv7.backward(*ins, None, s["ck"], s["dy"], None, chunk=wl.chunk, out=s["g"])
+        wkv7.backward(*ins, None, s["ck"], s["dy"], None, chunk=wl.chunk, sa=s["sa"], out=s["g"])
         if ev is not None:
             ev[2].record(stream)
 

@@ -71,31 +71,37 @@ int wkv7_num_chunks(int T, int chunk);
  *           min(T, (c+1)*chunk) - 1, so the last entry equals hT (T % chunk
  *           may be non-zero: the last chunk is then shorter).
  *   hT      (B,H,D,D) fp32 final state, or NULL.
+ *   sa      (B,T,H,D) fp32 output or NULL: sa_t = S_{t-1} a_t for every token and
+ *           state row (element (b,t,h,i) is row i).  Passing it to wkv7_backward
+ *           spares the backward its per-chunk recompute of these values.
  * Source: Forward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b,
-                 const float *h0, float *y, float *h_ckpt, float *hT, void *stream);
+                 const float *h0, float *y, float *h_ckpt, float *hT, float *sa, void *stream);
 
 /*
  * Checkpointed backward (vector-Jacobian product of wkv7_forward).
  *   h0      the forward's initial state, or NULL for zeros.
  *   h_ckpt  the forward's checkpoints (B,H,C,D,D), required when T > 0; the same
  *           chunk value must be passed.
+ *   sa      the forward's `sa` output (B,T,H,D), or NULL: then each chunk is first
+ *           run forward from its start checkpoint (h0 for the first) to recompute it.
  *   dy      (B,T,H,D) fp32 gradient of the loss w.r.t. y, required.
  *   dhT     (B,H,D,D) fp32 gradient w.r.t. hT, or NULL for zeros.
  *   dr, dw, dk, dv, da, db  (B,T,H,D) fp32 outputs, required.
  *   dh0     (B,H,D,D) fp32 gradient w.r.t. h0, or NULL (not written).
- * Each chunk is recomputed forward from its start checkpoint (h0 for the first)
- * to obtain sa, then walked in reverse from its end checkpoint, the earlier
- * states rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).
+ * Each chunk is walked in reverse from its end checkpoint, the earlier states
+ * rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).  Column sums are
+ * taken in a fixed order (no atomics): results are deterministic.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
                   const void *r, const void *w, const void *k,
                   const void *v, const void *a, const void *b,
-                  const float *h0, const float *h_ckpt, const float *dy, const float *dhT,
+                  const float *h0, const float *h_ckpt, const float *sa,
+                  const float *dy, const float *dhT,
                   float *dr, float *dw, float *dk, float *dv, float *da, float *db,
                   float *dh0, void *stream);
 

@@ -28,8 +28,8 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "wkv7_num_chunks": (_I, [_I, _I]),
-    "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P]),
-    "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P] * 7 + [_P]),
+    "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
+    "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
     "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
     "wkv7_strerror": (ctypes.c_char_p, [_I]),
     "wkv7_last_cuda_error": (ctypes.c_char_p, []),
@@ -120,12 +120,14 @@ def _check_f32(t, shape, name, where, dev):
 
 
 def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True, final_state: bool = True,
-            out=None, stream=None):
+            save_sa: bool = False, out=None, stream=None):
     """WKV7 forward.  r..b: (B, T, H, 64) float32/bfloat16 CUDA tensors; h0: (B, H, 64, 64) float32 or None.
 
     Returns (y, h_ckpt, hT): y (B,T,H,64) fp32; h_ckpt (B,H,C,64,64) fp32 (None when
-    checkpoints=False); hT (B,H,64,64) fp32 (None when final_state=False).  `out` may give
-    preallocated (y, h_ckpt, hT).
+    checkpoints=False); hT (B,H,64,64) fp32 (None when final_state=False).  With
+    save_sa=True a fourth tensor sa (B,T,H,64) fp32 is returned (sa_t = S_{t-1} a_t per
+    state row), which `backward` accepts to skip its recompute.  `out` may give
+    preallocated (y, h_ckpt, hT) or (y, h_ckpt, hT, sa).
     """
     torch = _torch()
     B, T, H, D = r.shape
@@ -133,25 +135,31 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
     C = num_chunks(T, chunk)
     dev = r.device
     if out is not None:
-        y, ck, hT = out
+        y, ck, hT = out[:3]
+        sa = out[3] if len(out) > 3 else None
     else:
         y = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
         ck = torch.empty((B, H, C, D, D), dtype=torch.float32, device=dev) if checkpoints else None
         hT = torch.empty((B, H, D, D), dtype=torch.float32, device=dev) if final_state else None
+        sa = torch.empty((B, T, H, D), dtype=torch.float32, device=dev) if save_sa else None
     _check_f32(h0, (B, H, D, D), "h0", "wkv7.forward", dev)
     _check_f32(y, (B, T, H, D), "y", "wkv7.forward", dev)
     _check_f32(ck, (B, H, C, D, D), "h_ckpt", "wkv7.forward", dev)
     _check_f32(hT, (B, H, D, D), "hT", "wkv7.forward", dev)
-    st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT)),
+    _check_f32(sa, (B, T, H, D), "sa", "wkv7.forward", dev)
+    st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)),
                           _stream(stream))
     _check(st, "wkv7_forward")
+    if save_sa or (out is not None and len(out) > 3):
+        return y, ck, hT, sa
     return y, ck, hT
 
 
 def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_dh0: bool = True,
-             out=None, stream=None):
+             sa=None, out=None, stream=None):
     """Checkpointed WKV7 backward.  Returns (dr, dw, dk, dv, da, db, dh0), all fp32 (dh0 None when
-    need_dh0=False).  h_ckpt must come from `forward` with the same chunk."""
+    need_dh0=False).  h_ckpt must come from `forward` with the same chunk; `sa` is the forward's
+    saved sa (save_sa=True) or None, in which case each chunk recomputes it."""
     torch = _torch()
     B, T, H, D = r.shape
     _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.backward")
@@ -159,6 +167,7 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
     dev = r.device
     _check_f32(h0, (B, H, D, D), "h0", "wkv7.backward", dev)
     _check_f32(h_ckpt, (B, H, C, D, D), "h_ckpt", "wkv7.backward", dev)
+    _check_f32(sa, (B, T, H, D), "sa", "wkv7.backward", dev)
     _check_f32(dy, (B, T, H, D), "dy", "wkv7.backward", dev)
     _check_f32(dhT, (B, H, D, D), "dhT", "wkv7.backward", dev)
     if out is not None:
@@ -169,7 +178,8 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
     for name, g in zip(("dr", "dw", "dk", "dv", "da", "db"), grads[:6]):
         _check_f32(g, (B, T, H, D), name, "wkv7.backward", dev)
     _check_f32(grads[6], (B, H, D, D), "dh0", "wkv7.backward", dev)
-    st = lib.wkv7_backward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, dy, dhT)),
+    st = lib.wkv7_backward(B, T, H, D, chunk, _in_dtype(r),
+                           *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, sa, dy, dhT)),
                            *map(_ptr, grads), _stream(stream))
     _check(st, "wkv7_backward")
     return tuple(grads)

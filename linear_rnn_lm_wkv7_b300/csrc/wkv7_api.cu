@@ -55,6 +55,21 @@ int check_ptrs(std::initializer_list<const void*> required, std::initializer_lis
 
 }  // namespace
 
+namespace wkv7 {
+
+int num_sms() {
+  static thread_local int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace wkv7
+
 extern "C" {
 
 int wkv7_version(void) { return kVersion; }
@@ -81,12 +96,12 @@ const char* wkv7_last_cuda_error(void) { return g_last_cuda_error; }
 
 int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
                  const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
-                 float* h_ckpt, float* hT, void* stream) {
+                 float* h_ckpt, float* hT, float* sa, void* stream) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
   if (T > 0) {
-    if ((st = check_ptrs({r, w, k, v, a, b, y}, {h0, h_ckpt, hT}))) return st;
+    if ((st = check_ptrs({r, w, k, v, a, b, y}, {h0, h_ckpt, hT, sa}))) return st;
   } else if ((st = check_ptrs({}, {h0, hT}))) {
     return st;
   }
@@ -94,19 +109,19 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void
   p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
   p.bf16 = in_dtype == WKV7_BF16;
   p.in = {r, w, k, v, a, b};
-  p.h0 = h0; p.y = y; p.h_ckpt = h_ckpt; p.hT = hT;
+  p.h0 = h0; p.y = y; p.h_ckpt = h_ckpt; p.hT = hT; p.sa = T > 0 ? sa : nullptr;
   return record_cuda(wkv7::launch_forward(p, static_cast<cudaStream_t>(stream)));
 }
 
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
                   const void* k, const void* v, const void* a, const void* b, const float* h0,
-                  const float* h_ckpt, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
+                  const float* h_ckpt, const float* sa, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
                   float* dv, float* da, float* db, float* dh0, void* stream) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
   if (T > 0) {
-    if ((st = check_ptrs({r, w, k, v, a, b, h_ckpt, dy, dr, dw, dk, dv, da, db}, {h0, dhT, dh0}))) return st;
+    if ((st = check_ptrs({r, w, k, v, a, b, h_ckpt, dy, dr, dw, dk, dv, da, db}, {h0, sa, dhT, dh0}))) return st;
   } else if ((st = check_ptrs({}, {h0, dhT, dh0}))) {
     return st;
   }
@@ -114,7 +129,7 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const voi
   p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
   p.bf16 = in_dtype == WKV7_BF16;
   p.in = {r, w, k, v, a, b};
-  p.h0 = h0; p.h_ckpt = h_ckpt; p.dy = dy; p.dhT = dhT;
+  p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
   p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
   return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
 }

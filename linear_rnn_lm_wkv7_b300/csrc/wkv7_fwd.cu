@@ -41,8 +41,8 @@ struct FwdLayout {
   // raw (input dtype) buffer, double-buffered: W, K, B, R [kTile][64], A [kTileA][64], V [kTile][ROWS]
   static constexpr int kRawElems = 4 * kTile * kD + kTileA * kD + kTile * ROWS;
   static constexpr size_t kRawBytes = ((kRawElems * sizeof(Tin)) + 15) / 16 * 16;
-  // fp32 tiles: W, K, B, R, C [kTile][64]; KA, BA [kTile]; V, Y [kTile][ROWS]
-  static constexpr int kF32 = 5 * kTile * kD + 2 * kTile + 2 * kTile * ROWS;
+  // fp32 tiles: W, K, B, R, C [kTile][64]; KA, BA [kTile]; V, Y, SA [kTile][ROWS]
+  static constexpr int kF32 = 5 * kTile * kD + 2 * kTile + 3 * kTile * ROWS;
   static constexpr size_t kBytes = 2 * kRawBytes + sizeof(float) * kF32;
 };
 
@@ -86,7 +86,7 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
            const float* __restrict__ h0, float* __restrict__ y, float* __restrict__ h_ckpt,
-           float* __restrict__ hT) {
+           float* __restrict__ hT, float* __restrict__ sa_out) {
   constexpr int NT = ROWS * 4;
   constexpr int NW = NT / 32;
   constexpr int NRB = kD / ROWS;
@@ -107,6 +107,7 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
   float* fBA = fKA + kTile;
   float* fV = fBA + kTile;
   float* fY = fV + kTile * ROWS;
+  float* fSA = fY + kTile * ROWS;
 
   const int bh = blockIdx.x / NRB;
   const int rb = blockIdx.x - bh * NRB;
@@ -229,6 +230,8 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
       const float4 v4 = *reinterpret_cast<const float4*>(fV + tt * ROWS + rloc);
       const float ka = fKA[tt], ba = fBA[tt];
       const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+      if (sa_out != nullptr && l16 == 0)
+        *reinterpret_cast<float4*>(fSA + tt * ROWS + rloc) = make_float4(sa[0], sa[1], sa[2], sa[3]);
 
       // lookahead row sums on the state before this token
       float P[4];
@@ -269,6 +272,7 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
       const int tt = e / ROWS;
       const int rr = e % ROWS;
       y[base + (size_t)(t0 + tt) * tstride + rb * ROWS + rr] = fY[e];
+      if (sa_out != nullptr) sa_out[base + (size_t)(t0 + tt) * tstride + rb * ROWS + rr] = fSA[e];
     }
   }
 
@@ -290,7 +294,7 @@ cudaError_t launch_fwd_cfg(const FwdArgs& p, cudaStream_t stream) {
   const unsigned grid = (unsigned)p.B * p.H * (kD / ROWS);
   kern<<<grid, NT, smem, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
                                    (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
-                                   (const Tin*)p.in.b, p.h0, p.y, p.h_ckpt, p.hT);
+                                   (const Tin*)p.in.b, p.h0, p.y, p.h_ckpt, p.hT, p.sa);
   return cudaGetLastError();
 }
 

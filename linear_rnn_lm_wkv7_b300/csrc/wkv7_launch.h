@@ -24,6 +24,7 @@ struct FwdArgs {
   float* y;
   float* h_ckpt;
   float* hT;
+  float* sa;  // (B,T,H,D) fp32 sa_t per row, or null
 };
 
 struct BwdArgs {
@@ -32,6 +33,7 @@ struct BwdArgs {
   TokenInputs in;
   const float* h0;
   const float* h_ckpt;
+  const float* sa;  // saved by the forward, or null (then recomputed per chunk)
   const float* dy;
   const float* dhT;
   float *dr, *dw, *dk, *dv, *da, *db;
@@ -45,6 +47,9 @@ struct DecodeArgs {
   float* state;
   float* y;
 };
+
+// multiprocessor count of the current device (cached per device)
+int num_sms();
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);

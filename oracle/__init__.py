@@ -54,7 +54,7 @@ def _bind(path: str):
     lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     I = ctypes.c_int
-    lib.wkv7_oracle_forward.argtypes = [I] * 5 + [P] * 10
+    lib.wkv7_oracle_forward.argtypes = [I] * 5 + [P] * 11
     lib.wkv7_oracle_forward.restype = I
     lib.wkv7_oracle_backward.argtypes = [I] * 6 + [P] * 17
     lib.wkv7_oracle_backward.restype = I
@@ -86,18 +86,20 @@ class Oracle:
     def __init__(self, lib_path: str):
         self.lib = _bind(lib_path)
 
-    def forward(self, r, w, k, v, a, b, h0=None, chunk: int = 32):
-        """y (B,T,H,D), h_ckpt (B,H,C,D,D), hT (B,H,D,D) in fp64."""
+    def forward(self, r, w, k, v, a, b, h0=None, chunk: int = 32, want_sa: bool = False):
+        """y (B,T,H,D), h_ckpt (B,H,C,D,D), hT (B,H,D,D) in fp64; with want_sa also
+        sa (B,T,H,D), sa_t = S_{t-1} a_t per row."""
         r, w, k, v, a, b, h0 = map(_f64, (r, w, k, v, a, b, h0))
         B, T, H, D = r.shape
         C = num_chunks(T, chunk)
         y = np.zeros((B, T, H, D))
         ck = np.zeros((B, H, C, D, D))
         hT = np.zeros((B, H, D, D))
-        rc = self.lib.wkv7_oracle_forward(B, T, H, D, chunk, *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT)))
+        sa = np.zeros((B, T, H, D)) if want_sa else None
+        rc = self.lib.wkv7_oracle_forward(B, T, H, D, chunk, *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)))
         if rc:
             raise RuntimeError(f"oracle forward failed: {rc}")
-        return y, ck, hT
+        return (y, ck, hT, sa) if want_sa else (y, ck, hT)
 
     def backward(self, r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, mode: str = "ckpt"):
         """dr, dw, dk, dv, da, db (B,T,H,D) and dh0 (B,H,D,D) in fp64.

@@ -78,11 +78,12 @@ static void step_forward(int D, double *S, double *sa,
 
 int wkv7_oracle_num_chunks(int T, int chunk) { return (T + chunk - 1) / chunk; }
 
-/* forward: y (B,T,H,D); h_ckpt (B,H,C,D,D) or NULL; hT (B,H,D,D) or NULL; h0 NULL = zeros */
+/* forward: y (B,T,H,D); h_ckpt (B,H,C,D,D) or NULL; hT (B,H,D,D) or NULL; h0 NULL = zeros;
+ * sa_out (B,T,H,D) or NULL receives sa_t = S_{t-1} a_t of every token and row */
 int wkv7_oracle_forward(int B, int T, int H, int D, int chunk,
                         const double *r, const double *w, const double *k,
                         const double *v, const double *a, const double *bb,
-                        const double *h0, double *y, double *h_ckpt, double *hT)
+                        const double *h0, double *y, double *h_ckpt, double *hT, double *sa_out)
 {
     if (B < 0 || T < 0 || H < 0 || D <= 0 || chunk <= 0) return 1;
     const int C = wkv7_oracle_num_chunks(T, chunk);
@@ -96,6 +97,7 @@ int wkv7_oracle_forward(int B, int T, int H, int D, int chunk,
             for (int t = 0; t < T; t++) {
                 size_t o = tix(b, t, h, T, H, D);
                 step_forward(D, S, sa, w + o, k + o, v + o, a + o, bb + o);
+                if (sa_out) memcpy(sa_out + o, sa, sizeof(double) * D);
                 for (int i = 0; i < D; i++) {
                     double s = 0.0;
                     for (int j = 0; j < D; j++) s += S[i * D + j] * r[o + j];
@@ -118,7 +120,7 @@ int wkv7_oracle_decode(int B, int H, int D, double *state,
                        const double *r, const double *w, const double *k,
                        const double *v, const double *a, const double *bb, double *y)
 {
-    return wkv7_oracle_forward(B, 1, H, D, 1, r, w, k, v, a, bb, state, y, NULL, state);
+    return wkv7_oracle_forward(B, 1, H, D, 1, r, w, k, v, a, bb, state, y, NULL, state, NULL);
 }
 
 /* reverse walk over tokens t1-1 .. t0 of one head.  states[t - t0] is the state before

@@ -106,28 +106,33 @@ def pin_delta_rule(orc):
                 assert np.allclose(got, x["v"][bb, t, hh], rtol=0, atol=1e-12), (t, got)
 
 
-def _matrix_forward(x, h0):
-    """Matrix form written independently: h_t = h_{t-1} @ (diag(w_t) + outer(a_t, b_t)) + outer(v_t, k_t)."""
+def _matrix_forward(x, h0, want_sa=False):
+    """Matrix form written independently: h_t = h_{t-1} @ (diag(w_t) + outer(a_t, b_t)) + outer(v_t, k_t).
+
+    With want_sa the third result is h_{t-1} @ a_t per token (the 'sa' of the page's listing)."""
     B, T, H, D = x["r"].shape
     y = np.zeros((B, T, H, D))
+    sa = np.zeros((B, T, H, D))
     states = np.zeros((B, H, T, D, D))
     for bb in range(B):
         for hh in range(H):
             S = np.zeros((D, D)) if h0 is None else h0[bb, hh].copy()
             for t in range(T):
+                sa[bb, t, hh] = S @ x["a"][bb, t, hh]
                 M = np.diag(x["w"][bb, t, hh]) + np.outer(x["a"][bb, t, hh], x["b"][bb, t, hh])
                 S = S @ M + np.outer(x["v"][bb, t, hh], x["k"][bb, t, hh])
                 states[bb, hh, t] = S
                 y[bb, t, hh] = S @ x["r"][bb, t, hh]
-    return y, states
+    return (y, states, sa) if want_sa else (y, states)
 
 
 def pin_matrix_form(orc):
     """General inputs against the numpy-matmul transition-matrix form; checkpoints = states at chunk ends."""
     x = _small(4, T=23, D=7, h0_std=0.2)
-    y, ck, hT = orc.forward(x["r"], x["w"], x["k"], x["v"], x["a"], x["b"], x["h0"], chunk=5)
-    yr, states = _matrix_forward(x, x["h0"])
+    y, ck, hT, sa = orc.forward(x["r"], x["w"], x["k"], x["v"], x["a"], x["b"], x["h0"], chunk=5, want_sa=True)
+    yr, states, sar = _matrix_forward(x, x["h0"], want_sa=True)
     assert _rel(y, yr) < 1e-12, _rel(y, yr)
+    assert _rel(sa, sar) < 1e-12, _rel(sa, sar)
     assert _rel(hT, states[:, :, -1]) < 1e-12
     T = y.shape[1]
     ends = [min(T, (c + 1) * 5) - 1 for c in range((T + 4) // 5)]   # ragged last chunk

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "wkv7.h")
 
 P = ctypes.c_void_p
-ALIGNED = [P(0x1000 + 64 * i) for i in range(24)]   # fake device addresses: never dereferenced
+ALIGNED = [P(0x1000 + 64 * i) for i in range(26)]   # fake device addresses: never dereferenced
 MISALIGNED = P(0x2008)
 
 
@@ -46,12 +46,12 @@ def test_num_chunks_and_version():
 
 
 def fwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None):
-    p = list(ALIGNED[:10]) if ptrs is None else ptrs
+    p = list(ALIGNED[:11]) if ptrs is None else ptrs
     return wkv7.lib.wkv7_forward(B, T, H, D, chunk, dt, *p, None)
 
 
 def bwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None):
-    p = list(ALIGNED[:17]) if ptrs is None else ptrs
+    p = list(ALIGNED[:18]) if ptrs is None else ptrs
     return wkv7.lib.wkv7_backward(B, T, H, D, chunk, dt, *p, None)
 
 
@@ -72,38 +72,39 @@ def test_forward_backward_reject_bad_sizes(kw, status):
 
 @pytest.mark.parametrize("idx", range(7))
 def test_forward_requires_inputs_and_y(idx):
-    p = list(ALIGNED[:10])
+    p = list(ALIGNED[:11])
     req = [0, 1, 2, 3, 4, 5, 7]            # r w k v a b y
     p[req[idx]] = None
     assert fwd(ptrs=p) == 1
 
 
 def test_forward_optional_outputs_may_be_null():
-    # h0, h_ckpt, hT are optional: with them NULL the call passes validation and would launch, so
+    # h0, h_ckpt, hT, sa are optional: with them NULL the call passes validation and would launch, so
     # only check that misaligned optional pointers are rejected (no launch happens on that path)
-    for i in (6, 8, 9):
-        p = list(ALIGNED[:10])
+    for i in (6, 8, 9, 10):
+        p = list(ALIGNED[:11])
         p[i] = MISALIGNED
         assert fwd(ptrs=p) == 3
 
 
-@pytest.mark.parametrize("i", range(10))
+@pytest.mark.parametrize("i", range(11))
 def test_forward_rejects_misaligned(i):
-    p = list(ALIGNED[:10])
+    p = list(ALIGNED[:11])
     p[i] = MISALIGNED
     assert fwd(ptrs=p) == 3
 
 
-@pytest.mark.parametrize("i", [0, 1, 2, 3, 4, 5, 7, 8, 10, 11, 12, 13, 14, 15])
+# r w k v a b | h0 h_ckpt sa dy dhT | dr dw dk dv da db dh0: required = inputs, h_ckpt, dy, grads
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4, 5, 7, 9, 11, 12, 13, 14, 15, 16])
 def test_backward_requires(i):
-    p = list(ALIGNED[:17])
+    p = list(ALIGNED[:18])
     p[i] = None
     assert bwd(ptrs=p) == 1
 
 
-@pytest.mark.parametrize("i", range(17))
+@pytest.mark.parametrize("i", range(18))
 def test_backward_rejects_misaligned(i):
-    p = list(ALIGNED[:17])
+    p = list(ALIGNED[:18])
     p[i] = MISALIGNED
     assert bwd(ptrs=p) == 3
 

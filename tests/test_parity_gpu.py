@@ -49,18 +49,21 @@ def host(t):
     return None if t is None else t.detach().double().cpu().numpy()
 
 
-def run_gpu(wkv7, x, dtype, chunk=32):
+def run_gpu(wkv7, x, dtype, chunk=32, saved_sa=True):
+    """Forward then backward; with saved_sa the forward's sa feeds the backward, else the
+    backward recomputes sa per chunk."""
     ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
-    y, ck, hT = wkv7.forward(*ins, h0, chunk=chunk)
-    grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk)
+    y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True)
+    grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk,
+                          sa=sa if saved_sa else None)
     torch.cuda.synchronize()
-    return host(y), host(ck), host(hT), [host(g) for g in grads]
+    return host(y), host(ck), host(hT), [host(g) for g in grads], host(sa)
 
 
 def check(x, gpu, chunk, heads=None):
     """Compare against the oracle; `heads` = list of (b, h) to restrict the oracle to."""
-    y, ck, hT, grads = gpu
+    y, ck, hT, grads, sa = gpu
     names = ("dr", "dw", "dk", "dv", "da", "db")
     if heads is None:
         sel = [(slice(None), slice(None))]
@@ -70,8 +73,9 @@ def check(x, gpu, chunk, heads=None):
         xs = {n: x[n][sb, :, sh] for n in "rwkvab"}
         h0 = None if x.get("h0") is None else x["h0"][sb, sh]
         dhT = None if x.get("dhT") is None else x["dhT"][sb, sh]
-        yo, cko, hTo = oracle.forward(*(xs[n] for n in "rwkvab"), h0, chunk=chunk)
+        yo, cko, hTo, sao = oracle.forward(*(xs[n] for n in "rwkvab"), h0, chunk=chunk, want_sa=True)
         assert rel(y[sb, :, sh], yo) <= TOL_FWD, ("y", rel(y[sb, :, sh], yo))
+        assert rel(sa[sb, :, sh], sao) <= TOL_FWD, ("sa", rel(sa[sb, :, sh], sao))
         assert rel(hT[sb, sh], hTo) <= TOL_FWD, ("hT", rel(hT[sb, sh], hTo))
         assert rel(ck[sb, sh], cko) <= TOL_FWD, ("h_ckpt", rel(ck[sb, sh], cko))
         go = oracle.backward(*(xs[n] for n in "rwkvab"), h0, cko, x["dy"][sb, :, sh], dhT, chunk=chunk, mode="ckpt")
@@ -82,20 +86,23 @@ def check(x, gpu, chunk, heads=None):
     assert np.array_equal(ck[:, :, -1], hT)
 
 
+@pytest.mark.parametrize("saved_sa", [True, False], ids=["saved_sa", "recompute_sa"])
 @pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
-def test_workload_parity_full(wkv7, name):
+def test_workload_parity_full(wkv7, name, saved_sa):
     wl = gen.WORKLOADS[name]
     x = gen.full(wl)
-    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk), wl.chunk)
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, saved_sa), wl.chunk)
 
 
-def test_workload_parity_wide7b_sampled_heads(wkv7):
+@pytest.mark.parametrize("saved_sa", [True, False], ids=["saved_sa", "recompute_sa"])
+def test_workload_parity_wide7b_sampled_heads(wkv7, saved_sa):
+    """128 heads: more than half the SM count, so the backward runs one CTA per head."""
     wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
     x = gen.full(wl)
-    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk)
+    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk, saved_sa)
     check(x, gpu, wl.chunk, heads=[(0, 0), (1, 37), (0, 63)])
     # every head: properties that hold at any size
-    y, ck, hT, grads = gpu
+    y, ck, hT, grads, _ = gpu
     assert all(np.isfinite(g).all() for g in grads[:6]) and np.isfinite(y).all()
 
 
@@ -106,7 +113,25 @@ def test_workload_parity_wide7b_sampled_heads(wkv7):
 ])
 def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
     x = gen.random_small(B * 100 + T + H, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    check(x, run_gpu(wkv7, x, dtype, chunk), chunk)
+    check(x, run_gpu(wkv7, x, dtype, chunk, saved_sa=True), chunk)
+    check(x, run_gpu(wkv7, x, dtype, chunk, saved_sa=False), chunk)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_heads_one_cta_per_head(wkv7, dtype):
+    """B*H = 78 heads (more than half of 148 SMs): the one-CTA-per-head backward, ragged T."""
+    x = gen.random_small(77, B=3, T=45, H=26, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    for saved in (True, False):
+        check(x, run_gpu(wkv7, x, dtype, 32, saved), 32, heads=[(0, 0), (1, 13), (2, 25)])
+
+
+def test_backward_is_deterministic(wkv7):
+    """Column sums are taken in a fixed order: two backward calls agree bit for bit."""
+    x = gen.random_small(8, B=4, T=96, H=6, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
+    a = run_gpu(wkv7, x, "bf16", 32)
+    b = run_gpu(wkv7, x, "bf16", 32)
+    for ga, gb in zip(a[3], b[3]):
+        assert np.array_equal(ga, gb)
 
 
 def test_no_h0_no_dhT_no_dh0(wkv7):
