@@ -50,6 +50,10 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
+                   help="default: the debug training shape (the headline line); others for extra measurements")
+    p.add_argument("--sa", choices=["saved", "recompute"], default="saved",
+                   help="backward reads the forward's saved sa, or recomputes it per chunk")
     return p.parse_args()
 
 
@@ -191,7 +195,10 @@ def cpu_baseline(wl, seconds: float):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    wl = gen.WORKLOADS[WORKLOAD]
+    wl = gen.WORKLOADS[args.workload]
+    if wl.decode:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the training workloads only"}))
+        return
     xs = {b: (gen.token_inputs(wl, b), gen.dy_init(wl, b)) for b in range(wl.B)}
     heads = [(b, h) for b in range(wl.B) for h in range(wl.H)][:12]  # bounded sample: 12 of 72 heads
     frac = len(heads) / (wl.B * wl.H)
@@ -216,23 +223,119 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------------------ GPU arm
 
+def decode_bytes(wl, in_bytes: int):
+    """Minimum HBM bytes of one decode step: state read + write, six inputs, y."""
+    n = wl.B * wl.H * wl.D
+    return 2 * wl.B * wl.H * wl.D * wl.D * 4 + 6 * n * in_bytes + 4 * n
+
+
+def run_decode(args, rank, world, local_rank):
+    """7B decode: every step advances all B sequences by one token through all 32 x 64 heads, in place."""
+    import torch
+    import linear_rnn_lm_wkv7_b300 as wkv7
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS[args.workload]
+    B, H, D = wl.B, wl.H, wl.D
+    rows = [gen.token_inputs(wl, b) for b in range(B)]
+    host_in = {n: torch.from_numpy(np.stack([rw[n][0] for rw in rows])).to(torch.bfloat16) for n in "rwkvab"}
+    ins = {n: t.to(dev) for n, t in host_in.items()}
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed)
+    state = torch.randn((B, H, D, D), generator=g, device=dev) * wl.h0_std   # 8.6 GB, > L2: no flush needed
+    y = torch.empty((B, H, D), device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        wkv7.decode(state, *(ins[n] for n in "rwkvab"), y=y)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    ms = e0.elapsed_time(e1) / args.steps
+    # end to end: inputs from pinned host memory, y back to the host; the state stays resident
+    pin_in = {n: t.pin_memory() for n, t in host_in.items()}
+    pin_y = torch.empty((B, H, D), pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in pin_in.values())
+    d2h = pin_y.numel() * 4
+
+    def e2e_step():
+        for n in "rwkvab":
+            ins[n].copy_(pin_in[n], non_blocking=True)
+        step()
+        pin_y.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(max(1, args.e2e_steps)):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / max(1, args.e2e_steps)
+    if rank != 0:
+        return
+    hbm, peak_kind, _ = measured_peaks()
+    nbytes = decode_bytes(wl, 2)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "WKV7 decode tokens/s (7B state: 32 layers x 64 heads x 64x64 fp32 per sequence)",
+        "value": world * B / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded: inputs wkv7_inputs.py, state torch.randn)",
+        "config": {"workload": wl.name, "B": B, "H": H, "D": D, "inputs": "bf16", "state": "fp32, in place",
+                   "l2": f"state {B * H * D * D * 4 / 1e9:.1f} GB > 126 MB L2"},
+        "roofline": {"bound": "hbm", "kernel": "wkv7_decode", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "algorithmic_bytes": nbytes, "avg_launch_ms": ms},
+        "clocks": clocks, "gpu_launches": args.steps,
+        "e2e": {"value": world * B / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import linear_rnn_lm_wkv7_b300 as wkv7
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = gen.WORKLOADS[WORKLOAD]
+    wl = gen.WORKLOADS[args.workload]
+    if wl.decode:
+        return run_decode(args, rank, world, local_rank)
+    saved = args.sa == "saved"
     B, T, H, D = wl.B, wl.T, wl.H, wl.D
     C = wkv7.num_chunks(T, wl.chunk)
 
     x = gen.full(wl)   # same seeded batch on every rank (each rank owns an independent replica)
-    host_in = {n: torch.from_numpy(x[n]).to(torch.bfloat16) for n in "rwkvab"}
+    host_in = {n: torch.from_numpy(x[n]).to(torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
+               for n in "rwkvab"}
     host_dy = torch.from_numpy(x["dy"])
+    host_h0 = None if x["h0"] is None else torch.from_numpy(x["h0"])
+    host_dhT = None if x["dhT"] is None else torch.from_numpy(x["dhT"])
 
     def make_set():
         s = {n: host_in[n].to(dev) for n in "rwkvab"}
         s["dy"] = host_dy.to(dev)
+        s["h0"] = None if host_h0 is None else host_h0.to(dev)
+        s["dhT"] = None if host_dhT is None else host_dhT.to(dev)
         s["y"] = torch.empty((B, T, H, D), device=dev)
         s["ck"] = torch.empty((B, H, C, D, D), device=dev)
         s["hT"] = torch.empty((B, H, D, D), device=dev)
@@ -247,10 +350,11 @@ def run_ours(args, rank, world, local_rank):
         ins = [s[n] for n in "rwkvab"]
         if ev is not None:
             ev[0].record(stream)
-        wkv7.forward(*ins, None, chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"]))
+        wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"] if saved else None))
         if ev is not None:
             ev[1].record(stream)
-        wkv7.backward(*ins, None, s["ck"], s["dy"], None, chunk=wl.chunk, sa=s["sa"], out=s["g"])
+        wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"] if saved else None,
+                      out=s["g"])
         if ev is not None:
             ev[2].record(stream)
 
@@ -302,10 +406,15 @@ def run_ours(args, rank, world, local_rank):
         h2d = sum(t.numel() * t.element_size() for t in pin_in.values()) + pin_dy.numel() * 4
         d2h = pin_y.numel() * 4 + sum(t.numel() * 4 for t in pin_g)
 
+        pin_st = {n: t.pin_memory() for n, t in (("h0", host_h0), ("dhT", host_dhT)) if t is not None}
+        h2d += sum(t.numel() * 4 for t in pin_st.values())
+
         def e2e_step():
             for n in "rwkvab":
                 s[n].copy_(pin_in[n], non_blocking=True)
             s["dy"].copy_(pin_dy, non_blocking=True)
+            for n, t in pin_st.items():
+                s[n].copy_(t, non_blocking=True)
             step(s)
             pin_y.copy_(s["y"], non_blocking=True)
             for hg, dg in zip(pin_g, s["g"]):
@@ -334,7 +443,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
 
-    fwd_b, bwd_b = byte_counts(wl, 2)
+    fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
     hbm, peak_kind, peaks = measured_peaks()
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
     dom = ("wkv7_bwd", bwd_b, b_ms, "wkv7_bwd.cu") if b_ms >= f_ms else ("wkv7_fwd", fwd_b, f_ms, "wkv7_fwd.cu")
@@ -348,8 +457,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, wkv7_inputs.py)",
-        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": "bf16",
-                   "state": "fp32", "parallelism": f"replicas x{world} (independent batches, no collective)",
+        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": wl.dtype,
+                   "state": "fp32", "sa": args.sa, "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "l2": f"{N_SETS} rotating input/output sets "
                          f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
