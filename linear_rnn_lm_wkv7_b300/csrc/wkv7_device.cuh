@@ -146,6 +146,83 @@ __device__ __forceinline__ float4 raw4(const __nv_bfloat16* p) {
   return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
 
+// ---- sums over all 32 lanes of NV per-lane values (NV a power of two, 2 <= NV <= 32).
+// Reduce-scatter: each level halves the values a lane keeps (it keeps the half selected by its
+// lane bit, adds the partner's copy of that half); once one value is left the remaining levels
+// are a plain butterfly.  Afterwards lane l holds the full sum of value index rs32_index<NV>(l).
+template <int NV>
+__device__ __forceinline__ int rs32_index(int lane) {
+  int idx = 0, n = NV, mask = 16;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    if (n > 1) {
+      n >>= 1;
+      if (lane & mask) idx += n;
+    }
+    mask >>= 1;
+  }
+  return idx;
+}
+
+template <int NV>
+__device__ __forceinline__ float rs32(const float (&x)[NV], int lane) {
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = x[i];
+  int n = NV;
+#pragma unroll
+  for (int mask = 16; mask >= 1; mask >>= 1) {
+    if (n > 1) {
+      const int h = n >> 1;
+      const bool up = (lane & mask) != 0;
+#pragma unroll
+      for (int m = 0; m < NV / 2; ++m) {
+        if (m < h) {
+          const float keep = up ? v[h + m] : v[m];
+          const float send = up ? v[m] : v[h + m];
+          v[m] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+    }
+  }
+  return v[0];
+}
+
+// After rs32<2*NP>: lanes with lane bit 16 clear hold the first NP sums (index rs32_index).
+// Hand every lane all NP of them.
+template <int NP>
+__device__ __forceinline__ void ag32_low(float u, int lane, float (&out)[NP]) {
+  static_assert(NP == 2 || NP == 4 || NP == 8, "2, 4 or 8 values");
+  const float t = __shfl_xor_sync(0xffffffffu, u, 16);
+  float g[NP];
+  g[0] = (lane & 16) ? t : u;  // value index = rs32_index<2*NP>(lane) with the top bit dropped
+  // index bits of the remaining levels, lowest weight first: lane masks 16/NP ... 8
+  int have = 1;
+#pragma unroll
+  for (int wgt = 1; wgt < NP; wgt <<= 1) {
+    const int mask = 16 / (2 * NP) * 2 * wgt;  // lane mask carrying index weight `wgt`
+    const bool up = (lane & mask) != 0;
+    float o[NP / 2];
+#pragma unroll
+    for (int m = 0; m < NP / 2; ++m)
+      if (m < have) o[m] = __shfl_xor_sync(0xffffffffu, g[m], mask);
+#pragma unroll
+    for (int m = NP / 2 - 1; m >= 0; --m) {
+      if (m < have) {
+        const float mine = g[m];
+        g[m] = up ? o[m] : mine;
+        g[have + m] = up ? mine : o[m];
+      }
+    }
+    have <<= 1;
+  }
+#pragma unroll
+  for (int i = 0; i < NP; ++i) out[i] = g[i];
+}
+
 // 4-wide dot products of 4 state rows with one float4 (two packed fp32x2 FMAs each)
 __device__ __forceinline__ void dot4x4(const float2 (&S)[4][2], float4 c, float (&out)[4]) {
 #pragma unroll
