@@ -49,15 +49,20 @@ namespace {
 
 constexpr int kCT = 32;  // stage capacity in tokens (chunk <= 32)
 constexpr int kNG = 5;   // column gradients in slab order: dr, dw, dk, db, da
-constexpr int kNW = 8;   // warps per CTA
-constexpr int kNT = 32 * kNW;
+
+#ifndef WKV7_BWD_NW2
+#define WKV7_BWD_NW2 8  // warps per CTA with two CTAs per head
+#endif
+#ifndef WKV7_BWD_ST2
+#define WKV7_BWD_ST2 4  // tokens per column-sum sub-tile with two CTAs per head
+#endif
 
 constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16; }
 
-template <typename Tin, int NCL, int ST>
+template <typename Tin, int NCL, int NW, int ST>
 struct BwdSmem {
   static constexpr int ROWS = kD / NCL;
-  static constexpr int R = ROWS / kNW;   // rows per thread
+  static constexpr int R = ROWS / NW;    // rows per thread
   static constexpr int CPC = kD / NCL;   // columns of the column gradients this CTA writes
   // raw stage (cp.async target): Tin [5][kCT][kD] (w k a b r), Tin [kCT][ROWS] (v), f32 [kCT][ROWS] (dy, sa)
   static constexpr size_t oCol = 0;
@@ -71,15 +76,15 @@ struct BwdSmem {
   static constexpr size_t oRowT = oTile + 7 * kCT * kD * 4;
   static constexpr size_t oScal = oRowT + 3 * kCT * ROWS * 4;
   static constexpr size_t oDv = oScal + 2 * kCT * 4;
-  static constexpr size_t oSlab = oDv + kCT * ROWS * 4;                                 // f32 [kNW][ST][kNG][kD]
-  static constexpr size_t oPart = oSlab + (size_t)kNW * ST * kNG * kD * 4;               // f32 [kNG][kCT][CPC]
+  static constexpr size_t oSlab = oDv + kCT * ROWS * 4;                                 // f32 [NW][ST][kNG][kD]
+  static constexpr size_t oPart = oSlab + (size_t)NW * ST * kNG * kD * 4;                // f32 [kNG][kCT][CPC]
   static constexpr size_t oRecv = oPart + (NCL > 1 ? (size_t)kNG * kCT * CPC * 4 : 0);  // f32 [2][kNG][kCT][CPC]
   static constexpr size_t kBytes = oRecv + (NCL > 1 ? (size_t)2 * kNG * kCT * CPC * 4 : 0);
 };
 enum { TW = 0, TWI = 1, TK = 2, TA = 3, TB = 4, TR = 5, TCB = 6 };
 
 // cp.async copies of one chunk's inputs into the raw stage
-template <typename Tin, int ROWS, bool SAVED>
+template <typename Tin, int ROWS, int kNT, bool SAVED>
 __device__ __forceinline__ void issue_stage(unsigned char* stg, size_t oV, size_t oDy, size_t oSa, int t0, int n,
                                             size_t base, size_t tstride, int rbase, const Tin* __restrict__ w,
                                             const Tin* __restrict__ k, const Tin* __restrict__ a,
@@ -132,8 +137,8 @@ __device__ __forceinline__ void lds_rows(const float* p, float (&o)[R]) {
   }
 }
 
-template <typename Tin, int NCL, int ST, bool SAVED>
-__global__ void __launch_bounds__(kNT, 1)
+template <typename Tin, int NCL, int NW, int ST, bool SAVED>
+__global__ void __launch_bounds__(32 * NW, 1)
 bwd_kernel(int T, int H, int chunk, int nchunks,
            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
@@ -142,8 +147,9 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
            float* __restrict__ dr, float* __restrict__ dw, float* __restrict__ dk,
            float* __restrict__ dv, float* __restrict__ da, float* __restrict__ db,
            float* __restrict__ dh0) {
-  using L = BwdSmem<Tin, NCL, ST>;
+  using L = BwdSmem<Tin, NCL, NW, ST>;
   constexpr int ROWS = L::ROWS, R = L::R, RP = R / 2, CPC = L::CPC;
+  constexpr int kNT = 32 * NW, kNW = NW;
   static_assert(NCL == 1 || NCL == 2, "one or two row blocks per head");
   static_assert(R == 4 || R == 8, "4 or 8 rows per thread");
   static_assert(kCT % ST == 0, "sub-tiles divide the stage");
@@ -201,7 +207,7 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
 
   if (nchunks > 0) {
     const int t0 = (nchunks - 1) * chunk;
-    issue_stage<Tin, ROWS, SAVED>(sm, L::oV, L::oDy, L::oSa, t0, T - t0, base, tstride, rbase, w, k, a, b, r, v, dy,
+    issue_stage<Tin, ROWS, kNT, SAVED>(sm, L::oV, L::oDy, L::oSa, t0, T - t0, base, tstride, rbase, w, k, a, b, r, v, dy,
                                   sa_in);
     cp_async_commit();
   }
@@ -237,10 +243,10 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
     cp_async_wait<0>();
     __syncthreads();  // this chunk's raw stage has landed; the previous chunk's tiles are no longer read
 
-    // ---- widen to fp32 tiles: 8 lanes per token (8 columns each); one token per 8 threads
-    {
+    // ---- widen to fp32 tiles: 8 lanes per token (8 columns each)
+    for (int tg = 0; tg < kCT; tg += kNT / 8) {
       const Tin* col = reinterpret_cast<const Tin*>(sm);
-      const int tt = tid >> 3;
+      const int tt = tg + (tid >> 3);
       const int c8 = (tid & 7) * 8;
       float ab = 0.f, rb = 0.f;
       if (tt < n) {
@@ -281,6 +287,8 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
         sAb[tt] = ab;
         sRb[tt] = rb;
       }
+    }
+    {
       const Tin* vr = reinterpret_cast<const Tin*>(sm + L::oV);
       const float* dyr = reinterpret_cast<const float*>(sm + L::oDy);
       const float* sar = reinterpret_cast<const float*>(sm + L::oSa);
@@ -292,7 +300,7 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
     }
     __syncthreads();  // tiles complete; the raw stage is free
     if (ci > 0) {
-      issue_stage<Tin, ROWS, SAVED>(sm, L::oV, L::oDy, L::oSa, (ci - 1) * chunk, chunk, base, tstride, rbase, w, k, a,
+      issue_stage<Tin, ROWS, kNT, SAVED>(sm, L::oV, L::oDy, L::oSa, (ci - 1) * chunk, chunk, base, tstride, rbase, w, k, a,
                                     b, r, v, dy, sa_in);
       cp_async_commit();
     }
@@ -526,16 +534,16 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
   }
 }
 
-template <typename Tin, int NCL, int ST, bool SAVED>
+template <typename Tin, int NCL, int NW, int ST, bool SAVED>
 cudaError_t launch_bwd_cfg(const BwdArgs& p, cudaStream_t stream) {
-  using L = BwdSmem<Tin, NCL, ST>;
+  using L = BwdSmem<Tin, NCL, NW, ST>;
   static_assert(L::kBytes <= 232448, "shared memory per CTA");
-  auto kern = bwd_kernel<Tin, NCL, ST, SAVED>;
+  auto kern = bwd_kernel<Tin, NCL, NW, ST, SAVED>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.B * p.H * NCL);
-  cfg.blockDim = dim3(kNT);
+  cfg.blockDim = dim3(32 * NW);
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -553,8 +561,8 @@ cudaError_t launch_bwd_cfg(const BwdArgs& p, cudaStream_t stream) {
 template <typename Tin, bool SAVED>
 cudaError_t launch_bwd_t(const BwdArgs& p, cudaStream_t stream) {
   // two row blocks per head when that still fits the GPU in one wave
-  if ((long long)p.B * p.H * 2 <= num_sms()) return launch_bwd_cfg<Tin, 2, 4, SAVED>(p, stream);
-  return launch_bwd_cfg<Tin, 1, 4, SAVED>(p, stream);
+  if ((long long)p.B * p.H * 2 <= num_sms()) return launch_bwd_cfg<Tin, 2, WKV7_BWD_NW2, WKV7_BWD_ST2, SAVED>(p, stream);
+  return launch_bwd_cfg<Tin, 1, 8, 4, SAVED>(p, stream);
 }
 
 }  // namespace
