@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
                    help="default: the debug training shape (the headline line); others for extra measurements")
+    p.add_argument("--decode-batch", type=int, default=0,
+                   help="decode workload only: number of sequences (default: the workload's 256)")
     p.add_argument("--sa", choices=["saved", "recompute"], default="saved",
                    help="backward reads the forward's saved sa, or recomputes it per chunk")
     return p.parse_args()
@@ -237,6 +239,9 @@ def run_decode(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = gen.WORKLOADS[args.workload]
+    if args.decode_batch > 0:
+        import dataclasses
+        wl = dataclasses.replace(wl, B=args.decode_batch)
     B, H, D = wl.B, wl.H, wl.D
     rows = [gen.token_inputs(wl, b) for b in range(B)]
     host_in = {n: torch.from_numpy(np.stack([rw[n][0] for rw in rows])).to(torch.bfloat16) for n in "rwkvab"}
