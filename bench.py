@@ -47,7 +47,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
@@ -414,27 +414,58 @@ def run_ours(args, rank, world, local_rank):
         pin_st = {n: t.pin_memory() for n, t in (("h0", host_h0), ("dhT", host_dhT)) if t is not None}
         h2d += sum(t.numel() * 4 for t in pin_st.values())
 
-        def e2e_step():
-            for n in "rwkvab":
-                s[n].copy_(pin_in[n], non_blocking=True)
-            s["dy"].copy_(pin_dy, non_blocking=True)
-            for n, t in pin_st.items():
-                s[n].copy_(t, non_blocking=True)
-            step(s)
-            pin_y.copy_(s["y"], non_blocking=True)
-            for hg, dg in zip(pin_g, s["g"]):
-                hg.copy_(dg, non_blocking=True)
+        # Pipelined across steps like an input pipeline: step i's host->device copies, compute and
+        # device->host copies run on three streams, two device buffer sets alternate, so the copies of
+        # step i+1 overlap the compute of step i.  Every step still copies all its inputs in and all
+        # its outputs (y and the seven gradients) back.
+        s_h2d, s_comp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
+        pin_out = [[pin_y, pin_g], [torch.empty_like(pin_y).pin_memory(), [torch.empty_like(g).pin_memory() for g in pin_g]]]
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
 
-        for _ in range(2):
-            e2e_step()
+        def e2e_step(i):
+            kq = i % 2
+            sb = sets[kq]
+            with torch.cuda.stream(s_h2d):
+                if used[kq]:
+                    s_h2d.wait_event(ev_out[kq])   # step i-2 has been read back: its buffers are free
+                for n in "rwkvab":
+                    sb[n].copy_(pin_in[n], non_blocking=True)
+                sb["dy"].copy_(pin_dy, non_blocking=True)
+                for n, t in pin_st.items():
+                    sb[n].copy_(t, non_blocking=True)
+                ev_in[kq].record(s_h2d)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[kq])
+                step(sb)
+                ev_done[kq].record(s_comp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[kq])
+                hy, hg = pin_out[kq]
+                hy.copy_(sb["y"], non_blocking=True)
+                for h_, d_ in zip(hg, sb["g"]):
+                    h_.copy_(d_, non_blocking=True)
+                ev_out[kq].record(s_d2h)
+            used[kq] = True
+
+        def run_e2e(nsteps, first):
+            for i in range(nsteps):
+                e2e_step(first + i)
+            for st in (s_h2d, s_comp, s_d2h):
+                stream.wait_stream(st)
+
+        run_e2e(2, 0)
         torch.cuda.synchronize()
         if dist:
             tdist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        for st in (s_h2d, s_comp, s_d2h):
+            st.wait_event(e0)
+        run_e2e(args.e2e_steps, 2)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
