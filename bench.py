@@ -110,6 +110,25 @@ def profiled_traffic(kernel: str, workload: str, src_sha: str):
     return None
 
 
+# ------------------------------------------------------------------------------ ranks
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks of the default process group (the slowest replica
+    sets the job's time); `value` itself when no group is initialised."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(per_rank_tokens: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job throughput: every rank processes its own batch (weak scaling)."""
+    return world * per_rank_tokens / (elapsed_ms_max / 1e3)
+
+
 # ------------------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -273,7 +292,7 @@ def run_decode(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
     clocks = clk.summary()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
     # end to end: inputs from pinned host memory, y back to the host; the state stays resident
     pin_in = {n: t.pin_memory() for n, t in host_in.items()}
     pin_y = torch.empty((B, H, D), pin_memory=True)
@@ -293,7 +312,7 @@ def run_decode(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / max(1, args.e2e_steps)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / max(1, args.e2e_steps)
     if rank != 0:
         return
     hbm, peak_kind, _ = measured_peaks()
@@ -393,11 +412,8 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = start.elapsed_time(stop)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    tokens_per_s = world * B * T * args.steps / (elapsed_ms / 1e3)
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    tokens_per_s = job_tokens_per_s(B * T * args.steps, world, elapsed_ms)
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -468,12 +484,8 @@ def run_ours(args, rank, world, local_rank):
         run_e2e(args.e2e_steps, 2)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([ems], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * B * T * args.e2e_steps / (ems / 1e3), "unit": "tokens/s",
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": job_tokens_per_s(B * T * args.e2e_steps, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:

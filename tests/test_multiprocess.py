@@ -1,0 +1,84 @@
+"""CPU tests of the multi-rank bench logic with two gloo processes (no GPU): the job time is the
+slowest rank's, throughput counts every rank's batch, and only rank 0 prints the reference line."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, results):
+    import torch.distributed as tdist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = 10.0 + 7.5 * rank                 # rank 1 is the slow replica
+        got = bench.max_over_ranks(mine, "cpu")
+        results[rank] = (got, bench.job_tokens_per_s(12288, world, got))
+    finally:
+        tdist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        results = mgr.dict()
+        mp.start_processes(_worker, args=(world, port, results), nprocs=world, start_method="spawn")
+        res = dict(results)
+    assert res[0][0] == res[1][0] == 17.5           # every rank sees the slowest rank's time
+    assert res[0][1] == pytest.approx(2 * 12288 / 0.0175)
+
+
+def test_single_process_passthrough():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+    assert bench.job_tokens_per_s(100, 1, 1000.0) == pytest.approx(100.0)
+
+
+def test_reference_arm_only_rank0_prints():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:  # the parsed arguments the reference arm reads
+        workload = bench.WORKLOAD
+        steps = 1
+        warmup = 0
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(A, rank=1, world=2)
+    assert buf.getvalue() == ""
+
+
+def test_reference_arm_decode_workload_is_unavailable():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        workload = "decode7b_b256_h2048"
+        steps = 1
+        warmup = 0
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(A, rank=0, world=1)
+    line = json.loads(buf.getvalue())
+    assert line["impl"] == "reference" and "unavailable" in line
