@@ -54,6 +54,8 @@ def parse_args():
                    help="default: the debug training shape (the headline line); others for extra measurements")
     p.add_argument("--decode-batch", type=int, default=0,
                    help="decode workload only: number of sequences (default: the workload's 256)")
+    p.add_argument("--bwd", choices=["two-phase", "single"], default="two-phase",
+                   help="two-phase backward with a workspace (needs --sa saved), or the single-pass backward")
     p.add_argument("--sa", choices=["saved", "recompute"], default="saved",
                    help="backward reads the forward's saved sa, or recomputes it per chunk")
     return p.parse_args()
@@ -364,6 +366,8 @@ def run_ours(args, rank, world, local_rank):
         s["ck"] = torch.empty((B, H, C, D, D), device=dev)
         s["hT"] = torch.empty((B, H, D, D), device=dev)
         s["sa"] = torch.empty((B, T, H, D), device=dev)
+        s["ws"] = torch.empty(wkv7.backward_workspace_size(B, T, H, D, wl.chunk), dtype=torch.uint8, device=dev) \
+            if args.bwd == "two-phase" else None
         s["g"] = [torch.empty((B, T, H, D), device=dev) for _ in range(6)] + [torch.empty((B, H, D, D), device=dev)]
         return s
 
@@ -378,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
         wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"] if saved else None,
-                      out=s["g"])
+                      workspace=s["ws"], out=s["g"])
         if ev is not None:
             ev[2].record(stream)
 
@@ -494,7 +498,9 @@ def run_ours(args, rank, world, local_rank):
     fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
     hbm, peak_kind, peaks = measured_peaks()
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    dom = ("wkv7_bwd", bwd_b, b_ms, "wkv7_bwd.cu") if b_ms >= f_ms else ("wkv7_fwd", fwd_b, f_ms, "wkv7_fwd.cu")
+    bwd_name, bwd_src = ("wkv7_bwd_two_phase", "wkv7_bwd2.cu") if (saved and args.bwd == "two-phase") \
+        else ("wkv7_bwd", "wkv7_bwd.cu")
+    dom = (bwd_name, bwd_b, b_ms, bwd_src) if b_ms >= f_ms else ("wkv7_fwd", fwd_b, f_ms, "wkv7_fwd.cu")
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     sha = kernel_source_sha(dom[3])
     traffic = profiled_traffic(dom[0], wl.name, sha)
@@ -506,7 +512,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, wkv7_inputs.py)",
         "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": wl.dtype,
-                   "state": "fp32", "sa": args.sa, "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "state": "fp32", "sa": args.sa, "backward": args.bwd if args.sa == "saved" else "single", "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "l2": f"{N_SETS} rotating input/output sets "
                          f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -514,9 +520,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "algorithmic_bytes": dom[1], "avg_launch_ms": dom[2]},
         "roofline_step": {"definition": "max(HBM bytes / peak BW, 8*D^2 FLOP per head-token / FP32 peak) / step time",
                           "bytes": fwd_b + bwd_b, "roofline_ms": roof_s * 1e3, "frac": roof_s / step_s},
-        "kernels_ms": {"wkv7_fwd": f_ms, "wkv7_bwd": b_ms},
+        "kernels_ms": {"wkv7_fwd": f_ms, bwd_name: b_ms},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if (saved and args.bwd == "two-phase") else 2) * args.steps,
         "e2e": e2e,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -43,6 +43,8 @@
 #ifndef WKV7_H
 #define WKV7_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -56,7 +58,8 @@ typedef enum {
     WKV7_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned */
     WKV7_ERR_DTYPE = 4,    /* in_dtype is not WKV7_F32 / WKV7_BF16 */
     WKV7_ERR_CUDA = 5,     /* the CUDA runtime reported an error at launch */
-    WKV7_ERR_TIMEOUT = 6   /* a bounded device-side wait gave up (reserved) */
+    WKV7_ERR_TIMEOUT = 6,  /* a bounded device-side wait gave up (reserved) */
+    WKV7_ERR_WORKSPACE = 7 /* the backward's workspace is smaller than wkv7_backward_workspace_size */
 } wkv7_status;
 
 /* Number of checkpoints the forward writes: ceil(T / chunk); 0 for T == 0. */
@@ -92,9 +95,18 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
  *   dhT     (B,H,D,D) fp32 gradient w.r.t. hT, or NULL for zeros.
  *   dr, dw, dk, dv, da, db  (B,T,H,D) fp32 outputs, required.
  *   dh0     (B,H,D,D) fp32 gradient w.r.t. h0, or NULL (not written).
+ *   workspace, workspace_bytes
+ *           device scratch of at least wkv7_backward_workspace_size() bytes, 256-byte
+ *           aligned, owned by the caller and reused freely between calls; or NULL / 0.
+ *           With a workspace and a saved sa the backward runs in two phases: one pass
+ *           over the sequence walks the state gradient (writing dv, dh0, and into the
+ *           workspace every dsa and the state gradient at every chunk end), then every
+ *           chunk of every head forms its column gradients (dr, dw, dk, da, db) at once.
+ *           Without one (or without sa) a single pass does everything.  Both give the
+ *           same results up to fp32 rounding.
  * Each chunk is walked in reverse from its end checkpoint, the earlier states
- * rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).  Column sums are
- * taken in a fixed order (no atomics): results are deterministic.
+ * rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).  Sums are taken in a
+ * fixed order (no atomics): results are deterministic.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
@@ -103,7 +115,11 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
                   const float *h0, const float *h_ckpt, const float *sa,
                   const float *dy, const float *dhT,
                   float *dr, float *dw, float *dk, float *dv, float *da, float *db,
-                  float *dh0, void *stream);
+                  float *dh0, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace the two-phase backward needs for these sizes (written to *bytes);
+ * returns a wkv7_status (the same size checks as wkv7_backward). */
+int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
 /*
  * One decode token for B sequences of H heads, state updated in place.

@@ -21,7 +21,7 @@ D_HEAD = 64
 MAX_CHUNK = 32
 
 STATUS = {0: "WKV7_OK", 1: "WKV7_ERR_ARG", 2: "WKV7_ERR_SHAPE", 3: "WKV7_ERR_ALIGN",
-          4: "WKV7_ERR_DTYPE", 5: "WKV7_ERR_CUDA", 6: "WKV7_ERR_TIMEOUT"}
+          4: "WKV7_ERR_DTYPE", 5: "WKV7_ERR_CUDA", 6: "WKV7_ERR_TIMEOUT", 7: "WKV7_ERR_WORKSPACE"}
 
 # every function the header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -29,7 +29,8 @@ _I = ctypes.c_int
 SIGNATURES = {
     "wkv7_num_chunks": (_I, [_I, _I]),
     "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
-    "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
+    "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
+    "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
     "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
     "wkv7_strerror": (ctypes.c_char_p, [_I]),
     "wkv7_last_cuda_error": (ctypes.c_char_p, []),
@@ -71,6 +72,13 @@ def num_chunks(T: int, chunk: int) -> int:
 
 def version() -> int:
     return lib.wkv7_version()
+
+
+def backward_workspace_size(B: int, T: int, H: int, D: int = D_HEAD, chunk: int = 32) -> int:
+    """Bytes of device workspace the two-phase backward needs."""
+    n = ctypes.c_size_t(0)
+    _check(lib.wkv7_backward_workspace_size(B, T, H, D, chunk, ctypes.byref(n)), "wkv7_backward_workspace_size")
+    return n.value
 
 
 # ------------------------------------------------------------------------------ torch API
@@ -156,10 +164,14 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
 
 
 def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_dh0: bool = True,
-             sa=None, out=None, stream=None):
+             sa=None, workspace="auto", out=None, stream=None):
     """Checkpointed WKV7 backward.  Returns (dr, dw, dk, dv, da, db, dh0), all fp32 (dh0 None when
     need_dh0=False).  h_ckpt must come from `forward` with the same chunk; `sa` is the forward's
-    saved sa (save_sa=True) or None, in which case each chunk recomputes it."""
+    saved sa (save_sa=True) or None, in which case each chunk recomputes it.
+
+    workspace: "auto" (default) allocates the two-phase backward's scratch with torch when sa is
+    given; a uint8 CUDA tensor of at least backward_workspace_size() bytes is used as is; None runs
+    the single-pass backward."""
     torch = _torch()
     B, T, H, D = r.shape
     _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.backward")
@@ -178,9 +190,20 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
     for name, g in zip(("dr", "dw", "dk", "dv", "da", "db"), grads[:6]):
         _check_f32(g, (B, T, H, D), name, "wkv7.backward", dev)
     _check_f32(grads[6], (B, H, D, D), "dh0", "wkv7.backward", dev)
+    ws, ws_bytes = None, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        if sa is not None and T > 0:
+            ws_bytes = backward_workspace_size(B, T, H, D, chunk)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    elif workspace is not None:
+        if workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("wkv7.backward: workspace must be a contiguous uint8 tensor on the inputs' device")
+        ws, ws_bytes = workspace, workspace.numel()
     st = lib.wkv7_backward(B, T, H, D, chunk, _in_dtype(r),
                            *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, sa, dy, dhT)),
-                           *map(_ptr, grads), _stream(stream))
+                           *map(_ptr, grads), _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "wkv7_backward")
     return tuple(grads)
 

@@ -88,6 +88,7 @@ const char* wkv7_strerror(int status) {
     case WKV7_ERR_DTYPE: return "unsupported input dtype: use WKV7_F32 or WKV7_BF16";
     case WKV7_ERR_CUDA: return "CUDA error at launch (see wkv7_last_cuda_error)";
     case WKV7_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case WKV7_ERR_WORKSPACE: return "workspace smaller than wkv7_backward_workspace_size()";
     default: return "unknown wkv7 status";
   }
 }
@@ -116,7 +117,8 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
                   const void* k, const void* v, const void* a, const void* b, const float* h0,
                   const float* h_ckpt, const float* sa, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
-                  float* dv, float* da, float* db, float* dh0, void* stream) {
+                  float* dv, float* da, float* db, float* dh0, void* workspace, size_t workspace_bytes,
+                  void* stream) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
@@ -131,7 +133,20 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const voi
   p.in = {r, w, k, v, a, b};
   p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
   p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
+  if (workspace != nullptr && p.sa != nullptr) {
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
+    if (workspace_bytes < wkv7::backward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
+    return record_cuda(wkv7::launch_backward_two_phase(p, workspace, static_cast<cudaStream_t>(stream)));
+  }
   return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
+}
+
+int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t* bytes) {
+  int st = check_sizes(B, T, H, D, chunk);
+  if (st) return st;
+  if (bytes == nullptr) return WKV7_ERR_ARG;
+  *bytes = wkv7::backward_workspace_bytes(B, T, H, chunk);
+  return WKV7_OK;
 }
 
 int wkv7_decode(int B, int H, int D, int in_dtype, float* state, const void* r, const void* w, const void* k,

@@ -1,0 +1,511 @@
+// WKV7 checkpointed backward on sm_103a, in two phases.
+//
+// Source: "RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel
+// architecture", Backward listing: chunks walked in reverse from the exact checkpoints,
+// the previous state rebuilt as (h - v k - sa b) / w, the VJP giving dr, dw, dk, dv, da,
+// db.  With X_t the gradient w.r.t. the state S_t after token t, including y_t's term:
+//     X_t     = X'_t + dy_t r_t^T          (X'_t from later tokens; X'_{T-1} = dhT)
+//     dsa_t   = X_t b_t,   dv_t = X_t k_t                     (row sums)
+//     X'_{t-1} = X_t diag(w_t) + dsa_t a_t^T
+//     dr_t = S_t^T dy_t,  dk_t = X_t^T v_t,  db_t = X_t^T sa_t (column sums)
+//     S_{t-1} = (S_t - v_t k_t^T - sa_t b_t^T) diag(1/w_t)
+//     dw_t = colsum(X_t o S_{t-1}),  da_t = S_{t-1}^T dsa_t    (column sums)
+// The state-gradient recurrence needs only the row sums; the column sums need X_t and S_t
+// but nothing serial once X at each chunk end and every dsa_t are known.  So:
+//
+// Phase 1 (one pass over the sequence, like the forward): X is walked in reverse with
+// only its row sums -- dsa_t by a one-token lookahead
+//     dsa_{t-1} = X_t (w_t o b_{t-1}) + dsa_t (a_t . b_{t-1}) + dy_{t-1} (r_{t-1} . b_{t-1})
+// and dv_t -- writing dv, dsa (workspace), X at every chunk end (workspace) and dh0.
+// Mapping as the forward: a head in two row blocks of 32 rows, thread = 4 rows x 4
+// columns, 16-lane row sums, tiles of 32 tokens staged with cp.async (here in reverse).
+//
+// Phase 2 (every chunk of every head at once): one CTA per (head, chunk) walks the chunk
+// in reverse from S = h_ckpt[c] and X = X at the chunk end, rebuilding S by the page's
+// formula and X with the known dsa, and forms the five column sums.  Thread = 32 rows x 2
+// columns of S and X (row pairs as fp32x2); a column sum is a sum over the thread's 32
+// rows plus one shuffle with the lane holding the other 32 rows: no shared-memory
+// reduction, no barrier inside the walk.
+#include "wkv7_device.cuh"
+#include "wkv7_launch.h"
+
+namespace wkv7 {
+namespace {
+
+// ============================================================================ phase 1
+
+constexpr int kTile = 32;          // tokens per staged tile
+constexpr int kRows1 = 32;         // state rows per CTA
+constexpr int kNT1 = kRows1 * 4;   // 128 threads: 8 row groups x 16 lanes
+constexpr int kNW1 = kNT1 / 32;
+
+template <typename Tin>
+struct P1Smem {
+  // raw stage (x2), token row index u = t - (tlo - 1): w, a, k rows 1..nt; b, r rows 0..nt;
+  // dy (fp32, this CTA's rows) rows 0..nt
+  static constexpr int kRawCols = 5 * (kTile + 1) * kD;
+  static constexpr size_t kRawT = ((kRawCols * sizeof(Tin)) + 15) / 16 * 16;
+  static constexpr size_t kRawDy = (kTile + 1) * kRows1 * 4;
+  static constexpr size_t kRaw = kRawT + kRawDy;
+  // fp32 tiles indexed by tt = t - tlo: W, A, K, CB (w_t o b_{t-1}), R1 (r_{t-1}) [kTile][kD];
+  // AB (a_t . b_{t-1}), RB (r_{t-1} . b_{t-1}) [kTile]; DY1 (dy_{t-1}) [kTile][kRows1];
+  // outputs DSA, DV [kTile][kRows1]
+  static constexpr size_t oTiles = 2 * kRaw;
+  static constexpr int kF32 = 5 * kTile * kD + 2 * kTile + 3 * kTile * kRows1;
+  static constexpr size_t kBytes = oTiles + (size_t)kF32 * 4;
+};
+
+// cp.async copies for the tile of tokens [tlo, thi): w, a, k of tokens tlo..thi-1 and b, r, dy
+// of tokens tlo-1..thi-1 (token tlo-1 only when tlo > 0)
+template <typename Tin>
+__device__ __forceinline__ void p1_issue(unsigned char* raw, int tlo, int thi, size_t base, size_t tstride, int rcol,
+                                         const Tin* __restrict__ w, const Tin* __restrict__ a,
+                                         const Tin* __restrict__ k, const Tin* __restrict__ b,
+                                         const Tin* __restrict__ r, const float* __restrict__ dy) {
+  constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+  constexpr int EPC = 16 / (int)sizeof(Tin);
+  Tin* cols = reinterpret_cast<Tin*>(raw);
+  const int ulo = tlo > 0 ? 0 : 1;  // first valid row index u (u = t - tlo + 1)
+  const int nu = thi - tlo + 1;      // rows 0 .. nu-1
+  const Tin* srcs[5] = {w, a, k, b, r};
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    const int u0 = q < 3 ? 1 : ulo;  // w, a, k only for the tile's own tokens
+    for (int e = threadIdx.x; e < (nu - u0) * CPR; e += kNT1) {
+      const int u = u0 + e / CPR, pc = e % CPR;
+      cp_async16(cols + (q * (kTile + 1) + u) * kD + pc * EPC,
+                 srcs[q] + base + (size_t)(tlo - 1 + u) * tstride + pc * EPC);
+    }
+  }
+  float* dyr = reinterpret_cast<float*>(raw + P1Smem<Tin>::kRawT);
+  constexpr int FPR = kRows1 / 4;
+  for (int e = threadIdx.x; e < (nu - ulo) * FPR; e += kNT1) {
+    const int u = ulo + e / FPR, pc = e % FPR;
+    cp_async16(dyr + u * kRows1 + pc * 4, dy + base + (size_t)(tlo - 1 + u) * tstride + rcol + pc * 4);
+  }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kNT1, 1)
+gwalk_kernel(int T, int H, int chunk, int nchunks,
+             const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
+             const Tin* __restrict__ a, const Tin* __restrict__ b,
+             const float* __restrict__ dy, const float* __restrict__ dhT,
+             float* __restrict__ dv, float* __restrict__ dh0,
+             float* __restrict__ dsa_ws, float* __restrict__ xck_ws) {
+  using L = P1Smem<Tin>;
+  constexpr int NRB = kD / kRows1;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+  float* fW = reinterpret_cast<float*>(sm + L::oTiles);
+  float* fA = fW + kTile * kD;
+  float* fK = fA + kTile * kD;
+  float* fCB = fK + kTile * kD;
+  float* fR1 = fCB + kTile * kD;
+  float* fAB = fR1 + kTile * kD;
+  float* fRB = fAB + kTile;
+  float* fDY1 = fRB + kTile;
+  float* fDSA = fDY1 + kTile * kRows1;
+  float* fDV = fDSA + kTile * kRows1;
+
+  const int bh = blockIdx.x / NRB;
+  const int rb = blockIdx.x - bh * NRB;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int l16 = tid & 15;
+  const int rloc = 4 * (tid >> 4);
+  const int row0 = rb * kRows1 + rloc;
+  const int j0 = 4 * l16;
+  const int qrow = rs_row(l16);
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const size_t sbase = (size_t)bh * kD * kD;
+  const int ntiles = (T + kTile - 1) / kTile;
+
+  // X: starts at dhT, then gains dy_{T-1} r_{T-1}^T
+  float2 X[4][2];
+  if (dhT != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x4 = __ldg(reinterpret_cast<const float4*>(dhT + sbase + (size_t)(row0 + i) * kD + j0));
+      X[i][0] = lo2(x4);
+      X[i][1] = hi2(x4);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i][0] = X[i][1] = make_float2(0.f, 0.f);
+  }
+  float dsa[4] = {0.f, 0.f, 0.f, 0.f};
+  if (T > 0) {
+    const size_t o = base + (size_t)(T - 1) * tstride;
+    const float4 r4 = load4(r + o + j0);
+    const float4 b4 = load4(b + o + j0);
+    const float4 d4 = __ldg(reinterpret_cast<const float4*>(dy + o + row0));
+    const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      X[i][0] = __ffma2_rn(bcast2(dd[i]), lo2(r4), X[i][0]);
+      X[i][1] = __ffma2_rn(bcast2(dd[i]), hi2(r4), X[i][1]);
+    }
+    dot4x4(X, b4, dsa);
+    butterfly4(dsa);
+    p1_issue<Tin>(sm, max(0, T - kTile), T, base, tstride, rb * kRows1, w, a, k, b, r, dy);
+    cp_async_commit();
+  }
+
+  for (int it = 0; it < ntiles; ++it) {
+    const int thi = T - it * kTile;
+    const int tlo = max(0, thi - kTile);
+    const int nt = thi - tlo;
+    unsigned char* raw = sm + (size_t)(it & 1) * L::kRaw;
+    if (it + 1 < ntiles) {
+      p1_issue<Tin>(sm + (size_t)((it + 1) & 1) * L::kRaw, max(0, tlo - kTile), tlo, base, tstride, rb * kRows1, w, a,
+                    k, b, r, dy);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // this tile's stage has landed; the previous tile's fp32 data is consumed
+
+    // ---- widen (8 lanes per token): W A K, CB = w_t o b_{t-1}, R1 = r_{t-1}, AB, RB
+    {
+      const Tin* cols = reinterpret_cast<const Tin*>(raw);
+      const Tin* rW = cols;
+      const Tin* rA = cols + (kTile + 1) * kD;
+      const Tin* rK = cols + 2 * (kTile + 1) * kD;
+      const Tin* rB = cols + 3 * (kTile + 1) * kD;
+      const Tin* rR = cols + 4 * (kTile + 1) * kD;
+      for (int tg = warp * 4; tg < nt; tg += kNW1 * 4) {
+        const int tt = tg + (lane >> 3);  // token tlo + tt, row u = tt + 1; previous token row tt
+        const int c8 = (lane & 7) * 8;
+        float ab = 0.f, rb1 = 0.f;
+        if (tt < nt) {
+          float ww[8], aa[8], kk[8], bp[8], rp[8], cb[8];
+          raw8(rW + (tt + 1) * kD + c8, ww);
+          raw8(rA + (tt + 1) * kD + c8, aa);
+          raw8(rK + (tt + 1) * kD + c8, kk);
+          if (tlo + tt > 0) {
+            raw8(rB + tt * kD + c8, bp);
+            raw8(rR + tt * kD + c8, rp);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) bp[u] = rp[u] = 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            cb[u] = ww[u] * bp[u];
+            ab = fmaf(aa[u], bp[u], ab);
+            rb1 = fmaf(rp[u], bp[u], rb1);
+          }
+          store8(fW + tt * kD + c8, ww);
+          store8(fA + tt * kD + c8, aa);
+          store8(fK + tt * kD + c8, kk);
+          store8(fCB + tt * kD + c8, cb);
+          store8(fR1 + tt * kD + c8, rp);
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+          ab += __shfl_xor_sync(0xffffffffu, ab, m);
+          rb1 += __shfl_xor_sync(0xffffffffu, rb1, m);
+        }
+        if (tt < nt && (lane & 7) == 0) {
+          fAB[tt] = ab;
+          fRB[tt] = rb1;
+        }
+      }
+      const float* dyr = reinterpret_cast<const float*>(raw + L::kRawT);
+      for (int e = tid; e < nt * kRows1; e += kNT1) {
+        const int tt = e / kRows1;
+        fDY1[e] = (tlo + tt > 0) ? dyr[e] : 0.f;  // row tt of the stage = token tlo + tt - 1
+      }
+    }
+    __syncthreads();
+
+    // ---- the reverse walk over the tile
+#pragma unroll 2
+    for (int tt = nt - 1; tt >= 0; --tt) {
+      const int t = tlo + tt;
+      const float4 w4 = *reinterpret_cast<const float4*>(fW + tt * kD + j0);
+      const float4 a4 = *reinterpret_cast<const float4*>(fA + tt * kD + j0);
+      const float4 k4 = *reinterpret_cast<const float4*>(fK + tt * kD + j0);
+      const float4 cb4 = *reinterpret_cast<const float4*>(fCB + tt * kD + j0);
+      const float4 r14 = *reinterpret_cast<const float4*>(fR1 + tt * kD + j0);
+      const float4 dp4 = *reinterpret_cast<const float4*>(fDY1 + tt * kRows1 + rloc);
+      const float ab = fAB[tt], rb1 = fRB[tt];
+      const float dp[4] = {dp4.x, dp4.y, dp4.z, dp4.w};
+      if (l16 == 0) *reinterpret_cast<float4*>(fDSA + tt * kRows1 + rloc) = make_float4(dsa[0], dsa[1], dsa[2], dsa[3]);
+
+      // X at this chunk's last token is the start of phase 2's walk over the chunk
+      if (xck_ws != nullptr && ((t + 1) % chunk == 0 || t == T - 1)) {
+        float* dst = xck_ws + ((size_t)bh * nchunks + t / chunk) * kD * kD + (size_t)row0 * kD + j0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(dst + i * kD) = make_float4(X[i][0].x, X[i][0].y, X[i][1].x, X[i][1].y);
+      }
+      // dv_t = X_t k_t, and the lookahead row sums X_t (w_t o b_{t-1})
+      float pv[4], P[4];
+      dot4x4(X, k4, pv);
+      dot4x4(X, cb4, P);
+      const float dvq = reduce_scatter4(pv, l16);
+      if ((l16 & 3) == 0) fDV[tt * kRows1 + rloc + qrow] = dvq;
+      butterfly4(P);
+      // X <- X w + dsa a + dy_{t-1} r_{t-1}
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 q2 = bcast2(dsa[i]), e2 = bcast2(dp[i]);
+        X[i][0] = __ffma2_rn(X[i][0], lo2(w4), __ffma2_rn(q2, lo2(a4), __fmul2_rn(e2, lo2(r14))));
+        X[i][1] = __ffma2_rn(X[i][1], hi2(w4), __ffma2_rn(q2, hi2(a4), __fmul2_rn(e2, hi2(r14))));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dsa[i] = fmaf(dsa[i], ab, fmaf(dp[i], rb1, P[i]));
+    }
+    __syncthreads();
+    for (int e = tid; e < nt * kRows1; e += kNT1) {
+      const int tt = e / kRows1;
+      const int rr = e % kRows1;
+      const size_t o = base + (size_t)(tlo + tt) * tstride + rb * kRows1 + rr;
+      dv[o] = fDV[e];
+      dsa_ws[o] = fDSA[e];
+    }
+  }
+
+  if (dh0 != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(dh0 + sbase + (size_t)(row0 + i) * kD + j0) =
+          make_float4(X[i][0].x, X[i][0].y, X[i][1].x, X[i][1].y);
+  }
+}
+
+// ============================================================================ phase 2
+
+constexpr int kNT2 = 64;  // 2 warps: warp q covers columns 32q .. 32q+31, all 64 rows
+constexpr int kRP = 16;   // row pairs per thread (32 rows)
+
+template <typename Tin>
+struct P2Smem {
+  // raw inputs of the chunk: w, k, a, b, r, v [kTile][kD] (input dtype); sa, dsa, dy fp32 [kTile][kD]
+  static constexpr size_t oCols = 0;
+  static constexpr size_t kColsBytes = ((6 * kTile * kD * sizeof(Tin)) + 15) / 16 * 16;
+  static constexpr size_t oSa = oCols + kColsBytes;
+  static constexpr size_t oDsa = oSa + kTile * kD * 4;
+  static constexpr size_t oDy = oDsa + kTile * kD * 4;
+  // widened: v fp32 [kTile][kD], 1/w fp32 [kTile][kD]
+  static constexpr size_t oV = oDy + kTile * kD * 4;
+  static constexpr size_t oWi = oV + kTile * kD * 4;
+  static constexpr size_t kBytes = oWi + kTile * kD * 4;
+};
+
+template <typename Tin>
+__device__ __forceinline__ float2 col2(const Tin* p) {
+  if constexpr (sizeof(Tin) == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(bf16_lo(u), bf16_hi(u));
+  } else {
+    return *reinterpret_cast<const float2*>(p);
+  }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kNT2)
+colgrad_kernel(int T, int H, int chunk, int nchunks,
+               const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
+               const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
+               const float* __restrict__ h_ckpt, const float* __restrict__ sa, const float* __restrict__ dy,
+               const float* __restrict__ dsa_ws, const float* __restrict__ xck_ws,
+               float* __restrict__ dr, float* __restrict__ dw, float* __restrict__ dk,
+               float* __restrict__ da, float* __restrict__ db) {
+  using L = P2Smem<Tin>;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+  const Tin* cW = reinterpret_cast<const Tin*>(sm + L::oCols);
+  const Tin* cK = cW + kTile * kD;
+  const Tin* cA = cW + 2 * kTile * kD;
+  const Tin* cB = cW + 3 * kTile * kD;
+  const Tin* cR = cW + 4 * kTile * kD;
+  const Tin* cV = cW + 5 * kTile * kD;
+  const float* sSa = reinterpret_cast<const float*>(sm + L::oSa);
+  const float* sDsa = reinterpret_cast<const float*>(sm + L::oDsa);
+  const float* sDy = reinterpret_cast<const float*>(sm + L::oDy);
+  float* sV = reinterpret_cast<float*>(sm + L::oV);
+  float* sWi = reinterpret_cast<float*>(sm + L::oWi);
+
+  const int ci = blockIdx.x % nchunks;
+  const int bh = blockIdx.x / nchunks;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int c0 = 2 * (16 * (tid >> 5) + (lane & 15));  // columns c0, c0 + 1
+  const int half = lane >> 4;                          // rows 32*half .. 32*half + 31
+  const int r0 = 32 * half;
+  const int t0 = ci * chunk;
+  const int n = min(chunk, T - t0);
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const size_t cko = ((size_t)bh * nchunks + ci) * kD * kD;
+
+  // ---- stage the chunk's inputs
+  {
+    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    Tin* cols = reinterpret_cast<Tin*>(sm + L::oCols);
+    const Tin* srcs[6] = {w, k, a, b, r, v};
+#pragma unroll
+    for (int q = 0; q < 6; ++q)
+      for (int e = tid; e < n * CPR; e += kNT2) {
+        const int tt = e / CPR, pc = e % CPR;
+        cp_async16(cols + (q * kTile + tt) * kD + pc * EPC, srcs[q] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+      }
+    const float* fsrc[3] = {sa, dsa_ws, dy};
+    float* fdst[3] = {reinterpret_cast<float*>(sm + L::oSa), reinterpret_cast<float*>(sm + L::oDsa),
+                      reinterpret_cast<float*>(sm + L::oDy)};
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      for (int e = tid; e < n * (kD / 4); e += kNT2) {
+        const int tt = e / (kD / 4), pc = e % (kD / 4);
+        cp_async16(fdst[q] + tt * kD + pc * 4, fsrc[q] + base + (size_t)(t0 + tt) * tstride + pc * 4);
+      }
+    cp_async_commit();
+  }
+  // ---- S = h_ckpt[ci], X = X at the chunk's last token: rows r0.., columns c0, c0+1, as row pairs
+  float2 S[kRP][2], X[kRP][2];
+#pragma unroll
+  for (int p = 0; p < kRP; ++p) {
+    const size_t o0 = cko + (size_t)(r0 + 2 * p) * kD + c0;
+    const float2 se = __ldg(reinterpret_cast<const float2*>(h_ckpt + o0));
+    const float2 so = __ldg(reinterpret_cast<const float2*>(h_ckpt + o0 + kD));
+    const float2 xe = __ldg(reinterpret_cast<const float2*>(xck_ws + o0));
+    const float2 xo = __ldg(reinterpret_cast<const float2*>(xck_ws + o0 + kD));
+    S[p][0] = make_float2(se.x, so.x);
+    S[p][1] = make_float2(se.y, so.y);
+    X[p][0] = make_float2(xe.x, xo.x);
+    X[p][1] = make_float2(xe.y, xo.y);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  for (int e = tid; e < n * kD; e += kNT2) {
+    sV[e] = to_f32(cV[e]);
+    sWi[e] = 1.0f / to_f32(cW[e]);
+  }
+  __syncthreads();
+
+  // ---- reverse walk over the chunk
+  for (int tt = n - 1; tt >= 0; --tt) {
+    const float2 w2 = col2<Tin>(cW + tt * kD + c0);
+    const float2 wi2 = *reinterpret_cast<const float2*>(sWi + tt * kD + c0);
+    const float2 k2 = col2<Tin>(cK + tt * kD + c0);
+    const float2 a2 = col2<Tin>(cA + tt * kD + c0);
+    const float2 b2 = col2<Tin>(cB + tt * kD + c0);
+    const bool more = tt > 0;
+    const float2 rp2 = more ? col2<Tin>(cR + (tt - 1) * kD + c0) : make_float2(0.f, 0.f);
+    const float2 wb[2] = {bcast2(w2.x), bcast2(w2.y)}, wib[2] = {bcast2(wi2.x), bcast2(wi2.y)};
+    const float2 nkb[2] = {bcast2(-k2.x), bcast2(-k2.y)}, ab2[2] = {bcast2(a2.x), bcast2(a2.y)};
+    const float2 nbb[2] = {bcast2(-b2.x), bcast2(-b2.y)}, rpb[2] = {bcast2(rp2.x), bcast2(rp2.y)};
+    const float* rv = sV + tt * kD + r0;
+    const float* rs = sSa + tt * kD + r0;
+    const float* rq = sDsa + tt * kD + r0;
+    const float* rd = sDy + tt * kD + r0;
+    const float* re = sDy + (tt - 1) * kD + r0;  // dy_{t-1}, read only when `more`
+
+    float2 cdr[2], cdw[2], cdk[2], cdb[2], cda[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) cdr[c] = cdw[c] = cdk[c] = cdb[c] = cda[c] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int p4 = 0; p4 < kRP / 2; ++p4) {  // 4 rows (2 row pairs) per step
+      const float4 v4 = *reinterpret_cast<const float4*>(rv + 4 * p4);
+      const float4 s4 = *reinterpret_cast<const float4*>(rs + 4 * p4);
+      const float4 q4 = *reinterpret_cast<const float4*>(rq + 4 * p4);
+      const float4 d4 = *reinterpret_cast<const float4*>(rd + 4 * p4);
+      const float4 e4 = more ? *reinterpret_cast<const float4*>(re + 4 * p4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int p = 2 * p4 + h;
+        const float2 v2 = h ? hi2(v4) : lo2(v4);
+        const float2 s2 = h ? hi2(s4) : lo2(s4);
+        const float2 q2 = h ? hi2(q4) : lo2(q4);
+        const float2 d2 = h ? hi2(d4) : lo2(d4);
+        const float2 e2 = h ? hi2(e4) : lo2(e4);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          cdr[c] = __ffma2_rn(d2, S[p][c], cdr[c]);
+          const float2 sp = __fmul2_rn(__ffma2_rn(s2, nbb[c], __ffma2_rn(v2, nkb[c], S[p][c])), wib[c]);
+          S[p][c] = sp;
+          cdw[c] = __ffma2_rn(X[p][c], sp, cdw[c]);
+          cdk[c] = __ffma2_rn(X[p][c], v2, cdk[c]);
+          cdb[c] = __ffma2_rn(X[p][c], s2, cdb[c]);
+          cda[c] = __ffma2_rn(q2, sp, cda[c]);
+          X[p][c] = __ffma2_rn(X[p][c], wb[c], __ffma2_rn(q2, ab2[c], __fmul2_rn(e2, rpb[c])));
+        }
+      }
+    }
+    // sum over this thread's 32 rows, then with the lane holding the other 32 rows
+    float g[10] = {cdr[0].x + cdr[0].y, cdr[1].x + cdr[1].y, cdw[0].x + cdw[0].y, cdw[1].x + cdw[1].y,
+                   cdk[0].x + cdk[0].y, cdk[1].x + cdk[1].y, cdb[0].x + cdb[0].y, cdb[1].x + cdb[1].y,
+                   cda[0].x + cda[0].y, cda[1].x + cda[1].y};
+#pragma unroll
+    for (int u = 0; u < 10; ++u) g[u] += __shfl_xor_sync(0xffffffffu, g[u], 16);
+    if (half == 0) {
+      const size_t o = base + (size_t)(t0 + tt) * tstride + c0;
+      *reinterpret_cast<float2*>(dr + o) = make_float2(g[0], g[1]);
+      *reinterpret_cast<float2*>(dw + o) = make_float2(g[2], g[3]);
+      *reinterpret_cast<float2*>(dk + o) = make_float2(g[4], g[5]);
+      *reinterpret_cast<float2*>(db + o) = make_float2(g[6], g[7]);
+      *reinterpret_cast<float2*>(da + o) = make_float2(g[8], g[9]);
+    }
+  }
+}
+
+template <typename Tin>
+cudaError_t launch_bwd2_t(const BwdArgs& p, float* dsa_ws, float* xck_ws, cudaStream_t stream) {
+  {
+    const size_t smem = P1Smem<Tin>::kBytes;
+    static_assert(P1Smem<Tin>::kBytes <= 232448, "shared memory per CTA");
+    auto kern = gwalk_kernel<Tin>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = (unsigned)p.B * p.H * (kD / kRows1);
+    kern<<<grid, kNT1, smem, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
+                                       (const Tin*)p.in.k, (const Tin*)p.in.a, (const Tin*)p.in.b, p.dy, p.dhT,
+                                       p.dv, p.dh0, dsa_ws, xck_ws);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (p.nchunks == 0) return cudaSuccess;
+  {
+    const size_t smem = P2Smem<Tin>::kBytes;
+    static_assert(P2Smem<Tin>::kBytes <= 232448, "shared memory per CTA");
+    auto kern = colgrad_kernel<Tin>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = (unsigned)p.B * p.H * p.nchunks;
+    kern<<<grid, kNT2, smem, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
+                                       (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
+                                       (const Tin*)p.in.b, p.h_ckpt, p.sa, p.dy, dsa_ws, xck_ws, p.dr, p.dw, p.dk,
+                                       p.da, p.db);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int B, int T, int H, int chunk) {
+  const size_t C = T > 0 ? (size_t)((T + chunk - 1) / chunk) : 0;
+  const size_t dsa = (size_t)B * T * H * kD * 4;
+  const size_t xck = (size_t)B * H * C * kD * kD * 4;
+  return (dsa + 255) / 256 * 256 + xck;
+}
+
+cudaError_t launch_backward_two_phase(const BwdArgs& p, void* workspace, cudaStream_t stream) {
+  float* dsa_ws = static_cast<float*>(workspace);
+  const size_t dsa = (size_t)p.B * p.T * p.H * kD * 4;
+  float* xck_ws = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + (dsa + 255) / 256 * 256);
+  return p.bf16 ? launch_bwd2_t<__nv_bfloat16>(p, dsa_ws, xck_ws, stream)
+                : launch_bwd2_t<float>(p, dsa_ws, xck_ws, stream);
+}
+
+}  // namespace wkv7

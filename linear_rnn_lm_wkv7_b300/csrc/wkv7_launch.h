@@ -53,6 +53,11 @@ int num_sms();
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
+
+// two-phase backward (needs the saved sa): workspace of backward_workspace_bytes() bytes,
+// 256-byte aligned, holding dsa (B,T,H,D) and the state gradient at every chunk end (B,H,C,D,D)
+size_t backward_workspace_bytes(int B, int T, int H, int chunk);
+cudaError_t launch_backward_two_phase(const BwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace wkv7

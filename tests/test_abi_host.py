@@ -50,9 +50,9 @@ def fwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None):
     return wkv7.lib.wkv7_forward(B, T, H, D, chunk, dt, *p, None)
 
 
-def bwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None):
+def bwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None, ws=None, ws_bytes=0):
     p = list(ALIGNED[:18]) if ptrs is None else ptrs
-    return wkv7.lib.wkv7_backward(B, T, H, D, chunk, dt, *p, None)
+    return wkv7.lib.wkv7_backward(B, T, H, D, chunk, dt, *p, ws, ws_bytes, None)
 
 
 def dec(B=2, H=3, D=64, dt=0, ptrs=None):
@@ -118,6 +118,24 @@ def test_decode_validation(i):
     assert dec(ptrs=p) == 3
     assert dec(D=16) == 2
     assert dec(dt=3) == 4
+
+
+def test_workspace_size_query():
+    n = wkv7.backward_workspace_size(12, 1024, 6, 64, 32)
+    dsa = 12 * 1024 * 6 * 64 * 4
+    xck = 12 * 6 * 32 * 64 * 64 * 4
+    assert n == (dsa + 255) // 256 * 256 + xck
+    assert wkv7.backward_workspace_size(1, 0, 1, 64, 32) == 0
+    with pytest.raises(wkv7.WKV7Error):
+        wkv7.backward_workspace_size(1, 32, 1, 32, 32)      # D != 64
+    assert wkv7.lib.wkv7_backward_workspace_size(1, 32, 1, 64, 32, None) == 1
+
+
+def test_backward_rejects_small_or_misaligned_workspace():
+    # with sa given (index 8) a workspace selects the two-phase path: it is checked before any launch
+    need = wkv7.backward_workspace_size(2, 64, 3, 64, 32)
+    assert bwd(ws=P(0x100000), ws_bytes=need - 1) == 7
+    assert bwd(ws=P(0x100000 + 128), ws_bytes=need) == 3
 
 
 def test_binding_rejects_cpu_tensors():

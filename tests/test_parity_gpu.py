@@ -49,14 +49,18 @@ def host(t):
     return None if t is None else t.detach().double().cpu().numpy()
 
 
-def run_gpu(wkv7, x, dtype, chunk=32, saved_sa=True):
-    """Forward then backward; with saved_sa the forward's sa feeds the backward, else the
-    backward recomputes sa per chunk."""
+# backward paths: the two-phase backward (saved sa + workspace), the single pass reading the
+# saved sa, the single pass recomputing sa per chunk
+MODES = ["two_phase", "single_saved_sa", "single_recompute"]
+
+
+def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase"):
     ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
     y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True)
-    grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk,
-                          sa=sa if saved_sa else None)
+    kw = {"two_phase": dict(sa=sa), "single_saved_sa": dict(sa=sa, workspace=None),
+          "single_recompute": dict(sa=None)}[mode]
+    grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk, **kw)
     torch.cuda.synchronize()
     return host(y), host(ck), host(hT), [host(g) for g in grads], host(sa)
 
@@ -86,20 +90,20 @@ def check(x, gpu, chunk, heads=None):
     assert np.array_equal(ck[:, :, -1], hT)
 
 
-@pytest.mark.parametrize("saved_sa", [True, False], ids=["saved_sa", "recompute_sa"])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
-def test_workload_parity_full(wkv7, name, saved_sa):
+def test_workload_parity_full(wkv7, name, mode):
     wl = gen.WORKLOADS[name]
     x = gen.full(wl)
-    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, saved_sa), wl.chunk)
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, mode), wl.chunk)
 
 
-@pytest.mark.parametrize("saved_sa", [True, False], ids=["saved_sa", "recompute_sa"])
-def test_workload_parity_wide7b_sampled_heads(wkv7, saved_sa):
-    """128 heads: more than half the SM count, so the backward runs one CTA per head."""
+@pytest.mark.parametrize("mode", MODES)
+def test_workload_parity_wide7b_sampled_heads(wkv7, mode):
+    """128 heads: more than half the SM count, so the single-pass backward runs one CTA per head."""
     wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
     x = gen.full(wl)
-    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk, saved_sa)
+    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk, mode)
     check(x, gpu, wl.chunk, heads=[(0, 0), (1, 37), (0, 63)])
     # every head: properties that hold at any size
     y, ck, hT, grads, _ = gpu
@@ -113,25 +117,42 @@ def test_workload_parity_wide7b_sampled_heads(wkv7, saved_sa):
 ])
 def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
     x = gen.random_small(B * 100 + T + H, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    check(x, run_gpu(wkv7, x, dtype, chunk, saved_sa=True), chunk)
-    check(x, run_gpu(wkv7, x, dtype, chunk, saved_sa=False), chunk)
+    for mode in MODES:
+        check(x, run_gpu(wkv7, x, dtype, chunk, mode), chunk)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_many_heads_one_cta_per_head(wkv7, dtype):
     """B*H = 78 heads (more than half of 148 SMs): the one-CTA-per-head backward, ragged T."""
     x = gen.random_small(77, B=3, T=45, H=26, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    for saved in (True, False):
-        check(x, run_gpu(wkv7, x, dtype, 32, saved), 32, heads=[(0, 0), (1, 13), (2, 25)])
+    for mode in MODES:
+        check(x, run_gpu(wkv7, x, dtype, 32, mode), 32, heads=[(0, 0), (1, 13), (2, 25)])
 
 
-def test_backward_is_deterministic(wkv7):
-    """Column sums are taken in a fixed order: two backward calls agree bit for bit."""
+@pytest.mark.parametrize("mode", MODES)
+def test_backward_is_deterministic(wkv7, mode):
+    """Sums are taken in a fixed order: two backward calls agree bit for bit."""
     x = gen.random_small(8, B=4, T=96, H=6, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
-    a = run_gpu(wkv7, x, "bf16", 32)
-    b = run_gpu(wkv7, x, "bf16", 32)
+    a = run_gpu(wkv7, x, "bf16", 32, mode)
+    b = run_gpu(wkv7, x, "bf16", 32, mode)
     for ga, gb in zip(a[3], b[3]):
         assert np.array_equal(ga, gb)
+
+
+def test_explicit_workspace_and_too_small_workspace(wkv7):
+    """A caller-owned workspace gives the same gradients as the automatic one; a smaller one is refused."""
+    x = gen.random_small(9, B=2, T=70, H=3, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
+    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    h0 = dev32(x["h0"])
+    y, ck, hT, sa = wkv7.forward(*ins, h0, save_sa=True)
+    need = wkv7.backward_workspace_size(2, 70, 3)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    g1 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa, workspace=ws)
+    g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa)
+    for p, q in zip(g1, g2):
+        assert torch.equal(p, q)
+    with pytest.raises(wkv7.WKV7Error):
+        wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa, workspace=ws[: need - 256])
 
 
 def test_no_h0_no_dhT_no_dh0(wkv7):
