@@ -156,6 +156,8 @@ gwalk_kernel(int T, int H, int chunk, int nchunks,
     cp_async_commit();
   }
 
+  // tokens until (and including) the next chunk end walking down: the chunk of token T-1 ends at T-1
+  int to_end = 0;
   for (int it = 0; it < ntiles; ++it) {
     const int thi = T - it * kTile;
     const int tlo = max(0, thi - kTile);
@@ -240,11 +242,15 @@ gwalk_kernel(int T, int H, int chunk, int nchunks,
       if (l16 == 0) *reinterpret_cast<float4*>(fDSA + tt * kRows1 + rloc) = make_float4(dsa[0], dsa[1], dsa[2], dsa[3]);
 
       // X at this chunk's last token is the start of phase 2's walk over the chunk
-      if (xck_ws != nullptr && ((t + 1) % chunk == 0 || t == T - 1)) {
-        float* dst = xck_ws + ((size_t)bh * nchunks + t / chunk) * kD * kD + (size_t)row0 * kD + j0;
+      if (to_end == 0) {
+        const int c = t / chunk;
+        to_end = t - c * chunk;  // tokens below t in this chunk
+        float* dst = xck_ws + ((size_t)bh * nchunks + c) * kD * kD + (size_t)row0 * kD + j0;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<float4*>(dst + i * kD) = make_float4(X[i][0].x, X[i][0].y, X[i][1].x, X[i][1].y);
+      } else {
+        --to_end;
       }
       // dv_t = X_t k_t, and the lookahead row sums X_t (w_t o b_{t-1})
       float pv[4], P[4];
@@ -294,10 +300,9 @@ struct P2Smem {
   static constexpr size_t oSa = oCols + kColsBytes;
   static constexpr size_t oDsa = oSa + kTile * kD * 4;
   static constexpr size_t oDy = oDsa + kTile * kD * 4;
-  // widened: v fp32 [kTile][kD], 1/w fp32 [kTile][kD]
+  // widened: v fp32 [kTile][kD]
   static constexpr size_t oV = oDy + kTile * kD * 4;
-  static constexpr size_t oWi = oV + kTile * kD * 4;
-  static constexpr size_t kBytes = oWi + kTile * kD * 4;
+  static constexpr size_t kBytes = oV + kTile * kD * 4;
 };
 
 template <typename Tin>
@@ -332,7 +337,6 @@ colgrad_kernel(int T, int H, int chunk, int nchunks,
   const float* sDsa = reinterpret_cast<const float*>(sm + L::oDsa);
   const float* sDy = reinterpret_cast<const float*>(sm + L::oDy);
   float* sV = reinterpret_cast<float*>(sm + L::oV);
-  float* sWi = reinterpret_cast<float*>(sm + L::oWi);
 
   const int ci = blockIdx.x % nchunks;
   const int bh = blockIdx.x / nchunks;
@@ -388,16 +392,13 @@ colgrad_kernel(int T, int H, int chunk, int nchunks,
   }
   cp_async_wait<0>();
   __syncthreads();
-  for (int e = tid; e < n * kD; e += kNT2) {
-    sV[e] = to_f32(cV[e]);
-    sWi[e] = 1.0f / to_f32(cW[e]);
-  }
+  for (int e = tid; e < n * kD; e += kNT2) sV[e] = to_f32(cV[e]);
   __syncthreads();
 
   // ---- reverse walk over the chunk
   for (int tt = n - 1; tt >= 0; --tt) {
     const float2 w2 = col2<Tin>(cW + tt * kD + c0);
-    const float2 wi2 = *reinterpret_cast<const float2*>(sWi + tt * kD + c0);
+    const float2 wi2 = make_float2(1.0f / w2.x, 1.0f / w2.y);
     const float2 k2 = col2<Tin>(cK + tt * kD + c0);
     const float2 a2 = col2<Tin>(cA + tt * kD + c0);
     const float2 b2 = col2<Tin>(cB + tt * kD + c0);
