@@ -59,7 +59,8 @@ typedef enum {
     WKV7_ERR_DTYPE = 4,    /* in_dtype is not WKV7_F32 / WKV7_BF16 */
     WKV7_ERR_CUDA = 5,     /* the CUDA runtime reported an error at launch */
     WKV7_ERR_TIMEOUT = 6,  /* a bounded device-side wait gave up (reserved) */
-    WKV7_ERR_WORKSPACE = 7 /* the backward's workspace is smaller than wkv7_backward_workspace_size */
+    WKV7_ERR_WORKSPACE = 7, /* the backward's workspace is smaller than wkv7_backward_workspace_size */
+    WKV7_ERR_SCRATCH_LIMIT = 8 /* wkv7_backward_noalloc: needs more than WKV7_NOALLOC_SCRATCH_BYTES */
 } wkv7_status;
 
 /* Number of checkpoints the forward writes: ceil(T / chunk); 0 for T == 0. */
@@ -120,6 +121,39 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
 /* Bytes of workspace the two-phase backward needs for these sizes (written to *bytes);
  * returns a wkv7_status (the same size checks as wkv7_backward). */
 int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
+
+/* Bytes of device scratch the library owns for wkv7_backward_noalloc (64 MiB). */
+#define WKV7_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * The two-phase backward without any workspace argument and without allocating.
+ *
+ * For callers that cannot allocate device memory on the call path or hand the library
+ * any: a host framework that gives an operator only its input and output buffers and no
+ * allocator, or a latency-critical loop that must not risk cudaMalloc (which may
+ * synchronise the device).  The scratch lives in one fixed array of
+ * WKV7_NOALLOC_SCRATCH_BYTES inside the library, reserved on every GPU that loads the
+ * library until the process exits.  There is no counterpart of this in the source pages:
+ * it is a packaging of the same computation as wkv7_backward with a workspace.
+ *
+ *   Arguments, layouts and results: as wkv7_backward, with `sa` required (the forward's
+ *   saved sa) and no workspace.  Problems whose wkv7_backward_workspace_size exceeds
+ *   WKV7_NOALLOC_SCRATCH_BYTES return WKV7_ERR_SCRATCH_LIMIT (B12 T1024 H6 needs ~57 MB;
+ *   use wkv7_backward with a workspace for larger ones).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   and caches it; make that first call before capturing a stream on that device.
+ *   All calls share the one array and it keeps the previous call's contents; nothing in
+ *   it needs clearing (each call writes every scratch value before reading it).  Calls
+ *   whose work overlaps on the GPU (different streams, or different host threads) race on
+ *   the array: serialise them.
+ */
+int wkv7_backward_noalloc(int B, int T, int H, int D, int chunk, int in_dtype,
+                          const void *r, const void *w, const void *k,
+                          const void *v, const void *a, const void *b,
+                          const float *h0, const float *h_ckpt, const float *sa,
+                          const float *dy, const float *dhT,
+                          float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                          float *dh0, void *stream);
 
 /*
  * One decode token for B sequences of H heads, state updated in place.

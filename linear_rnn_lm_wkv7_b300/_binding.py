@@ -21,7 +21,8 @@ D_HEAD = 64
 MAX_CHUNK = 32
 
 STATUS = {0: "WKV7_OK", 1: "WKV7_ERR_ARG", 2: "WKV7_ERR_SHAPE", 3: "WKV7_ERR_ALIGN",
-          4: "WKV7_ERR_DTYPE", 5: "WKV7_ERR_CUDA", 6: "WKV7_ERR_TIMEOUT", 7: "WKV7_ERR_WORKSPACE"}
+          4: "WKV7_ERR_DTYPE", 5: "WKV7_ERR_CUDA", 6: "WKV7_ERR_TIMEOUT", 7: "WKV7_ERR_WORKSPACE",
+          8: "WKV7_ERR_SCRATCH_LIMIT"}
 
 # every function the header declares, with (restype, argtypes)
 _P = ctypes.c_void_p
@@ -31,6 +32,7 @@ SIGNATURES = {
     "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
     "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "wkv7_backward_noalloc": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
     "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
     "wkv7_strerror": (ctypes.c_char_p, [_I]),
     "wkv7_last_cuda_error": (ctypes.c_char_p, []),

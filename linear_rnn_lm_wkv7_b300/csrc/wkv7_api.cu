@@ -57,6 +57,8 @@ int check_ptrs(std::initializer_list<const void*> required, std::initializer_lis
 
 namespace wkv7 {
 
+int record_cuda_status(cudaError_t err) { return record_cuda(err); }
+
 int num_sms() {
   static thread_local int cached[64] = {0};
   int dev = 0;
@@ -89,6 +91,9 @@ const char* wkv7_strerror(int status) {
     case WKV7_ERR_CUDA: return "CUDA error at launch (see wkv7_last_cuda_error)";
     case WKV7_ERR_TIMEOUT: return "a bounded device-side wait gave up";
     case WKV7_ERR_WORKSPACE: return "workspace smaller than wkv7_backward_workspace_size()";
+    case WKV7_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the library's fixed WKV7_NOALLOC_SCRATCH_BYTES: use wkv7_backward "
+             "with a workspace";
     default: return "unknown wkv7 status";
   }
 }

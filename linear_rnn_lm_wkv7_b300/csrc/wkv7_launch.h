@@ -51,6 +51,10 @@ struct DecodeArgs {
 // multiprocessor count of the current device (cached per device)
 int num_sms();
 
+// WKV7_OK for cudaSuccess; otherwise records the CUDA error text for wkv7_last_cuda_error()
+// and returns WKV7_ERR_CUDA
+int record_cuda_status(cudaError_t err);
+
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
 

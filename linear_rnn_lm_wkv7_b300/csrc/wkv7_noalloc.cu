@@ -1,0 +1,78 @@
+// wkv7_backward_noalloc: the two-phase backward with its scratch in a fixed array that
+// the library itself owns, for callers that cannot hand the library device memory.
+//
+// The scratch is one file-scope __device__ array.  Loading the library reserves it on
+// every GPU that loads it, for as long as the process lives.  In host code the array's
+// name is only a host-side stand-in for the device symbol, never a device address, so
+// its device address is looked up with cudaGetSymbolAddress -- once per device, on the
+// first call made with that device current -- and that address is what the kernels get.
+#include <stdint.h>
+
+#include <mutex>
+
+#include "wkv7.h"
+#include "wkv7_launch.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_backward_scratch[WKV7_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// device address of g_backward_scratch on the current device (looked up once per device)
+int scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return wkv7::record_cuda_status(err);
+  if (dev < 0 || dev >= kMaxDevices) return WKV7_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_backward_scratch);
+    if (err != cudaSuccess) return wkv7::record_cuda_status(err);
+    if (p == nullptr) return WKV7_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return WKV7_OK;
+}
+
+bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+}  // namespace
+
+extern "C" int wkv7_backward_noalloc(int B, int T, int H, int D, int chunk, int in_dtype, const void* r,
+                                     const void* w, const void* k, const void* v, const void* a, const void* b,
+                                     const float* h0, const float* h_ckpt, const float* sa, const float* dy,
+                                     const float* dhT, float* dr, float* dw, float* dk, float* dv, float* da,
+                                     float* db, float* dh0, void* stream) {
+  size_t need = 0;
+  int st = wkv7_backward_workspace_size(B, T, H, D, chunk, &need);  // the same size checks as wkv7_backward
+  if (st) return st;
+  if (in_dtype != WKV7_F32 && in_dtype != WKV7_BF16) return WKV7_ERR_DTYPE;
+  if (T > 0) {
+    const void* required[] = {r, w, k, v, a, b, h_ckpt, sa, dy, dr, dw, dk, dv, da, db};
+    for (const void* p : required)
+      if (p == nullptr) return WKV7_ERR_ARG;
+    for (const void* p : required)
+      if (misaligned16(p)) return WKV7_ERR_ALIGN;
+  }
+  for (const void* p : {static_cast<const void*>(h0), static_cast<const void*>(dhT), static_cast<const void*>(dh0)})
+    if (p != nullptr && misaligned16(p)) return WKV7_ERR_ALIGN;
+  if (need > (size_t)WKV7_NOALLOC_SCRATCH_BYTES) return WKV7_ERR_SCRATCH_LIMIT;
+
+  void* scratch = nullptr;
+  if ((st = scratch_address(&scratch))) return st;
+
+  wkv7::BwdArgs p;
+  p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
+  p.bf16 = in_dtype == WKV7_BF16;
+  p.in = {r, w, k, v, a, b};
+  p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
+  p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
+  // every scratch element the kernels read is written earlier in the same call (phase 1
+  // writes each dsa and each chunk-end state gradient before phase 2 reads it): nothing to clear
+  return wkv7::record_cuda_status(wkv7::launch_backward_two_phase(p, scratch, static_cast<cudaStream_t>(stream)));
+}

@@ -138,6 +138,18 @@ def test_backward_rejects_small_or_misaligned_workspace():
     assert bwd(ws=P(0x100000 + 128), ws_bytes=need) == 3
 
 
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    # 7B-width slice B2 T4096 H64 needs ~400 MB of scratch: refused before anything is launched
+    need = wkv7.backward_workspace_size(2, 4096, 64, 64, 32)
+    assert need > 64 * 1024 * 1024
+    p = list(ALIGNED[:18])
+    assert wkv7.lib.wkv7_backward_noalloc(2, 4096, 64, 64, 32, 1, *p, None) == 8
+    assert b"WKV7_NOALLOC_SCRATCH_BYTES" in wkv7.lib.wkv7_strerror(8)
+    # sa is required
+    p[8] = None
+    assert wkv7.lib.wkv7_backward_noalloc(2, 64, 3, 64, 32, 1, *p, None) == 1
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     x = torch.zeros(1, 32, 1, 64)
