@@ -232,4 +232,49 @@ __device__ __forceinline__ void dot4x4(const float2 (&S)[4][2], float4 c, float 
   }
 }
 
+// The same for R rows (R = 2 or 4)
+template <int R>
+__device__ __forceinline__ void dot_rows(const float2 (&S)[R][2], float4 c, float (&out)[R]) {
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const float2 p2 = __ffma2_rn(S[i][1], hi2(c), __fmul2_rn(S[i][0], lo2(c)));
+    out[i] = p2.x + p2.y;
+  }
+}
+
+// ---- row sums over the 16 lanes of a row group for R rows per lane (R = 2 or 4).
+// rs16<R>: reduce-scatter (halving levels, then a plain butterfly); lane l16 ends with the
+// full sum of row rs16_row<R>(l16); for R = 4 this is reduce_scatter4 / rs_row exactly.
+// Every lane with l16 % (16/R) == 0 holds a distinct row.
+template <int R>
+__device__ __forceinline__ int rs16_row(int l16) {
+  return R == 4 ? rs_row(l16) : ((l16 >> 3) & 1);
+}
+
+template <int R>
+__device__ __forceinline__ float rs16(const float (&x)[R], int l16) {
+  static_assert(R == 2 || R == 4, "2 or 4 rows");
+  if constexpr (R == 4) {
+    return reduce_scatter4(x, l16);
+  } else {
+    const bool b3 = (l16 & 8) != 0;
+    float k = b3 ? x[1] : x[0];
+    const float s = b3 ? x[0] : x[1];
+    k += __shfl_xor_sync(0xffffffffu, s, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 1);
+    return k;
+  }
+}
+
+// all-reduce of R rows over 16 lanes, 4 dependent levels (R = 4: butterfly4 exactly)
+template <int R>
+__device__ __forceinline__ void butterfly16(float (&x)[R]) {
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1)
+#pragma unroll
+    for (int i = 0; i < R; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], m);
+}
+
 }  // namespace wkv7

@@ -6,10 +6,10 @@
 // with a copy of S written after every `chunk` tokens.
 //
 // Mapping.  Rows of a head never interact in the forward, so a head is split into
-// 64/ROWS row blocks, one CTA each.  Thread = 4 rows x 4 columns of the state, in
+// 64/ROWS row blocks, one CTA each.  Thread = RPT rows x 4 columns of the state, in
 // registers for the whole sequence; the 16 lanes of a row group own column blocks 4g
 // (g = lane % 16), so a half-warp reads one contiguous 256-byte row of each per-token
-// vector without bank conflicts, and every value a lane loads feeds four rows.  (A
+// vector without bank conflicts, and every value a lane loads feeds RPT rows.  (A
 // 128-bit shared load whose lanes hit distinct addresses costs 4 wavefronts; loads
 // feeding one row per lane made the shared-memory pipe the limit.)
 //
@@ -20,7 +20,7 @@
 // parallel with token t's update.  c_t = w_t o a_{t+1} and the scalars k_t . a_{t+1},
 // b_t . a_{t+1} do not depend on the state; they are formed once per CTA per tile.
 // That row sum is a 4-level butterfly (shortest dependent chain); y, off the chain,
-// uses the cheaper 5-shuffle reduce-scatter.
+// uses the cheaper reduce-scatter.
 //
 // Staging.  Tiles of 32 tokens of w, k, a, b, r (+ one token of a ahead) and the CTA's
 // slice of v are copied to shared memory with cp.async, double-buffered so the copy of
@@ -80,19 +80,20 @@ __device__ __forceinline__ void issue_tile(Tin* raw, int t0, int nt, int na, siz
   }
 }
 
-template <typename Tin, int ROWS>
-__global__ void __launch_bounds__(ROWS * 4, 1)
+template <typename Tin, int ROWS, int RPT>
+__global__ void __launch_bounds__(ROWS * 16 / RPT, 1)
 fwd_kernel(int T, int H, int chunk, int nchunks,
            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
            const float* __restrict__ h0, float* __restrict__ y, float* __restrict__ h_ckpt,
            float* __restrict__ hT, float* __restrict__ sa_out) {
-  constexpr int NT = ROWS * 4;
+  constexpr int NT = ROWS * 16 / RPT;
   constexpr int NW = NT / 32;
   constexpr int NRB = kD / ROWS;
   using Lay = FwdLayout<Tin, ROWS>;
+  static_assert(RPT == 2 || RPT == 4, "2 or 4 rows per thread");
   static_assert(ROWS * (int)sizeof(Tin) % 16 == 0, "v slice must be whole 16-byte pieces");
-  static_assert(ROWS % 8 == 0, "a warp holds 8 rows");
+  static_assert(ROWS % (2 * RPT) == 0, "a warp holds two row groups");
 
   extern __shared__ float4 smem4[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
@@ -117,27 +118,27 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int l16 = tid & 15;
-  const int rloc = 4 * (tid >> 4);    // first local row of this thread
+  const int rloc = RPT * (tid >> 4);  // first local row of this thread
   const int row0 = rb * ROWS + rloc;  // first row within the head
   const int j0 = 4 * l16;             // first column
-  const int qrow = rs_row(l16);       // row whose y this lane ends up holding
+  const int qrow = rs16_row<RPT>(l16);  // row whose y this lane ends up holding
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
   const size_t sbase = (size_t)bh * kD * kD;
   const int ntiles = (T + kTile - 1) / kTile;
 
   // state: S[i] = row row0+i, columns j0..j0+3 as two float2
-  float2 S[4][2];
+  float2 S[RPT][2];
   if (h0 != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RPT; ++i) {
       const float4 x = __ldg(reinterpret_cast<const float4*>(h0 + sbase + (size_t)(row0 + i) * kD + j0));
       S[i][0] = lo2(x);
       S[i][1] = hi2(x);
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[i][0] = S[i][1] = make_float2(0.f, 0.f);
+    for (int i = 0; i < RPT; ++i) S[i][0] = S[i][1] = make_float2(0.f, 0.f);
   }
 
   if (ntiles > 0) {
@@ -146,10 +147,12 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
   }
 
   // sa for token 0 (the state before it is h0)
-  float sa[4] = {0.f, 0.f, 0.f, 0.f};
+  float sa[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) sa[i] = 0.f;
   if (T > 0) {
-    dot4x4(S, load4(a + base + j0), sa);
-    butterfly4(sa);
+    dot_rows<RPT>(S, load4(a + base + j0), sa);
+    butterfly16<RPT>(sa);
   }
 
   int to_ckpt = chunk;
@@ -227,20 +230,27 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
       const float4 k4 = *reinterpret_cast<const float4*>(fK + tt * kD + j0);
       const float4 b4 = *reinterpret_cast<const float4*>(fB + tt * kD + j0);
       const float4 r4 = *reinterpret_cast<const float4*>(fR + tt * kD + j0);
-      const float4 v4 = *reinterpret_cast<const float4*>(fV + tt * ROWS + rloc);
       const float ka = fKA[tt], ba = fBA[tt];
-      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-      if (sa_out != nullptr && l16 == 0)
-        *reinterpret_cast<float4*>(fSA + tt * ROWS + rloc) = make_float4(sa[0], sa[1], sa[2], sa[3]);
+      float vv[RPT];
+      if constexpr (RPT == 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(fV + tt * ROWS + rloc);
+        vv[0] = v4.x, vv[1] = v4.y, vv[2] = v4.z, vv[3] = v4.w;
+        if (sa_out != nullptr && l16 == 0)
+          *reinterpret_cast<float4*>(fSA + tt * ROWS + rloc) = make_float4(sa[0], sa[1], sa[2], sa[3]);
+      } else {
+        const float2 v2 = *reinterpret_cast<const float2*>(fV + tt * ROWS + rloc);
+        vv[0] = v2.x, vv[1] = v2.y;
+        if (sa_out != nullptr && l16 == 0) *reinterpret_cast<float2*>(fSA + tt * ROWS + rloc) = make_float2(sa[0], sa[1]);
+      }
 
       // lookahead row sums on the state before this token
-      float P[4];
-      dot4x4(S, c4, P);
-      butterfly4(P);
+      float P[RPT];
+      dot_rows<RPT>(S, c4, P);
+      butterfly16<RPT>(P);
 
       // S <- S w + v k + sa b
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < RPT; ++i) {
         const float2 s2 = make_float2(sa[i], sa[i]);
         const float2 v2 = make_float2(vv[i], vv[i]);
         const float2 u0 = __ffma2_rn(v2, lo2(k4), __fmul2_rn(s2, lo2(b4)));
@@ -249,12 +259,12 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
         S[i][1] = __ffma2_rn(S[i][1], hi2(w4), u1);
       }
       // y = S r
-      float yp[4];
-      dot4x4(S, r4, yp);
-      const float yq = reduce_scatter4(yp, l16);
-      if ((l16 & 3) == 0) fY[tt * ROWS + rloc + qrow] = yq;
+      float yp[RPT];
+      dot_rows<RPT>(S, r4, yp);
+      const float yq = rs16<RPT>(yp, l16);
+      if ((l16 & (16 / RPT - 1)) == 0) fY[tt * ROWS + rloc + qrow] = yq;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sa[i] = fmaf(sa[i], ba, fmaf(vv[i], ka, P[i]));
+      for (int i = 0; i < RPT; ++i) sa[i] = fmaf(sa[i], ba, fmaf(vv[i], ka, P[i]));
 
       const int t = t0 + tt;
       if (--to_ckpt == 0 || t == T - 1) {
@@ -262,7 +272,7 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
         if (h_ckpt != nullptr) {
           float* dst = h_ckpt + ((size_t)bh * nchunks + t / chunk) * kD * kD + (size_t)row0 * kD + j0;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < RPT; ++i)
             *reinterpret_cast<float4*>(dst + i * kD) = make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
         }
       }
@@ -278,17 +288,17 @@ fwd_kernel(int T, int H, int chunk, int nchunks,
 
   if (hT != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < RPT; ++i)
       *reinterpret_cast<float4*>(hT + sbase + (size_t)(row0 + i) * kD + j0) =
           make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
   }
 }
 
-template <typename Tin, int ROWS>
+template <typename Tin, int ROWS, int RPT>
 cudaError_t launch_fwd_cfg(const FwdArgs& p, cudaStream_t stream) {
-  constexpr int NT = ROWS * 4;
+  constexpr int NT = ROWS * 16 / RPT;
   const size_t smem = FwdLayout<Tin, ROWS>::kBytes;
-  auto kern = fwd_kernel<Tin, ROWS>;
+  auto kern = fwd_kernel<Tin, ROWS, RPT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)p.B * p.H * (kD / ROWS);
@@ -300,8 +310,17 @@ cudaError_t launch_fwd_cfg(const FwdArgs& p, cudaStream_t stream) {
 
 }  // namespace
 
+template <typename Tin>
+cudaError_t launch_fwd_t(const FwdArgs& p, cudaStream_t stream) {
+  // Measured at 32 rows per CTA: when every row block has an SM of its own, 2 rows per thread (8 warps)
+  // beat 4 rows per thread (4 warps) by 4-5%; past one wave the smaller per-thread tile loses (13%
+  // slower at 256 row blocks), its extra shuffles and loads no longer hidden.
+  if ((long long)p.B * p.H * (kD / 32) <= num_sms()) return launch_fwd_cfg<Tin, 32, 2>(p, stream);
+  return launch_fwd_cfg<Tin, 32, 4>(p, stream);
+}
+
 cudaError_t launch_forward(const FwdArgs& p, cudaStream_t stream) {
-  return p.bf16 ? launch_fwd_cfg<__nv_bfloat16, 32>(p, stream) : launch_fwd_cfg<float, 32>(p, stream);
+  return p.bf16 ? launch_fwd_t<__nv_bfloat16>(p, stream) : launch_fwd_t<float>(p, stream);
 }
 
 }  // namespace wkv7
