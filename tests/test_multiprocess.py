@@ -82,3 +82,32 @@ def test_reference_arm_decode_workload_is_unavailable():
         bench.run_reference(A, rank=0, world=1)
     line = json.loads(buf.getvalue())
     assert line["impl"] == "reference" and "unavailable" in line
+
+
+def test_reference_arm_runs_the_oracle_over_a_process_pool():
+    """The reference arm on the small oracle workload: one JSON line, value > 0, cores = pool size."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        workload = "oracle_b1_t128_h2"
+        steps = 1
+        warmup = 1
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(A, rank=0, world=1)
+    line = json.loads(buf.getvalue())
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["cores"] == min(os.cpu_count() or 1, 2)
+    assert line["e2e"]["value"] == line["value"]
+
+
+def test_cpu_baseline_reports_pool_and_single_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+    import wkv7_inputs as gen
+
+    cb = bench.cpu_baseline(gen.WORKLOADS["oracle_b1_t128_h2"], 0.2)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
