@@ -86,6 +86,19 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const float *h0, float *y, float *h_ckpt, float *hT, float *sa, void *stream);
 
 /*
+ * The same forward, arguments and results as wkv7_forward, always advanced token by token.
+ * wkv7_forward advances 16 tokens at a time in the closed form of the recurrence over those
+ * tokens (dense products on tensor cores, agreeing with this one to ~1e-7 relative at the
+ * training shapes) when chunk is a multiple of 16 and B*H*2 row blocks fit one wave of SMs, and
+ * runs this one otherwise.  Kept callable for comparison and as the plain per-token path.
+ */
+int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
+                            const void *r, const void *w, const void *k,
+                            const void *v, const void *a, const void *b,
+                            const float *h0, float *y, float *h_ckpt, float *hT, float *sa,
+                            void *stream);
+
+/*
  * Checkpointed backward (vector-Jacobian product of wkv7_forward).
  *   h0      the forward's initial state, or NULL for zeros.
  *   h_ckpt  the forward's checkpoints (B,H,C,D,D), required when T > 0; the same

@@ -30,6 +30,7 @@ _I = ctypes.c_int
 SIGNATURES = {
     "wkv7_num_chunks": (_I, [_I, _I]),
     "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
+    "wkv7_forward_sequential": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
     "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
     "wkv7_backward_noalloc": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
@@ -130,15 +131,19 @@ def _check_f32(t, shape, name, where, dev):
 
 
 def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True, final_state: bool = True,
-            save_sa: bool = False, out=None, stream=None):
+            save_sa: bool = False, out=None, stream=None, kernel: str = "auto"):
     """WKV7 forward.  r..b: (B, T, H, 64) float32/bfloat16 CUDA tensors; h0: (B, H, 64, 64) float32 or None.
 
     Returns (y, h_ckpt, hT): y (B,T,H,64) fp32; h_ckpt (B,H,C,64,64) fp32 (None when
     checkpoints=False); hT (B,H,64,64) fp32 (None when final_state=False).  With
     save_sa=True a fourth tensor sa (B,T,H,64) fp32 is returned (sa_t = S_{t-1} a_t per
     state row), which `backward` accepts to skip its recompute.  `out` may give
-    preallocated (y, h_ckpt, hT) or (y, h_ckpt, hT, sa).
+    preallocated (y, h_ckpt, hT) or (y, h_ckpt, hT, sa).  kernel="auto" is `wkv7_forward`
+    (16-token sub-chunks when chunk % 16 == 0 and the B*H*2 row blocks fit one wave of SMs);
+    "sequential" is `wkv7_forward_sequential`.
     """
+    if kernel not in ("auto", "sequential"):
+        raise ValueError(f"wkv7.forward: kernel must be 'auto' or 'sequential', got {kernel!r}")
     torch = _torch()
     B, T, H, D = r.shape
     _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.forward")
@@ -157,9 +162,9 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
     _check_f32(ck, (B, H, C, D, D), "h_ckpt", "wkv7.forward", dev)
     _check_f32(hT, (B, H, D, D), "hT", "wkv7.forward", dev)
     _check_f32(sa, (B, T, H, D), "sa", "wkv7.forward", dev)
-    st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)),
-                          _stream(stream))
-    _check(st, "wkv7_forward")
+    fn = lib.wkv7_forward if kernel == "auto" else lib.wkv7_forward_sequential
+    st = fn(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)), _stream(stream))
+    _check(st, "wkv7_forward" if kernel == "auto" else "wkv7_forward_sequential")
     if save_sa or (out is not None and len(out) > 3):
         return y, ck, hT, sa
     return y, ck, hT

@@ -100,9 +100,10 @@ const char* wkv7_strerror(int status) {
 
 const char* wkv7_last_cuda_error(void) { return g_last_cuda_error; }
 
-int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
-                 const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
-                 float* h_ckpt, float* hT, float* sa, void* stream) {
+namespace {
+int forward_impl(bool sequential, int B, int T, int H, int D, int chunk, int in_dtype, const void* r,
+                 const void* w, const void* k, const void* v, const void* a, const void* b, const float* h0,
+                 float* y, float* h_ckpt, float* hT, float* sa, void* stream) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
@@ -116,7 +117,21 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void
   p.bf16 = in_dtype == WKV7_BF16;
   p.in = {r, w, k, v, a, b};
   p.h0 = h0; p.y = y; p.h_ckpt = h_ckpt; p.hT = hT; p.sa = T > 0 ? sa : nullptr;
-  return record_cuda(wkv7::launch_forward(p, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  return record_cuda(sequential ? wkv7::launch_forward_sequential(p, st_) : wkv7::launch_forward(p, st_));
+}
+}  // namespace
+
+int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                 const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
+                 float* h_ckpt, float* hT, float* sa, void* stream) {
+  return forward_impl(false, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, stream);
+}
+
+int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                            const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
+                            float* h_ckpt, float* hT, float* sa, void* stream) {
+  return forward_impl(true, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, stream);
 }
 
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,

@@ -1,0 +1,736 @@
+// WKV7 forward on sm_103a in sub-chunks of 16 tokens, the dense contractions on tensor cores.
+//
+// Recurrence ("RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel
+// architecture", Forward listing), per head, state S (rows i = value, columns j = key):
+//     sa_t = S_{t-1} a_t;   S_t = S_{t-1} diag(w_t) + v_t k_t^T + sa_t b_t^T;   y_t = S_t r_t
+// with S written out after every `chunk` tokens.
+//
+// Sub-chunk form (exact in real arithmetic).  Over 16 tokens t = 0..15 starting from S, with
+// gamma_t = w_0 o .. o w_t (per column) and gamma_L = gamma_15:
+//     A^_t = a_t o gamma_{t-1},  R^_t = r_t o gamma_t,  K~_s = k_s / gamma_s,  B~_s = b_s / gamma_s,
+//     K-_s = k_s o gamma_L / gamma_s,  B-_s = b_s o gamma_L / gamma_s
+//     M_ab = tril(A^ B~^T, -1), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T), M_rk = tril(R^ K~^T)
+//     SA = (I - M_ab)^-1 (A^ S^T + M_ak V)                  (rows t: sa_t)
+//     Y  = R^ S^T + M_rk V + M_rb SA                         (rows t: y_t)
+//     S' = S diag(gamma_L) + V^T K- + SA^T B-
+// Unrolling S_t over the sub-chunk gives these directly: sa_t and y_t are dots of the start state
+// with decayed a_t / r_t plus the sub-chunk's own rank-one terms, coupled through sa by the unit
+// lower-triangular system (I - M_ab).  The serial chain is one sub-chunk step per 16 tokens.
+//
+// Precision.  Products of fp32 operands on the tensor cores use three TF32 passes (x = hi + lo,
+// hi lo + lo hi + hi hi), fp32 accumulation: ~1e-7 relative against the fp64 recurrence at the
+// training shapes (one TF32 pass gives ~3e-4).  (I - M_ab)^-1, M_ak / M_rk times V and the decay
+// factors are plain fp32.  1/gamma grows like (1/w)^16; a sub-chunk whose gamma_L falls below
+// 1e-30 in some column is instead advanced token by token (exact, slow), so any w in (0, 1] is
+// handled.
+//
+// Mapping: one CTA per (head, 32-row block), 12 warps.  Warps 0-1 hold the CTA's 32 x 64 slice of
+// S as mma.sync m16n8k8 accumulator tiles (warp m = rows 16m..16m+15) and run the chain; warps 2-11
+// prepare the next sub-chunk (decays, the four 16x16 coupling matrices and U = V^T K- on tensor
+// cores, (I - M_ab)^-1 by 4x4 / 8x8 blocks, the fp32 corrections) one sub-chunk ahead, and write
+// the previous sub-chunk's y and sa.  One CTA barrier per sub-chunk.  An accumulator tile is
+// reused directly as the A operand of the next product by permuting the contraction index inside
+// each 8-block (logical k = q <-> column 2q, k = q + 4 <-> column 2q + 1); the B operands are
+// stored in shared memory already split into hi/lo and paired to match.
+#include "wkv7_device.cuh"
+#include "wkv7_launch.h"
+
+namespace wkv7 {
+namespace {
+
+constexpr int kL = 16;     // tokens per sub-chunk
+constexpr int kR = 32;     // state rows per CTA
+constexpr int kNT = 384;   // threads per CTA
+constexpr int kNP = 320;   // preparing threads (warps 2-11)
+constexpr int kChainThreads = 64;
+
+// padded row strides: 16-byte (hi0, hi1, lo0, lo1) words for the split pair arrays, floats otherwise
+constexpr int kSP = 36;    // [16][32 pairs] (+4): A^, R^, K~, B~
+constexpr int kSM = 12;    // [16][8 pairs] (+4): (I - M_ab)^-1, M_rb
+constexpr int kSJ = 66;    // [8 token pairs][64] (+2): K-, B-
+constexpr int kSV = 34;    // [8 token pairs][32] (+2): V
+constexpr int kSC = 24;    // [32][16] fp32 (+8): the V corrections of sa and y
+constexpr int kSU = 72;    // [32][64] fp32 (+8): U = V^T K-, and the state in the token-by-token path
+constexpr int kSO = 36;    // [16][32] fp32 (+4): y / sa staging
+constexpr float kMinDecay = 1e-30f;
+
+template <typename Tin>
+struct Lay {
+  // raw input stage (x2): w, k, a, b, r [kL][64], v [kL][32]
+  static constexpr size_t kRaw = ((5 * kL * kD + kL * kR) * sizeof(Tin) + 15) / 16 * 16;
+  static constexpr size_t oRaw = 0;
+  // chain buffer (x2): what the chain reads for one sub-chunk
+  static constexpr size_t cAH = 0;                          // uint4 [16][kSP]
+  static constexpr size_t cRH = cAH + 16 * kSP * 16;
+  static constexpr size_t cTI = cRH + 16 * kSP * 16;        // uint4 [16][kSM]
+  static constexpr size_t cMRB = cTI + 16 * kSM * 16;
+  static constexpr size_t cCAK = cMRB + 16 * kSM * 16;      // float [32][kSC]: V^T M_ak^T
+  static constexpr size_t cCY = cCAK + 32 * kSC * 4;        // float [32][kSC]: V^T M_rk^T
+  static constexpr size_t cU = cCY + 32 * kSC * 4;          // float [32][kSU]
+  static constexpr size_t cBB = cU + 32 * kSU * 4;          // uint4 [8][kSJ]
+  static constexpr size_t cGL = cBB + 8 * kSJ * 16;         // float [64]
+  static constexpr size_t cMeta = cGL + 64 * 4;             // int [4]: token-by-token flag, tokens
+  static constexpr size_t kChain = cMeta + 16;
+  // in the token-by-token path the same buffer holds the fp32 inputs: w k a b r [16][64], v [16][32]
+  static constexpr size_t cFW = 0;
+  static constexpr size_t kFallbackInputs = (5 * kL * kD + kL * kR) * 4;
+  static_assert(kFallbackInputs <= cCAK, "token-by-token inputs fit below the corrections");
+  static constexpr size_t oChain = oRaw + 2 * kRaw;
+  // preparation scratch
+  static constexpr size_t oG = oChain + 2 * kChain;          // float [16][64] gamma
+  static constexpr size_t oKT = oG + kL * kD * 4;            // uint4 [16][kSP]
+  static constexpr size_t oBT = oKT + 16 * kSP * 16;
+  static constexpr size_t oKB = oBT + 16 * kSP * 16;         // uint4 [8][kSJ]
+  static constexpr size_t oVP = oKB + 8 * kSJ * 16;          // uint4 [8][kSV]
+  static constexpr size_t oMAK = oVP + 8 * kSV * 16;         // uint4 [16][kSM] each: M_ak, M_rk split
+  static constexpr size_t oMRK = oMAK + 16 * kSM * 16;
+  static constexpr size_t oMAB = oMRK + 16 * kSM * 16;       // float [16][16]: M_ab, (I - M_ab)^-1, temp
+  static constexpr size_t oTI = oMAB + 1024;
+  static constexpr size_t oTMP = oTI + 1024;
+  // output staging (x2): y, sa [16][kSO]
+  static constexpr size_t oOut = oTMP + 1024;
+  static constexpr size_t kOut = 2 * kL * kSO * 4;
+  // state of the token-by-token path: float [32][kSU]
+  static constexpr size_t oFS = oOut + 2 * kOut;
+  static constexpr size_t kBytes = oFS + kR * kSU * 4;
+};
+
+// ---------------------------------------------------------------- tensor-core helpers
+
+// x = hi + lo, hi = x rounded to the nearest TF32 value (ties away from zero: adding half a TF32
+// unit to the magnitude bits, then dropping the low 13), lo = x - hi exactly, |lo| <= 2^-11 |x|;
+// the tensor core reads lo's top 19 bits.  Relative error ~2^-22 per product in three passes.
+// (Finite x below 2^127 only -- every operand here is.)
+__device__ __forceinline__ void split(float x, uint32_t& hi, uint32_t& lo) {
+  hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+
+// (hi x0, hi x1, lo x0, lo x1)
+__device__ __forceinline__ uint4 split_pair(float x0, float x1) {
+  uint4 q;
+  split(x0, q.x, q.z);
+  split(x1, q.y, q.w);
+  return q;
+}
+
+struct FragA {
+  uint32_t h[4], l[4];
+};
+struct FragB {
+  uint32_t h[2], l[2];
+};
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += A B in three TF32 passes, the small terms first
+__device__ __forceinline__ void mma3(float (&d)[4], const FragA& a, const FragB& b) {
+  mma_tf32(d, a.l, b.h[0], b.h[1]);
+  mma_tf32(d, a.h, b.l[0], b.l[1]);
+  mma_tf32(d, a.h, b.h[0], b.h[1]);
+}
+
+// An accumulator tile (rows g, g+8; columns 2q, 2q+1 of an 8-block) as the A operand of a product
+// contracting over those columns, with k = q <-> column 2q and k = q + 4 <-> column 2q + 1.
+__device__ __forceinline__ FragA frag_from_acc(const float (&c)[4]) {
+  FragA a;
+  split(c[0], a.h[0], a.l[0]);
+  split(c[2], a.h[1], a.l[1]);
+  split(c[1], a.h[2], a.l[2]);
+  split(c[3], a.h[3], a.l[3]);
+  return a;
+}
+
+// A operand from split pairs: row g -> (a0, a2), row g + 8 -> (a1, a3)
+__device__ __forceinline__ FragA frag_a(uint4 r0, uint4 r8) {
+  FragA a;
+  a.h[0] = r0.x; a.h[2] = r0.y; a.l[0] = r0.z; a.l[2] = r0.w;
+  a.h[1] = r8.x; a.h[3] = r8.y; a.l[1] = r8.z; a.l[3] = r8.w;
+  return a;
+}
+
+__device__ __forceinline__ FragB frag_b(uint4 q) {
+  FragB b;
+  b.h[0] = q.x; b.h[1] = q.y; b.l[0] = q.z; b.l[1] = q.w;
+  return b;
+}
+
+__device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, %0;\n" ::"n"(kNP) : "memory"); }
+__device__ __forceinline__ void bar_chain() { asm volatile("bar.sync 2, %0;\n" ::"n"(kChainThreads) : "memory"); }
+// preparing warps 1-9
+__device__ __forceinline__ void bar_rest() { asm volatile("bar.sync 3, %0;\n" ::"n"(kNP - 32) : "memory"); }
+
+template <typename Tin>
+__device__ __forceinline__ float raw_at(const Tin* p) {
+  return to_f32(*p);
+}
+
+// two consecutive raw values (the pair starts on an even element)
+__device__ __forceinline__ float2 raw2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 raw2(const __nv_bfloat16* p) {
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(bf16_lo(u), bf16_hi(u));
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <typename Tin>
+__global__ void __launch_bounds__(kNT, 1)
+fwdc_kernel(int T, int H, int chunk, int nchunks,
+            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
+            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
+            const float* __restrict__ h0, float* __restrict__ y, float* __restrict__ h_ckpt,
+            float* __restrict__ hT, float* __restrict__ sa_out) {
+  using LY = Lay<Tin>;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+
+  const int bh = blockIdx.x >> 1;
+  const int rb = blockIdx.x & 1;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const size_t sbase = (size_t)bh * kD * kD;
+  const int nsub = (T + kL - 1) / kL;
+
+  auto raw_buf = [&](int m) { return reinterpret_cast<Tin*>(sm + LY::oRaw + (size_t)(m & 1) * LY::kRaw); };
+  auto chain_buf = [&](int m) { return sm + LY::oChain + (size_t)(m & 1) * LY::kChain; };
+  auto out_y = [&](int m) { return reinterpret_cast<float*>(sm + LY::oOut + (size_t)(m & 1) * LY::kOut); };
+  auto out_sa = [&](int m) { return out_y(m) + kL * kSO; };
+
+  if (warp < 2) {
+    // =========================================================== chain warps
+    const int mi = warp;
+    const int g = lane >> 2, q = lane & 3;
+    const int row = rb * kR + mi * 16 + g;  // rows row and row + 8 of the head
+    float S[8][4];
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj) {
+      if (h0 != nullptr) {
+        const float2 s0 = __ldg(reinterpret_cast<const float2*>(h0 + sbase + (size_t)row * kD + nj * 8 + 2 * q));
+        const float2 s8 = __ldg(reinterpret_cast<const float2*>(h0 + sbase + (size_t)(row + 8) * kD + nj * 8 + 2 * q));
+        S[nj][0] = s0.x; S[nj][1] = s0.y; S[nj][2] = s8.x; S[nj][3] = s8.y;
+      } else {
+        S[nj][0] = S[nj][1] = S[nj][2] = S[nj][3] = 0.f;
+      }
+    }
+    __syncthreads();  // the preparation of sub-chunk 0 is done
+
+    for (int n = 0; n < nsub; ++n) {
+      const unsigned char* cb = chain_buf(n);
+      const int* meta = reinterpret_cast<const int*>(cb + LY::cMeta);
+      const int slow = meta[0];
+      const int nm = meta[1];
+      float* fy = out_y(n);
+      float* fsa = out_sa(n);
+      if (!slow) {
+        const uint4* AH = reinterpret_cast<const uint4*>(cb + LY::cAH);
+        const uint4* RH = reinterpret_cast<const uint4*>(cb + LY::cRH);
+        const uint4* TI = reinterpret_cast<const uint4*>(cb + LY::cTI);
+        const uint4* MRB = reinterpret_cast<const uint4*>(cb + LY::cMRB);
+        const float* CAK = reinterpret_cast<const float*>(cb + LY::cCAK);
+        const float* CY = reinterpret_cast<const float*>(cb + LY::cCY);
+        const float* U = reinterpret_cast<const float*>(cb + LY::cU);
+        const uint4* BB = reinterpret_cast<const uint4*>(cb + LY::cBB);
+        const float* GL = reinterpret_cast<const float*>(cb + LY::cGL);
+        const int i0 = mi * 16 + g;  // local rows i0, i0 + 8
+
+        // P^T = V^T M_ak^T + S A^T and Y^T = V^T M_rk^T + S R^T (rows i, tokens t).  Every tensor-core
+        // product accumulates from zero in two accumulators per tile (the tensor core's own
+        // accumulation does not round to nearest) and is added to the rest with fp32 adds.
+        float P[2][2][4], Y[2][2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) P[nt][0][e] = P[nt][1][e] = Y[nt][0][e] = Y[nt][1][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const FragA as = frag_from_acc(S[kk]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            mma3(P[nt][kk & 1], as, frag_b(AH[(nt * 8 + g) * kSP + kk * 4 + q]));
+            mma3(Y[nt][kk & 1], as, frag_b(RH[(nt * 8 + g) * kSP + kk * 4 + q]));
+          }
+        }
+        float Pt[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 c0 = *reinterpret_cast<const float2*>(CY + i0 * kSC + nt * 8 + 2 * q);
+          const float2 c8 = *reinterpret_cast<const float2*>(CY + (i0 + 8) * kSC + nt * 8 + 2 * q);
+          const float2 d0 = *reinterpret_cast<const float2*>(CAK + i0 * kSC + nt * 8 + 2 * q);
+          const float2 d8 = *reinterpret_cast<const float2*>(CAK + (i0 + 8) * kSC + nt * 8 + 2 * q);
+          const float cy[4] = {c0.x, c0.y, c8.x, c8.y}, cak[4] = {d0.x, d0.y, d8.x, d8.y};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            Pt[nt][e] = (P[nt][0][e] + P[nt][1][e]) + cak[e];
+            Y[nt][0][e] = (Y[nt][0][e] + Y[nt][1][e]) + cy[e];
+          }
+        }
+
+        // SA^T = P^T (I - M_ab)^-T
+        float SA[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) SA[nt][0] = SA[nt][1] = SA[nt][2] = SA[nt][3] = 0.f;
+        {
+          const FragA p0 = frag_from_acc(Pt[0]);
+          const FragA p1 = frag_from_acc(Pt[1]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            mma3(SA[nt], p0, frag_b(TI[(nt * 8 + g) * kSM + q]));
+            mma3(SA[nt], p1, frag_b(TI[(nt * 8 + g) * kSM + 4 + q]));
+          }
+        }
+        const FragA s0 = frag_from_acc(SA[0]);
+        const FragA s1 = frag_from_acc(SA[1]);
+        // Y^T += SA^T M_rb^T
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float yb[4] = {0.f, 0.f, 0.f, 0.f};
+          mma3(yb, s0, frag_b(MRB[(nt * 8 + g) * kSM + q]));
+          mma3(yb, s1, frag_b(MRB[(nt * 8 + g) * kSM + 4 + q]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) Y[nt][0][e] += yb[e];
+        }
+        // stage y and sa as [t][i]
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int t0 = nt * 8 + 2 * q;
+          fy[t0 * kSO + i0] = Y[nt][0][0];
+          fy[(t0 + 1) * kSO + i0] = Y[nt][0][1];
+          fy[t0 * kSO + i0 + 8] = Y[nt][0][2];
+          fy[(t0 + 1) * kSO + i0 + 8] = Y[nt][0][3];
+          fsa[t0 * kSO + i0] = SA[nt][0];
+          fsa[(t0 + 1) * kSO + i0] = SA[nt][1];
+          fsa[t0 * kSO + i0 + 8] = SA[nt][2];
+          fsa[(t0 + 1) * kSO + i0 + 8] = SA[nt][3];
+        }
+        // S <- S diag(gamma_L) + U + SA^T B-
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj) {
+          const float2 gl = *reinterpret_cast<const float2*>(GL + nj * 8 + 2 * q);
+          const float2 u0 = *reinterpret_cast<const float2*>(U + i0 * kSU + nj * 8 + 2 * q);
+          const float2 u8 = *reinterpret_cast<const float2*>(U + (i0 + 8) * kSU + nj * 8 + 2 * q);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma3(d, s0, frag_b(BB[q * kSJ + nj * 8 + g]));
+          mma3(d, s1, frag_b(BB[(4 + q) * kSJ + nj * 8 + g]));
+          S[nj][0] = fmaf(S[nj][0], gl.x, u0.x + d[0]);
+          S[nj][1] = fmaf(S[nj][1], gl.y, u0.y + d[1]);
+          S[nj][2] = fmaf(S[nj][2], gl.x, u8.x + d[2]);
+          S[nj][3] = fmaf(S[nj][3], gl.y, u8.y + d[3]);
+        }
+      } else {
+        // ---- token by token (decay too strong for the sub-chunk form)
+        float* FS = reinterpret_cast<float*>(sm + LY::oFS);
+        const float* FW = reinterpret_cast<const float*>(cb + LY::cFW);
+        const float* FK = FW + kL * kD;
+        const float* FA = FK + kL * kD;
+        const float* FB = FA + kL * kD;
+        const float* FR = FB + kL * kD;
+        const float* FV = FR + kL * kD;
+        const int i0 = mi * 16 + g;
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj) {
+          *reinterpret_cast<float2*>(FS + i0 * kSU + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
+          *reinterpret_cast<float2*>(FS + (i0 + 8) * kSU + nj * 8 + 2 * q) = make_float2(S[nj][2], S[nj][3]);
+        }
+        bar_chain();
+        const int ti = tid >> 1, half = tid & 1, c0 = 32 * half;
+        float Sr[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) Sr[c] = FS[ti * kSU + c0 + c];
+        for (int t = 0; t < nm; ++t) {
+          float s = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s = fmaf(Sr[c], FA[t * kD + c0 + c], s);
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          const float vi = FV[t * kR + ti];
+          float yy = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            Sr[c] = fmaf(Sr[c], FW[t * kD + c0 + c], fmaf(vi, FK[t * kD + c0 + c], s * FB[t * kD + c0 + c]));
+            yy = fmaf(Sr[c], FR[t * kD + c0 + c], yy);
+          }
+          yy += __shfl_xor_sync(0xffffffffu, yy, 1);
+          if (half == 0) {
+            fy[t * kSO + ti] = yy;
+            fsa[t * kSO + ti] = s;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) FS[ti * kSU + c0 + c] = Sr[c];
+        bar_chain();
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj) {
+          const float2 s0 = *reinterpret_cast<const float2*>(FS + i0 * kSU + nj * 8 + 2 * q);
+          const float2 s8 = *reinterpret_cast<const float2*>(FS + (i0 + 8) * kSU + nj * 8 + 2 * q);
+          S[nj][0] = s0.x; S[nj][1] = s0.y; S[nj][2] = s8.x; S[nj][3] = s8.y;
+        }
+        bar_chain();  // FS is free for the next sub-chunk
+      }
+
+      // y and sa of this sub-chunk to global memory (both chain warps have staged theirs)
+      bar_chain();
+      for (int e = tid; e < nm * kR; e += kChainThreads) {
+        const int t = e >> 5, i = e & 31;
+        const size_t o = base + (size_t)(n * kL + t) * tstride + rb * kR + i;
+        y[o] = fy[t * kSO + i];
+        if (sa_out != nullptr) sa_out[o] = fsa[t * kSO + i];
+      }
+
+      // checkpoint after the sub-chunk's last token when it ends a chunk (or the sequence)
+      const int tlast = n * kL + nm - 1;
+      if (h_ckpt != nullptr && ((tlast + 1) % chunk == 0 || tlast == T - 1)) {
+        float* dst = h_ckpt + ((size_t)bh * nchunks + tlast / chunk) * kD * kD;
+#pragma unroll
+        for (int nj = 0; nj < 8; ++nj) {
+          *reinterpret_cast<float2*>(dst + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
+          *reinterpret_cast<float2*>(dst + (size_t)(row + 8) * kD + nj * 8 + 2 * q) = make_float2(S[nj][2], S[nj][3]);
+        }
+      }
+      __syncthreads();  // end of period n
+    }
+    if (hT != nullptr) {
+#pragma unroll
+      for (int nj = 0; nj < 8; ++nj) {
+        *reinterpret_cast<float2*>(hT + sbase + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
+        *reinterpret_cast<float2*>(hT + sbase + (size_t)(row + 8) * kD + nj * 8 + 2 * q) =
+            make_float2(S[nj][2], S[nj][3]);
+      }
+    }
+    return;
+  }
+
+  // ============================================================= preparing warps
+  const int pt = tid - kChainThreads;  // 0 .. 319
+  const int pw = pt >> 5;              // 0 .. 9
+  const int g = lane >> 2, q = lane & 3;
+  float* G = reinterpret_cast<float*>(sm + LY::oG);
+  uint4* KT = reinterpret_cast<uint4*>(sm + LY::oKT);
+  uint4* BT = reinterpret_cast<uint4*>(sm + LY::oBT);
+  uint4* KB = reinterpret_cast<uint4*>(sm + LY::oKB);
+  uint4* VP = reinterpret_cast<uint4*>(sm + LY::oVP);
+  uint4* MAK = reinterpret_cast<uint4*>(sm + LY::oMAK);
+  uint4* MRK = reinterpret_cast<uint4*>(sm + LY::oMRK);
+  float* MAB = reinterpret_cast<float*>(sm + LY::oMAB);
+  float* TIf = reinterpret_cast<float*>(sm + LY::oTI);
+  float* TMP = reinterpret_cast<float*>(sm + LY::oTMP);
+
+  // cp.async copies of sub-chunk m's inputs (tokens beyond T are not copied; they read as padding)
+  auto issue = [&](int m) {
+    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    constexpr int VPR = kR * (int)sizeof(Tin) / 16;
+    Tin* dst = raw_buf(m);
+    const int t0 = m * kL;
+    const int nm = min(kL, T - t0);
+    const Tin* srcs[5] = {w, k, a, b, r};
+#pragma unroll
+    for (int s = 0; s < 5; ++s)
+      for (int e = pt; e < nm * CPR; e += kNP) {
+        const int t = e / CPR, pc = e % CPR;
+        cp_async16(dst + (s * kL + t) * kD + pc * EPC, srcs[s] + base + (size_t)(t0 + t) * tstride + pc * EPC);
+      }
+    for (int e = pt; e < nm * VPR; e += kNP) {
+      const int t = e / VPR, pc = e % VPR;
+      cp_async16(dst + 5 * kL * kD + t * kR + pc * EPC, v + base + (size_t)(t0 + t) * tstride + rb * kR + pc * EPC);
+    }
+    cp_async_commit();
+  };
+
+  // everything the chain needs for sub-chunk m, into chain buffer m & 1 (its raw inputs have landed)
+  auto prepare = [&](int m) {
+    const Tin* raw = raw_buf(m);
+    const Tin* rw = raw;
+    const Tin* rk = raw + kL * kD;
+    const Tin* ra = raw + 2 * kL * kD;
+    const Tin* rbv = raw + 3 * kL * kD;
+    const Tin* rr = raw + 4 * kL * kD;
+    const Tin* rv = raw + 5 * kL * kD;
+    unsigned char* cb = chain_buf(m);
+    int* meta = reinterpret_cast<int*>(cb + LY::cMeta);
+    const int nm = min(kL, T - m * kL);
+
+    // ---- P0: gamma_t = w_0 o .. o w_t down each column; V split in token pairs
+    if (pt < kD) {
+      const int j = pt;
+      float wv[kL];
+#pragma unroll
+      for (int t = 0; t < kL; ++t) wv[t] = t < nm ? raw_at(rw + t * kD + j) : 1.f;
+      float gm = 1.f;
+#pragma unroll
+      for (int t = 0; t < kL; ++t) {
+        gm *= wv[t];
+        G[t * kD + j] = gm;
+      }
+      if (pt == 0) {
+        meta[0] = 0;
+        meta[1] = nm;
+      }
+    } else {
+      for (int e = pt - kD; e < (kL / 2) * kR; e += kNP - kD) {
+        const int tp = e >> 5, i = e & 31;
+        const float v0 = 2 * tp < nm ? raw_at(rv + 2 * tp * kR + i) : 0.f;
+        const float v1 = 2 * tp + 1 < nm ? raw_at(rv + (2 * tp + 1) * kR + i) : 0.f;
+        VP[tp * kSV + i] = split_pair(v0, v1);
+      }
+    }
+    bar_prep();
+
+    // ---- P1: decayed vectors split for the tensor cores, by 2 x 2 blocks (tokens 2tp, 2tp+1; columns
+    // 2jp, 2jp+1): column pairs for A^, R^, K~, B~ and token pairs for K-, B-; the decay guard
+    {
+      uint4* AH = reinterpret_cast<uint4*>(cb + LY::cAH);
+      uint4* RH = reinterpret_cast<uint4*>(cb + LY::cRH);
+      uint4* BB = reinterpret_cast<uint4*>(cb + LY::cBB);
+      float* GL = reinterpret_cast<float*>(cb + LY::cGL);
+      for (int e = pt; e < (kL / 2) * (kD / 2); e += kNP) {
+        const int tp = e >> 5, jp = e & 31, j = 2 * jp;
+        const int t0 = 2 * tp, t1 = t0 + 1;
+        const float2 gprev = t0 > 0 ? *reinterpret_cast<const float2*>(G + (t0 - 1) * kD + j) : make_float2(1.f, 1.f);
+        const float2 g0 = *reinterpret_cast<const float2*>(G + t0 * kD + j);
+        const float2 g1 = *reinterpret_cast<const float2*>(G + t1 * kD + j);
+        const float2 i0 = make_float2(__fdividef(1.f, g0.x), __fdividef(1.f, g0.y));
+        const float2 i1 = make_float2(__fdividef(1.f, g1.x), __fdividef(1.f, g1.y));
+        const float2 gl = *reinterpret_cast<const float2*>(G + (kL - 1) * kD + j);
+        const float2 z = make_float2(0.f, 0.f);
+        const bool v0 = t0 < nm, v1 = t1 < nm;
+        const float2 a0 = v0 ? raw2(ra + t0 * kD + j) : z, a1 = v1 ? raw2(ra + t1 * kD + j) : z;
+        const float2 b0 = v0 ? raw2(rbv + t0 * kD + j) : z, b1 = v1 ? raw2(rbv + t1 * kD + j) : z;
+        const float2 k0 = v0 ? raw2(rk + t0 * kD + j) : z, k1 = v1 ? raw2(rk + t1 * kD + j) : z;
+        const float2 r0 = v0 ? raw2(rr + t0 * kD + j) : z, r1 = v1 ? raw2(rr + t1 * kD + j) : z;
+        AH[t0 * kSP + jp] = split_pair(a0.x * gprev.x, a0.y * gprev.y);
+        AH[t1 * kSP + jp] = split_pair(a1.x * g0.x, a1.y * g0.y);
+        RH[t0 * kSP + jp] = split_pair(r0.x * g0.x, r0.y * g0.y);
+        RH[t1 * kSP + jp] = split_pair(r1.x * g1.x, r1.y * g1.y);
+        KT[t0 * kSP + jp] = split_pair(k0.x * i0.x, k0.y * i0.y);
+        KT[t1 * kSP + jp] = split_pair(k1.x * i1.x, k1.y * i1.y);
+        BT[t0 * kSP + jp] = split_pair(b0.x * i0.x, b0.y * i0.y);
+        BT[t1 * kSP + jp] = split_pair(b1.x * i1.x, b1.y * i1.y);
+        // gamma_L / gamma_t
+        const float f00 = gl.x * i0.x, f01 = gl.y * i0.y, f10 = gl.x * i1.x, f11 = gl.y * i1.y;
+        KB[tp * kSJ + j] = split_pair(k0.x * f00, k1.x * f10);
+        KB[tp * kSJ + j + 1] = split_pair(k0.y * f01, k1.y * f11);
+        BB[tp * kSJ + j] = split_pair(b0.x * f00, b1.x * f10);
+        BB[tp * kSJ + j + 1] = split_pair(b0.y * f01, b1.y * f11);
+      }
+      if (pt < kD) {
+        const float gl = G[(kL - 1) * kD + pt];
+        GL[pt] = gl;
+        if (!(gl >= kMinDecay)) meta[0] = 1;
+      }
+    }
+    bar_prep();
+
+    if (meta[0]) {
+      // token-by-token sub-chunk: the chain reads fp32 inputs instead of the matrices
+      float* FW = reinterpret_cast<float*>(cb + LY::cFW);
+      for (int e = pt; e < 5 * kL * kD; e += kNP) {
+        const int s5 = e / (kL * kD), t = (e - s5 * kL * kD) >> 6;
+        FW[e] = t < nm ? raw_at(raw + e) : (s5 == 0 ? 1.f : 0.f);
+      }
+      for (int e = pt; e < kL * kR; e += kNP) FW[5 * kL * kD + e] = (e >> 5) < nm ? raw_at(rv + e) : 0.f;
+      return;
+    }
+
+    // ---- P2: the coupling matrices (16 x 16, K = 64) and U = V^T K- (32 x 64, K = 16) on tensor cores.
+    // Preparing warp 0 forms M_ab and goes straight on to (I - M_ab)^-1 (the longest dependent
+    // path); warps 1-9 form M_ak, M_rb, M_rk and U, then C_AK = V^T M_ak^T and C_Y = V^T M_rk^T.
+    {
+      const uint4* AH = reinterpret_cast<const uint4*>(cb + LY::cAH);
+      const uint4* RH = reinterpret_cast<const uint4*>(cb + LY::cRH);
+      uint4* MRB = reinterpret_cast<uint4*>(cb + LY::cMRB);
+      float* U = reinterpret_cast<float*>(cb + LY::cU);
+      // one coupling-matrix tile: job = 4 x (R^ rows) + 2 x (K~ columns) + nt; even and odd k-steps
+      // in separate accumulators; A^-rows strictly lower (s < t), R^-rows lower with the diagonal
+      auto mjob = [&](int job) {
+        const int xr = job >> 2, yk = (job >> 1) & 1, nt = job & 1;
+        const uint4* X = xr ? RH : AH;
+        const uint4* Yv = yk ? KT : BT;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma3(acc[kk & 1], frag_a(X[g * kSP + kk * 4 + q], X[(g + 8) * kSP + kk * 4 + q]),
+               frag_b(Yv[(nt * 8 + g) * kSP + kk * 4 + q]));
+        const int s0 = nt * 8 + 2 * q;
+        const int lim0 = xr ? g : g - 1, lim8 = xr ? g + 8 : g + 7;
+        const float m00 = s0 <= lim0 ? acc[0][0] + acc[1][0] : 0.f;
+        const float m01 = s0 + 1 <= lim0 ? acc[0][1] + acc[1][1] : 0.f;
+        const float m80 = s0 <= lim8 ? acc[0][2] + acc[1][2] : 0.f;
+        const float m81 = s0 + 1 <= lim8 ? acc[0][3] + acc[1][3] : 0.f;
+        if (!xr && !yk) {  // M_ab: fp32 for the inverse
+          *reinterpret_cast<float2*>(MAB + g * 16 + s0) = make_float2(m00, m01);
+          *reinterpret_cast<float2*>(MAB + (g + 8) * 16 + s0) = make_float2(m80, m81);
+        } else {           // split pairs [t][s / 2], the B operand of products contracting over s
+          uint4* M = xr ? (yk ? MRK : MRB) : MAK;
+          M[g * kSM + nt * 4 + q] = split_pair(m00, m01);
+          M[(g + 8) * kSM + nt * 4 + q] = split_pair(m80, m81);
+        }
+      };
+      // the eight U tiles of rows um*16 .. um*16+15, one accumulator each
+      auto ujob8 = [&](int um) {
+        float acc[8][4] = {};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const FragA av = frag_a(VP[(kk * 4 + q) * kSV + um * 16 + g], VP[(kk * 4 + q) * kSV + um * 16 + g + 8]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mma3(acc[u], av, frag_b(KB[(kk * 4 + q) * kSJ + u * 8 + g]));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          *reinterpret_cast<float2*>(U + (um * 16 + g) * kSU + u * 8 + 2 * q) = make_float2(acc[u][0], acc[u][1]);
+          *reinterpret_cast<float2*>(U + (um * 16 + g + 8) * kSU + u * 8 + 2 * q) = make_float2(acc[u][2], acc[u][3]);
+        }
+      };
+
+      if (pw == 0) {
+        mjob(0);
+        mjob(1);
+        __syncwarp();
+        // ---- (I - M_ab)^-1: unit lower, by 4x4 diagonal blocks, then 8x8, then 16x16
+        for (int e = lane; e < 256; e += 32) TIf[e] = 0.f;
+        __syncwarp();
+        if (lane < 16) {  // 4x4 diagonal blocks by forward substitution, entries in registers
+          const int p = lane >> 2, c = lane & 3, o = 4 * p;
+          const float n10 = MAB[(o + 1) * 16 + o], n20 = MAB[(o + 2) * 16 + o], n21 = MAB[(o + 2) * 16 + o + 1];
+          const float n30 = MAB[(o + 3) * 16 + o], n31 = MAB[(o + 3) * 16 + o + 1], n32 = MAB[(o + 3) * 16 + o + 2];
+          const float x0 = c == 0 ? 1.f : 0.f;
+          const float x1 = c == 1 ? 1.f : (c < 1 ? n10 * x0 : 0.f);
+          const float x2 = c == 2 ? 1.f : (c < 2 ? fmaf(n21, x1, n20 * x0) : 0.f);
+          const float x3 = c == 3 ? 1.f : fmaf(n32, x2, fmaf(n31, x1, n30 * x0));
+          TIf[o * 16 + o + c] = x0;
+          TIf[(o + 1) * 16 + o + c] = x1;
+          TIf[(o + 2) * 16 + o + c] = x2;
+          TIf[(o + 3) * 16 + o + c] = x3;
+        }
+        __syncwarp();
+        {  // 8x8 blocks: lower-left 4x4 = D1^-1 (N21 D0^-1)
+          const int bq = lane >> 4, rr = (lane >> 2) & 3, c = lane & 3, o = 8 * bq;
+          float z = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) z = fmaf(MAB[(o + 4 + rr) * 16 + o + u], TIf[(o + u) * 16 + o + c], z);
+          TMP[(o + 4 + rr) * 16 + o + c] = z;
+          __syncwarp();
+          float x = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x = fmaf(TIf[(o + 4 + rr) * 16 + o + 4 + u], TMP[(o + 4 + u) * 16 + o + c], x);
+          TIf[(o + 4 + rr) * 16 + o + c] = x;
+        }
+        __syncwarp();
+        {  // 16x16: lower-left 8x8 = B^-1 (N21 A^-1)
+          float z[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = lane + 32 * h, rr = e >> 3, c = e & 7;
+            float s2 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s2 = fmaf(MAB[(8 + rr) * 16 + u], TIf[u * 16 + c], s2);
+            z[h] = s2;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = lane + 32 * h;
+            TMP[(8 + (e >> 3)) * 16 + (e & 7)] = z[h];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = lane + 32 * h, rr = e >> 3, c = e & 7;
+            float s2 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s2 = fmaf(TIf[(8 + rr) * 16 + 8 + u], TMP[(8 + u) * 16 + c], s2);
+            z[h] = s2;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = lane + 32 * h;
+            TIf[(8 + (e >> 3)) * 16 + (e & 7)] = z[h];
+          }
+        }
+        __syncwarp();
+        uint4* TI = reinterpret_cast<uint4*>(cb + LY::cTI);
+        for (int e = lane; e < 16 * 8; e += 32) {
+          const int t = e >> 3, sp = e & 7;
+          TI[t * kSM + sp] = split_pair(TIf[t * 16 + 2 * sp], TIf[t * 16 + 2 * sp + 1]);
+        }
+      } else {
+        if (pw <= 6) {
+          mjob(pw + 1);  // jobs 2-7: M_ak, M_rb, M_rk
+        } else if (pw <= 8) {
+          ujob8(pw - 7);
+        }
+        bar_rest();
+        if (pw <= 8) {  // C_AK (jb < 4) and C_Y tiles: (which, um, nt) = (jb >> 2, (jb >> 1) & 1, jb & 1)
+          float* CAK = reinterpret_cast<float*>(cb + LY::cCAK);
+          float* CY = reinterpret_cast<float*>(cb + LY::cCY);
+          const int jb = pw - 1;
+          const int which = jb >> 2, um = (jb >> 1) & 1, nt = jb & 1;
+          const uint4* M = which ? MRK : MAK;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma3(acc, frag_a(VP[(kk * 4 + q) * kSV + um * 16 + g], VP[(kk * 4 + q) * kSV + um * 16 + g + 8]),
+                 frag_b(M[(nt * 8 + g) * kSM + kk * 4 + q]));
+          float* C = which ? CY : CAK;
+          *reinterpret_cast<float2*>(C + (um * 16 + g) * kSC + nt * 8 + 2 * q) = make_float2(acc[0], acc[1]);
+          *reinterpret_cast<float2*>(C + (um * 16 + g + 8) * kSC + nt * 8 + 2 * q) = make_float2(acc[2], acc[3]);
+        }
+      }
+    }
+  };
+
+  if (nsub > 0) {
+    issue(0);
+    if (nsub > 1) issue(1);
+    if (nsub > 1) cp_async_wait<1>(); else cp_async_wait<0>();
+    bar_prep();
+    prepare(0);
+  }
+  __syncthreads();  // sub-chunk 0 prepared
+
+  for (int n = 0; n < nsub; ++n) {
+    if (n + 1 < nsub) {
+      // raw buffer n & 1 held sub-chunk n, prepared in the previous period: refill with n + 2
+      if (n + 2 < nsub) {
+        issue(n + 2);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      bar_prep();  // sub-chunk n + 1's inputs are visible to every preparing thread
+      prepare(n + 1);
+    }
+    __syncthreads();  // end of period n
+  }
+}
+
+template <typename Tin>
+cudaError_t launch_fwdc_t(const FwdArgs& p, cudaStream_t stream) {
+  using LY = Lay<Tin>;
+  static_assert(LY::kBytes <= 232448, "shared memory per CTA");
+  auto kern = fwdc_kernel<Tin>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kBytes);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = (unsigned)p.B * p.H * 2;
+  kern<<<grid, kNT, LY::kBytes, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
+                                         (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
+                                         (const Tin*)p.in.b, p.h0, p.y, p.h_ckpt, p.hT, p.sa);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward_chunked(const FwdArgs& p, cudaStream_t stream) {
+  return p.bf16 ? launch_fwdc_t<__nv_bfloat16>(p, stream) : launch_fwdc_t<float>(p, stream);
+}
+
+}  // namespace wkv7

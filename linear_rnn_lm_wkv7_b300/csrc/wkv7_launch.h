@@ -55,7 +55,10 @@ int num_sms();
 // and returns WKV7_ERR_CUDA
 int record_cuda_status(cudaError_t err);
 
+// the forward: sub-chunks of 16 tokens on tensor cores when chunk is a multiple of 16, else token by token
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_forward_sequential(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
 
 // two-phase backward (needs the saved sa): workspace of backward_workspace_bytes() bytes,

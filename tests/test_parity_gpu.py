@@ -54,10 +54,15 @@ def host(t):
 MODES = ["two_phase", "single_saved_sa", "single_recompute"]
 
 
-def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase"):
+# forward kernels: "auto" (16-token sub-chunks on tensor cores when chunk % 16 == 0 and the
+# B*H*2 row blocks fit one wave of SMs) and the token-by-token "sequential" one
+FWD = ["auto", "sequential"]
+
+
+def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase", fwd="auto"):
     ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
-    y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True)
+    y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True, kernel=fwd)
     kw = {"two_phase": dict(sa=sa), "single_saved_sa": dict(sa=sa, workspace=None),
           "single_recompute": dict(sa=None)}[mode]
     grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk, **kw)
@@ -65,7 +70,7 @@ def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase"):
     return host(y), host(ck), host(hT), [host(g) for g in grads], host(sa)
 
 
-def check(x, gpu, chunk, heads=None):
+def check(x, gpu, chunk, heads=None, with_grads=True):
     """Compare against the oracle; `heads` = list of (b, h) to restrict the oracle to."""
     y, ck, hT, grads, sa = gpu
     names = ("dr", "dw", "dk", "dv", "da", "db")
@@ -82,6 +87,8 @@ def check(x, gpu, chunk, heads=None):
         assert rel(sa[sb, :, sh], sao) <= TOL_FWD, ("sa", rel(sa[sb, :, sh], sao))
         assert rel(hT[sb, sh], hTo) <= TOL_FWD, ("hT", rel(hT[sb, sh], hTo))
         assert rel(ck[sb, sh], cko) <= TOL_FWD, ("h_ckpt", rel(ck[sb, sh], cko))
+        if not with_grads:
+            continue
         go = oracle.backward(*(xs[n] for n in "rwkvab"), h0, cko, x["dy"][sb, :, sh], dhT, chunk=chunk, mode="ckpt")
         for name, g, ref in zip(names, grads[:6], go[:6]):
             assert rel(g[sb, :, sh], ref) <= TOL_BWD, (name, rel(g[sb, :, sh], ref))
@@ -96,6 +103,31 @@ def test_workload_parity_full(wkv7, name, mode):
     wl = gen.WORKLOADS[name]
     x = gen.full(wl)
     check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, mode), wl.chunk)
+
+
+@pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
+def test_workload_parity_sequential_forward(wkv7, name):
+    """The token-by-token forward at the workloads' chunk (where `auto` takes sub-chunks)."""
+    wl = gen.WORKLOADS[name]
+    x = gen.full(wl)
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "two_phase", fwd="sequential"), wl.chunk)
+
+
+@pytest.mark.parametrize("name", ["debug_b12_t1024_h6", "wide7b_b2_t4096_h64"])
+def test_forward_kernels_agree(wkv7, name):
+    """Sub-chunk and token-by-token forwards on every head: y, sa and states agree to fp32 level.
+    The 7B-width case takes one batch row (64 heads, 4096 tokens, w near 1) so that its 128 row
+    blocks fit one wave and `auto` runs the sub-chunk kernel."""
+    wl = gen.WORKLOADS[name]
+    x = gen.full(wl, with_grad=False)
+    if wl.B * wl.H * 2 > 148:
+        x = {n: (None if t is None else t[:1]) for n, t in x.items()}
+    ins = [dev(x[n], wl.dtype) for n in "rwkvab"]
+    h0 = dev32(x.get("h0"))
+    outs = [wkv7.forward(*ins, h0, chunk=wl.chunk, save_sa=True, kernel=kk) for kk in FWD]
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert rel(host(a), host(b)) <= 2e-6
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -119,6 +151,26 @@ def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
     x = gen.random_small(B * 100 + T + H, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
     for mode in MODES:
         check(x, run_gpu(wkv7, x, dtype, chunk, mode), chunk)
+    check(x, run_gpu(wkv7, x, dtype, chunk, "two_phase", fwd="sequential"), chunk)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2)])
+def test_strong_decay_forward(wkv7, dtype, lo, hi):
+    """Decays far below the workloads' range.  With w in (0.005, 0.05) the 16-token decay drops
+    under 1e-30 in some sub-chunks, which then advance token by token; (0.02, 0.2) stays in the
+    sub-chunk form with 1/gamma up to ~1e27.  The first 40 tokens keep the workloads' decay, so
+    one sequence mixes both paths.  Forward only: the backward's division by w amplifies rounding
+    by (1/w)^31 here, as the page warns."""
+    x = gen.random_small(4242, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    rng = np.random.default_rng(7)
+    w = x["w"].copy()
+    w[:, 40:] = lo + (hi - lo) * rng.random(w[:, 40:].shape)
+    if dtype == "bf16":
+        w = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    x["w"] = w.astype(np.float32)
+    for fwd in FWD:
+        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd=fwd), 32, with_grads=False)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
