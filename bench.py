@@ -56,6 +56,8 @@ def parse_args():
                    help="decode workload only: number of sequences (default: the workload's 256)")
     p.add_argument("--bwd", choices=["two-phase", "single"], default="two-phase",
                    help="two-phase backward with a workspace (needs --sa saved), or the single-pass backward")
+    p.add_argument("--fwd", choices=["auto", "sequential"], default="auto",
+                   help="forward kernel: auto = 16-token sub-chunks where they apply, sequential = token by token")
     p.add_argument("--graph", choices=["on", "off"], default="on",
                    help="time the step as CUDA-graph replays (one graph per input set) instead of eager calls")
     p.add_argument("--sa", choices=["saved", "recompute"], default="saved",
@@ -482,7 +484,8 @@ def run_ours(args, rank, world, local_rank):
         ins = [s[n] for n in "rwkvab"]
         if ev is not None:
             ev[0].record(stream)
-        wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"] if saved else None))
+        wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"] if saved else None),
+                     kernel=args.fwd)
         if ev is not None:
             ev[1].record(stream)
         wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"] if saved else None,
@@ -642,7 +645,10 @@ def run_ours(args, rank, world, local_rank):
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
     bwd_name, bwd_src = ("wkv7_bwd_two_phase", "wkv7_bwd2.cu") if (saved and args.bwd == "two-phase") \
         else ("wkv7_bwd", "wkv7_bwd.cu")
-    dom = (bwd_name, bwd_b, b_ms, bwd_src) if b_ms >= f_ms else ("wkv7_fwd", fwd_b, f_ms, "wkv7_fwd.cu")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    chunked = args.fwd == "auto" and wl.chunk % 16 == 0 and B * H * 2 <= sms
+    fwd_name, fwd_src = ("wkv7_fwd_chunked", "wkv7_fwdc.cu") if chunked else ("wkv7_fwd", "wkv7_fwd.cu")
+    dom = (bwd_name, bwd_b, b_ms, bwd_src) if b_ms >= f_ms else (fwd_name, fwd_b, f_ms, fwd_src)
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     sha = kernel_source_sha(dom[3])
     traffic = profiled_traffic(dom[0], wl.name, sha)
@@ -655,7 +661,8 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, wkv7_inputs.py)",
         "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": wl.dtype,
-                   "state": "fp32", "sa": args.sa, "backward": args.bwd if args.sa == "saved" else "single",
+                   "state": "fp32", "sa": args.sa, "forward": fwd_name,
+                   "backward": args.bwd if args.sa == "saved" else "single",
                    "launch": launch, "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "l2": f"{N_SETS} rotating input/output sets "
                          f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"},
@@ -667,7 +674,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline_step_derived": {"definition": "max(HBM bytes / peak BW, 28*D^2 FLOP per head-token / FP32 peak) "
                                                 "/ step time", "flops": derived_flops(wl),
                                   "roofline_ms": roof_d * 1e3, "frac": roof_d / step_s},
-        "kernels_ms": {"wkv7_fwd": f_ms, bwd_name: b_ms, "timing": "eager calls, CUDA events around each"},
+        "kernels_ms": {fwd_name: f_ms, bwd_name: b_ms, "timing": "eager calls, CUDA events around each"},
         "clocks": clocks,
         "gpu_launches": (3 if (saved and args.bwd == "two-phase") else 2) * args.steps,
         "e2e": e2e,
