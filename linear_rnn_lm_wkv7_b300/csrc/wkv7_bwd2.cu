@@ -463,7 +463,11 @@ colgrad_kernel(int T, int H, int chunk, int nchunks,
 
 template <typename Tin>
 cudaError_t launch_bwd2_t(const BwdArgs& p, float* dsa_ws, float* xck_ws, cudaStream_t stream) {
-  {
+  if (p.chunk % 16 == 0 && p.T > 0 && (long long)p.B * p.H * (kD / kRows1) <= num_sms()) {
+    // the walk as the forward recurrence run backwards, in 16-step sub-chunks on tensor cores
+    cudaError_t err = launch_gwalk_chunked(p, dsa_ws, xck_ws, stream);
+    if (err != cudaSuccess) return err;
+  } else {
     const size_t smem = P1Smem<Tin>::kBytes;
     static_assert(P1Smem<Tin>::kBytes <= 232448, "shared memory per CTA");
     auto kern = gwalk_kernel<Tin>;

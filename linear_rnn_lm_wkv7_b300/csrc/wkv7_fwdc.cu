@@ -32,6 +32,8 @@
 // reused directly as the A operand of the next product by permuting the contraction index inside
 // each 8-block (logical k = q <-> column 2q, k = q + 4 <-> column 2q + 1); the B operands are
 // stored in shared memory already split into hi/lo and paired to match.
+#include <type_traits>
+
 #include "wkv7_device.cuh"
 #include "wkv7_launch.h"
 
@@ -54,10 +56,10 @@ constexpr int kSU = 72;    // [32][64] fp32 (+8): U = V^T K-, and the state in t
 constexpr int kSO = 36;    // [16][32] fp32 (+4): y / sa staging
 constexpr float kMinDecay = 1e-30f;
 
-template <typename Tin>
+template <typename Tin, typename TV>
 struct Lay {
-  // raw input stage (x2): w, k, a, b, r [kL][64], v [kL][32]
-  static constexpr size_t kRaw = ((5 * kL * kD + kL * kR) * sizeof(Tin) + 15) / 16 * 16;
+  // raw input stage (x2): w, k, a, b, r [kL][64] (Tin), then v [kL][32] (TV)
+  static constexpr size_t kRaw = (5 * kL * kD * sizeof(Tin) + 15) / 16 * 16 + (kL * kR * sizeof(TV) + 15) / 16 * 16;
   static constexpr size_t oRaw = 0;
   // chain buffer (x2): what the chain reads for one sub-chunk
   static constexpr size_t cAH = 0;                          // uint4 [16][kSP]
@@ -180,14 +182,38 @@ __device__ __forceinline__ float2 raw2(const __nv_bfloat16* p) {
 
 // ---------------------------------------------------------------- the kernel
 
-template <typename Tin>
+// Pointers of one call.  Forward: the inputs, s0 = h0, y, ck = h_ckpt, sT = hT, sa.  Gradient walk
+// (GRAD): the inputs with v = dy (fp32), s0 = dhT, y = dv, ck = X at the chunk ends, sT = dh0,
+// sa = dsa (every one of them laid out as in the forward).
+struct FwdcPtrs {
+  const void *r, *w, *k, *v, *a, *b;
+  const float* s0;
+  float *y, *ck, *sT, *sa;
+};
+
+// all-ones (bf16 or fp32 1.0) or all-zero 16 bytes
+template <typename T>
+__device__ __forceinline__ uint4 fill16(bool one) {
+  const uint32_t u = !one ? 0u : (sizeof(T) == 2 ? 0x3f803f80u : 0x3f800000u);
+  return make_uint4(u, u, u, u);
+}
+
+template <typename Tin, bool GRAD>
 __global__ void __launch_bounds__(kNT, 1)
-fwdc_kernel(int T, int H, int chunk, int nchunks,
-            const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
-            const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
-            const float* __restrict__ h0, float* __restrict__ y, float* __restrict__ h_ckpt,
-            float* __restrict__ hT, float* __restrict__ sa_out) {
-  using LY = Lay<Tin>;
+fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
+  using TV = typename std::conditional<GRAD, float, Tin>::type;
+  using LY = Lay<Tin, TV>;
+  const Tin* __restrict__ r = static_cast<const Tin*>(P.r);
+  const Tin* __restrict__ w = static_cast<const Tin*>(P.w);
+  const Tin* __restrict__ k = static_cast<const Tin*>(P.k);
+  const TV* __restrict__ v = static_cast<const TV*>(P.v);
+  const Tin* __restrict__ a = static_cast<const Tin*>(P.a);
+  const Tin* __restrict__ b = static_cast<const Tin*>(P.b);
+  const float* __restrict__ h0 = P.s0;
+  float* __restrict__ y = P.y;
+  float* __restrict__ h_ckpt = P.ck;
+  float* __restrict__ hT = P.sT;
+  float* __restrict__ sa_out = P.sa;
   extern __shared__ float4 smem4[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
 
@@ -201,7 +227,13 @@ fwdc_kernel(int T, int H, int chunk, int nchunks,
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
   const size_t sbase = (size_t)bh * kD * kD;
-  const int nsub = (T + kL - 1) / kL;
+  // Sub-chunk schedule over the steps.  Forward: steps = tokens, 16 per sub-chunk.  Gradient walk:
+  // T + 1 steps, step s for token T - 1 - s (the last one yields dh0); a first sub-chunk of one
+  // step and a second of ((T - 1) % 16) + 1 put every chunk end on a sub-chunk end.
+  const int len2 = GRAD && T > 0 ? (T - 1) % kL + 1 : 0;
+  const int nsub = GRAD ? (T > 0 ? 2 + (T - len2) / kL : 0) : (T + kL - 1) / kL;
+  auto sub_start = [&](int m) { return GRAD ? (m == 0 ? 0 : (m == 1 ? 1 : 1 + len2 + kL * (m - 2))) : m * kL; };
+  auto sub_len = [&](int m) { return GRAD ? (m == 0 ? 1 : (m == 1 ? len2 : kL)) : min(kL, T - m * kL); };
 
   auto raw_buf = [&](int m) { return reinterpret_cast<Tin*>(sm + LY::oRaw + (size_t)(m & 1) * LY::kRaw); };
   auto chain_buf = [&](int m) { return sm + LY::oChain + (size_t)(m & 1) * LY::kChain; };
@@ -380,17 +412,28 @@ fwdc_kernel(int T, int H, int chunk, int nchunks,
 
       // y and sa of this sub-chunk to global memory (both chain warps have staged theirs)
       bar_chain();
+      const int tau0 = sub_start(n);
       for (int e = tid; e < nm * kR; e += kChainThreads) {
         const int t = e >> 5, i = e & 31;
-        const size_t o = base + (size_t)(n * kL + t) * tstride + rb * kR + i;
-        y[o] = fy[t * kSO + i];
-        if (sa_out != nullptr) sa_out[o] = fsa[t * kSO + i];
+        if (!GRAD) {
+          const size_t o = base + (size_t)(tau0 + t) * tstride + rb * kR + i;
+          y[o] = fy[t * kSO + i];
+          if (sa_out != nullptr) sa_out[o] = fsa[t * kSO + i];
+        } else {  // step s: y' is dv at token T-1-s, sa' is dsa at token T-s
+          const int st = tau0 + t;
+          if (st <= T - 1) y[base + (size_t)(T - 1 - st) * tstride + rb * kR + i] = fy[t * kSO + i];
+          if (st >= 1) sa_out[base + (size_t)(T - st) * tstride + rb * kR + i] = fsa[t * kSO + i];
+        }
       }
 
-      // checkpoint after the sub-chunk's last token when it ends a chunk (or the sequence)
-      const int tlast = n * kL + nm - 1;
-      if (h_ckpt != nullptr && ((tlast + 1) % chunk == 0 || tlast == T - 1)) {
-        float* dst = h_ckpt + ((size_t)bh * nchunks + tlast / chunk) * kD * kD;
+      // the state after the sub-chunk's last step when that ends a chunk (forward: token 32c+31 or
+      // T-1; gradient walk: step T-1-t for a chunk end t, i.e. X_t)
+      const int tlast = tau0 + nm - 1;
+      const bool at_end = GRAD ? (tlast < T && (tlast == 0 || (T - tlast) % chunk == 0))
+                               : ((tlast + 1) % chunk == 0 || tlast == T - 1);
+      const int cidx = GRAD ? (T - 1 - tlast) / chunk : tlast / chunk;
+      if (h_ckpt != nullptr && at_end) {
+        float* dst = h_ckpt + ((size_t)bh * nchunks + cidx) * kD * kD;
 #pragma unroll
         for (int nj = 0; nj < 8; ++nj) {
           *reinterpret_cast<float2*>(dst + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
@@ -425,24 +468,44 @@ fwdc_kernel(int T, int H, int chunk, int nchunks,
   float* TIf = reinterpret_cast<float*>(sm + LY::oTI);
   float* TMP = reinterpret_cast<float*>(sm + LY::oTMP);
 
-  // cp.async copies of sub-chunk m's inputs (tokens beyond T are not copied; they read as padding)
+  // cp.async copies of sub-chunk m's inputs; steps past the sub-chunk are not copied and read as
+  // padding.  Gradient walk: slots w, k, a, b, r, v take w, r, b, a, k at tokens T - s (w, a, b) or
+  // T - 1 - s (k, r) and dy at T - 1 - s; a step outside [0, T) gets w = 1 and zeros.
   auto issue = [&](int m) {
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
     constexpr int EPC = 16 / (int)sizeof(Tin);
-    constexpr int VPR = kR * (int)sizeof(Tin) / 16;
+    constexpr int VPR = kR * (int)sizeof(TV) / 16;
+    constexpr int EPV = 16 / (int)sizeof(TV);
     Tin* dst = raw_buf(m);
-    const int t0 = m * kL;
-    const int nm = min(kL, T - t0);
+    TV* dstv = reinterpret_cast<TV*>(dst + 5 * kL * kD);
+    const int t0 = sub_start(m);
+    const int nm = sub_len(m);
     const Tin* srcs[5] = {w, k, a, b, r};
+    if (GRAD) {
+      srcs[1] = r;
+      srcs[2] = b;
+      srcs[3] = a;
+      srcs[4] = k;
+    }
 #pragma unroll
-    for (int s = 0; s < 5; ++s)
+    for (int s5 = 0; s5 < 5; ++s5)
       for (int e = pt; e < nm * CPR; e += kNP) {
         const int t = e / CPR, pc = e % CPR;
-        cp_async16(dst + (s * kL + t) * kD + pc * EPC, srcs[s] + base + (size_t)(t0 + t) * tstride + pc * EPC);
+        Tin* d = dst + (s5 * kL + t) * kD + pc * EPC;
+        const int tok = !GRAD ? t0 + t : ((s5 == 0 || s5 == 2 || s5 == 3) ? T - (t0 + t) : T - 1 - (t0 + t));
+        if (tok >= 0 && tok < T)
+          cp_async16(d, srcs[s5] + base + (size_t)tok * tstride + pc * EPC);
+        else
+          *reinterpret_cast<uint4*>(d) = fill16<Tin>(s5 == 0);
       }
     for (int e = pt; e < nm * VPR; e += kNP) {
       const int t = e / VPR, pc = e % VPR;
-      cp_async16(dst + 5 * kL * kD + t * kR + pc * EPC, v + base + (size_t)(t0 + t) * tstride + rb * kR + pc * EPC);
+      TV* d = dstv + t * kR + pc * EPV;
+      const int tok = GRAD ? T - 1 - (t0 + t) : t0 + t;
+      if (tok >= 0)
+        cp_async16(d, v + base + (size_t)tok * tstride + rb * kR + pc * EPV);
+      else
+        *reinterpret_cast<uint4*>(d) = fill16<TV>(false);
     }
     cp_async_commit();
   };
@@ -455,10 +518,10 @@ fwdc_kernel(int T, int H, int chunk, int nchunks,
     const Tin* ra = raw + 2 * kL * kD;
     const Tin* rbv = raw + 3 * kL * kD;
     const Tin* rr = raw + 4 * kL * kD;
-    const Tin* rv = raw + 5 * kL * kD;
+    const TV* rv = reinterpret_cast<const TV*>(raw + 5 * kL * kD);
     unsigned char* cb = chain_buf(m);
     int* meta = reinterpret_cast<int*>(cb + LY::cMeta);
-    const int nm = min(kL, T - m * kL);
+    const int nm = sub_len(m);
 
     // ---- P0: gamma_t = w_0 o .. o w_t down each column; V split in token pairs
     if (pt < kD) {
@@ -713,24 +776,31 @@ fwdc_kernel(int T, int H, int chunk, int nchunks,
   }
 }
 
-template <typename Tin>
-cudaError_t launch_fwdc_t(const FwdArgs& p, cudaStream_t stream) {
-  using LY = Lay<Tin>;
+template <typename Tin, bool GRAD>
+cudaError_t launch_fwdc_t(int B, int T, int H, int chunk, int nchunks, const FwdcPtrs& P, cudaStream_t stream) {
+  using TV = typename std::conditional<GRAD, float, Tin>::type;
+  using LY = Lay<Tin, TV>;
   static_assert(LY::kBytes <= 232448, "shared memory per CTA");
-  auto kern = fwdc_kernel<Tin>;
+  auto kern = fwdc_kernel<Tin, GRAD>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kBytes);
   if (err != cudaSuccess) return err;
-  const unsigned grid = (unsigned)p.B * p.H * 2;
-  kern<<<grid, kNT, LY::kBytes, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
-                                         (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
-                                         (const Tin*)p.in.b, p.h0, p.y, p.h_ckpt, p.hT, p.sa);
+  const unsigned grid = (unsigned)B * H * 2;
+  kern<<<grid, kNT, LY::kBytes, stream>>>(T, H, chunk, nchunks, P);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_forward_chunked(const FwdArgs& p, cudaStream_t stream) {
-  return p.bf16 ? launch_fwdc_t<__nv_bfloat16>(p, stream) : launch_fwdc_t<float>(p, stream);
+  const FwdcPtrs P{p.in.r, p.in.w, p.in.k, p.in.v, p.in.a, p.in.b, p.h0, p.y, p.h_ckpt, p.hT, p.sa};
+  return p.bf16 ? launch_fwdc_t<__nv_bfloat16, false>(p.B, p.T, p.H, p.chunk, p.nchunks, P, stream)
+                : launch_fwdc_t<float, false>(p.B, p.T, p.H, p.chunk, p.nchunks, P, stream);
+}
+
+cudaError_t launch_gwalk_chunked(const BwdArgs& p, float* dsa_ws, float* xck_ws, cudaStream_t stream) {
+  const FwdcPtrs P{p.in.r, p.in.w, p.in.k, p.dy, p.in.a, p.in.b, p.dhT, p.dv, xck_ws, p.dh0, dsa_ws};
+  return p.bf16 ? launch_fwdc_t<__nv_bfloat16, true>(p.B, p.T, p.H, p.chunk, p.nchunks, P, stream)
+                : launch_fwdc_t<float, true>(p.B, p.T, p.H, p.chunk, p.nchunks, P, stream);
 }
 
 }  // namespace wkv7

@@ -65,6 +65,9 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
 // 256-byte aligned, holding dsa (B,T,H,D) and the state gradient at every chunk end (B,H,C,D,D)
 size_t backward_workspace_bytes(int B, int T, int H, int chunk);
 cudaError_t launch_backward_two_phase(const BwdArgs& a, void* workspace, cudaStream_t stream);
+// phase 1 of the two-phase backward (the state-gradient walk writing dv, dsa, X at the chunk ends and
+// dh0) by the 16-step sub-chunk kernel: chunk % 16 == 0, T >= 1
+cudaError_t launch_gwalk_chunked(const BwdArgs& a, float* dsa_ws, float* xck_ws, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace wkv7
