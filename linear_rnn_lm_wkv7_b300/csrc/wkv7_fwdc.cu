@@ -25,13 +25,16 @@
 // handled.
 //
 // Mapping: one CTA per (head, 32-row block), 12 warps.  Warps 0-1 hold the CTA's 32 x 64 slice of
-// S as mma.sync m16n8k8 accumulator tiles (warp m = rows 16m..16m+15) and run the chain; warps 2-11
-// prepare the next sub-chunk (decays, the four 16x16 coupling matrices and U = V^T K- on tensor
-// cores, (I - M_ab)^-1 by 4x4 / 8x8 blocks, the fp32 corrections) one sub-chunk ahead, and write
-// the previous sub-chunk's y and sa.  One CTA barrier per sub-chunk.  An accumulator tile is
-// reused directly as the A operand of the next product by permuting the contraction index inside
-// each 8-block (logical k = q <-> column 2q, k = q + 4 <-> column 2q + 1); the B operands are
-// stored in shared memory already split into hi/lo and paired to match.
+// S as mma.sync m16n8k8 accumulator tiles (warp m = rows 16m..16m+15), run the chain and write y
+// and sa; warps 2-11 prepare the next sub-chunk (decays, the four 16x16 coupling matrices and
+// U = V^T K- on tensor cores, (I - M_ab)^-1 by 4x4 / 8x8 / 16x16 blocks, the V corrections on tensor
+// cores) one sub-chunk ahead.  One CTA barrier per sub-chunk.  An accumulator tile is reused
+// directly as the A operand of the next product by permuting the contraction index inside each
+// 8-block (logical k = q <-> column 2q, k = q + 4 <-> column 2q + 1); the B operands are stored in
+// shared memory already split into hi/lo and paired to match.
+//
+// The same kernel runs the backward's state-gradient walk (GRAD): that recurrence, read from the
+// last token down, has the forward's form with the inputs remapped (see FwdcPtrs and `issue`).
 #include <type_traits>
 
 #include "wkv7_device.cuh"
@@ -167,6 +170,9 @@ __device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, %0;\n" ::
 __device__ __forceinline__ void bar_chain() { asm volatile("bar.sync 2, %0;\n" ::"n"(kChainThreads) : "memory"); }
 // preparing warps 1-9
 __device__ __forceinline__ void bar_rest() { asm volatile("bar.sync 3, %0;\n" ::"n"(kNP - 32) : "memory"); }
+// preparing warp 1 hands its M_ab tile to warp 0
+__device__ __forceinline__ void bar_pair_sync() { asm volatile("bar.sync 4, 64;\n" ::: "memory"); }
+__device__ __forceinline__ void bar_pair_arrive() { asm volatile("bar.arrive 4, 64;\n" ::: "memory"); }
 
 template <typename Tin>
 __device__ __forceinline__ float raw_at(const Tin* p) {
@@ -413,16 +419,18 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       // y and sa of this sub-chunk to global memory (both chain warps have staged theirs)
       bar_chain();
       const int tau0 = sub_start(n);
-      for (int e = tid; e < nm * kR; e += kChainThreads) {
-        const int t = e >> 5, i = e & 31;
+      for (int e = tid; e < nm * (kR / 4); e += kChainThreads) {
+        const int t = e >> 3, i = (e & 7) * 4;
+        const float4 vy = *reinterpret_cast<const float4*>(fy + t * kSO + i);
+        const float4 vs = *reinterpret_cast<const float4*>(fsa + t * kSO + i);
         if (!GRAD) {
           const size_t o = base + (size_t)(tau0 + t) * tstride + rb * kR + i;
-          y[o] = fy[t * kSO + i];
-          if (sa_out != nullptr) sa_out[o] = fsa[t * kSO + i];
+          *reinterpret_cast<float4*>(y + o) = vy;
+          if (sa_out != nullptr) *reinterpret_cast<float4*>(sa_out + o) = vs;
         } else {  // step s: y' is dv at token T-1-s, sa' is dsa at token T-s
           const int st = tau0 + t;
-          if (st <= T - 1) y[base + (size_t)(T - 1 - st) * tstride + rb * kR + i] = fy[t * kSO + i];
-          if (st >= 1) sa_out[base + (size_t)(T - st) * tstride + rb * kR + i] = fsa[t * kSO + i];
+          if (st <= T - 1) *reinterpret_cast<float4*>(y + base + (size_t)(T - 1 - st) * tstride + rb * kR + i) = vy;
+          if (st >= 1) *reinterpret_cast<float4*>(sa_out + base + (size_t)(T - st) * tstride + rb * kR + i) = vs;
         }
       }
 
@@ -528,7 +536,9 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       const int j = pt;
       float wv[kL];
 #pragma unroll
-      for (int t = 0; t < kL; ++t) wv[t] = t < nm ? raw_at(rw + t * kD + j) : 1.f;
+      for (int t = 0; t < kL; ++t) wv[t] = raw_at(rw + t * kD + j);  // all 16 rows: no dependent guards
+#pragma unroll
+      for (int t = 0; t < kL; ++t) wv[t] = t < nm ? wv[t] : 1.f;
       float gm = 1.f;
 #pragma unroll
       for (int t = 0; t < kL; ++t) {
@@ -567,10 +577,13 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
         const float2 gl = *reinterpret_cast<const float2*>(G + (kL - 1) * kD + j);
         const float2 z = make_float2(0.f, 0.f);
         const bool v0 = t0 < nm, v1 = t1 < nm;
-        const float2 a0 = v0 ? raw2(ra + t0 * kD + j) : z, a1 = v1 ? raw2(ra + t1 * kD + j) : z;
-        const float2 b0 = v0 ? raw2(rbv + t0 * kD + j) : z, b1 = v1 ? raw2(rbv + t1 * kD + j) : z;
-        const float2 k0 = v0 ? raw2(rk + t0 * kD + j) : z, k1 = v1 ? raw2(rk + t1 * kD + j) : z;
-        const float2 r0 = v0 ? raw2(rr + t0 * kD + j) : z, r1 = v1 ? raw2(rr + t1 * kD + j) : z;
+        // rows past the sub-chunk hold stale bits: load unconditionally, select zeros
+        float2 a0 = raw2(ra + t0 * kD + j), a1 = raw2(ra + t1 * kD + j);
+        float2 b0 = raw2(rbv + t0 * kD + j), b1 = raw2(rbv + t1 * kD + j);
+        float2 k0 = raw2(rk + t0 * kD + j), k1 = raw2(rk + t1 * kD + j);
+        float2 r0 = raw2(rr + t0 * kD + j), r1 = raw2(rr + t1 * kD + j);
+        if (!v0) a0 = b0 = k0 = r0 = z;
+        if (!v1) a1 = b1 = k1 = r1 = z;
         AH[t0 * kSP + jp] = split_pair(a0.x * gprev.x, a0.y * gprev.y);
         AH[t1 * kSP + jp] = split_pair(a1.x * g0.x, a1.y * g0.y);
         RH[t0 * kSP + jp] = split_pair(r0.x * g0.x, r0.y * g0.y);
@@ -657,8 +670,7 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
 
       if (pw == 0) {
         mjob(0);
-        mjob(1);
-        __syncwarp();
+        bar_pair_sync();  // warp 1 has stored the other M_ab tile
         // ---- (I - M_ab)^-1: unit lower, by 4x4 diagonal blocks, then 8x8, then 16x16
         for (int e = lane; e < 256; e += 32) TIf[e] = 0.f;
         __syncwarp();
@@ -726,10 +738,13 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
           TI[t * kSM + sp] = split_pair(TIf[t * 16 + 2 * sp], TIf[t * 16 + 2 * sp + 1]);
         }
       } else {
-        if (pw <= 6) {
-          mjob(pw + 1);  // jobs 2-7: M_ak, M_rb, M_rk
-        } else if (pw <= 8) {
-          ujob8(pw - 7);
+        if (pw == 1) {
+          mjob(1);
+          bar_pair_arrive();
+        } else if (pw <= 7) {
+          mjob(pw);  // jobs 2-7: M_ak, M_rb, M_rk
+        } else {
+          ujob8(pw - 8);
         }
         bar_rest();
         if (pw <= 8) {  // C_AK (jb < 4) and C_Y tiles: (which, um, nt) = (jb >> 2, (jb >> 1) & 1, jb & 1)
