@@ -97,11 +97,12 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback", {}
 
 
-def kernel_source_sha(name: str) -> str:
-    path = os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", name)
+def kernel_source_sha(names) -> str:
+    """sha256 of the given kernel file(s) (name or tuple, in order) then wkv7_device.cuh, 12 hex digits."""
+    names = (names,) if isinstance(names, str) else tuple(names)
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", "wkv7_device.cuh")):
-        with open(p, "rb") as f:
+    for n in names + ("wkv7_device.cuh",):
+        with open(os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
@@ -643,7 +644,8 @@ def run_ours(args, rank, world, local_rank):
     fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
     hbm, peak_kind, peaks = measured_peaks()
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    bwd_name, bwd_src = ("wkv7_bwd_two_phase", "wkv7_bwd2.cu") if (saved and args.bwd == "two-phase") \
+    # the two-phase backward's walk runs on the sub-chunk kernel: its traffic row is keyed by both files
+    bwd_name, bwd_src = ("wkv7_bwd_two_phase", ("wkv7_bwd2.cu", "wkv7_fwdc.cu")) if (saved and args.bwd == "two-phase") \
         else ("wkv7_bwd", "wkv7_bwd.cu")
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     chunked = args.fwd == "auto" and wl.chunk % 16 == 0 and B * H * 2 <= sms
