@@ -27,7 +27,7 @@
 // Mapping: one CTA per (head, 32-row block), 12 warps.  Warps 0-1 hold the CTA's 32 x 64 slice of
 // S as mma.sync m16n8k8 accumulator tiles (warp m = rows 16m..16m+15), run the chain and write y
 // and sa; warps 2-11 prepare the next sub-chunk (decays, the four 16x16 coupling matrices and
-// U = V^T K- on tensor cores, (I - M_ab)^-1 by 4x4 / 8x8 / 16x16 blocks, the V corrections on tensor
+// U = V^T K- on tensor cores, (I - M_ab)^-1 by forward substitution, a column per lane, the V corrections on tensor
 // cores) one sub-chunk ahead.  One CTA barrier per sub-chunk.  An accumulator tile is reused
 // directly as the A operand of the next product by permuting the contraction index inside each
 // 8-block (logical k = q <-> column 2q, k = q + 4 <-> column 2q + 1); the B operands are stored in
@@ -67,8 +67,8 @@ struct Lay {
   // chain buffer (x2): what the chain reads for one sub-chunk
   static constexpr size_t cAH = 0;                          // uint4 [16][kSP]
   static constexpr size_t cRH = cAH + 16 * kSP * 16;
-  static constexpr size_t cTI = cRH + 16 * kSP * 16;        // uint4 [16][kSM]
-  static constexpr size_t cMRB = cTI + 16 * kSM * 16;
+  static constexpr size_t cTI = cRH + 16 * kSP * 16;        // float [16][kSC]: (I - M_ab)^-1
+  static constexpr size_t cMRB = cTI + 16 * kSC * 4;        // uint4 [16][kSM]
   static constexpr size_t cCAK = cMRB + 16 * kSM * 16;      // float [32][kSC]: V^T M_ak^T
   static constexpr size_t cCY = cCAK + 32 * kSC * 4;        // float [32][kSC]: V^T M_rk^T
   static constexpr size_t cU = cCY + 32 * kSC * 4;          // float [32][kSU]
@@ -89,11 +89,9 @@ struct Lay {
   static constexpr size_t oVP = oKB + 8 * kSJ * 16;          // uint4 [8][kSV]
   static constexpr size_t oMAK = oVP + 8 * kSV * 16;         // uint4 [16][kSM] each: M_ak, M_rk split
   static constexpr size_t oMRK = oMAK + 16 * kSM * 16;
-  static constexpr size_t oMAB = oMRK + 16 * kSM * 16;       // float [16][16]: M_ab, (I - M_ab)^-1, temp
-  static constexpr size_t oTI = oMAB + 1024;
-  static constexpr size_t oTMP = oTI + 1024;
+  static constexpr size_t oMAB = oMRK + 16 * kSM * 16;       // float [16][16]: M_ab
   // output staging (x2): y, sa [16][kSO]
-  static constexpr size_t oOut = oTMP + 1024;
+  static constexpr size_t oOut = oMAB + 1024;
   static constexpr size_t kOut = 2 * kL * kSO * 4;
   // state of the token-by-token path: float [32][kSU]
   static constexpr size_t oFS = oOut + 2 * kOut;
@@ -158,6 +156,14 @@ __device__ __forceinline__ FragA frag_a(uint4 r0, uint4 r8) {
   a.h[0] = r0.x; a.h[2] = r0.y; a.l[0] = r0.z; a.l[2] = r0.w;
   a.h[1] = r8.x; a.h[3] = r8.y; a.l[1] = r8.z; a.l[3] = r8.w;
   return a;
+}
+
+// B operand from an fp32 pair (b0, b1), split here
+__device__ __forceinline__ FragB frag_b2(float2 v) {
+  FragB b;
+  split(v.x, b.h[0], b.l[0]);
+  split(v.y, b.h[1], b.l[1]);
+  return b;
 }
 
 __device__ __forceinline__ FragB frag_b(uint4 q) {
@@ -274,7 +280,7 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       if (!slow) {
         const uint4* AH = reinterpret_cast<const uint4*>(cb + LY::cAH);
         const uint4* RH = reinterpret_cast<const uint4*>(cb + LY::cRH);
-        const uint4* TI = reinterpret_cast<const uint4*>(cb + LY::cTI);
+        const float* TI = reinterpret_cast<const float*>(cb + LY::cTI);
         const uint4* MRB = reinterpret_cast<const uint4*>(cb + LY::cMRB);
         const float* CAK = reinterpret_cast<const float*>(cb + LY::cCAK);
         const float* CY = reinterpret_cast<const float*>(cb + LY::cCY);
@@ -324,8 +330,8 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
           const FragA p1 = frag_from_acc(Pt[1]);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            mma3(SA[nt], p0, frag_b(TI[(nt * 8 + g) * kSM + q]));
-            mma3(SA[nt], p1, frag_b(TI[(nt * 8 + g) * kSM + 4 + q]));
+            mma3(SA[nt], p0, frag_b2(*reinterpret_cast<const float2*>(TI + (nt * 8 + g) * kSC + 2 * q)));
+            mma3(SA[nt], p1, frag_b2(*reinterpret_cast<const float2*>(TI + (nt * 8 + g) * kSC + 8 + 2 * q)));
           }
         }
         const FragA s0 = frag_from_acc(SA[0]);
@@ -473,8 +479,6 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
   uint4* MAK = reinterpret_cast<uint4*>(sm + LY::oMAK);
   uint4* MRK = reinterpret_cast<uint4*>(sm + LY::oMRK);
   float* MAB = reinterpret_cast<float*>(sm + LY::oMAB);
-  float* TIf = reinterpret_cast<float*>(sm + LY::oTI);
-  float* TMP = reinterpret_cast<float*>(sm + LY::oTMP);
 
   // cp.async copies of sub-chunk m's inputs; steps past the sub-chunk are not copied and read as
   // padding.  Gradient walk: slots w, k, a, b, r, v take w, r, b, a, k at tokens T - s (w, a, b) or
@@ -626,23 +630,26 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       const uint4* RH = reinterpret_cast<const uint4*>(cb + LY::cRH);
       uint4* MRB = reinterpret_cast<uint4*>(cb + LY::cMRB);
       float* U = reinterpret_cast<float*>(cb + LY::cU);
-      // one coupling-matrix tile: job = 4 x (R^ rows) + 2 x (K~ columns) + nt; even and odd k-steps
-      // in separate accumulators; A^-rows strictly lower (s < t), R^-rows lower with the diagonal
+      // one coupling-matrix tile: job = 4 x (R^ rows) + 2 x (K~ columns) + nt; k-steps in four
+      // accumulators; A^-rows strictly lower (s < t), R^-rows lower with the diagonal
       auto mjob = [&](int job) {
         const int xr = job >> 2, yk = (job >> 1) & 1, nt = job & 1;
         const uint4* X = xr ? RH : AH;
         const uint4* Yv = yk ? KT : BT;
-        float acc[2][4] = {};
+        float acc[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma3(acc[kk & 1], frag_a(X[g * kSP + kk * 4 + q], X[(g + 8) * kSP + kk * 4 + q]),
+          mma3(acc[kk & 3], frag_a(X[g * kSP + kk * 4 + q], X[(g + 8) * kSP + kk * 4 + q]),
                frag_b(Yv[(nt * 8 + g) * kSP + kk * 4 + q]));
+        float sum[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
         const int s0 = nt * 8 + 2 * q;
         const int lim0 = xr ? g : g - 1, lim8 = xr ? g + 8 : g + 7;
-        const float m00 = s0 <= lim0 ? acc[0][0] + acc[1][0] : 0.f;
-        const float m01 = s0 + 1 <= lim0 ? acc[0][1] + acc[1][1] : 0.f;
-        const float m80 = s0 <= lim8 ? acc[0][2] + acc[1][2] : 0.f;
-        const float m81 = s0 + 1 <= lim8 ? acc[0][3] + acc[1][3] : 0.f;
+        const float m00 = s0 <= lim0 ? sum[0] : 0.f;
+        const float m01 = s0 + 1 <= lim0 ? sum[1] : 0.f;
+        const float m80 = s0 <= lim8 ? sum[2] : 0.f;
+        const float m81 = s0 + 1 <= lim8 ? sum[3] : 0.f;
         if (!xr && !yk) {  // M_ab: fp32 for the inverse
           *reinterpret_cast<float2*>(MAB + g * 16 + s0) = make_float2(m00, m01);
           *reinterpret_cast<float2*>(MAB + (g + 8) * 16 + s0) = make_float2(m80, m81);
@@ -671,71 +678,24 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       if (pw == 0) {
         mjob(0);
         bar_pair_sync();  // warp 1 has stored the other M_ab tile
-        // ---- (I - M_ab)^-1: unit lower, by 4x4 diagonal blocks, then 8x8, then 16x16
-        for (int e = lane; e < 256; e += 32) TIf[e] = 0.f;
-        __syncwarp();
-        if (lane < 16) {  // 4x4 diagonal blocks by forward substitution, entries in registers
-          const int p = lane >> 2, c = lane & 3, o = 4 * p;
-          const float n10 = MAB[(o + 1) * 16 + o], n20 = MAB[(o + 2) * 16 + o], n21 = MAB[(o + 2) * 16 + o + 1];
-          const float n30 = MAB[(o + 3) * 16 + o], n31 = MAB[(o + 3) * 16 + o + 1], n32 = MAB[(o + 3) * 16 + o + 2];
-          const float x0 = c == 0 ? 1.f : 0.f;
-          const float x1 = c == 1 ? 1.f : (c < 1 ? n10 * x0 : 0.f);
-          const float x2 = c == 2 ? 1.f : (c < 2 ? fmaf(n21, x1, n20 * x0) : 0.f);
-          const float x3 = c == 3 ? 1.f : fmaf(n32, x2, fmaf(n31, x1, n30 * x0));
-          TIf[o * 16 + o + c] = x0;
-          TIf[(o + 1) * 16 + o + c] = x1;
-          TIf[(o + 2) * 16 + o + c] = x2;
-          TIf[(o + 3) * 16 + o + c] = x3;
-        }
-        __syncwarp();
-        {  // 8x8 blocks: lower-left 4x4 = D1^-1 (N21 D0^-1)
-          const int bq = lane >> 4, rr = (lane >> 2) & 3, c = lane & 3, o = 8 * bq;
-          float z = 0.f;
+        // ---- (I - M_ab)^-1, unit lower: column c solves (I - M_ab) x = e_c by forward substitution,
+        // x_t = [t == c] + sum_{u < t} M_ab[t][u] x_u, in lane c's registers (lanes 16-31 repeat
+        // columns 0-15); rows of M_ab are broadcast loads.  Stored fp32; the chain splits it.
+        {
+          const int c = lane & 15;
+          float x[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) z = fmaf(MAB[(o + 4 + rr) * 16 + o + u], TIf[(o + u) * 16 + o + c], z);
-          TMP[(o + 4 + rr) * 16 + o + c] = z;
-          __syncwarp();
-          float x = 0.f;
+          for (int t = 0; t < 16; ++t) {
+            float acc = t == c ? 1.f : 0.f;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) x = fmaf(TIf[(o + 4 + rr) * 16 + o + 4 + u], TMP[(o + 4 + u) * 16 + o + c], x);
-          TIf[(o + 4 + rr) * 16 + o + c] = x;
-        }
-        __syncwarp();
-        {  // 16x16: lower-left 8x8 = B^-1 (N21 A^-1)
-          float z[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = lane + 32 * h, rr = e >> 3, c = e & 7;
-            float s2 = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) s2 = fmaf(MAB[(8 + rr) * 16 + u], TIf[u * 16 + c], s2);
-            z[h] = s2;
+            for (int u = 0; u < t; ++u) acc = fmaf(MAB[t * 16 + u], x[u], acc);
+            x[t] = acc;
           }
+          float* TI = reinterpret_cast<float*>(cb + LY::cTI);
+          if (lane < 16) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = lane + 32 * h;
-            TMP[(8 + (e >> 3)) * 16 + (e & 7)] = z[h];
+            for (int t = 0; t < 16; ++t) TI[t * kSC + c] = x[t];
           }
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = lane + 32 * h, rr = e >> 3, c = e & 7;
-            float s2 = 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) s2 = fmaf(TIf[(8 + rr) * 16 + 8 + u], TMP[(8 + u) * 16 + c], s2);
-            z[h] = s2;
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = lane + 32 * h;
-            TIf[(8 + (e >> 3)) * 16 + (e & 7)] = z[h];
-          }
-        }
-        __syncwarp();
-        uint4* TI = reinterpret_cast<uint4*>(cb + LY::cTI);
-        for (int e = lane; e < 16 * 8; e += 32) {
-          const int t = e >> 3, sp = e & 7;
-          TI[t * kSM + sp] = split_pair(TIf[t * 16 + 2 * sp], TIf[t * 16 + 2 * sp + 1]);
         }
       } else {
         if (pw == 1) {
