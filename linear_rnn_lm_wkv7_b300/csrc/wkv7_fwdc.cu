@@ -57,6 +57,9 @@ constexpr int kSV = 34;    // [8 token pairs][32] (+2): V
 constexpr int kSC = 24;    // [32][16] fp32 (+8): the V corrections of sa and y
 constexpr int kSU = 72;    // [32][64] fp32 (+8): U = V^T K-, and the state in the token-by-token path
 constexpr int kSO = 36;    // [16][32] fp32 (+4): y / sa staging
+constexpr int kSF = 72;    // [16][64] fp32 (+8): K~, B~
+constexpr int kSJ2 = 68;   // [8 token pairs][64] float2 (+4): K-
+constexpr int kSV2 = 36;   // [8 token pairs][32] float2 (+4): V
 constexpr float kMinDecay = 1e-30f;
 
 template <typename Tin, typename TV>
@@ -83,11 +86,11 @@ struct Lay {
   static constexpr size_t oChain = oRaw + 2 * kRaw;
   // preparation scratch
   static constexpr size_t oG = oChain + 2 * kChain;          // float [16][64] gamma
-  static constexpr size_t oKT = oG + kL * kD * 4;            // uint4 [16][kSP]
-  static constexpr size_t oBT = oKT + 16 * kSP * 16;
-  static constexpr size_t oKB = oBT + 16 * kSP * 16;         // uint4 [8][kSJ]
-  static constexpr size_t oVP = oKB + 8 * kSJ * 16;          // uint4 [8][kSV]
-  static constexpr size_t oMAK = oVP + 8 * kSV * 16;         // uint4 [16][kSM] each: M_ak, M_rk split
+  static constexpr size_t oKT = oG + kL * kD * 4;            // float [16][kSF]: K~, B~
+  static constexpr size_t oBT = oKT + 16 * kSF * 4;
+  static constexpr size_t oKB = oBT + 16 * kSF * 4;          // float2 [8][kSJ2]: K- in token pairs
+  static constexpr size_t oVP = oKB + 8 * kSJ2 * 8;          // float2 [8][kSV2]: V in token pairs
+  static constexpr size_t oMAK = oVP + 8 * kSV2 * 8;          // uint4 [16][kSM] each: M_ak, M_rk split
   static constexpr size_t oMRK = oMAK + 16 * kSM * 16;
   static constexpr size_t oMAB = oMRK + 16 * kSM * 16;       // float [16][16]: M_ab
   // output staging (x2): y, sa [16][kSO]
@@ -155,6 +158,16 @@ __device__ __forceinline__ FragA frag_a(uint4 r0, uint4 r8) {
   FragA a;
   a.h[0] = r0.x; a.h[2] = r0.y; a.l[0] = r0.z; a.l[2] = r0.w;
   a.h[1] = r8.x; a.h[3] = r8.y; a.l[1] = r8.z; a.l[3] = r8.w;
+  return a;
+}
+
+// A operand from fp32 pairs: row g -> (a0, a2), row g + 8 -> (a1, a3), split here
+__device__ __forceinline__ FragA frag_a2(float2 r0, float2 r8) {
+  FragA a;
+  split(r0.x, a.h[0], a.l[0]);
+  split(r0.y, a.h[2], a.l[2]);
+  split(r8.x, a.h[1], a.l[1]);
+  split(r8.y, a.h[3], a.l[3]);
   return a;
 }
 
@@ -472,10 +485,10 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
   const int pw = pt >> 5;              // 0 .. 9
   const int g = lane >> 2, q = lane & 3;
   float* G = reinterpret_cast<float*>(sm + LY::oG);
-  uint4* KT = reinterpret_cast<uint4*>(sm + LY::oKT);
-  uint4* BT = reinterpret_cast<uint4*>(sm + LY::oBT);
-  uint4* KB = reinterpret_cast<uint4*>(sm + LY::oKB);
-  uint4* VP = reinterpret_cast<uint4*>(sm + LY::oVP);
+  float* KT = reinterpret_cast<float*>(sm + LY::oKT);
+  float* BT = reinterpret_cast<float*>(sm + LY::oBT);
+  float2* KB = reinterpret_cast<float2*>(sm + LY::oKB);
+  float2* VP = reinterpret_cast<float2*>(sm + LY::oVP);
   uint4* MAK = reinterpret_cast<uint4*>(sm + LY::oMAK);
   uint4* MRK = reinterpret_cast<uint4*>(sm + LY::oMRK);
   float* MAB = reinterpret_cast<float*>(sm + LY::oMAB);
@@ -558,7 +571,7 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
         const int tp = e >> 5, i = e & 31;
         const float v0 = 2 * tp < nm ? raw_at(rv + 2 * tp * kR + i) : 0.f;
         const float v1 = 2 * tp + 1 < nm ? raw_at(rv + (2 * tp + 1) * kR + i) : 0.f;
-        VP[tp * kSV + i] = split_pair(v0, v1);
+        VP[tp * kSV2 + i] = make_float2(v0, v1);
       }
     }
     bar_prep();
@@ -592,14 +605,14 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
         AH[t1 * kSP + jp] = split_pair(a1.x * g0.x, a1.y * g0.y);
         RH[t0 * kSP + jp] = split_pair(r0.x * g0.x, r0.y * g0.y);
         RH[t1 * kSP + jp] = split_pair(r1.x * g1.x, r1.y * g1.y);
-        KT[t0 * kSP + jp] = split_pair(k0.x * i0.x, k0.y * i0.y);
-        KT[t1 * kSP + jp] = split_pair(k1.x * i1.x, k1.y * i1.y);
-        BT[t0 * kSP + jp] = split_pair(b0.x * i0.x, b0.y * i0.y);
-        BT[t1 * kSP + jp] = split_pair(b1.x * i1.x, b1.y * i1.y);
+        *reinterpret_cast<float2*>(KT + t0 * kSF + j) = make_float2(k0.x * i0.x, k0.y * i0.y);
+        *reinterpret_cast<float2*>(KT + t1 * kSF + j) = make_float2(k1.x * i1.x, k1.y * i1.y);
+        *reinterpret_cast<float2*>(BT + t0 * kSF + j) = make_float2(b0.x * i0.x, b0.y * i0.y);
+        *reinterpret_cast<float2*>(BT + t1 * kSF + j) = make_float2(b1.x * i1.x, b1.y * i1.y);
         // gamma_L / gamma_t
         const float f00 = gl.x * i0.x, f01 = gl.y * i0.y, f10 = gl.x * i1.x, f11 = gl.y * i1.y;
-        KB[tp * kSJ + j] = split_pair(k0.x * f00, k1.x * f10);
-        KB[tp * kSJ + j + 1] = split_pair(k0.y * f01, k1.y * f11);
+        KB[tp * kSJ2 + j] = make_float2(k0.x * f00, k1.x * f10);
+        KB[tp * kSJ2 + j + 1] = make_float2(k0.y * f01, k1.y * f11);
         BB[tp * kSJ + j] = split_pair(b0.x * f00, b1.x * f10);
         BB[tp * kSJ + j + 1] = split_pair(b0.y * f01, b1.y * f11);
       }
@@ -635,12 +648,12 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
       auto mjob = [&](int job) {
         const int xr = job >> 2, yk = (job >> 1) & 1, nt = job & 1;
         const uint4* X = xr ? RH : AH;
-        const uint4* Yv = yk ? KT : BT;
+        const float* Yv = yk ? KT : BT;
         float acc[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma3(acc[kk & 3], frag_a(X[g * kSP + kk * 4 + q], X[(g + 8) * kSP + kk * 4 + q]),
-               frag_b(Yv[(nt * 8 + g) * kSP + kk * 4 + q]));
+               frag_b2(*reinterpret_cast<const float2*>(Yv + (nt * 8 + g) * kSF + kk * 8 + 2 * q)));
         float sum[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) sum[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
@@ -664,9 +677,9 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
         float acc[8][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const FragA av = frag_a(VP[(kk * 4 + q) * kSV + um * 16 + g], VP[(kk * 4 + q) * kSV + um * 16 + g + 8]);
+          const FragA av = frag_a2(VP[(kk * 4 + q) * kSV2 + um * 16 + g], VP[(kk * 4 + q) * kSV2 + um * 16 + g + 8]);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mma3(acc[u], av, frag_b(KB[(kk * 4 + q) * kSJ + u * 8 + g]));
+          for (int u = 0; u < 8; ++u) mma3(acc[u], av, frag_b2(KB[(kk * 4 + q) * kSJ2 + u * 8 + g]));
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -716,7 +729,7 @@ fwdc_kernel(int T, int H, int chunk, int nchunks, FwdcPtrs P) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            mma3(acc, frag_a(VP[(kk * 4 + q) * kSV + um * 16 + g], VP[(kk * 4 + q) * kSV + um * 16 + g + 8]),
+            mma3(acc, frag_a2(VP[(kk * 4 + q) * kSV2 + um * 16 + g], VP[(kk * 4 + q) * kSV2 + um * 16 + g + 8]),
                  frag_b(M[(nt * 8 + g) * kSM + kk * 4 + q]));
           float* C = which ? CY : CAK;
           *reinterpret_cast<float2*>(C + (um * 16 + g) * kSC + nt * 8 + 2 * q) = make_float2(acc[0], acc[1]);
