@@ -2,13 +2,12 @@
 //
 // Source: "RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel
 // architecture", Backward listing: chunks walked in reverse from the exact checkpoints,
-// the previous state rebuilt as (h - v k - sa b) / w, the VJP giving dr, dw, dk, dv, da,
-// db.  With X_t the gradient w.r.t. the state S_t after token t, including y_t's term:
+// the VJP giving dr, dw, dk, dv, da, db.  With X_t the gradient w.r.t. the state S_t after
+// token t, including y_t's term:
 //     X_t     = X'_t + dy_t r_t^T          (X'_t from later tokens; X'_{T-1} = dhT)
 //     dsa_t   = X_t b_t,   dv_t = X_t k_t                     (row sums)
 //     X'_{t-1} = X_t diag(w_t) + dsa_t a_t^T
 //     dr_t = S_t^T dy_t,  dk_t = X_t^T v_t,  db_t = X_t^T sa_t (column sums)
-//     S_{t-1} = (S_t - v_t k_t^T - sa_t b_t^T) diag(1/w_t)
 //     dw_t = colsum(X_t o S_{t-1}),  da_t = S_{t-1}^T dsa_t    (column sums)
 // The state-gradient recurrence needs only the row sums; the column sums need X_t and S_t
 // but nothing serial once X at each chunk end and every dsa_t are known.  So:
@@ -19,13 +18,26 @@
 // and dv_t -- writing dv, dsa (workspace), X at every chunk end (workspace) and dh0.
 // Mapping as the forward: a head in two row blocks of 32 rows, thread = 4 rows x 4
 // columns, 16-lane row sums, tiles of 32 tokens staged with cp.async (here in reverse).
+// (With chunk % 16 == 0 the walk runs instead on the 16-token sub-chunk kernel.)
 //
-// Phase 2 (every chunk of every head at once): one CTA per (head, chunk) walks the chunk
-// in reverse from S = h_ckpt[c] and X = X at the chunk end, rebuilding S by the page's
-// formula and X with the known dsa, and forms the five column sums.  Thread = 32 rows x 2
-// columns of S and X (row pairs as fp32x2); a column sum is a sum over the thread's 32
-// rows plus one shuffle with the lane holding the other 32 rows: no shared-memory
-// reduction, no barrier inside the walk.
+// Phase 2 (every chunk of every head at once): one CTA per (head, chunk), in two passes
+// over the chunk, neither of which divides by w (the page's rebuild of S_{t-1} as
+// (S_t - v k^T - sa b^T) / w amplifies the checkpoint's rounding by 1/w per token):
+//   pass A walks X down from X at the chunk end -- dk_t, db_t;
+//   pass B runs S up from the state before the chunk (h_ckpt[c-1], or h0) -- da_t, dr_t;
+//   dw_t, the one sum that needs X_t and S_{t-1} together, comes from a column recurrence:
+//   with Z'_t = colsum(X'_t o S_t),
+//       w_t o dw_t = Z'_{t-1} - a_t o da_t,  Z'_t = w_t o dw_t + k_t o dk_t + b_t o db_t - r_t o dr_t
+//   (both from the two recurrences above), started from Z'_{t0-1} summed at the chunk start.
+//   Where w_t < 1/32 the division by w_t would cost digits, and dw_t is summed directly with
+//   X_t rebuilt from the chunk end (exact, rare).
+// Each pass keeps its matrix scaled by a running decay product per column (X_t = M o rho_t,
+// S_t = M o gamma_t), so a token's update is two FMAs per element with coefficients
+// a/rho, r/rho (k/gamma, b/gamma) computed once per column; where the product would fall
+// below 2^-40 the step is taken unscaled (M <- M * product + ...), so any w >= 0 works.
+// Thread = 16 rows x 4 columns of M (row pairs as fp32x2; blocks of 4 rows interleaved over
+// the four row quarters); a column sum is the thread's rows plus a reduce-scatter over the
+// four row-quarter lanes, which leaves each lane one finished column.
 #include "wkv7_device.cuh"
 #include "wkv7_launch.h"
 
@@ -290,7 +302,13 @@ gwalk_kernel(int T, int H, int chunk, int nchunks,
 // ============================================================================ phase 2
 
 constexpr int kNT2 = 64;  // 2 warps: warp q covers columns 32q .. 32q+31, all 64 rows
-constexpr int kRP = 16;   // row pairs per thread (32 rows)
+constexpr int kRP = 8;    // row pairs per thread (16 rows)
+constexpr int kCT = 4;    // columns per thread
+// a column's running decay product below 2^-40 is folded back into the state (keeps 1/product finite)
+constexpr float kRenorm = 9.094947017729282e-13f;
+// below this w_t, w_t dw_t (a difference of column sums) loses too many digits when divided by w_t:
+// dw_t is then summed directly from X_t and S_{t-1}
+constexpr float kWTiny = 0.03125f;
 
 template <typename Tin>
 struct P2Smem {
@@ -305,13 +323,133 @@ struct P2Smem {
   static constexpr size_t kBytes = oV + kTile * kD * 4;
 };
 
+// four consecutive columns of a token row
 template <typename Tin>
-__device__ __forceinline__ float2 col2(const Tin* p) {
+__device__ __forceinline__ void col4(const Tin* p, float (&o)[kCT]) {
   if constexpr (sizeof(Tin) == 2) {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-    return make_float2(bf16_lo(u), bf16_hi(u));
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    o[0] = bf16_lo(u.x), o[1] = bf16_hi(u.x), o[2] = bf16_lo(u.y), o[3] = bf16_hi(u.y);
   } else {
-    return *reinterpret_cast<const float2*>(p);
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    o[0] = f.x, o[1] = f.y, o[2] = f.z, o[3] = f.w;
+  }
+}
+
+template <typename Tin>
+__device__ __forceinline__ float col1(const Tin* p) {
+  return to_f32(*p);
+}
+
+// A thread's rows: blocks of 4 rows, interleaved over the four row quarters (r0 = 4 rq) so that the
+// quarters' reads of a token's row vector are 64 contiguous bytes.  Row pair p starts at prow(r0, p).
+__device__ __forceinline__ int prow(int r0, int p) { return 16 * (p >> 1) + r0 + 2 * (p & 1); }
+
+// the thread's row pairs (p < kRP) of columns c0 .. c0+3 of a row-major 64 x 64 fp32 matrix
+__device__ __forceinline__ void load_block(const float* __restrict__ m, int r0, int c0, float2 (&o)[kRP][kCT]) {
+#pragma unroll
+  for (int p = 0; p < kRP; ++p) {
+    const float4 e = __ldg(reinterpret_cast<const float4*>(m + (size_t)prow(r0, p) * kD + c0));
+    const float4 f = __ldg(reinterpret_cast<const float4*>(m + (size_t)(prow(r0, p) + 1) * kD + c0));
+    o[p][0] = make_float2(e.x, f.x);
+    o[p][1] = make_float2(e.y, f.y);
+    o[p][2] = make_float2(e.z, f.z);
+    o[p][3] = make_float2(e.w, f.w);
+  }
+}
+
+// The sums of x[c][j] over the four row-quarter lanes (lane bits 3 and 4), reduce-scattered: the lane
+// with row quarter rq ends with both sums of column own(rq) = 2 (rq & 1) + (rq >> 1).
+template <int NJ>
+__device__ __forceinline__ void rs_cols(const float (&x)[kCT][NJ], int rq, float (&out)[NJ]) {
+  const bool b0 = rq & 1, b1 = rq & 2;
+  float k[2][NJ];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const float send = b0 ? x[cc][j] : x[2 + cc][j];
+      const float keep = b0 ? x[2 + cc][j] : x[cc][j];
+      k[cc][j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const float send = b1 ? k[0][j] : k[1][j];
+    const float keep = b1 ? k[1][j] : k[0][j];
+    out[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+}
+
+// The running decay product of a column: next[c] = scale[c] * w[c].  Where it would drop below kRenorm
+// the step is taken unscaled instead -- M[:, c] is multiplied by f[c] = scale[c] * w[c] in the update and
+// next[c] = 1 -- so no coefficient is ever divided by a tiny product (any w >= 0 works).  Returns whether
+// any lane of the warp takes such a step (then the sweep multiplies M by f).
+__device__ __forceinline__ bool decay_step(const float (&scale)[kCT], const float (&wv)[kCT], float (&next)[kCT],
+                                           float2 (&f)[kCT]) {
+  bool any = false;
+#pragma unroll
+  for (int c = 0; c < kCT; ++c) {
+    next[c] = scale[c] * wv[c];
+    const bool fold = next[c] < kRenorm;
+    f[c] = bcast2(fold ? next[c] : 1.f);
+    if (fold) next[c] = 1.f;
+    any |= fold;
+  }
+  return __any_sync(0xffffffffu, any);
+}
+
+// Pass A step at one token (M = X_t / rho_t): acc[0] += v_t o M, acc[1] += sa_t o M, then
+// M <- M * f + dsa_t ca^T + dy_{t-1} cr^T
+template <bool kFold>
+__device__ __forceinline__ void sweep_a(float2 (&M)[kRP][kCT], const float* rv, const float* rs, const float* rq,
+                                        const float* re, const float2 (&ca)[kCT], const float2 (&cr)[kCT],
+                                        const float2 (&f)[kCT], float2 (&acc)[2][kCT][2]) {
+#pragma unroll
+  for (int p4 = 0; p4 < kRP / 2; ++p4) {
+    const float4 v4 = *reinterpret_cast<const float4*>(rv + 16 * p4);
+    const float4 s4 = *reinterpret_cast<const float4*>(rs + 16 * p4);
+    const float4 q4 = *reinterpret_cast<const float4*>(rq + 16 * p4);
+    const float4 e4 = *reinterpret_cast<const float4*>(re + 16 * p4);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int p = 2 * p4 + h;
+      const float2 v2 = h ? hi2(v4) : lo2(v4), s2 = h ? hi2(s4) : lo2(s4);
+      const float2 q2 = h ? hi2(q4) : lo2(q4), e2 = h ? hi2(e4) : lo2(e4);
+#pragma unroll
+      for (int c = 0; c < kCT; ++c) {
+        acc[0][c][h] = p4 == 0 ? __fmul2_rn(v2, M[p][c]) : __ffma2_rn(v2, M[p][c], acc[0][c][h]);
+        acc[1][c][h] = p4 == 0 ? __fmul2_rn(s2, M[p][c]) : __ffma2_rn(s2, M[p][c], acc[1][c][h]);
+        const float2 m = kFold ? __fmul2_rn(M[p][c], f[c]) : M[p][c];
+        M[p][c] = __ffma2_rn(q2, ca[c], __ffma2_rn(e2, cr[c], m));
+      }
+    }
+  }
+}
+
+// Pass B step at one token (M = S_{t-1} / gamma_{t-1}): acc[0] += dsa_t o M, M <- M * f + v_t ck^T +
+// sa_t cb^T, acc[1] += dy_t o M
+template <bool kFold>
+__device__ __forceinline__ void sweep_b(float2 (&M)[kRP][kCT], const float* rq, const float* rv, const float* rs,
+                                        const float* rd, const float2 (&ck)[kCT], const float2 (&cb)[kCT],
+                                        const float2 (&f)[kCT], float2 (&acc)[2][kCT][2]) {
+#pragma unroll
+  for (int p4 = 0; p4 < kRP / 2; ++p4) {
+    const float4 q4 = *reinterpret_cast<const float4*>(rq + 16 * p4);
+    const float4 v4 = *reinterpret_cast<const float4*>(rv + 16 * p4);
+    const float4 s4 = *reinterpret_cast<const float4*>(rs + 16 * p4);
+    const float4 d4 = *reinterpret_cast<const float4*>(rd + 16 * p4);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int p = 2 * p4 + h;
+      const float2 q2 = h ? hi2(q4) : lo2(q4), v2 = h ? hi2(v4) : lo2(v4);
+      const float2 s2 = h ? hi2(s4) : lo2(s4), d2 = h ? hi2(d4) : lo2(d4);
+#pragma unroll
+      for (int c = 0; c < kCT; ++c) {
+        acc[0][c][h] = p4 == 0 ? __fmul2_rn(q2, M[p][c]) : __ffma2_rn(q2, M[p][c], acc[0][c][h]);
+        const float2 m = kFold ? __fmul2_rn(M[p][c], f[c]) : M[p][c];
+        M[p][c] = __ffma2_rn(v2, ck[c], __ffma2_rn(s2, cb[c], m));
+        acc[1][c][h] = p4 == 0 ? __fmul2_rn(d2, M[p][c]) : __ffma2_rn(d2, M[p][c], acc[1][c][h]);
+      }
+    }
   }
 }
 
@@ -320,8 +458,8 @@ __global__ void __launch_bounds__(kNT2)
 colgrad_kernel(int T, int H, int chunk, int nchunks,
                const Tin* __restrict__ r, const Tin* __restrict__ w, const Tin* __restrict__ k,
                const Tin* __restrict__ v, const Tin* __restrict__ a, const Tin* __restrict__ b,
-               const float* __restrict__ h_ckpt, const float* __restrict__ sa, const float* __restrict__ dy,
-               const float* __restrict__ dsa_ws, const float* __restrict__ xck_ws,
+               const float* __restrict__ h0, const float* __restrict__ h_ckpt, const float* __restrict__ sa,
+               const float* __restrict__ dy, const float* __restrict__ dsa_ws, const float* __restrict__ xck_ws,
                float* __restrict__ dr, float* __restrict__ dw, float* __restrict__ dk,
                float* __restrict__ da, float* __restrict__ db) {
   using L = P2Smem<Tin>;
@@ -344,14 +482,17 @@ colgrad_kernel(int T, int H, int chunk, int nchunks,
   const int hi = bh - bi * H;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int c0 = 2 * (16 * (tid >> 5) + (lane & 15));  // columns c0, c0 + 1
-  const int half = lane >> 4;                          // rows 32*half .. 32*half + 31
-  const int r0 = 32 * half;
+  const int c0 = 32 * (tid >> 5) + 4 * (lane & 7);  // columns c0 .. c0+3
+  const int rq = lane >> 3;                         // rows 16 i + 4 rq .. 16 i + 4 rq + 3, i < 4
+  const int r0 = 4 * rq;
+  const int own = 2 * (rq & 1) + (rq >> 1);         // the column c0 + own this lane finishes
   const int t0 = ci * chunk;
   const int n = min(chunk, T - t0);
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
-  const size_t cko = ((size_t)bh * nchunks + ci) * kD * kD;
+  const float* xend = xck_ws + ((size_t)bh * nchunks + ci) * kD * kD;
+  const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
+                           : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
 
   // ---- stage the chunk's inputs
   {
@@ -376,88 +517,179 @@ colgrad_kernel(int T, int H, int chunk, int nchunks,
       }
     cp_async_commit();
   }
-  // ---- S = h_ckpt[ci], X = X at the chunk's last token: rows r0.., columns c0, c0+1, as row pairs
-  float2 S[kRP][2], X[kRP][2];
-#pragma unroll
-  for (int p = 0; p < kRP; ++p) {
-    const size_t o0 = cko + (size_t)(r0 + 2 * p) * kD + c0;
-    const float2 se = __ldg(reinterpret_cast<const float2*>(h_ckpt + o0));
-    const float2 so = __ldg(reinterpret_cast<const float2*>(h_ckpt + o0 + kD));
-    const float2 xe = __ldg(reinterpret_cast<const float2*>(xck_ws + o0));
-    const float2 xo = __ldg(reinterpret_cast<const float2*>(xck_ws + o0 + kD));
-    S[p][0] = make_float2(se.x, so.x);
-    S[p][1] = make_float2(se.y, so.y);
-    X[p][0] = make_float2(xe.x, xo.x);
-    X[p][1] = make_float2(xe.y, xo.y);
-  }
+  // M = X at the chunk's last token (rho = 1): rows r0 .. r0+15, columns c0 .. c0+3, as row pairs
+  float2 M[kRP][kCT];
+  load_block(xend, r0, c0, M);
   cp_async_wait<0>();
   __syncthreads();
   for (int e = tid; e < n * kD; e += kNT2) sV[e] = to_f32(cV[e]);
   __syncthreads();
 
-  // ---- reverse walk over the chunk
+  // ---- pass A, tokens n-1 .. 0: X_t = M o rho_t (columns), X'_{t-1} = X_t diag(w_t) + dsa_t a_t^T,
+  // X_{t-1} = X'_{t-1} + dy_{t-1} r_{t-1}^T; dk_t = X_t^T v_t, db_t = X_t^T sa_t
+  float rho[kCT] = {1.f, 1.f, 1.f, 1.f};
   for (int tt = n - 1; tt >= 0; --tt) {
-    const float2 w2 = col2<Tin>(cW + tt * kD + c0);
-    const float2 wi2 = make_float2(1.0f / w2.x, 1.0f / w2.y);
-    const float2 k2 = col2<Tin>(cK + tt * kD + c0);
-    const float2 a2 = col2<Tin>(cA + tt * kD + c0);
-    const float2 b2 = col2<Tin>(cB + tt * kD + c0);
-    const bool more = tt > 0;
-    const float2 rp2 = more ? col2<Tin>(cR + (tt - 1) * kD + c0) : make_float2(0.f, 0.f);
-    const float2 wb[2] = {bcast2(w2.x), bcast2(w2.y)}, wib[2] = {bcast2(wi2.x), bcast2(wi2.y)};
-    const float2 nkb[2] = {bcast2(-k2.x), bcast2(-k2.y)}, ab2[2] = {bcast2(a2.x), bcast2(a2.y)};
-    const float2 nbb[2] = {bcast2(-b2.x), bcast2(-b2.y)}, rpb[2] = {bcast2(rp2.x), bcast2(rp2.y)};
-    const float* rv = sV + tt * kD + r0;
-    const float* rs = sSa + tt * kD + r0;
-    const float* rq = sDsa + tt * kD + r0;
-    const float* rd = sDy + tt * kD + r0;
-    const float* re = sDy + (tt - 1) * kD + r0;  // dy_{t-1}, read only when `more`
+    const int tm = tt > 0 ? tt - 1 : 0;  // dy_{t-1}, r_{t-1}; token 0 of the chunk takes none
+    float wv[kCT], av[kCT], rv[kCT];
+    col4<Tin>(cW + tt * kD + c0, wv);
+    col4<Tin>(cA + tt * kD + c0, av);
+    col4<Tin>(cR + tm * kD + c0, rv);
+    float rn[kCT];
+    float2 f[kCT];
+    const bool fold = decay_step(rho, wv, rn, f);
+    float2 ca[kCT], cr[kCT];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c) {
+      const float ir = __fdividef(1.f, rn[c]);
+      ca[c] = bcast2(av[c] * ir);
+      cr[c] = bcast2(tt > 0 ? rv[c] * ir : 0.f);
+    }
+    const float* rvp = sV + tt * kD + r0;
+    const float* rsp = sSa + tt * kD + r0;
+    const float* rqp = sDsa + tt * kD + r0;
+    const float* rep = sDy + tm * kD + r0;
+    float2 acc[2][kCT][2];
+    if (fold)
+      sweep_a<true>(M, rvp, rsp, rqp, rep, ca, cr, f, acc);
+    else
+      sweep_a<false>(M, rvp, rsp, rqp, rep, ca, cr, f, acc);
+    float x[kCT][2], g[2];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float2 s = __fadd2_rn(acc[j][c][0], acc[j][c][1]);
+        x[c][j] = (s.x + s.y) * rho[c];
+      }
+    rs_cols<2>(x, rq, g);
+    const size_t o = base + (size_t)(t0 + tt) * tstride + c0 + own;
+    dk[o] = g[0];
+    db[o] = g[1];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c) rho[c] = rn[c];
+  }
 
-    float2 cdr[2], cdw[2], cdk[2], cdb[2], cda[2];
+  // ---- M = S_{t0-1} (the state before the chunk; gamma = 1) and Z'_{t0-1} = colsum(X'_{t0-1} o S_{t0-1})
+  float zq;
+  {
+    float2 S[kRP][kCT];
+    if (s0 != nullptr) {
+      load_block(s0, r0, c0, S);
+    } else {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) cdr[c] = cdw[c] = cdk[c] = cdb[c] = cda[c] = make_float2(0.f, 0.f);
+      for (int p = 0; p < kRP; ++p)
 #pragma unroll
-    for (int p4 = 0; p4 < kRP / 2; ++p4) {  // 4 rows (2 row pairs) per step
-      const float4 v4 = *reinterpret_cast<const float4*>(rv + 4 * p4);
-      const float4 s4 = *reinterpret_cast<const float4*>(rs + 4 * p4);
-      const float4 q4 = *reinterpret_cast<const float4*>(rq + 4 * p4);
-      const float4 d4 = *reinterpret_cast<const float4*>(rd + 4 * p4);
-      const float4 e4 = more ? *reinterpret_cast<const float4*>(re + 4 * p4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < kCT; ++c) S[p][c] = make_float2(0.f, 0.f);
+    }
+    float2 z[kCT];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int p = 2 * p4 + h;
-        const float2 v2 = h ? hi2(v4) : lo2(v4);
-        const float2 s2 = h ? hi2(s4) : lo2(s4);
-        const float2 q2 = h ? hi2(q4) : lo2(q4);
-        const float2 d2 = h ? hi2(d4) : lo2(d4);
-        const float2 e2 = h ? hi2(e4) : lo2(e4);
+    for (int c = 0; c < kCT; ++c) z[c] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          cdr[c] = __ffma2_rn(d2, S[p][c], cdr[c]);
-          const float2 sp = __fmul2_rn(__ffma2_rn(s2, nbb[c], __ffma2_rn(v2, nkb[c], S[p][c])), wib[c]);
-          S[p][c] = sp;
-          cdw[c] = __ffma2_rn(X[p][c], sp, cdw[c]);
-          cdk[c] = __ffma2_rn(X[p][c], v2, cdk[c]);
-          cdb[c] = __ffma2_rn(X[p][c], s2, cdb[c]);
-          cda[c] = __ffma2_rn(q2, sp, cda[c]);
-          X[p][c] = __ffma2_rn(X[p][c], wb[c], __ffma2_rn(q2, ab2[c], __fmul2_rn(e2, rpb[c])));
+    for (int p = 0; p < kRP; ++p)
+#pragma unroll
+      for (int c = 0; c < kCT; ++c) {
+        z[c] = __ffma2_rn(M[p][c], S[p][c], z[c]);
+        M[p][c] = S[p][c];
+      }
+    float x[kCT][1], g[1];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c) x[c][0] = (z[c].x + z[c].y) * rho[c];
+    rs_cols<1>(x, rq, g);
+    zq = g[0];
+  }
+
+  // ---- pass B, tokens 0 .. n-1: S_t = M o gamma_t; da_t = S_{t-1}^T dsa_t, dr_t = S_t^T dy_t and
+  //   w_t o dw_t = Z'_{t-1} - a_t o da_t,  Z'_t = w_t o dw_t + k_t o dk_t + b_t o db_t - r_t o dr_t
+  // with Z'_t = colsum(X'_t o S_t) (X'_t: X_t without dy_t r_t^T); this lane carries Z' of column c0 + own
+  float gam[kCT] = {1.f, 1.f, 1.f, 1.f};
+  for (int tt = 0; tt < n; ++tt) {
+    float wv[kCT], kv[kCT], bv[kCT];
+    col4<Tin>(cW + tt * kD + c0, wv);
+    col4<Tin>(cK + tt * kD + c0, kv);
+    col4<Tin>(cB + tt * kD + c0, bv);
+    const size_t o = base + (size_t)(t0 + tt) * tstride + c0 + own;
+    const float dko = dk[o], dbo = db[o];  // written by this thread in pass A
+    const float wo = col1<Tin>(cW + tt * kD + c0 + own), ko = col1<Tin>(cK + tt * kD + c0 + own);
+    const float bo = col1<Tin>(cB + tt * kD + c0 + own), ao = col1<Tin>(cA + tt * kD + c0 + own);
+    const float ro = col1<Tin>(cR + tt * kD + c0 + own);
+
+    // direct dw_t = colsum(X_t o S_{t-1}) where w_t is tiny: X_t rebuilt from the chunk end
+    float dwd = 0.f;
+    {
+      bool tiny = false;
+#pragma unroll
+      for (int c = 0; c < kCT; ++c) tiny |= wv[c] < kWTiny;
+      if (__any_sync(0xffffffffu, tiny)) {
+        float x[kCT][1], g[1];
+#pragma unroll
+        for (int c = 0; c < kCT; ++c) x[c][0] = 0.f;
+#pragma unroll
+        for (int p = 0; p < kRP; ++p) {
+          float2 X[kCT];
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const float4 e = __ldg(reinterpret_cast<const float4*>(xend + (size_t)(prow(r0, p) + hr) * kD + c0));
+            const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+            for (int c = 0; c < kCT; ++c) (hr ? X[c].y : X[c].x) = ev[c];
+          }
+          for (int u = n - 1; u > tt; --u) {
+            float wu[kCT], au[kCT], ru[kCT];
+            col4<Tin>(cW + u * kD + c0, wu);
+            col4<Tin>(cA + u * kD + c0, au);
+            col4<Tin>(cR + (u - 1) * kD + c0, ru);
+            const float2 q2 = *reinterpret_cast<const float2*>(sDsa + u * kD + prow(r0, p));
+            const float2 e2 = *reinterpret_cast<const float2*>(sDy + (u - 1) * kD + prow(r0, p));
+#pragma unroll
+            for (int c = 0; c < kCT; ++c)
+              X[c] = __ffma2_rn(X[c], bcast2(wu[c]), __ffma2_rn(q2, bcast2(au[c]), __fmul2_rn(e2, bcast2(ru[c]))));
+          }
+#pragma unroll
+          for (int c = 0; c < kCT; ++c) {
+            const float2 m = __fmul2_rn(X[c], M[p][c]);
+            x[c][0] += (m.x + m.y) * gam[c];
+          }
         }
+        rs_cols<1>(x, rq, g);
+        dwd = g[0];
       }
     }
-    // sum over this thread's 32 rows, then with the lane holding the other 32 rows
-    float g[10] = {cdr[0].x + cdr[0].y, cdr[1].x + cdr[1].y, cdw[0].x + cdw[0].y, cdw[1].x + cdw[1].y,
-                   cdk[0].x + cdk[0].y, cdk[1].x + cdk[1].y, cdb[0].x + cdb[0].y, cdb[1].x + cdb[1].y,
-                   cda[0].x + cda[0].y, cda[1].x + cda[1].y};
+
+    float gn[kCT];
+    float2 f[kCT];
+    const bool fold = decay_step(gam, wv, gn, f);
+    float2 ck[kCT], cb[kCT];
 #pragma unroll
-    for (int u = 0; u < 10; ++u) g[u] += __shfl_xor_sync(0xffffffffu, g[u], 16);
-    if (half == 0) {
-      const size_t o = base + (size_t)(t0 + tt) * tstride + c0;
-      *reinterpret_cast<float2*>(dr + o) = make_float2(g[0], g[1]);
-      *reinterpret_cast<float2*>(dw + o) = make_float2(g[2], g[3]);
-      *reinterpret_cast<float2*>(dk + o) = make_float2(g[4], g[5]);
-      *reinterpret_cast<float2*>(db + o) = make_float2(g[6], g[7]);
-      *reinterpret_cast<float2*>(da + o) = make_float2(g[8], g[9]);
+    for (int c = 0; c < kCT; ++c) {
+      const float ig = __fdividef(1.f, gn[c]);
+      ck[c] = bcast2(kv[c] * ig);
+      cb[c] = bcast2(bv[c] * ig);
     }
+    const float* rqp = sDsa + tt * kD + r0;
+    const float* rvp = sV + tt * kD + r0;
+    const float* rsp = sSa + tt * kD + r0;
+    const float* rdp = sDy + tt * kD + r0;
+    float2 acc[2][kCT][2];
+    if (fold)
+      sweep_b<true>(M, rqp, rvp, rsp, rdp, ck, cb, f, acc);
+    else
+      sweep_b<false>(M, rqp, rvp, rsp, rdp, ck, cb, f, acc);
+    float x[kCT][2], g[2];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c) {
+      const float2 sA = __fadd2_rn(acc[0][c][0], acc[0][c][1]);
+      const float2 sR = __fadd2_rn(acc[1][c][0], acc[1][c][1]);
+      x[c][0] = (sA.x + sA.y) * gam[c];  // gamma_{t-1}
+      x[c][1] = (sR.x + sR.y) * gn[c];   // gamma_t
+    }
+    rs_cols<2>(x, rq, g);
+    const float wdw = fmaf(-ao, g[0], zq);
+    dw[o] = wo < kWTiny ? dwd : wdw * __fdividef(1.f, wo);
+    da[o] = g[0];
+    dr[o] = g[1];
+    zq = fmaf(-ro, g[1], fmaf(bo, dbo, fmaf(ko, dko, wdw)));
+#pragma unroll
+    for (int c = 0; c < kCT; ++c) gam[c] = gn[c];
   }
 }
 
@@ -490,7 +722,7 @@ cudaError_t launch_bwd2_t(const BwdArgs& p, float* dsa_ws, float* xck_ws, cudaSt
     const unsigned grid = (unsigned)p.B * p.H * p.nchunks;
     kern<<<grid, kNT2, smem, stream>>>(p.T, p.H, p.chunk, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
                                        (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
-                                       (const Tin*)p.in.b, p.h_ckpt, p.sa, p.dy, dsa_ws, xck_ws, p.dr, p.dw, p.dk,
+                                       (const Tin*)p.in.b, p.h0, p.h_ckpt, p.sa, p.dy, dsa_ws, xck_ws, p.dr, p.dw, p.dk,
                                        p.da, p.db);
     return cudaGetLastError();
   }

@@ -160,8 +160,9 @@ def test_strong_decay_forward(wkv7, dtype, lo, hi):
     """Decays far below the workloads' range.  With w in (0.005, 0.05) the 16-token decay drops
     under 1e-30 in some sub-chunks, which then advance token by token; (0.02, 0.2) stays in the
     sub-chunk form with 1/gamma up to ~1e27.  The first 40 tokens keep the workloads' decay, so
-    one sequence mixes both paths.  Forward only: the backward's division by w amplifies rounding
-    by (1/w)^31 here, as the page warns."""
+    one sequence mixes both paths.  Forward only here: the single-pass backward rebuilds the state
+    by dividing by w, which amplifies rounding by (1/w)^31 at these decays, as the page warns; the
+    two-phase backward, which never divides by w, is checked under the same decays below."""
     x = gen.random_small(4242, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
     rng = np.random.default_rng(7)
     w = x["w"].copy()
@@ -171,6 +172,22 @@ def test_strong_decay_forward(wkv7, dtype, lo, hi):
     x["w"] = w.astype(np.float32)
     for fwd in FWD:
         check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd=fwd), 32, with_grads=False)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2)])
+def test_strong_decay_backward_two_phase(wkv7, dtype, lo, hi):
+    """The two-phase backward under the same strong decays: its column gradients run the state
+    forward from the chunk's start and the state gradient backward from the chunk's end, with no
+    division by w, so the gradients stay within tolerance; dw where w < 1/32 is summed directly."""
+    x = gen.random_small(4243, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    rng = np.random.default_rng(8)
+    w = x["w"].copy()
+    w[:, 40:] = lo + (hi - lo) * rng.random(w[:, 40:].shape)
+    if dtype == "bf16":
+        w = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    x["w"] = w.astype(np.float32)
+    check(x, run_gpu(wkv7, x, dtype, 32, "two_phase"), 32)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
