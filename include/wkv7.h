@@ -117,12 +117,15 @@ int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
  *           workspace every dsa and the state gradient at every chunk end) -- 16 tokens per
  *           step in the closed form of that recurrence when chunk % 16 == 0 and the B*H*2
  *           row blocks fit one wave of SMs, else token by token -- then every chunk of
- *           every head forms its column gradients (dr, dw, dk, da, db) at once.
- *           Without one (or without sa) a single pass does everything.  Both give the
- *           same results up to fp32 rounding.
- * Each chunk is walked in reverse from its end checkpoint, the earlier states
- * rebuilt as (h - v k^T - sa b^T) / w (column j divided by w_j).  Sums are taken in a
- * fixed order (no atomics): results are deterministic.
+ *           every head forms its column gradients (dr, dw, dk, da, db) at once, running
+ *           the state forward from the checkpoint before the chunk (h0 for the first) and
+ *           the state gradient backward from the chunk end, with no division by w.
+ *           Without one (or without sa) a single pass does everything: each chunk is
+ *           walked in reverse from its end checkpoint, the earlier states rebuilt as
+ *           (h - v k^T - sa b^T) / w (column j divided by w_j), which amplifies rounding
+ *           by 1/w per token.  The two-phase results are ~1e-7 of exact at ordinary
+ *           decays; the single pass's ~5e-4.
+ * Sums are taken in a fixed order (no atomics): results are deterministic.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
