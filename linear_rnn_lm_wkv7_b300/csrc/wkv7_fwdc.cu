@@ -53,7 +53,6 @@ constexpr int kChainThreads = 64;
 constexpr int kSP = 36;    // [16][32 pairs] (+4): A^, R^, K~, B~
 constexpr int kSM = 12;    // [16][8 pairs] (+4): (I - M_ab)^-1, M_rb
 constexpr int kSJ = 66;    // [8 token pairs][64] (+2): K-, B-
-constexpr int kSV = 34;    // [8 token pairs][32] (+2): V
 constexpr int kSC = 24;    // [32][16] fp32 (+8): the V corrections of sa and y
 constexpr int kSU = 72;    // [32][64] fp32 (+8): U = V^T K-, and the state in the token-by-token path
 constexpr int kSO = 36;    // [16][32] fp32 (+4): y / sa staging

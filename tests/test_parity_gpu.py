@@ -191,6 +191,22 @@ def test_strong_decay_backward_two_phase(wkv7, dtype, lo, hi):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_and_vanishing_decay_two_phase(wkv7, dtype):
+    """w = 0 (the state forgets a column entirely) and w = 1e-30 at scattered tokens and columns, in
+    both forward kernels and the two-phase backward (whose column pass takes such steps unscaled and
+    sums dw directly there).  Both values are exact in bf16 and fp32."""
+    x = gen.random_small(4244, B=2, T=96, H=2, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    rng = np.random.default_rng(9)
+    w = x["w"].copy()
+    pick = rng.random(w.shape)
+    w[pick < 0.02] = 0.0
+    w[(pick >= 0.02) & (pick < 0.04)] = 1e-30
+    x["w"] = w.astype(np.float32)
+    for fwd in FWD:
+        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd=fwd), 32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_many_heads_one_cta_per_head(wkv7, dtype):
     """B*H = 78 heads (more than half of 148 SMs): the one-CTA-per-head backward, ragged T."""
     x = gen.random_small(77, B=3, T=45, H=26, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
