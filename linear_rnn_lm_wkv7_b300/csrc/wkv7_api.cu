@@ -153,10 +153,12 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const voi
   p.in = {r, w, k, v, a, b};
   p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
   p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
-  if (workspace != nullptr && p.sa != nullptr) {
+  if (workspace != nullptr && (chunk == 32 || p.sa != nullptr)) {
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
     if (workspace_bytes < wkv7::backward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
-    return record_cuda(wkv7::launch_backward_two_phase(p, workspace, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    return record_cuda(chunk == 32 ? wkv7::launch_backward_transition(p, workspace, st_)
+                                   : wkv7::launch_backward_two_phase(p, workspace, st_));
   }
   return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
 }

@@ -1,0 +1,584 @@
+// WKV7 backward: the column gradients dr, dw, dk, da, db of every 32-token chunk at once, in matrix
+// form on tensor cores.
+//
+// Source: "RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel architecture", Backward
+// listing (chunks walked in reverse from the exact checkpoints; VJP for dr, dw, dk, dv, da, db).  With
+// X_t the gradient w.r.t. the state after token t (including dy_t r_t^T) and S_t the state:
+//     dr_t = S_t^T dy_t,  dk_t = X_t^T v_t,  db_t = X_t^T sa_t,  da_t = S_{t-1}^T dsa_t,
+//     dw_t = colsum(X_t o S_{t-1}),  dsa_t = X_t b_t,  X_{t-1} = X_t diag(w_t) + dsa_t a_t^T + dy_{t-1} r_{t-1}^T.
+// The walk (the transition-chain kernel run backwards) leaves X at every chunk end and dv, dh0.
+//
+// Matrix form of one chunk of n tokens (t = 0..31, steps past n padded with w = 1 and zeros), from S0
+// (the state before the chunk), X_e (X at its last token) and S_e (the state after it), with gamma,
+// A^, R^, K~, B~, M_ab, M_ak, M_rb and T = (I - M_ab)^-1 as in the transition-chain kernel and
+// Xb = (X_e - dy_{n-1} r_{n-1}^T) diag(gamma_{n-1}) (the gradient from later tokens, decayed):
+//     SA  = T U,    U = A^ S0^T + M_ak V                      (rows t: sa_t, recomputed)
+//     DSA = T^T W,  W = B~ Xb^T + M_rb^T DY                   (rows t: dsa_t)
+//     L1 = tril(DY V^T), L2 = tril(DY SA^T), L3 = tril(DSA V^T, -1), L4 = tril(DSA SA^T, -1)
+//     DR = Gamma   o (DY  S0 + L1 K~ + L2 B~)
+//     DA = Gamma_- o (DSA S0 + L3 K~ + L4 B~)                 (Gamma_- row t = gamma_{t-1})
+//     DK = Gamma^-1 o (V  Xb + L3^T A^ + L1^T R^)
+//     DB = Gamma^-1 o (SA Xb + L4^T A^ + L2^T R^)
+// (X_t diag(gamma_t) and S_t diag(1/gamma_t) unrolled over the chunk: every column sum above becomes a
+// dot of the chunk's own vectors, masked to the tokens before or after t).  dw follows per column
+// from Z_t = colsum(X_t o S_t): Z_{n-1} = colsum(X_e o S_e), w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
+// Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1}.  No state is divided by w.
+//
+// A chunk whose gamma_31 falls below 1e-20 in some column (or is not finite), or that has some w_t
+// below 1/32 (where dividing w_t o dw_t by w_t would cost digits), takes the exact token-by-token
+// column passes instead (sa and dsa by their own recurrences, then wkv7_colpass.cuh).
+//
+// Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
+// fp32 accumulation; operands are stored once, row-major, split into bf16 hi and lo, and read with
+// ldmatrix (.trans for the transposed uses).  Mapping: one CTA of 8 warps per (head, chunk).
+#include <type_traits>
+
+#include "wkv7_colpass.cuh"
+#include "wkv7_device.cuh"
+#include "wkv7_launch.h"
+#include "wkv7_mma.cuh"
+
+namespace wkv7 {
+namespace {
+
+using namespace mma;
+
+constexpr int kL = 32;
+constexpr int kNT = 256;
+constexpr int kLD64 = 72;  // row stride (bf16 elements) of 64-wide operands
+constexpr int kLD32 = 40;  // of 32-wide operands
+constexpr float kMinGamma = 1e-20f;
+constexpr float kWMin = 0.03125f;
+
+__host__ __device__ constexpr int rm_bytes(int rows, int ld) { return 2 * rows * ld * 2; }  // hi + lo
+
+template <typename Tin>
+struct Lay {
+  // ---- long-lived
+  static constexpr int oG = 0;                                  // float [32][64] gamma
+  static constexpr int oZP = oG + 32 * 64 * 4;                  // float [4][64] colsum partials
+  static constexpr int oMeta = oZP + 4 * 64 * 4;                // int [4]
+  static constexpr int oWc = oMeta + 16 + 240;                  // float [32][64] w (1 past n)
+  static constexpr int oAh = oWc + 32 * 64 * 4;
+  static constexpr int oBt = oAh + rm_bytes(32, kLD64);
+  static constexpr int oKt = oBt + rm_bytes(32, kLD64);
+  static constexpr int oRh = oKt + rm_bytes(32, kLD64);
+  static constexpr int oS0 = oRh + rm_bytes(32, kLD64);
+  static constexpr int oXb = oS0 + rm_bytes(64, kLD64);
+  static constexpr int oV = oXb + rm_bytes(64, kLD64);
+  static constexpr int oDY = oV + rm_bytes(32, kLD64);
+  static constexpr int oSA = oDY + rm_bytes(32, kLD64);
+  static constexpr int oDSA = oSA + rm_bytes(32, kLD64);
+  static constexpr int oB = oDSA + rm_bytes(32, kLD64);
+  // ---- phase scratch B: raw inputs first (w, k, a, b, r, v [32][64] Tin; dy fp32 [32][64]) ...
+  static constexpr int oRaw = oB;
+  static constexpr int kRawIn = 6 * kL * kD * (int)sizeof(Tin);
+  static constexpr int oDyRaw = oRaw + kRawIn;
+  static constexpr int kRawEnd = oDyRaw + kL * kD * 4;
+  // ... then U, W, M_ak, M_rb, T, M_ab (fp32), TI, E; then L1..L4 over U and W
+  static constexpr int oU = oB;
+  static constexpr int oW = oU + rm_bytes(32, kLD64);
+  static constexpr int oMak = oW + rm_bytes(32, kLD64);
+  static constexpr int oMrb = oMak + rm_bytes(32, kLD32);
+  static constexpr int oT = oMrb + rm_bytes(32, kLD32);
+  static constexpr int kSM = 36;
+  static constexpr int oMab = oT + rm_bytes(32, kLD32);         // float [32][36]
+  static constexpr int oTI = oMab + 32 * kSM * 4;               // float [32][36]
+  static constexpr int oE = oTI + 32 * kSM * 4;                 // float [16][16]
+  static constexpr int kPhaseEnd = oE + 16 * 16 * 4;
+  static constexpr int oL = oB;                                 // L1..L4 (32 x 32 each)
+  static_assert(oL + 4 * rm_bytes(32, kLD32) <= oT, "L1..L4 fit over U, W, M_ak, M_rb");
+  static constexpr int kBytes = (kRawEnd > kPhaseEnd ? kRawEnd : kPhaseEnd);
+  // ---- fallback (token-by-token column passes): fp32 [32][64] sa, dsa, v over A^ .. R^
+  static constexpr int oFSa = oAh;
+  static constexpr int oFDsa = oFSa + kL * kD * 4;
+  static constexpr int oFV = oFDsa + kL * kD * 4;
+  static_assert(oFV + kL * kD * 4 <= oS0, "fallback arrays fit over A^ .. R^");
+  // ---- output staging over A^ .. Xb (after the last products): DR, DA, DK, DB, then r o dr, a o da,
+  // k o dk, b o db, fp32 [32][64] each
+  static constexpr int oStage = oAh;
+  static_assert(oStage + 8 * kL * kD * 4 <= oV, "staging fits over A^ .. Xb");
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kNT, 1)
+colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
+              const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
+              const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
+              const float* __restrict__ dy, const float* __restrict__ xck, float* __restrict__ dr,
+              float* __restrict__ dw, float* __restrict__ dk, float* __restrict__ da, float* __restrict__ db) {
+  using LY = Lay<Tin>;
+  constexpr bool kVExact = sizeof(Tin) == 2;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+
+  const int ci = blockIdx.x % nchunks;
+  const int bh = blockIdx.x / nchunks;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int t0 = ci * kL;
+  const int n = min(kL, T - t0);
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const float* xend = xck + ((size_t)bh * nchunks + ci) * kD * kD;
+  const float* send = h_ckpt + ((size_t)bh * nchunks + ci) * kD * kD;
+  const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
+                           : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
+
+  float* G = reinterpret_cast<float*>(sm + LY::oG);
+  float* Wc = reinterpret_cast<float*>(sm + LY::oWc);
+  float* ZP = reinterpret_cast<float*>(sm + LY::oZP);
+  int* meta = reinterpret_cast<int*>(sm + LY::oMeta);
+  Tin* raw = reinterpret_cast<Tin*>(sm + LY::oRaw);
+  const Tin* rw = raw;
+  const Tin* rk = raw + kL * kD;
+  const Tin* ra = raw + 2 * kL * kD;
+  const Tin* rbv = raw + 3 * kL * kD;
+  const Tin* rr = raw + 4 * kL * kD;
+  const Tin* rv = raw + 5 * kL * kD;
+  float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
+  auto bfp = [&](int off) { return reinterpret_cast<__nv_bfloat16*>(sm + off); };
+  const RM Ah{bfp(LY::oAh), 32 * kLD64, kLD64}, Bt{bfp(LY::oBt), 32 * kLD64, kLD64};
+  const RM Kt{bfp(LY::oKt), 32 * kLD64, kLD64}, Rh{bfp(LY::oRh), 32 * kLD64, kLD64};
+  const RM S0{bfp(LY::oS0), 64 * kLD64, kLD64}, Xb{bfp(LY::oXb), 64 * kLD64, kLD64};
+  const RM Vm{bfp(LY::oV), 32 * kLD64, kLD64}, DY{bfp(LY::oDY), 32 * kLD64, kLD64};
+  const RM SA{bfp(LY::oSA), 32 * kLD64, kLD64}, DSA{bfp(LY::oDSA), 32 * kLD64, kLD64};
+  const RM U{bfp(LY::oU), 32 * kLD64, kLD64}, W{bfp(LY::oW), 32 * kLD64, kLD64};
+  const RM Mak{bfp(LY::oMak), 32 * kLD32, kLD32}, Mrb{bfp(LY::oMrb), 32 * kLD32, kLD32};
+  const RM Tm{bfp(LY::oT), 32 * kLD32, kLD32};
+  const RM L1{bfp(LY::oL), 32 * kLD32, kLD32}, L2{bfp(LY::oL + rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
+  const RM L3{bfp(LY::oL + 2 * rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
+  const RM L4{bfp(LY::oL + 3 * rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
+  float* Mab = reinterpret_cast<float*>(sm + LY::oMab);
+  float* TI = reinterpret_cast<float*>(sm + LY::oTI);
+  float* E = reinterpret_cast<float*>(sm + LY::oE);
+  constexpr int SM = LY::kSM;
+
+  // ---- P0: the chunk's inputs (rows past n are not copied); colsum(X_e o S_e) partials meanwhile
+  {
+    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    const Tin* srcs[6] = {w, k, a, b, r, v};
+#pragma unroll
+    for (int s6 = 0; s6 < 6; ++s6)
+      for (int e = tid; e < n * CPR; e += kNT) {
+        const int tt = e / CPR, pc = e % CPR;
+        cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+      }
+    for (int e = tid; e < n * (kD / 4); e += kNT) {
+      const int tt = e / (kD / 4), pc = e % (kD / 4);
+      cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
+    }
+    cp_async_commit();
+    const int j = tid & 63, part = tid >> 6;
+    float z = 0.f;
+#pragma unroll 4
+    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(__ldg(xend + i * kD + j), __ldg(send + i * kD + j), z);
+    ZP[part * 64 + j] = z;
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+
+  // ---- P1a: gamma down each column; the fallback flag
+  if (tid < kD) {
+    const int j = tid;
+    float gm = 1.f;
+    bool bad = false;
+#pragma unroll 8
+    for (int t = 0; t < kL; ++t) {
+      const float wt = t < n ? to_f32(rw[t * kD + j]) : 1.f;
+      bad |= !(wt >= kWMin);
+      gm *= wt;
+      G[t * kD + j] = gm;
+      Wc[t * kD + j] = wt;
+    }
+    bad |= !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+    const unsigned any = __ballot_sync(0xffffffffu, bad);
+    if (lane == 0) meta[warp] = any != 0u;
+  }
+  __syncthreads();
+  if ((meta[0] | meta[1]) != 0) {
+    // ================= fallback: sa and dsa by their per-token recurrences, then the exact column passes
+    float* fsa = reinterpret_cast<float*>(sm + LY::oFSa);
+    float* fdsa = reinterpret_cast<float*>(sm + LY::oFDsa);
+    float* fv = reinterpret_cast<float*>(sm + LY::oFV);
+    for (int e = tid; e < n * kD; e += kNT) fv[e] = to_f32(rv[e]);
+    if (tid < 64) {  // sa_t = S_{t-1} a_t, row tid, the state run up from S0
+      const int i = tid;
+      float Sr[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) Sr[j] = s0 != nullptr ? __ldg(s0 + i * kD + j) : 0.f;
+      for (int t = 0; t < n; ++t) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s = fmaf(Sr[j], to_f32(ra[t * kD + j]), s);
+        fsa[t * kD + i] = s;
+        const float vi = to_f32(rv[t * kD + i]);
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          Sr[j] = fmaf(Sr[j], to_f32(rw[t * kD + j]), fmaf(vi, to_f32(rk[t * kD + j]), s * to_f32(rbv[t * kD + j])));
+      }
+    } else if (tid < 128) {  // dsa_t = X_t b_t, row tid - 64, X walked down from X_e
+      const int i = tid - 64;
+      float Xr[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) Xr[j] = __ldg(xend + i * kD + j);
+      for (int t = n - 1; t >= 0; --t) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s = fmaf(Xr[j], to_f32(rbv[t * kD + j]), s);
+        fdsa[t * kD + i] = s;
+        const float e = t > 0 ? dyr[(t - 1) * kD + i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float rp = t > 0 ? to_f32(rr[(t - 1) * kD + j]) : 0.f;
+          Xr[j] = fmaf(Xr[j], to_f32(rw[t * kD + j]), fmaf(s, to_f32(ra[t * kD + j]), e * rp));
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < 64)
+      colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv, xend, s0, dr, dw, dk, da, db);
+    return;
+  }
+
+  // ---- P1b: operands.  Row pairs (t, j): A^, R^, K~, B~, V, DY (steps past n zero)
+  for (int e = tid; e < kL * (kD / 2); e += kNT) {
+    const int t = e >> 5, j = 2 * (e & 31);
+    const bool ok = t < n;
+    const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+    const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
+    const float ix = __frcp_rn(gt.x), iy = __frcp_rn(gt.y);
+    const float a0 = ok ? to_f32(ra[t * kD + j]) : 0.f, a1 = ok ? to_f32(ra[t * kD + j + 1]) : 0.f;
+    const float r0 = ok ? to_f32(rr[t * kD + j]) : 0.f, r1 = ok ? to_f32(rr[t * kD + j + 1]) : 0.f;
+    const float k0 = ok ? to_f32(rk[t * kD + j]) : 0.f, k1 = ok ? to_f32(rk[t * kD + j + 1]) : 0.f;
+    const float b0 = ok ? to_f32(rbv[t * kD + j]) : 0.f, b1 = ok ? to_f32(rbv[t * kD + j + 1]) : 0.f;
+    const float v0 = ok ? to_f32(rv[t * kD + j]) : 0.f, v1 = ok ? to_f32(rv[t * kD + j + 1]) : 0.f;
+    const float d0 = ok ? dyr[t * kD + j] : 0.f, d1 = ok ? dyr[t * kD + j + 1] : 0.f;
+    rm_store(Ah, t, j, a0 * gp.x, a1 * gp.y);
+    rm_store(Rh, t, j, r0 * gt.x, r1 * gt.y);
+    rm_store(Kt, t, j, k0 * ix, k1 * iy);
+    rm_store(Bt, t, j, b0 * ix, b1 * iy);
+    if (kVExact) rm_store_hi(Vm, t, j, v0, v1); else rm_store(Vm, t, j, v0, v1);
+    rm_store(DY, t, j, d0, d1);
+  }
+  // S0 and Xb = (X_e - dy_{n-1} r_{n-1}^T) diag(gamma_{n-1}) (rows i, columns j)
+  for (int e = tid; e < kD * (kD / 2); e += kNT) {
+    const int i = e >> 5, j = 2 * (e & 31);
+    const float2 s = s0 != nullptr ? __ldg(reinterpret_cast<const float2*>(s0 + i * kD + j)) : make_float2(0.f, 0.f);
+    rm_store(S0, i, j, s.x, s.y);
+    const float2 x = __ldg(reinterpret_cast<const float2*>(xend + i * kD + j));
+    const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
+    const float dl = dyr[(n - 1) * kD + i];
+    const float rl0 = to_f32(rr[(n - 1) * kD + j]), rl1 = to_f32(rr[(n - 1) * kD + j + 1]);
+    rm_store(Xb, i, j, fmaf(-dl, rl0, x.x) * gl.x, fmaf(-dl, rl1, x.y) * gl.y);
+  }
+  __syncthreads();
+
+  // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T); 12 jobs of
+  // (product, m-tile, pair of n-tiles), K = 64
+  for (int job = warp; job < 12; job += 8) {
+    const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
+    const bool strict = prod < 2;
+    float acc[2][4] = {};
+    if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
+      const RM& X = prod < 2 ? Ah : Rh;
+      const RM& Y = prod == 1 ? Kt : Bt;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(X, mt, kk, lane);
+        FragB f0, f1;
+        rm_b2(Y, 2 * np, kk, lane, f0, f1);
+        mma3(acc[0], fa, f0);
+        mma3(acc[1], fa, f1);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int nj = 2 * np + h;
+      const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+      float c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = tr + ((e >> 1) << 3), s = sc + (e & 1);
+        c[e] = (strict ? s < t : s <= t) ? acc[h][e] : 0.f;
+      }
+      if (prod == 0) {
+        *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+        *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
+      } else {
+        rm_store_acc(prod == 1 ? Mak : Mrb, mt, nj, lane, c);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- P3 || P4: warp 0 solves the diagonal blocks of T = (I - M_ab)^-1 (forward substitution, one column
+  // per lane: lanes 0-15 T11, lanes 16-31 T22); warps 1-7 form U = A^ S0^T + M_ak V and
+  // W = B~ Xb^T + M_rb^T DY (rows t, columns i): 16 jobs of (product, m-tile, 4 n-tiles)
+  if (warp == 0) {
+    const int off = lane < 16 ? 0 : 16;
+    const int c = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float acc = t == c ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) acc = fmaf(Mab[(off + t) * SM + off + u], x[u], acc);
+      x[t] = acc;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
+  } else {
+    for (int job = warp - 1; job < 16; job += 7) {
+      const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1
+      float acc[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(prod == 0 ? Ah : Bt, mt, kk, lane);
+        FragB f0, f1;
+        rm_b2(prod == 0 ? S0 : Xb, 2 * nq, kk, lane, f0, f1);
+        mma3(acc[0], fa, f0);
+        mma3(acc[1], fa, f1);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (prod == 0) {  // M_ak V: V is B[k = u][n = i] = V[u][i]
+          const FragA fa = rm_a(Mak, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Vm, 2 * nq, kk, lane, f0, f1, !kVExact);
+          if (kVExact) {
+            mma2b(acc[0], fa, f0);
+            mma2b(acc[1], fa, f1);
+          } else {
+            mma3(acc[0], fa, f0);
+            mma3(acc[1], fa, f1);
+          }
+        } else {  // M_rb^T DY
+          const FragA fa = rm_at(Mrb, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(DY, 2 * nq, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
+      }
+      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq, lane, acc[0]);
+      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq + 1, lane, acc[1]);
+    }
+  }
+  __syncthreads();
+  {  // E = A21 T11, then T21 = T22 E (A21 = M_ab[16..31][0..15])
+    const int t = tid >> 4, s = tid & 15;
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc = fmaf(Mab[(16 + t) * SM + u], TI[u * SM + s], acc);
+    E[t * 16 + s] = acc;
+  }
+  __syncthreads();
+  {
+    const int t = tid >> 4, s = tid & 15;
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * SM + 16 + u], E[u * 16 + s], acc);
+    TI[(16 + t) * SM + s] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 32 * 16; e += kNT) {  // T (rows t, columns u), zero above the diagonal
+    const int t = e >> 4, u = 2 * (e & 15);
+    rm_store(Tm, t, u, u <= t ? TI[t * SM + u] : 0.f, u + 1 <= t ? TI[t * SM + u + 1] : 0.f);
+  }
+  __syncthreads();
+
+  // ---- P5: SA = T U, DSA = T^T W (rows t, columns i; K = 32); 16 jobs (product, m-tile, 4 n-tiles)
+  for (int job = warp; job < 16; job += 8) {
+    const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      if (prod == 0 ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // T lower, T^T upper
+      const FragA fa = prod == 0 ? rm_a(Tm, mt, kk, lane) : rm_at(Tm, mt, kk, lane);
+      FragB f0, f1;
+      rm_bt2(prod == 0 ? U : W, 2 * nq, kk, lane, f0, f1);
+      mma3(acc[0], fa, f0);
+      mma3(acc[1], fa, f1);
+    }
+    rm_store_acc(prod == 0 ? SA : DSA, mt, 2 * nq, lane, acc[0]);
+    rm_store_acc(prod == 0 ? SA : DSA, mt, 2 * nq + 1, lane, acc[1]);
+  }
+  __syncthreads();
+
+  // ---- P6: L1 = tril(DY V^T), L2 = tril(DY SA^T), L3 = tril(DSA V^T, -1), L4 = tril(DSA SA^T, -1) (over U, W)
+  for (int job = warp; job < 16; job += 8) {
+    const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
+    const bool strict = prod >= 2;
+    const bool exactB = kVExact && (prod == 0 || prod == 2);
+    float acc[2][4] = {};
+    if (!(mt == 0 && np == 1)) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(prod < 2 ? DY : DSA, mt, kk, lane);
+        FragB f0, f1;
+        rm_b2((prod & 1) ? SA : Vm, 2 * np, kk, lane, f0, f1, !exactB);
+        if (exactB) {
+          mma2b(acc[0], fa, f0);
+          mma2b(acc[1], fa, f1);
+        } else {
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
+      }
+    }
+    const RM& Lx = prod == 0 ? L1 : (prod == 1 ? L2 : (prod == 2 ? L3 : L4));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int nj = 2 * np + h;
+      float c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = mt * 16 + g + ((e >> 1) << 3), s = nj * 8 + 2 * q + (e & 1);
+        c[e] = (strict ? s < t : s <= t) ? acc[h][e] : 0.f;
+      }
+      rm_store_acc(Lx, mt, nj, lane, c);
+    }
+  }
+  __syncthreads();
+
+  // ---- P7: DR, DA, DK, DB (rows t, columns j): 16 jobs of (product, m-tile, 4 n-tiles), each a K = 64
+  // product with S0 / Xb plus the masked K = 64 product; held in registers until every warp is done
+  float res[2][4][4];
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int job = warp + 8 * rep;
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
+    float (&acc)[4][4] = res[rep];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
+    const RM& B1 = prod < 2 ? S0 : Xb;
+    const bool exactA = kVExact && prod == 2;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
+#pragma unroll
+      for (int p2 = 0; p2 < 2; ++p2) {
+        FragB f0, f1;
+        rm_bt2(B1, 4 * nh + 2 * p2, kk, lane, f0, f1);
+        if (exactA) {
+          mma2(acc[2 * p2], fa, f0);
+          mma2(acc[2 * p2 + 1], fa, f1);
+        } else {
+          mma3(acc[2 * p2], fa, f0);
+          mma3(acc[2 * p2 + 1], fa, f1);
+        }
+      }
+    }
+    // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
+    // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {
+      const int blk = kq >> 1, kk = kq & 1;
+      const bool lowerA = prod < 2;
+      if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
+      const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
+      const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
+      const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
+#pragma unroll
+      for (int p2 = 0; p2 < 2; ++p2) {
+        FragB f0, f1;
+        rm_bt2(BB, 4 * nh + 2 * p2, kk, lane, f0, f1);
+        mma3(acc[2 * p2], fa, f0);
+        mma3(acc[2 * p2 + 1], fa, f1);
+      }
+    }
+  }
+  __syncthreads();  // every operand has been read: stage over A^ .. Xb
+  float* stage = reinterpret_cast<float*>(sm + LY::oStage);
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int job = warp + 8 * rep;
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
+    float* st = stage + prod * kL * kD;
+    float* sp = stage + (4 + prod) * kL * kD;  // times its own input (r, a, k, b) for the dw recurrence
+    const Tin* inp = prod == 0 ? r : (prod == 1 ? a : (prod == 2 ? k : b));
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int j = (4 * nh + x) * 8 + 2 * q;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int t = mt * 16 + g + 8 * hr;
+        const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+        const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
+        float2 sc;
+        if (prod == 0) sc = gt;
+        else if (prod == 1) sc = gp;
+        else sc = make_float2(__frcp_rn(gt.x), __frcp_rn(gt.y));
+        const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
+        *reinterpret_cast<float2*>(st + t * kD + j) = o;
+        float2 in = make_float2(0.f, 0.f);
+        if (t < n) {
+          const size_t gi = base + (size_t)(t0 + t) * tstride + j;
+          in = make_float2(to_f32(inp[gi]), to_f32(inp[gi + 1]));
+        }
+        *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- P8: write dr, da, dk, db; dw by the column recurrence of Z_t = colsum(X_t o S_t)
+  {
+    const float* sDR = stage;
+    const float* sDA = stage + kL * kD;
+    const float* sDK = stage + 2 * kL * kD;
+    const float* sDB = stage + 3 * kL * kD;
+    const float* sRDR = stage + 4 * kL * kD;
+    const float* sADA = stage + 5 * kL * kD;
+    const float* sKDK = stage + 6 * kL * kD;
+    const float* sBDB = stage + 7 * kL * kD;
+    for (int e = tid; e < n * (kD / 4); e += kNT) {
+      const int t = e >> 4, c = (e & 15) * 4;
+      const size_t o = base + (size_t)(t0 + t) * tstride + c;
+      *reinterpret_cast<float4*>(dr + o) = *reinterpret_cast<const float4*>(sDR + t * kD + c);
+      *reinterpret_cast<float4*>(da + o) = *reinterpret_cast<const float4*>(sDA + t * kD + c);
+      *reinterpret_cast<float4*>(dk + o) = *reinterpret_cast<const float4*>(sDK + t * kD + c);
+      *reinterpret_cast<float4*>(db + o) = *reinterpret_cast<const float4*>(sDB + t * kD + c);
+    }
+    if (tid < kD) {
+      const int j = tid;
+      float Z = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j];
+      for (int t = n - 1; t >= 0; --t) {
+        const float wdw = Z - sKDK[t * kD + j] - sBDB[t * kD + j];
+        dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
+        Z = wdw + sADA[t * kD + j] + (t > 0 ? sRDR[(t - 1) * kD + j] : 0.f);
+      }
+    }
+  }
+}
+
+template <typename Tin>
+cudaError_t launch_colmat_t(const BwdArgs& p, const float* xck_ws, cudaStream_t stream) {
+  using LY = Lay<Tin>;
+  static_assert(LY::kBytes <= 232448, "shared memory per CTA");
+  auto kern = colmat_kernel<Tin>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = (unsigned)p.B * p.H * p.nchunks;
+  kern<<<grid, kNT, LY::kBytes, stream>>>(p.T, p.H, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
+                                          (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
+                                          (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, xck_ws, p.dr, p.dw, p.dk, p.da,
+                                          p.db);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_colgrad_matrix(const BwdArgs& p, const float* xck_ws, cudaStream_t stream) {
+  if (p.nchunks == 0) return cudaSuccess;
+  return p.bf16 ? launch_colmat_t<__nv_bfloat16>(p, xck_ws, stream) : launch_colmat_t<float>(p, xck_ws, stream);
+}
+
+}  // namespace wkv7

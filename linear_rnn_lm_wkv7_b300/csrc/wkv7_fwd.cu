@@ -324,9 +324,11 @@ cudaError_t launch_forward_sequential(const FwdArgs& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_forward(const FwdArgs& p, cudaStream_t stream) {
-  // The sub-chunk kernel writes the state every 16 tokens, so checkpoints must fall on those; it
-  // holds one CTA per SM (183-205 KB of shared memory), so past one wave of row blocks the
-  // token-by-token kernel (two CTAs per SM) is faster (7B width, 256 row blocks: 1.32 vs 1.39 ms).
+  // 32-token chunks without a saved sa: the chain of transition products (one 64 x 64 product per chunk
+  // on the serial path).  Otherwise the 16-token sub-chunk kernel writes the state every 16 tokens, so
+  // checkpoints must fall on those; it holds one CTA per SM (183-205 KB of shared memory), so past one
+  // wave of row blocks the token-by-token kernel (two CTAs per SM) is faster.
+  if (p.chunk == 32 && p.sa == nullptr) return launch_forward_transition(p, stream);
   if (p.chunk % 16 == 0 && (long long)p.B * p.H * 2 <= num_sms()) return launch_forward_chunked(p, stream);
   return launch_forward_sequential(p, stream);
 }

@@ -68,6 +68,17 @@ cudaError_t launch_backward_two_phase(const BwdArgs& a, void* workspace, cudaStr
 // phase 1 of the two-phase backward (the state-gradient walk writing dv, dsa, X at the chunk ends and
 // dh0) by the 16-step sub-chunk kernel: chunk % 16 == 0, T >= 1
 cudaError_t launch_gwalk_chunked(const BwdArgs& a, float* dsa_ws, float* xck_ws, cudaStream_t stream);
+// the forward as a chain of 32-token transition products (chunk == 32; no saved sa), and the backward's
+// state-gradient walk on the same kernel: dv, the state gradient X at every chunk end into xck_ws
+// (B,H,C,D,D), dh0
+cudaError_t launch_forward_transition(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_gwalk_transition(const BwdArgs& a, float* xck_ws, cudaStream_t stream);
+// the column gradients dr, dw, dk, da, db of every 32-token chunk in matrix form, from the walk's X at
+// the chunk ends (xck_ws), the checkpoints and the inputs (no saved sa)
+cudaError_t launch_colgrad_matrix(const BwdArgs& a, const float* xck_ws, cudaStream_t stream);
+// the two-phase backward by the transition walk and the matrix column gradients (chunk == 32); workspace
+// as launch_backward_two_phase
+cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace wkv7

@@ -1,0 +1,251 @@
+// Tensor-core operands for the chunk kernels: warp-level bf16 mma (m16n8k16, fp32 accumulate) on
+// fp32 values split as x = hi + lo (hi = x rounded to bf16, lo = the remainder rounded to bf16), so a
+// product of two fp32 matrices is hi*hi + hi*lo + lo*hi (relative error ~2^-17 per product; the
+// dropped lo*lo term and lo's own rounding are ~2^-18).  An operand that is already an exact bf16
+// value (a bf16 input) has no lo part and takes two products.
+//
+// Pair tiles.  Every operand lives in shared memory as a "pair tile" array: an R x C fp32 matrix X
+// (R, C multiples of 16) is cut into 16 x 16 tiles, each stored as 32 lanes x 4 words, where a word
+// is the bf16 pair X[r][c], X[r][c+1] (c even).  For tile (r/16, c/16) and lane g*4 + q
+// (g = r % 8, q = (c % 8) / 2) the four words are
+//     w0 = (g, 2q)   w1 = (g, 2q + 8)   w2 = (g + 8, 2q)   w3 = (g + 8, 2q + 8)
+// (tile-relative row, column).  hi and lo words are two separate arrays of the same shape.  One
+// format serves both operands of mma.m16n8k16:
+//   - as A (rows m, contraction k) of X[m][k]:  a0 = w0, a1 = w2, a2 = w1, a3 = w3;
+//   - as B of a product contracting X's columns, B[k][n] = X[n][k] (i.e. "times X^T"): n-tile nt is
+//     half (nt & 1) of tile row nt / 2: b0 = w[2 (nt & 1)], b1 = w[2 (nt & 1) + 1].
+// A product contracting X's rows (B[k][n] = X[k][n]) takes the pair tiles of X^T instead.
+// An accumulator tile (m-tile mt, n8-tile nj) holds c0, c1 = (g, 2q, 2q + 1) and c2, c3 = (g + 8, ...):
+// exactly words w(nj & 1) and w(2 + (nj & 1)) of pair tile (mt, nj / 2) in the same lane, so a result
+// is stored as an operand of the next product by its own lane with no shuffle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace wkv7 {
+namespace mma {
+
+// packed bf16 pair (x in the low half) rounded to nearest
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+__device__ __forceinline__ float bf16_low(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_high(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// (x, y) -> hi pair, lo pair
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x, y);
+  lo = pack_bf16(x - bf16_low(hi), y - bf16_high(hi));
+}
+
+// x + y of a split pair word (hi + lo), low and high element
+__device__ __forceinline__ float2 join2(uint32_t hi, uint32_t lo) {
+  return make_float2(bf16_low(hi) + bf16_low(lo), bf16_high(hi) + bf16_high(lo));
+}
+
+struct FragA {
+  uint32_t h[4], l[4];
+};
+struct FragB {
+  uint32_t h[2], l[2];
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += A B for split A and B (small terms first)
+__device__ __forceinline__ void mma3(float (&d)[4], const FragA& a, const FragB& b) {
+  mma16816(d, a.l, b.h[0], b.h[1]);
+  mma16816(d, a.h, b.l[0], b.l[1]);
+  mma16816(d, a.h, b.h[0], b.h[1]);
+}
+// d += A B for an exact-bf16 A (hi only) and split B
+__device__ __forceinline__ void mma2(float (&d)[4], const FragA& a, const FragB& b) {
+  mma16816(d, a.h, b.l[0], b.l[1]);
+  mma16816(d, a.h, b.h[0], b.h[1]);
+}
+
+// ---- pair-tile addressing: word index of element pair (r, c) (c even) in an array with `tc` tiles per
+// tile row; the lo array sits `half` words after the hi array
+__device__ __forceinline__ int pt_word(int r, int c, int tc) {
+  const int tile = (r >> 4) * tc + (c >> 4);
+  const int lane = (r & 7) * 4 + ((c & 7) >> 1);
+  const int w = 2 * ((r >> 3) & 1) + ((c >> 3) & 1);
+  return (tile * 32 + lane) * 4 + w;
+}
+
+// store the split pair (x at (r, c), y at (r, c + 1)) into pair tiles (hi at p, lo at p + half)
+__device__ __forceinline__ void pt_store(uint32_t* p, int half, int r, int c, int tc, float x, float y) {
+  uint32_t hi, lo;
+  split2(x, y, hi, lo);
+  const int i = pt_word(r, c, tc);
+  p[i] = hi;
+  p[i + half] = lo;
+}
+// exact-bf16 pair (hi only)
+__device__ __forceinline__ void pt_store_hi(uint32_t* p, int r, int c, int tc, float x, float y) {
+  p[pt_word(r, c, tc)] = pack_bf16(x, y);
+}
+
+// A operand of tile (mt, kk) for this lane
+__device__ __forceinline__ FragA load_a(const uint32_t* p, int half, int tc, int mt, int kk, int lane) {
+  const int i = ((mt * tc + kk) * 32 + lane) * 4;
+  const uint4 h = *reinterpret_cast<const uint4*>(p + i);
+  const uint4 l = *reinterpret_cast<const uint4*>(p + half + i);
+  FragA a;
+  a.h[0] = h.x; a.h[1] = h.z; a.h[2] = h.y; a.h[3] = h.w;
+  a.l[0] = l.x; a.l[1] = l.z; a.l[2] = l.y; a.l[3] = l.w;
+  return a;
+}
+// A operand, hi words only (exact bf16 values)
+__device__ __forceinline__ FragA load_a_hi(const uint32_t* p, int tc, int mt, int kk, int lane) {
+  const int i = ((mt * tc + kk) * 32 + lane) * 4;
+  const uint4 h = *reinterpret_cast<const uint4*>(p + i);
+  FragA a;
+  a.h[0] = h.x; a.h[1] = h.z; a.h[2] = h.y; a.h[3] = h.w;
+  a.l[0] = a.l[1] = a.l[2] = a.l[3] = 0u;
+  return a;
+}
+// B operand of n-tile nt, k-tile kk (B[k][n] = X[n][k]) for this lane
+__device__ __forceinline__ FragB load_b(const uint32_t* p, int half, int tc, int nt, int kk, int lane) {
+  const int i = (((nt >> 1) * tc + kk) * 32 + lane) * 4 + 2 * (nt & 1);
+  const uint2 h = *reinterpret_cast<const uint2*>(p + i);
+  const uint2 l = *reinterpret_cast<const uint2*>(p + half + i);
+  FragB b;
+  b.h[0] = h.x; b.h[1] = h.y;
+  b.l[0] = l.x; b.l[1] = l.y;
+  return b;
+}
+
+// store accumulator tile (mt, nj) of a result into pair tiles by its own lane (see above)
+__device__ __forceinline__ void store_acc(uint32_t* p, int half, int tc, int mt, int nj, int lane, const float (&c)[4]) {
+  const int i = ((mt * tc + (nj >> 1)) * 32 + lane) * 4 + (nj & 1);
+  uint32_t hi, lo;
+  split2(c[0], c[1], hi, lo);
+  p[i] = hi;
+  p[i + half] = lo;
+  split2(c[2], c[3], hi, lo);
+  p[i + 2] = hi;
+  p[i + 2 + half] = lo;
+}
+// the fp32 values (hi + lo) at the positions of accumulator tile (mt, nj) of this lane
+__device__ __forceinline__ void load_acc_pos(const uint32_t* p, int half, int tc, int mt, int nj, int lane,
+                                             float (&c)[4]) {
+  const int i = ((mt * tc + (nj >> 1)) * 32 + lane) * 4 + (nj & 1);
+  const float2 x = join2(p[i], p[i + half]);
+  const float2 y = join2(p[i + 2], p[i + 2 + half]);
+  c[0] = x.x; c[1] = x.y; c[2] = y.x; c[3] = y.y;
+}
+
+// A operand of k-tile kk built from this lane's accumulator tiles 2kk, 2kk + 1 of the same m-tile
+__device__ __forceinline__ FragA frag_from_acc(const float (&c0)[4], const float (&c1)[4]) {
+  FragA a;
+  split2(c0[0], c0[1], a.h[0], a.l[0]);
+  split2(c0[2], c0[3], a.h[1], a.l[1]);
+  split2(c1[0], c1[1], a.h[2], a.l[2]);
+  split2(c1[2], c1[3], a.h[3], a.l[3]);
+  return a;
+}
+
+}  // namespace mma
+}  // namespace wkv7
+
+// ---------------------------------------------------------------------------------------------------
+// Row-major operands read with ldmatrix.  A matrix X is stored once, row-major, as bf16 hi and lo
+// arrays (lo `lo` elements after hi), `ld` elements per row (ld = 8 mod 64 -> the eight 16-byte rows of
+// an 8 x 8 block fall in distinct banks).  ldmatrix hands out the mma fragments of X itself or, with
+// .trans, of X^T, so one copy serves every product.
+namespace wkv7 {
+namespace mma {
+
+template <bool TRANS>
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const __nv_bfloat16* p) {
+  const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+  if (TRANS)
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+  else
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+struct RM {
+  __nv_bfloat16* p;  // hi array; lo array at p + lo
+  int lo;
+  int ld;
+};
+
+// A fragment (m-tile mt, k-tile kk) of X[m][k]
+__device__ __forceinline__ FragA rm_a(const RM& x, int mt, int kk, int lane) {
+  const int off = (mt * 16 + (lane & 15)) * x.ld + kk * 16 + (lane >> 4) * 8;
+  FragA f;
+  ldsm4<false>(f.h, x.p + off);
+  ldsm4<false>(f.l, x.p + x.lo + off);
+  return f;
+}
+__device__ __forceinline__ FragA rm_a_hi(const RM& x, int mt, int kk, int lane) {
+  const int off = (mt * 16 + (lane & 15)) * x.ld + kk * 16 + (lane >> 4) * 8;
+  FragA f;
+  ldsm4<false>(f.h, x.p + off);
+  f.l[0] = f.l[1] = f.l[2] = f.l[3] = 0u;
+  return f;
+}
+// A fragment (mt, kk) of X^T, i.e. A[m][k] = X[k][m]
+__device__ __forceinline__ FragA rm_at(const RM& x, int mt, int kk, int lane) {
+  const int off = (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + mt * 16 + ((lane >> 3) & 1) * 8;
+  FragA f;
+  ldsm4<true>(f.h, x.p + off);
+  ldsm4<true>(f.l, x.p + x.lo + off);
+  return f;
+}
+// B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = X[n][k] (a product "times X^T")
+__device__ __forceinline__ void rm_b2(const RM& x, int nt, int kk, int lane, FragB& b0, FragB& b1, bool with_lo = true) {
+  const int off = (nt * 8 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + kk * 16 + ((lane >> 3) & 1) * 8;
+  uint32_t h[4], l[4] = {0u, 0u, 0u, 0u};
+  ldsm4<false>(h, x.p + off);
+  if (with_lo) ldsm4<false>(l, x.p + x.lo + off);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+// B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = X[k][n] (a product "times X")
+__device__ __forceinline__ void rm_bt2(const RM& x, int nt, int kk, int lane, FragB& b0, FragB& b1, bool with_lo = true) {
+  const int off = (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * x.ld + nt * 8 + (lane >> 4) * 8;
+  uint32_t h[4], l[4] = {0u, 0u, 0u, 0u};
+  ldsm4<true>(h, x.p + off);
+  if (with_lo) ldsm4<true>(l, x.p + x.lo + off);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+// split pair (x at (r, c), y at (r, c + 1)), c even
+__device__ __forceinline__ void rm_store(const RM& x, int r, int c, float a, float b) {
+  uint32_t hi, lo;
+  split2(a, b, hi, lo);
+  *reinterpret_cast<uint32_t*>(x.p + r * x.ld + c) = hi;
+  *reinterpret_cast<uint32_t*>(x.p + x.lo + r * x.ld + c) = lo;
+}
+__device__ __forceinline__ void rm_store_hi(const RM& x, int r, int c, float a, float b) {
+  *reinterpret_cast<uint32_t*>(x.p + r * x.ld + c) = pack_bf16(a, b);
+}
+// accumulator tile (mt, nj) of a result into X
+__device__ __forceinline__ void rm_store_acc(const RM& x, int mt, int nj, int lane, const float (&c)[4]) {
+  const int r = mt * 16 + (lane >> 2), col = nj * 8 + 2 * (lane & 3);
+  rm_store(x, r, col, c[0], c[1]);
+  rm_store(x, r + 8, col, c[2], c[3]);
+}
+// d += A B for split A and an exact-bf16 B (hi only)
+__device__ __forceinline__ void mma2b(float (&d)[4], const FragA& a, const FragB& b) {
+  mma16816(d, a.l, b.h[0], b.h[1]);
+  mma16816(d, a.h, b.h[0], b.h[1]);
+}
+
+}  // namespace mma
+}  // namespace wkv7

@@ -53,13 +53,15 @@ extern "C" int wkv7_backward_noalloc(int B, int T, int H, int D, int chunk, int 
   if (st) return st;
   if (in_dtype != WKV7_F32 && in_dtype != WKV7_BF16) return WKV7_ERR_DTYPE;
   if (T > 0) {
-    const void* required[] = {r, w, k, v, a, b, h_ckpt, sa, dy, dr, dw, dk, dv, da, db};
+    const void* required[] = {r, w, k, v, a, b, h_ckpt, dy, dr, dw, dk, dv, da, db};
     for (const void* p : required)
       if (p == nullptr) return WKV7_ERR_ARG;
     for (const void* p : required)
       if (misaligned16(p)) return WKV7_ERR_ALIGN;
+    if (chunk != 32 && sa == nullptr) return WKV7_ERR_ARG;  // the two-phase backward off 32-token chunks reads it
   }
-  for (const void* p : {static_cast<const void*>(h0), static_cast<const void*>(dhT), static_cast<const void*>(dh0)})
+  for (const void* p : {static_cast<const void*>(h0), static_cast<const void*>(dhT), static_cast<const void*>(dh0),
+                        static_cast<const void*>(sa)})
     if (p != nullptr && misaligned16(p)) return WKV7_ERR_ALIGN;
   if (need > (size_t)WKV7_NOALLOC_SCRATCH_BYTES) return WKV7_ERR_SCRATCH_LIMIT;
 
@@ -72,7 +74,10 @@ extern "C" int wkv7_backward_noalloc(int B, int T, int H, int D, int chunk, int 
   p.in = {r, w, k, v, a, b};
   p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
   p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
-  // every scratch element the kernels read is written earlier in the same call (phase 1
-  // writes each dsa and each chunk-end state gradient before phase 2 reads it): nothing to clear
-  return wkv7::record_cuda_status(wkv7::launch_backward_two_phase(p, scratch, static_cast<cudaStream_t>(stream)));
+  // the same dispatch as wkv7_backward with a workspace.  Every scratch element the kernels read is
+  // written earlier in the same call (the walk writes each chunk-end state gradient, and each dsa when
+  // the column pass reads them, before the column pass runs): nothing to clear
+  const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  return wkv7::record_cuda_status(chunk == 32 ? wkv7::launch_backward_transition(p, scratch, st_)
+                                              : wkv7::launch_backward_two_phase(p, scratch, st_));
 }

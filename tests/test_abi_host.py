@@ -145,9 +145,9 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     p = list(ALIGNED[:18])
     assert wkv7.lib.wkv7_backward_noalloc(2, 4096, 64, 64, 32, 1, *p, None) == 8
     assert b"WKV7_NOALLOC_SCRATCH_BYTES" in wkv7.lib.wkv7_strerror(8)
-    # sa is required
+    # sa is required off 32-token chunks (the two-phase backward with a column pass that reads it)
     p[8] = None
-    assert wkv7.lib.wkv7_backward_noalloc(2, 64, 3, 64, 32, 1, *p, None) == 1
+    assert wkv7.lib.wkv7_backward_noalloc(2, 64, 3, 64, 16, 1, *p, None) == 1
 
 
 def test_binding_rejects_cpu_tensors():

@@ -1,8 +1,11 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs.
 
-Tolerances (relative L2 over the whole tensor, ||x - ref|| / ||ref||): y, hT and checkpoints
-<= 1e-4; every gradient <= 2e-3.  Layout and index mapping of the decode state are checked
-bit for bit with one-hot probes.
+Tolerances (relative L2 over the whole tensor, ||x - ref|| / ||ref||): y, hT, checkpoints and sa
+<= 1e-4; every gradient <= 2e-3.  Beside the whole-tensor figure every (b, h, t) row (and every
+(b, h) state) is checked on its own: ||x_row - ref_row|| / max(||ref_row||, median row norm) <= 10x
+the tensor tolerance, so a localised index mistake (one wrong token row or state, a wrong boundary)
+cannot hide in the average.  Layout and index mapping of the decode state are checked bit for bit
+with one-hot probes.
 """
 import numpy as np
 import pytest
@@ -15,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 TOL_FWD = 1e-4
 TOL_BWD = 2e-3
+ROW_FACTOR = 10.0
 
 
 @pytest.fixture(scope="module")
@@ -25,11 +29,33 @@ def wkv7():
     return m
 
 
+def sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
 def rel(x, ref):
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     n = np.linalg.norm(ref)
     return float(np.linalg.norm(x - ref) / (n if n > 0 else 1.0))
+
+
+def row_rel(x, ref, row_axes):
+    """Largest per-row error: rows are the trailing `row_axes` axes' complements (norm over the rest)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ax = tuple(range(x.ndim - row_axes, x.ndim))
+    err = np.sqrt(((x - ref) ** 2).sum(axis=ax))
+    nrm = np.sqrt((ref ** 2).sum(axis=ax))
+    floor = max(float(np.median(nrm)), 1e-30)
+    return float((err / np.maximum(nrm, floor)).max())
+
+
+def assert_close(name, x, ref, tol, row_axes):
+    e = rel(x, ref)
+    assert e <= tol, (name, e)
+    er = row_rel(x, ref, row_axes)
+    assert er <= ROW_FACTOR * tol, (name, "row", er)
 
 
 def dev(x, dtype):
@@ -49,152 +75,204 @@ def host(t):
     return None if t is None else t.detach().double().cpu().numpy()
 
 
-# backward paths: the two-phase backward (saved sa + workspace), the single pass reading the
-# saved sa, the single pass recomputing sa per chunk
+# forward kernels:
+#   "transition": wkv7_forward without a saved sa -> the chain of 32-token transition products at chunk 32
+#   "subchunk":   wkv7_forward saving sa -> 16-token sub-chunks (chunk % 16 == 0, one wave of row blocks)
+#   "sequential": wkv7_forward_sequential (token by token)
+FWD = ["transition", "subchunk", "sequential"]
+
+# backward paths: "two_phase" (a workspace: at chunk 32 the transition walk + matrix column gradients,
+# otherwise the two-phase backward with the forward's saved sa), the single pass reading the saved sa,
+# the single pass recomputing sa per chunk
 MODES = ["two_phase", "single_saved_sa", "single_recompute"]
 
 
-# forward kernels: "auto" (16-token sub-chunks on tensor cores when chunk % 16 == 0 and the
-# B*H*2 row blocks fit one wave of SMs) and the token-by-token "sequential" one
-FWD = ["auto", "sequential"]
-
-
-def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase", fwd="auto"):
+def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase", fwd="transition"):
     ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
-    y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True, kernel=fwd)
-    kw = {"two_phase": dict(sa=sa), "single_saved_sa": dict(sa=sa, workspace=None),
-          "single_recompute": dict(sa=None)}[mode]
+    if fwd == "transition":
+        y, ck, hT = wkv7.forward(*ins, h0, chunk=chunk)
+        sa = None
+    else:
+        y, ck, hT, sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True,
+                                     kernel="auto" if fwd == "subchunk" else "sequential")
+    if mode == "two_phase":
+        kw = dict(sa=sa, workspace="auto")
+    elif mode == "single_saved_sa":
+        if sa is None:
+            sa = wkv7.forward(*ins, h0, chunk=chunk, save_sa=True, kernel="sequential")[3]
+        kw = dict(sa=sa, workspace=None)
+    else:
+        kw = dict(sa=None, workspace=None)
     grads = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), chunk=chunk, **kw)
     torch.cuda.synchronize()
     return host(y), host(ck), host(hT), [host(g) for g in grads], host(sa)
 
 
-def check(x, gpu, chunk, heads=None, with_grads=True):
-    """Compare against the oracle; `heads` = list of (b, h) to restrict the oracle to."""
+def oracle_ref(x, chunk, heads=None, with_grads=True):
+    """fp64 oracle results, optionally for a list of (b, h) heads only (returned stacked as B' = len(heads), H = 1)."""
+    xs = x if heads is None else {n: np.stack([x[n][b, :, h] for b, h in heads])[:, :, None] for n in "rwkvab"}
+    pick = lambda t: None if t is None else (t if heads is None else np.stack([t[b, h] for b, h in heads])[:, None])
+    h0 = pick(x.get("h0"))
+    y, ck, hT, sa = oracle.forward(*(xs[n] for n in "rwkvab"), h0, chunk=chunk, want_sa=True)
+    out = dict(y=y, ck=ck, hT=hT, sa=sa)
+    if with_grads:
+        dy = x["dy"] if heads is None else np.stack([x["dy"][b, :, h] for b, h in heads])[:, :, None]
+        out["grads"] = oracle.backward(*(xs[n] for n in "rwkvab"), h0, ck, dy, pick(x.get("dhT")), chunk=chunk,
+                                       mode="ckpt")
+    return out
+
+
+def select(gpu, heads):
+    """The GPU results at the given (b, h) heads, stacked like oracle_ref(heads=...)."""
     y, ck, hT, grads, sa = gpu
-    names = ("dr", "dw", "dk", "dv", "da", "db")
-    if heads is None:
-        sel = [(slice(None), slice(None))]
-    else:
-        sel = [(slice(b, b + 1), slice(h, h + 1)) for b, h in heads]
-    for sb, sh in sel:
-        xs = {n: x[n][sb, :, sh] for n in "rwkvab"}
-        h0 = None if x.get("h0") is None else x["h0"][sb, sh]
-        dhT = None if x.get("dhT") is None else x["dhT"][sb, sh]
-        yo, cko, hTo, sao = oracle.forward(*(xs[n] for n in "rwkvab"), h0, chunk=chunk, want_sa=True)
-        assert rel(y[sb, :, sh], yo) <= TOL_FWD, ("y", rel(y[sb, :, sh], yo))
-        assert rel(sa[sb, :, sh], sao) <= TOL_FWD, ("sa", rel(sa[sb, :, sh], sao))
-        assert rel(hT[sb, sh], hTo) <= TOL_FWD, ("hT", rel(hT[sb, sh], hTo))
-        assert rel(ck[sb, sh], cko) <= TOL_FWD, ("h_ckpt", rel(ck[sb, sh], cko))
-        if not with_grads:
-            continue
-        go = oracle.backward(*(xs[n] for n in "rwkvab"), h0, cko, x["dy"][sb, :, sh], dhT, chunk=chunk, mode="ckpt")
-        for name, g, ref in zip(names, grads[:6], go[:6]):
-            assert rel(g[sb, :, sh], ref) <= TOL_BWD, (name, rel(g[sb, :, sh], ref))
-        assert rel(grads[6][sb, sh], go[6]) <= TOL_BWD, ("dh0", rel(grads[6][sb, sh], go[6]))
+    tok = lambda t: None if t is None else np.stack([t[b, :, h] for b, h in heads])[:, :, None]
+    st = lambda t: None if t is None else np.stack([t[b, h] for b, h in heads])[:, None]
+    return tok(y), st(ck), st(hT), [tok(g) for g in grads[:6]] + [st(grads[6])], tok(sa)
+
+
+def check(x, gpu, chunk, heads=None, with_grads=True, ref=None):
+    """Compare against the oracle, whole tensors and per row; `heads` = list of (b, h) to restrict to."""
+    if ref is None:
+        ref = oracle_ref(x, chunk, heads, with_grads)
+    y, ck, hT, grads, sa = gpu if heads is None else select(gpu, heads)
+    assert_close("y", y, ref["y"], TOL_FWD, 1)
+    if sa is not None:
+        assert_close("sa", sa, ref["sa"], TOL_FWD, 1)
+    assert_close("hT", hT, ref["hT"], TOL_FWD, 2)
+    assert_close("h_ckpt", ck, ref["ck"], TOL_FWD, 2)
+    if with_grads:
+        for name, g, r in zip(("dr", "dw", "dk", "dv", "da", "db"), grads[:6], ref["grads"][:6]):
+            assert_close(name, g, r, TOL_BWD, 1)
+        if grads[6] is not None:
+            assert_close("dh0", grads[6], ref["grads"][6], TOL_BWD, 2)
     # the last checkpoint is the final state, bit for bit
-    assert np.array_equal(ck[:, :, -1], hT)
+    full_ck, full_hT = gpu[1], gpu[2]
+    assert np.array_equal(full_ck[:, :, -1], full_hT)
 
 
-@pytest.mark.parametrize("mode", MODES)
+_REF = {}
+
+
+def workload_ref(name):
+    if name not in _REF:
+        wl = gen.WORKLOADS[name]
+        x = gen.full(wl)
+        _REF[name] = (x, oracle_ref(x, wl.chunk))
+    return _REF[name]
+
+
+@pytest.mark.parametrize("fwd,mode", [("transition", "two_phase"), ("transition", "single_recompute"),
+                                      ("subchunk", "two_phase"), ("subchunk", "single_saved_sa"),
+                                      ("sequential", "two_phase")])
 @pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
-def test_workload_parity_full(wkv7, name, mode):
+def test_workload_parity_full(wkv7, name, fwd, mode):
     wl = gen.WORKLOADS[name]
-    x = gen.full(wl)
-    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, mode), wl.chunk)
+    x, ref = workload_ref(name)
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, mode, fwd), wl.chunk, ref=ref)
 
 
-@pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
-def test_workload_parity_sequential_forward(wkv7, name):
-    """The token-by-token forward at the workloads' chunk (where `auto` takes sub-chunks)."""
-    wl = gen.WORKLOADS[name]
-    x = gen.full(wl)
-    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "two_phase", fwd="sequential"), wl.chunk)
+@pytest.mark.parametrize("fwd", ["transition", "sequential"])
+def test_workload_parity_wide7b_every_head(wkv7, fwd):
+    """The 7B-width slice (B2 T4096 H64, w near 1) against the oracle on all 128 heads, whole tensors and
+    per row, forward and the two-phase backward."""
+    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
+    x, ref = workload_ref("wide7b_b2_t4096_h64")
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "two_phase", fwd), wl.chunk, ref=ref)
+
+
+def test_workload_parity_wide7b_single_pass_sampled_heads(wkv7):
+    """The single-pass backward (one CTA per head past the SM count) on the 7B-width slice, sampled heads."""
+    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
+    x, _ = workload_ref("wide7b_b2_t4096_h64")
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "single_recompute", "transition"), wl.chunk,
+          heads=[(0, 0), (1, 37), (0, 63), (1, 5)])
+
+
+def test_subchunk_forward_wide7b_one_wave_against_the_oracle(wkv7):
+    """The 16-token sub-chunk forward on one batch row of the 7B-width slice (64 heads, 128 row blocks fit
+    one wave, so it runs), against the oracle on every head."""
+    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
+    x, ref = workload_ref("wide7b_b2_t4096_h64")
+    assert 64 * 2 <= sm_count()
+    x1 = {n: (None if t is None else t[:1]) for n, t in x.items()}
+    ref1 = {k_: (v_[:1] if k_ != "grads" else [g[:1] for g in v_]) for k_, v_ in ref.items()}
+    check(x1, run_gpu(wkv7, x1, wl.dtype, wl.chunk, "two_phase", "subchunk"), wl.chunk, ref=ref1)
 
 
 @pytest.mark.parametrize("name", ["debug_b12_t1024_h6", "wide7b_b2_t4096_h64"])
 def test_forward_kernels_agree(wkv7, name):
-    """Sub-chunk and token-by-token forwards on every head: y, sa and states agree to fp32 level.
-    The 7B-width case takes one batch row (64 heads, 4096 tokens, w near 1) so that its 128 row
-    blocks fit one wave and `auto` runs the sub-chunk kernel."""
+    """Transition, sub-chunk and token-by-token forwards on every head agree to fp32-level rounding."""
     wl = gen.WORKLOADS[name]
     x = gen.full(wl, with_grad=False)
-    if wl.B * wl.H * 2 > 148:
+    if wl.B * wl.H * 2 > sm_count():
         x = {n: (None if t is None else t[:1]) for n, t in x.items()}
     ins = [dev(x[n], wl.dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
-    outs = [wkv7.forward(*ins, h0, chunk=wl.chunk, save_sa=True, kernel=kk) for kk in FWD]
+    outs = [wkv7.forward(*ins, h0, chunk=wl.chunk)]
+    outs += [wkv7.forward(*ins, h0, chunk=wl.chunk, save_sa=True, kernel=kk)[:3] for kk in ("auto", "sequential")]
     torch.cuda.synchronize()
-    for a, b in zip(*outs):
-        assert rel(host(a), host(b)) <= 2e-6
-
-
-@pytest.mark.parametrize("mode", MODES)
-def test_workload_parity_wide7b_sampled_heads(wkv7, mode):
-    """128 heads: more than half the SM count, so the single-pass backward runs one CTA per head."""
-    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
-    x = gen.full(wl)
-    gpu = run_gpu(wkv7, x, wl.dtype, wl.chunk, mode)
-    check(x, gpu, wl.chunk, heads=[(0, 0), (1, 37), (0, 63)])
-    # every head: properties that hold at any size
-    y, ck, hT, grads, _ = gpu
-    assert all(np.isfinite(g).all() for g in grads[:6]) and np.isfinite(y).all()
+    for o in outs[1:]:
+        for p_, q_ in zip(outs[0], o):
+            assert rel(host(p_), host(q_)) <= 2e-5
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("B,T,H,chunk", [
     (1, 1, 1, 32), (1, 31, 1, 32), (2, 33, 3, 32), (1, 100, 2, 32), (3, 45, 1, 7), (1, 64, 5, 1),
-    (2, 96, 1, 16), (1, 32, 1, 32), (5, 70, 3, 32),
+    (2, 96, 1, 16), (1, 32, 1, 32), (5, 70, 3, 32), (2, 64, 2, 24),
 ])
 def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
     x = gen.random_small(B * 100 + T + H, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    for mode in MODES:
-        check(x, run_gpu(wkv7, x, dtype, chunk, mode), chunk)
-    check(x, run_gpu(wkv7, x, dtype, chunk, "two_phase", fwd="sequential"), chunk)
-
-
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2)])
-def test_strong_decay_forward(wkv7, dtype, lo, hi):
-    """Decays far below the workloads' range.  With w in (0.005, 0.05) the 16-token decay drops
-    under 1e-30 in some sub-chunks, which then advance token by token; (0.02, 0.2) stays in the
-    sub-chunk form with 1/gamma up to ~1e27.  The first 40 tokens keep the workloads' decay, so
-    one sequence mixes both paths.  Forward only here: the single-pass backward rebuilds the state
-    by dividing by w, which amplifies rounding by (1/w)^31 at these decays, as the page warns; the
-    two-phase backward, which never divides by w, is checked under the same decays below."""
-    x = gen.random_small(4242, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    rng = np.random.default_rng(7)
-    w = x["w"].copy()
-    w[:, 40:] = lo + (hi - lo) * rng.random(w[:, 40:].shape)
-    if dtype == "bf16":
-        w = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).float().numpy()
-    x["w"] = w.astype(np.float32)
+    ref = oracle_ref(x, chunk)
     for fwd in FWD:
-        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd=fwd), 32, with_grads=False)
+        for mode in MODES:
+            if fwd == "sequential" and mode != "two_phase":
+                continue
+            check(x, run_gpu(wkv7, x, dtype, chunk, mode, fwd), chunk, ref=ref)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2)])
-def test_strong_decay_backward_two_phase(wkv7, dtype, lo, hi):
-    """The two-phase backward under the same strong decays: its column gradients run the state
-    forward from the chunk's start and the state gradient backward from the chunk's end, with no
-    division by w, so the gradients stay within tolerance; dw where w < 1/32 is summed directly."""
-    x = gen.random_small(4243, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    rng = np.random.default_rng(8)
+def strong_decay(seed, dtype, lo, hi):
+    x = gen.random_small(seed, B=2, T=100, H=3, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
+    rng = np.random.default_rng(seed + 3765)
     w = x["w"].copy()
     w[:, 40:] = lo + (hi - lo) * rng.random(w[:, 40:].shape)
     if dtype == "bf16":
         w = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).float().numpy()
     x["w"] = w.astype(np.float32)
-    check(x, run_gpu(wkv7, x, dtype, 32, "two_phase"), 32)
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2), (0.3, 0.6)])
+def test_strong_decay_forward(wkv7, dtype, lo, hi):
+    """Decays far below the workloads' range.  In the transition chain a 32-token chunk whose decay product
+    falls under 1e-20 advances token by token; in the sub-chunk kernel a 16-token product under 1e-30.
+    (0.3, 0.6) stays in the transition form with 1/gamma up to ~1e17.  The first 40 tokens keep the
+    workloads' decay, so one sequence mixes both paths.  Forward only: the single-pass backward rebuilds the
+    state by dividing by w, which amplifies rounding by (1/w)^31 at these decays, as the page warns."""
+    x = strong_decay(4242, dtype, lo, hi)
+    ref = oracle_ref(x, 32, with_grads=False)
+    for fwd in FWD:
+        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd), 32, with_grads=False, ref=ref)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lo,hi", [(0.005, 0.05), (0.02, 0.2), (0.3, 0.6)])
+def test_strong_decay_backward_two_phase(wkv7, dtype, lo, hi):
+    """The two-phase backwards under the same strong decays: neither divides a state by w.  In the matrix
+    column gradients a chunk with some w below 1/32, or a decay product under 1e-20, takes the exact
+    token-by-token column passes."""
+    x = strong_decay(4243, dtype, lo, hi)
+    ref = oracle_ref(x, 32)
+    for fwd in ("transition", "subchunk"):
+        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd), 32, ref=ref)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zero_and_vanishing_decay_two_phase(wkv7, dtype):
-    """w = 0 (the state forgets a column entirely) and w = 1e-30 at scattered tokens and columns, in
-    both forward kernels and the two-phase backward (whose column pass takes such steps unscaled and
-    sums dw directly there).  Both values are exact in bf16 and fp32."""
+    """w = 0 (the state forgets a column entirely) and w = 1e-30 at scattered tokens and columns, in every
+    forward kernel and the two-phase backwards.  Both values are exact in bf16 and fp32."""
     x = gen.random_small(4244, B=2, T=96, H=2, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
     rng = np.random.default_rng(9)
     w = x["w"].copy()
@@ -202,16 +280,19 @@ def test_zero_and_vanishing_decay_two_phase(wkv7, dtype):
     w[pick < 0.02] = 0.0
     w[(pick >= 0.02) & (pick < 0.04)] = 1e-30
     x["w"] = w.astype(np.float32)
+    ref = oracle_ref(x, 32)
     for fwd in FWD:
-        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd=fwd), 32)
+        check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd), 32, ref=ref)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_many_heads_one_cta_per_head(wkv7, dtype):
-    """B*H = 78 heads (more than half of 148 SMs): the one-CTA-per-head backward, ragged T."""
+def test_many_heads(wkv7, dtype):
+    """B*H = 78 heads (156 row blocks, more than one wave of SMs), ragged T, every path."""
     x = gen.random_small(77, B=3, T=45, H=26, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
-    for mode in MODES:
-        check(x, run_gpu(wkv7, x, dtype, 32, mode), 32, heads=[(0, 0), (1, 13), (2, 25)])
+    heads = [(0, 0), (1, 13), (2, 25)]
+    ref = oracle_ref(x, 32, heads)
+    for fwd, mode in (("transition", "two_phase"), ("transition", "single_recompute"), ("subchunk", "single_saved_sa")):
+        check(x, run_gpu(wkv7, x, dtype, 32, mode, fwd), 32, heads=heads, ref=ref)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -224,20 +305,33 @@ def test_backward_is_deterministic(wkv7, mode):
         assert np.array_equal(ga, gb)
 
 
+def test_backward_without_sa_is_the_two_phase_path(wkv7):
+    """The backward called without the forward's sa (the plain forward's outputs only) and with a workspace
+    gives the same gradients as with sa: at chunk 32 the column gradients recompute sa themselves."""
+    x = gen.random_small(10, B=2, T=96, H=3, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
+    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    h0 = dev32(x["h0"])
+    y, ck, hT, sa = wkv7.forward(*ins, h0, save_sa=True, kernel="sequential")
+    g1 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa)
+    g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=None, workspace="auto")
+    for p_, q_ in zip(g1, g2):
+        assert torch.equal(p_, q_)
+
+
 def test_explicit_workspace_and_too_small_workspace(wkv7):
     """A caller-owned workspace gives the same gradients as the automatic one; a smaller one is refused."""
     x = gen.random_small(9, B=2, T=70, H=3, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
     ins = [dev(x[n], "bf16") for n in "rwkvab"]
     h0 = dev32(x["h0"])
-    y, ck, hT, sa = wkv7.forward(*ins, h0, save_sa=True)
+    y, ck, hT = wkv7.forward(*ins, h0)
     need = wkv7.backward_workspace_size(2, 70, 3)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    g1 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa, workspace=ws)
-    g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa)
-    for p, q in zip(g1, g2):
-        assert torch.equal(p, q)
+    g1 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), workspace=ws)
+    g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), workspace="auto")
+    for p_, q_ in zip(g1, g2):
+        assert torch.equal(p_, q_)
     with pytest.raises(wkv7.WKV7Error):
-        wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa, workspace=ws[: need - 256])
+        wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), workspace=ws[: need - 256])
 
 
 def test_no_h0_no_dhT_no_dh0(wkv7):
@@ -254,17 +348,16 @@ def test_no_h0_no_dhT_no_dh0(wkv7):
 
 
 def test_decay_exactly_one(wkv7):
-    """w == 1 everywhere (bf16 rounding can produce it): the divisions by w are exact."""
+    """w == 1 everywhere (bf16 rounding can produce it)."""
     x = gen.random_small(4, B=1, T=96, H=2, D=64, h0_std=0.1, dhT_std=1.0)
     x["w"] = np.ones_like(x["w"])
-    check(x, run_gpu(wkv7, x, "f32", 32), 32)
+    ref = oracle_ref(x, 32)
+    for fwd in FWD:
+        check(x, run_gpu(wkv7, x, "f32", 32, "two_phase", fwd), 32, ref=ref)
 
 
 def test_prefill_without_checkpoints_and_state_passing(wkv7):
-    """forward(T1) then forward(T2, h0 = hT) equals forward(T1 + T2) to fp32 rounding; h_ckpt may be skipped.
-
-    Not bit for bit: inside one call sa_t is formed by the one-token lookahead (a different, equal
-    expression), while the first token of a call forms it directly from h0."""
+    """forward(T1) then forward(T2, h0 = hT) equals forward(T1 + T2) to fp32 rounding; h_ckpt may be skipped."""
     x = gen.random_small(5, B=2, T=96, H=3, D=64, h0_std=0.1)
     ins = [dev(x[n], "bf16") for n in "rwkvab"]
     h0 = dev32(x["h0"])
@@ -272,8 +365,10 @@ def test_prefill_without_checkpoints_and_state_passing(wkv7):
     cut = 40
     y1, _, h1 = wkv7.forward(*(t[:, :cut].contiguous() for t in ins), h0, checkpoints=False)
     y2, _, h2 = wkv7.forward(*(t[:, cut:].contiguous() for t in ins), h1, checkpoints=False)
-    assert rel(host(torch.cat([y1, y2], dim=1)), host(y)) <= 1e-6
-    assert rel(host(h2), host(hT)) <= 1e-6
+    assert rel(host(torch.cat([y1, y2], dim=1)), host(y)) <= 2e-5
+    assert rel(host(h2), host(hT)) <= 2e-5
+    yo, _, hTo = oracle.forward(*(x[n] for n in "rwkvab"), x["h0"])
+    assert rel(host(y), yo) <= TOL_FWD and rel(host(hT), hTo) <= TOL_FWD
 
 
 def test_zero_tokens(wkv7):
@@ -291,13 +386,6 @@ def test_zero_tokens(wkv7):
 # ---------------------------------------------------------------------------------- decode
 
 
-def decode_inputs(wl, b_list):
-    rows = [gen.token_inputs(wl, b) for b in b_list]
-    ins = {n: np.stack([rw[n][0] for rw in rows]) for n in "rwkvab"}   # (B', H, D)
-    st = np.stack([gen.state_init(wl, b, "state") for b in b_list])
-    return ins, st
-
-
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_decode_small(wkv7, dtype):
     x = gen.random_small(6, B=3, T=1, H=5, D=64, h0_std=0.1, dtype=dtype)
@@ -308,7 +396,7 @@ def test_decode_small(wkv7, dtype):
     assert rel(host(y), yo) <= TOL_FWD and rel(host(state), so) <= TOL_FWD
     # decode == forward with T = 1
     yf, _, hf = wkv7.forward(*(dev(x[n], dtype) for n in "rwkvab"), dev32(x["h0"]))
-    assert rel(host(state), host(hf)) <= 1e-6 and rel(host(y), host(yf)[:, 0]) <= 1e-6
+    assert rel(host(state), host(hf)) <= 2e-5 and rel(host(y), host(yf)[:, 0]) <= 2e-5
 
 
 def test_decode_layout_probes(wkv7):
@@ -339,9 +427,9 @@ def test_decode_layout_probes(wkv7):
         assert np.array_equal(host(state), st)
 
 
-def test_decode7b_full_size_sampled(wkv7):
-    """7B decode step at full size (256 sequences x 2048 heads x 64 x 64 fp32 state, 8.6 GB);
-    the oracle checks sampled sequences, and every sequence must stay finite."""
+def test_decode7b_full_size_every_sequence(wkv7):
+    """7B decode step at full size (256 sequences x 2048 heads x 64 x 64 fp32 state, 8.6 GB): every
+    sequence against the oracle (streamed in blocks of 16 sequences), whole tensors and per head."""
     wl = gen.WORKLOADS["decode7b_b256_h2048"]
     B, H, D = wl.B, wl.H, wl.D
     state = torch.empty((B, H, D, D), dtype=torch.float32, device="cuda")
@@ -353,10 +441,21 @@ def test_decode7b_full_size_sampled(wkv7):
         state[b].copy_(torch.from_numpy(gen.state_init(wl, b, "state")))
     y = wkv7.decode(state, *(ins[n] for n in "rwkvab"))
     torch.cuda.synchronize()
-    sample = [0, 77, 255]
-    xi, st0 = decode_inputs(wl, sample)
-    yo, so = oracle.decode(st0, *(xi[n] for n in "rwkvab"))
-    for s, b in enumerate(sample):
-        assert rel(host(y[b]), yo[s]) <= TOL_FWD
-        assert rel(host(state[b]), so[s]) <= TOL_FWD
     assert torch.isfinite(y).all()
+    num_y = den_y = num_s = den_s = 0.0
+    worst = 0.0
+    for b0 in range(0, B, 16):   # the inputs of each block of sequences are drawn again (seeded per sequence)
+        bs = list(range(b0, min(B, b0 + 16)))
+        rows = [gen.token_inputs(wl, b) for b in bs]
+        xi = {n: np.stack([rw[n][0] for rw in rows]) for n in "rwkvab"}
+        st0 = np.stack([gen.state_init(wl, b, "state") for b in bs])
+        yo, so = oracle.decode(st0, *(xi[n] for n in "rwkvab"))
+        yg, sg = host(y[b0:b0 + len(bs)]), host(state[b0:b0 + len(bs)])
+        num_y += ((yg - yo) ** 2).sum()
+        den_y += (yo ** 2).sum()
+        num_s += ((sg - so) ** 2).sum()
+        den_s += (so ** 2).sum()
+        worst = max(worst, row_rel(yg, yo, 1), row_rel(sg, so, 2))
+    assert np.sqrt(num_y / den_y) <= TOL_FWD
+    assert np.sqrt(num_s / den_s) <= TOL_FWD
+    assert worst <= ROW_FACTOR * TOL_FWD
