@@ -77,20 +77,32 @@ int wkv7_num_chunks(int T, int chunk);
  *   hT      (B,H,D,D) fp32 final state, or NULL.
  *   sa      (B,T,H,D) fp32 output or NULL: sa_t = S_{t-1} a_t for every token and
  *           state row (element (b,t,h,i) is row i).  Passing it to wkv7_backward
- *           spares the backward its per-chunk recompute of these values.
+ *           selects the two-phase backward that reads it.
+ *   workspace, workspace_bytes
+ *           device scratch of at least wkv7_forward_workspace_size() bytes, 256-byte
+ *           aligned, owned by the caller; or NULL / 0.  Used at chunk == 32 without sa:
+ *           every 32-token chunk's transition operands are formed at once into it (a
+ *           chunk-parallel kernel), then one kernel runs the chain over the chunks reading
+ *           them.  Without it, the same chain runs with the operands formed inside the
+ *           chain kernel, one chunk ahead (slower).  With sa (or chunk != 32): 16-token
+ *           sub-chunks when chunk % 16 == 0 and the B*H*2 row blocks fit one wave of SMs,
+ *           else token by token.
+ * Results of every path agree with the token-by-token definition to ~1e-5 relative.
  * Source: Forward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b,
-                 const float *h0, float *y, float *h_ckpt, float *hT, float *sa, void *stream);
+                 const float *h0, float *y, float *h_ckpt, float *hT, float *sa,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes; 0 when chunk != 32);
+ * returns a wkv7_status (the same size checks as wkv7_forward). */
+int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
 /*
- * The same forward, arguments and results as wkv7_forward, always advanced token by token.
- * wkv7_forward advances 16 tokens at a time in the closed form of the recurrence over those
- * tokens (dense products on tensor cores, agreeing with this one to ~1e-7 relative at the
- * training shapes) when chunk is a multiple of 16 and B*H*2 row blocks fit one wave of SMs, and
- * runs this one otherwise.  Kept callable for comparison and as the plain per-token path.
+ * The same forward, arguments and results as wkv7_forward (without a workspace), always
+ * advanced token by token in fp32.  Kept callable for comparison and as the plain per-token path.
  */
 int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
                             const void *r, const void *w, const void *k,
@@ -112,19 +124,27 @@ int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
  *   workspace, workspace_bytes
  *           device scratch of at least wkv7_backward_workspace_size() bytes, 256-byte
  *           aligned, owned by the caller and reused freely between calls; or NULL / 0.
- *           With a workspace and a saved sa the backward runs in two phases: one pass
- *           over the sequence walks the state gradient (writing dv, dh0, and into the
- *           workspace every dsa and the state gradient at every chunk end) -- 16 tokens per
- *           step in the closed form of that recurrence when chunk % 16 == 0 and the B*H*2
- *           row blocks fit one wave of SMs, else token by token -- then every chunk of
- *           every head forms its column gradients (dr, dw, dk, da, db) at once, running
- *           the state forward from the checkpoint before the chunk (h0 for the first) and
- *           the state gradient backward from the chunk end, with no division by w.
- *           Without one (or without sa) a single pass does everything: each chunk is
- *           walked in reverse from its end checkpoint, the earlier states rebuilt as
- *           (h - v k^T - sa b^T) / w (column j divided by w_j), which amplifies rounding
- *           by 1/w per token.  The two-phase results are ~1e-7 of exact at ordinary
- *           decays; the single pass's ~5e-4.
+ *           With a workspace and no sa at chunk == 32 (the transition backward): every
+ *           32-token chunk's transition operands are formed at once; one pass over the chunks,
+ *           last to first, carries the state gradient G (w.r.t. the state after a chunk, from
+ *           every later token) back through the transposed transitions, writing G at each
+ *           chunk end into the workspace, and dh0; then every chunk forms dr, dw, dk, dv, da, db
+ *           at once in matrix form from the state before it (h_ckpt[c-1], or h0), G and the
+ *           state after it, recomputing sa -- no state is divided by w.  Chunks whose decays
+ *           are too strong for the matrix form (some w < 1/32, or a 32-token decay product
+ *           below 1e-20) take the exact token-by-token passes.  Results ~1e-5 of exact.
+ *           With a workspace and sa: the two-phase backward -- one pass over the sequence walks
+ *           the state gradient (16 tokens per step in the closed form when chunk % 16 == 0 and
+ *           the B*H*2 row blocks fit one wave of SMs, else token by token), then every chunk's
+ *           column gradients at once by two token-by-token passes, with no division by w
+ *           (~1e-7 of exact).
+ *           Without a workspace a single pass does everything: each chunk is walked in reverse
+ *           from the state at its end (the stored checkpoint with sa given; the chunk recomputed
+ *           from its start checkpoint without), the earlier states rebuilt as
+ *           (h - v k^T - sa b^T) / w (column j divided by w_j), which amplifies rounding by 1/w
+ *           per token, as the page warns: ~5e-4 of exact at the workloads' decays (w >= 0.55),
+ *           far worse where w is small (below ~0.05 it can exceed any useful tolerance); use a
+ *           workspace there.
  * Sums are taken in a fixed order (no atomics): results are deterministic.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).
  */
@@ -140,8 +160,8 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
  * returns a wkv7_status (the same size checks as wkv7_backward). */
 int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
-/* Bytes of device scratch the library owns for wkv7_backward_noalloc (64 MiB). */
-#define WKV7_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+/* Bytes of device scratch the library owns for wkv7_backward_noalloc (128 MiB). */
+#define WKV7_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 
 /*
  * The two-phase backward without any workspace argument and without allocating.
@@ -156,7 +176,7 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *
  *
  *   Arguments, layouts and results: as wkv7_backward, with `sa` required (the forward's
  *   saved sa) and no workspace.  Problems whose wkv7_backward_workspace_size exceeds
- *   WKV7_NOALLOC_SCRATCH_BYTES return WKV7_ERR_SCRATCH_LIMIT (B12 T1024 H6 needs ~57 MB;
+ *   WKV7_NOALLOC_SCRATCH_BYTES return WKV7_ERR_SCRATCH_LIMIT (B12 T1024 H6 needs ~96 MB;
  *   use wkv7_backward with a workspace for larger ones).
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *   and caches it; make that first call before capturing a stream on that device.

@@ -29,7 +29,8 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "wkv7_num_chunks": (_I, [_I, _I]),
-    "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
+    "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P, ctypes.c_size_t] + [_P]),
+    "wkv7_forward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
     "wkv7_forward_sequential": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
     "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
@@ -75,6 +76,13 @@ def num_chunks(T: int, chunk: int) -> int:
 
 def version() -> int:
     return lib.wkv7_version()
+
+
+def forward_workspace_size(B: int, T: int, H: int, D: int = D_HEAD, chunk: int = 32) -> int:
+    """Bytes of device workspace the forward uses (0 when it uses none)."""
+    n = ctypes.c_size_t(0)
+    _check(lib.wkv7_forward_workspace_size(B, T, H, D, chunk, ctypes.byref(n)), "wkv7_forward_workspace_size")
+    return n.value
 
 
 def backward_workspace_size(B: int, T: int, H: int, D: int = D_HEAD, chunk: int = 32) -> int:
@@ -131,16 +139,17 @@ def _check_f32(t, shape, name, where, dev):
 
 
 def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True, final_state: bool = True,
-            save_sa: bool = False, out=None, stream=None, kernel: str = "auto"):
+            save_sa: bool = False, out=None, stream=None, kernel: str = "auto", workspace="auto"):
     """WKV7 forward.  r..b: (B, T, H, 64) float32/bfloat16 CUDA tensors; h0: (B, H, 64, 64) float32 or None.
 
     Returns (y, h_ckpt, hT): y (B,T,H,64) fp32; h_ckpt (B,H,C,64,64) fp32 (None when
     checkpoints=False); hT (B,H,64,64) fp32 (None when final_state=False).  With
     save_sa=True a fourth tensor sa (B,T,H,64) fp32 is returned (sa_t = S_{t-1} a_t per
-    state row), which `backward` accepts to skip its recompute.  `out` may give
-    preallocated (y, h_ckpt, hT) or (y, h_ckpt, hT, sa).  kernel="auto" is `wkv7_forward`
-    (16-token sub-chunks when chunk % 16 == 0 and the B*H*2 row blocks fit one wave of SMs);
-    "sequential" is `wkv7_forward_sequential`.
+    state row), which `backward` accepts.  `out` may give preallocated (y, h_ckpt, hT) or
+    (y, h_ckpt, hT, sa).  kernel="auto" is `wkv7_forward`; "sequential" is
+    `wkv7_forward_sequential` (token by token).  workspace: "auto" (default) allocates the
+    forward's scratch with torch when it uses one (chunk 32 without sa); a uint8 CUDA tensor of
+    at least forward_workspace_size() bytes is used as is; None runs without one.
     """
     if kernel not in ("auto", "sequential"):
         raise ValueError(f"wkv7.forward: kernel must be 'auto' or 'sequential', got {kernel!r}")
@@ -162,9 +171,24 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
     _check_f32(ck, (B, H, C, D, D), "h_ckpt", "wkv7.forward", dev)
     _check_f32(hT, (B, H, D, D), "hT", "wkv7.forward", dev)
     _check_f32(sa, (B, T, H, D), "sa", "wkv7.forward", dev)
-    fn = lib.wkv7_forward if kernel == "auto" else lib.wkv7_forward_sequential
-    st = fn(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)), _stream(stream))
-    _check(st, "wkv7_forward" if kernel == "auto" else "wkv7_forward_sequential")
+    if kernel == "sequential":
+        st = lib.wkv7_forward_sequential(B, T, H, D, chunk, _in_dtype(r),
+                                         *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)), _stream(stream))
+        _check(st, "wkv7_forward_sequential")
+    else:
+        ws, ws_bytes = None, 0
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+            ws_bytes = forward_workspace_size(B, T, H, D, chunk) if sa is None and T > 0 else 0
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+        elif workspace is not None:
+            if workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+                raise ValueError("wkv7.forward: workspace must be a contiguous uint8 tensor on the inputs' device")
+            ws, ws_bytes = workspace, workspace.numel()
+        st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)),
+                              _ptr(ws), ws_bytes, _stream(stream))
+        _check(st, "wkv7_forward")
     if save_sa or (out is not None and len(out) > 3):
         return y, ck, hT, sa
     return y, ck, hT
@@ -176,9 +200,9 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
     need_dh0=False).  h_ckpt must come from `forward` with the same chunk; `sa` is the forward's
     saved sa (save_sa=True) or None, in which case each chunk recomputes it.
 
-    workspace: "auto" (default) allocates the two-phase backward's scratch with torch when sa is
-    given; a uint8 CUDA tensor of at least backward_workspace_size() bytes is used as is; None runs
-    the single-pass backward."""
+    workspace: "auto" (default) allocates the two-phase backward's scratch with torch (at chunk 32, or
+    with sa given); a uint8 CUDA tensor of at least backward_workspace_size() bytes is used as is;
+    None runs the single-pass backward."""
     torch = _torch()
     B, T, H, D = r.shape
     _check_inputs((r, w, k, v, a, b), (B, T, H, D), "wkv7.backward")
@@ -201,7 +225,7 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
-        if sa is not None and T > 0:
+        if T > 0 and (chunk == 32 or sa is not None):
             ws_bytes = backward_workspace_size(B, T, H, D, chunk)
             ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     elif workspace is not None:

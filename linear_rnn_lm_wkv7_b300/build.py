@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libwkv7.so")
 SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwdc.cu", "wkv7_chain.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu",
-           "wkv7_colmat.cu", "wkv7_decode.cu", "wkv7_noalloc.cu"]
+           "wkv7_colmat.cu", "wkv7_ops.cu", "wkv7_decode.cu", "wkv7_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 

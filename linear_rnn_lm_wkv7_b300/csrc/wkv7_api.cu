@@ -103,7 +103,8 @@ const char* wkv7_last_cuda_error(void) { return g_last_cuda_error; }
 namespace {
 int forward_impl(bool sequential, int B, int T, int H, int D, int chunk, int in_dtype, const void* r,
                  const void* w, const void* k, const void* v, const void* a, const void* b, const float* h0,
-                 float* y, float* h_ckpt, float* hT, float* sa, void* stream) {
+                 float* y, float* h_ckpt, float* hT, float* sa, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
@@ -118,20 +119,39 @@ int forward_impl(bool sequential, int B, int T, int H, int D, int chunk, int in_
   p.in = {r, w, k, v, a, b};
   p.h0 = h0; p.y = y; p.h_ckpt = h_ckpt; p.hT = hT; p.sa = T > 0 ? sa : nullptr;
   const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-  return record_cuda(sequential ? wkv7::launch_forward_sequential(p, st_) : wkv7::launch_forward(p, st_));
+  if (sequential) return record_cuda(wkv7::launch_forward_sequential(p, st_));
+  if (workspace != nullptr && chunk == 32 && p.sa == nullptr && T > 0) {
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
+    if (workspace_bytes < wkv7::forward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
+    unsigned char* ops = static_cast<unsigned char*>(workspace);
+    cudaError_t err = wkv7::launch_transition_ops(p, ops, st_);
+    if (err != cudaSuccess) return record_cuda(err);
+    return record_cuda(wkv7::launch_forward_from_ops(p, ops, st_));
+  }
+  return record_cuda(wkv7::launch_forward(p, st_));
 }
 }  // namespace
 
 int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
                  const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
-                 float* h_ckpt, float* hT, float* sa, void* stream) {
-  return forward_impl(false, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, stream);
+                 float* h_ckpt, float* hT, float* sa, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(false, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, workspace,
+                      workspace_bytes, stream);
 }
 
 int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
                             const void* k, const void* v, const void* a, const void* b, const float* h0, float* y,
                             float* h_ckpt, float* hT, float* sa, void* stream) {
-  return forward_impl(true, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, stream);
+  return forward_impl(true, B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, y, h_ckpt, hT, sa, nullptr, 0,
+                      stream);
+}
+
+int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t* bytes) {
+  int st = check_sizes(B, T, H, D, chunk);
+  if (st) return st;
+  if (bytes == nullptr) return WKV7_ERR_ARG;
+  *bytes = wkv7::forward_workspace_bytes(B, T, H, chunk);
+  return WKV7_OK;
 }
 
 int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
@@ -157,8 +177,8 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const voi
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
     if (workspace_bytes < wkv7::backward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    return record_cuda(chunk == 32 ? wkv7::launch_backward_transition(p, workspace, st_)
-                                   : wkv7::launch_backward_two_phase(p, workspace, st_));
+    return record_cuda(p.sa == nullptr ? wkv7::launch_backward_transition(p, workspace, st_)
+                                       : wkv7::launch_backward_two_phase(p, workspace, st_));
   }
   return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
 }

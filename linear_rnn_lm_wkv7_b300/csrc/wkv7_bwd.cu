@@ -357,6 +357,13 @@ bwd_kernel(int T, int H, int chunk, int nchunks,
         }
       }
       __syncwarp();  // each warp reads back only the sa rows it wrote
+      // walk back from the recomputed end state: it is the state these sa values belong to (the stored
+      // checkpoint carries the forward's own rounding, which the division by w below would amplify)
+#pragma unroll
+      for (int p = 0; p < RP; ++p) {
+        S[p][0] = Rs[p][0];
+        S[p][1] = Rs[p][1];
+      }
     }
 
     // ---- reverse walk over the chunk

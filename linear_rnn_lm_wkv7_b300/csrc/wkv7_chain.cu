@@ -9,30 +9,30 @@
 // Transition form (exact in real arithmetic).  Over a chunk of 32 tokens from state S0, with
 // gamma_t = w_0 o .. o w_t per column and
 //     A^_t = a_t o gamma_{t-1},  R^_t = r_t o gamma_t,  K~_t = k_t / gamma_t,  B~_t = b_t / gamma_t,
-//     K-_t = k_t o gamma_31 / gamma_t,  B-_t = b_t o gamma_31 / gamma_t,
 //     M_ab = tril(A^ B~^T, -1), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T), M_rk = tril(R^ K~^T),
-//     T = (I - M_ab)^-1,  B' = T^T B-,  C = M_rb T,
-// the state after the chunk and the chunk's outputs are
-//     S' = S0 diag(gamma_31) + S0 M' + V^T K',   M' = A^^T B',  K' = K- + M_ak^T B'
-//     Y  = R' S0^T + P V,                        R' = R^ + C A^,  P = M_rk + C M_ak
+//     T = (I - M_ab)^-1,  B' = (T^T B~) diag(gamma_31),  C = M_rb T,
+//     K' = K~ diag(gamma_31) + M_ak^T B',  P = M_rk + C M_ak,
+// the state after the chunk and the chunk's outputs are, with P1 = S0 A^^T (32 tokens wide),
+//     S' = S0 diag(gamma_31) + P1 B' + V^T K'
+//     Y^T = S0 R^^T + P1 C^T + V^T P^T                         (columns t: y_t)
 // (unrolling the recurrence: sa_t and y_t are dots of S0 with decayed a_t / r_t plus the chunk's own
 // rank-one terms, coupled through sa by the unit lower-triangular system (I - M_ab); eliminating sa
-// leaves one 64 x 64 product per chunk on the serial path).  Everything but S0 M' is independent
-// of the state and is prepared one chunk ahead.
+// leaves two dependent products, S0 A^^T then P1 B', on the serial path per 32 tokens).  Everything
+// but P1 and the products with S0 is independent of the state and is prepared one chunk ahead.
 //
 // Precision: tensor-core products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi,
-// see wkv7_mma.cuh), ~2^-17 relative each, fp32 accumulation; the diagonal part S0 diag(gamma_31)
-// in fp32.  1/gamma grows like prod(1/w); a chunk whose gamma_31 falls below 1e-20 in some column
-// (or is not finite) is advanced token by token instead (exact fp32), so any w in [0, 1] works.
+// wkv7_mma.cuh), ~2^-17 relative each, fp32 accumulation; S0 diag(gamma_31) in fp32.  1/gamma grows
+// like prod(1/w); a chunk whose gamma_31 falls below 1e-20 in some column (or is not finite) is
+// advanced token by token instead (exact fp32), so any w in [0, 1] works.
 //
-// Mapping: one CTA per (head, 32-row block), 12 warps, one CTA per SM.
-//   warps 0-1  (chain): rows 16m..16m+15 of the CTA's slice of S as mma accumulators; per chunk they
-//              store S as an operand for the output warps, form S M', add S o gamma_31 and V^T K',
-//              and write the checkpoint;
-//   warps 2-3  (output): V^T K' for the chain warps, then Y^T = S0 R'^T + V^T P^T, and y;
+// Operands are stored once, row-major, as bf16 hi and lo arrays, and read with ldmatrix (.trans
+// for the transposed uses).  Mapping: one CTA per (head, 32-row block), 12 warps, one CTA per SM.
+//   warps 0-1  (chain): rows 16m..16m+15 of the CTA's slice of S as mma accumulators; per chunk
+//              P1, S', Y (staged), the checkpoint;
+//   warps 2-3  (v): the chunk's v slice as an operand and N = V^T K' for the chain warps, then y;
 //   warps 4-11 (prep): the next chunk's decays, operands, coupling products, T (block forward
-//              substitution on CUDA cores) and M', K', R', P, into the other of two buffers.
-// One CTA barrier per chunk; the chain and output warps hand S and V^T K' over by named barriers.
+//              substitution on CUDA cores), B', C, K', P into the other of two buffers.
+// One CTA barrier per chunk; the chain and v warps hand N and y over by named barriers.
 //
 // The same kernel runs the backward's state-gradient walk (GRAD): read from the last token down,
 // that recurrence has the forward's form with w' = w_{t+1}, a' = b_{t+1}, b' = a_{t+1}, v' = dy_t,
@@ -56,75 +56,65 @@ constexpr int kR = 32;       // state rows per CTA
 constexpr int kNT = 384;     // threads
 constexpr int kNP = 256;     // prep threads (warps 4-11)
 constexpr int kFirstPrep = 128;
+constexpr int kLD64 = 72;    // row stride (bf16 elements) of 64-wide operands
+constexpr int kLD32 = 40;    // of 32-wide operands
 constexpr float kMinGamma = 1e-20f;
 
 // named barriers
 constexpr int kBarPrep = 1;   // prep warps
 constexpr int kBarChain = 2;  // chain warps
-constexpr int kBarS = 3;      // chain warps arrive (S stored), output warps wait
-constexpr int kBarN = 4;      // output warps arrive (V^T K' stored), chain warps wait
-constexpr int kBarOut = 5;    // output warps
+constexpr int kBarN = 3;      // v warps arrive (V^T K' stored), chain warps wait
+constexpr int kBarY = 4;      // chain warps arrive (y staged), v warps wait
+constexpr int kBarV = 5;      // v warps
 
 template <int ID, int N>
 __device__ __forceinline__ void bsync() { asm volatile("bar.sync %0, %1;\n" ::"n"(ID), "n"(N) : "memory"); }
 template <int ID, int N>
 __device__ __forceinline__ void barrive() { asm volatile("bar.arrive %0, %1;\n" ::"n"(ID), "n"(N) : "memory"); }
 
-// pair-tile array sizes in words (hi + lo) of an R x C matrix
-__host__ __device__ constexpr int pt_words(int r, int c) { return r * c; }
+__host__ __device__ constexpr int rmb(int rows, int ld) { return 2 * rows * ld * 2; }  // RM bytes, hi + lo
 
 template <typename Tin, typename TV>
 struct Lay {
-  // ---- prep scratch (byte offsets)
-  static constexpr size_t oG = 0;                                   // float [32][64] gamma; then M_ab^T fp32
-  static constexpr int kSMab = 36;                                  // row stride of M_ab^T [32][36]
-  static constexpr size_t oU1 = oG + 32 * 64 * 4;                    // B~, K~ (PT 32x64 each); then T^T, B'^T, C
-  static constexpr size_t oBt = oU1;
-  static constexpr size_t oKt = oU1 + pt_words(32, 64) * 4;
-  static constexpr size_t oTT = oU1;                                 // PT 32x32 (T^T)
-  static constexpr size_t oBpT = oU1 + pt_words(32, 32) * 4;         // PT 64x32 (B'^T)
-  static constexpr size_t oC = oBpT + pt_words(64, 32) * 4;          // PT 32x32 (C)
-  static constexpr size_t oRh = oU1 + 2 * pt_words(32, 64) * 4;      // PT 32x64 (R^)
-  static constexpr size_t oU2 = oRh + pt_words(32, 64) * 4;          // A^ (PT 32x64); then TI, E
-  static constexpr size_t oAh = oU2;
-  static constexpr int kSTI = 36;
-  static constexpr size_t oTI = oU2;                                 // float [32][36]
-  static constexpr size_t oE = oU2 + 32 * kSTI * 4;                  // float [16][16]
-  static constexpr size_t oAhT = oU2 + pt_words(32, 64) * 4;         // PT 64x32 (A^^T)
-  static constexpr size_t oBmT = oAhT + pt_words(64, 32) * 4;        // PT 64x32 (B-^T)
-  static constexpr size_t oKmT = oBmT + pt_words(64, 32) * 4;        // PT 64x32 (K-^T)
-  static constexpr size_t oMakT = oKmT + pt_words(64, 32) * 4;       // PT 32x32 (M_ak^T)
-  static constexpr size_t oMrb = oMakT + pt_words(32, 32) * 4;       // PT 32x32 (M_rb)
-  static constexpr size_t oMrk = oMrb + pt_words(32, 32) * 4;        // PT 32x32 (M_rk)
-  static constexpr size_t kPrepEnd = oMrk + pt_words(32, 32) * 4;
-  static_assert(oE + 16 * 16 * 4 <= oAhT, "TI and E fit in A^'s space");
-  static_assert(oC + pt_words(32, 32) * 4 <= oRh, "T^T, B'^T, C fit in B~ and K~'s space");
-  static_assert(32 * kSMab * 4 <= 32 * 64 * 4, "M_ab^T fits in gamma's space");
-  // ---- chain buffers (x2): what one chunk's chain and output steps read
-  static constexpr size_t cMT = 0;                                   // PT 64x64 (M'^T)
-  static constexpr size_t cKpT = cMT + pt_words(64, 64) * 4;         // PT 64x32 (K'^T)
-  static constexpr size_t cRp = cKpT + pt_words(64, 32) * 4;         // PT 32x64 (R')
-  static constexpr size_t cP = cRp + pt_words(32, 64) * 4;           // PT 32x32 (P)
-  static constexpr size_t cGL = cP + pt_words(32, 32) * 4;           // float [64] gamma_31
-  static constexpr size_t cMeta = cGL + 64 * 4;                      // int [4]: token-by-token flag
-  static constexpr size_t kChain = cMeta + 16;
-  static constexpr size_t oChain = kPrepEnd;
+  // ---- prep scratch
+  static constexpr int oG = 0;                          // float [32][64] gamma
+  static constexpr int oKt = oG + 32 * 64 * 4;          // RM 32x64: K~, B~
+  static constexpr int oBt = oKt + rmb(32, kLD64);
+  static constexpr int oMak = oBt + rmb(32, kLD64);     // RM 32x32: M_ak, M_rb, M_rk, T
+  static constexpr int oMrb = oMak + rmb(32, kLD32);
+  static constexpr int oMrk = oMrb + rmb(32, kLD32);
+  static constexpr int oT = oMrk + rmb(32, kLD32);
+  static constexpr int kSM = 36;
+  static constexpr int oMab = oT + rmb(32, kLD32);      // float [32][36]: M_ab
+  static constexpr int oTI = oMab + 32 * kSM * 4;       // float [32][36]: T
+  static constexpr int oE = oTI + 32 * kSM * 4;         // float [16][16]
+  static constexpr int kPrepEnd = oE + 16 * 16 * 4;
+  // ---- chain buffers (x2): A^, R^, B', K' (RM 32x64), C, P (RM 32x32), gamma_31, flags
+  static constexpr int cAh = 0;
+  static constexpr int cRh = cAh + rmb(32, kLD64);
+  static constexpr int cBp = cRh + rmb(32, kLD64);
+  static constexpr int cKp = cBp + rmb(32, kLD64);
+  static constexpr int cC = cKp + rmb(32, kLD64);
+  static constexpr int cP = cC + rmb(32, kLD32);
+  static constexpr int cGL = cP + rmb(32, kLD32);
+  static constexpr int cMeta = cGL + 64 * 4;
+  static constexpr int kChain = cMeta + 16;
+  static constexpr int oChain = kPrepEnd;
   // ---- raw inputs of the chunk being prepared: w, k, a, b, r [32][64]
-  static constexpr size_t oRaw = oChain + 2 * kChain;
-  static constexpr size_t kRaw = 5 * kL * kD * sizeof(Tin);
-  // ---- v of this CTA's rows, two chunks: [32 tokens][32 rows]
-  static constexpr size_t oV = oRaw + kRaw;
-  static constexpr size_t kV = kL * kR * sizeof(TV);
-  // ---- chain / output exchange
-  static constexpr size_t oS = oV + 2 * kV;                          // PT 32x64 (S of this CTA's rows)
-  static constexpr size_t oVT = oS + pt_words(32, 64) * 4;           // PT 32x32 (V^T: rows i, columns t)
-  static constexpr size_t oN = oVT + pt_words(32, 32) * 4;           // float [2 mt][8 nj][32 lanes][4]
+  static constexpr int oRaw = oChain + 2 * kChain;
+  static constexpr int kRaw = 5 * kL * kD * (int)sizeof(Tin);
+  // ---- v of this CTA's rows: raw [32 t][32 i] (x2), and as an operand V (RM 32 t x 32 i)
+  static constexpr int oVraw = oRaw + kRaw;
+  static constexpr int kVraw = kL * kR * (int)sizeof(TV);
+  static constexpr int oVop = oVraw + 2 * kVraw;
+  // ---- N (fp32, accumulator order [2 mt][8 nj][32 lanes][4]) and y staging [32 t][36]
+  static constexpr int oN = oVop + rmb(32, kLD32);
   static constexpr int kSY = 36;
-  static constexpr size_t oY = oN + 32 * 64 * 4;                     // float [32 t][36]
-  static constexpr size_t oFS = oN;                                  // token-by-token path: float [32][68] (N and Y)
+  static constexpr int oY = oN + 32 * 64 * 4;
+  static constexpr int oFS = oN;                        // token-by-token path: float [32][68] over N and y
   static constexpr int kSFS = 68;
-  static constexpr size_t kBytes = oY + kL * kSY * 4;
-  static_assert(oFS + 32 * kSFS * 4 <= kBytes, "token-by-token state fits over N and Y");
+  static constexpr int kBytes = oY + kL * kSY * 4;
+  static_assert(oFS + 32 * kSFS * 4 <= kBytes, "token-by-token state fits over N and y");
 };
 
 // Pointers of one call.  Forward: the inputs, s0 = h0, y, ck = h_ckpt, sT = hT.  Gradient walk
@@ -176,9 +166,19 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
   auto v_token = [&](int st) { return GRAD ? T - 1 - st : st; };
 
   unsigned char* const chain0 = sm + LY::oChain;
-  auto chain_buf = [&](int m) { return chain0 + (size_t)(m & 1) * LY::kChain; };
+  auto chain_buf = [&](int m) { return chain0 + (m & 1) * LY::kChain; };
+  auto bfp = [&](unsigned char* p, int off) { return reinterpret_cast<__nv_bfloat16*>(p + off); };
+  auto cbuf_rm64 = [&](unsigned char* cb, int off) { return RM{bfp(cb, off), 32 * kLD64, kLD64}; };
+  auto cbuf_rm32 = [&](unsigned char* cb, int off) { return RM{bfp(cb, off), 32 * kLD32, kLD32}; };
   Tin* const raw = reinterpret_cast<Tin*>(sm + LY::oRaw);
-  auto vbuf = [&](int m) { return reinterpret_cast<TV*>(sm + LY::oV + (size_t)(m & 1) * LY::kV); };
+  auto vraw = [&](int m) { return reinterpret_cast<TV*>(sm + LY::oVraw + (m & 1) * LY::kVraw); };
+  const RM Vop{bfp(sm, LY::oVop), 32 * kLD32, kLD32};
+  float* const nb = reinterpret_cast<float*>(sm + LY::oN);
+  float* const ys = reinterpret_cast<float*>(sm + LY::oY);
+  auto slow_flag = [&](const unsigned char* cb) {
+    const int* meta = reinterpret_cast<const int*>(cb + LY::cMeta);
+    return (meta[0] | meta[1]) != 0;
+  };
 
   if (warp < 2) {
     // =============================================================== chain warps
@@ -195,32 +195,82 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
         S[nj][0] = S[nj][1] = S[nj][2] = S[nj][3] = 0.f;
       }
     }
-    uint32_t* const pS = reinterpret_cast<uint32_t*>(sm + LY::oS);
-    const float* const nb = reinterpret_cast<const float*>(sm + LY::oN);
     __syncthreads();  // chunk 0 prepared
 
     for (int n = 0; n < nsub; ++n) {
-      const unsigned char* cb = chain_buf(n);
-      const int slow = reinterpret_cast<const int*>(cb + LY::cMeta)[0] | reinterpret_cast<const int*>(cb + LY::cMeta)[1];
+      unsigned char* cb = chain_buf(n);
       const int tau0 = sub_start(n);
       const int nm = sub_len(n);
-      if (!slow) {
-        // S (the state before the chunk) as an operand for the output warps
+      if (!slow_flag(cb)) {
+        const RM Ah = cbuf_rm64(cb, LY::cAh), Rh = cbuf_rm64(cb, LY::cRh), Bp = cbuf_rm64(cb, LY::cBp);
+        const RM Cm = cbuf_rm32(cb, LY::cC), Pm = cbuf_rm32(cb, LY::cP);
+        // A fragments of S (k = j), from the accumulators
+        FragA fs[4];
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj) store_acc(pS, pt_words(32, 64) / 2, 4, mt, nj, lane, S[nj]);
-        barrive<kBarS, 128>();
-        // S M'
-        const uint32_t* pMT = reinterpret_cast<const uint32_t*>(cb + LY::cMT);
-        float acc[8][4];
+        for (int kk = 0; kk < 4; ++kk) fs[kk] = frag_from_acc(S[2 * kk], S[2 * kk + 1]);
+        // P1 = S A^^T (16 rows x 32 tokens)
+        float p1[4][4] = {};
 #pragma unroll
-        for (int nj = 0; nj < 8; ++nj) acc[nj][0] = acc[nj][1] = acc[nj][2] = acc[nj][3] = 0.f;
+        for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const FragA fa = frag_from_acc(S[2 * kk], S[2 * kk + 1]);
+          for (int np = 0; np < 2; ++np) {
+            FragB f0, f1;
+            rm_b2(Ah, 2 * np, kk, lane, f0, f1);
+            mma3(p1[2 * np], fs[kk], f0);
+            mma3(p1[2 * np + 1], fs[kk], f1);
+          }
+        FragA fp[2];
+        fp[0] = frag_from_acc(p1[0], p1[1]);
+        fp[1] = frag_from_acc(p1[2], p1[3]);
+        // P1 B' (16 rows x 64 columns)
+        float acc[8][4] = {};
 #pragma unroll
-          for (int nj = 0; nj < 8; ++nj) mma3(acc[nj], fa, load_b(pMT, pt_words(64, 64) / 2, 4, nj, kk, lane));
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int nq = 0; nq < 4; ++nq) {
+            FragB f0, f1;
+            rm_bt2(Bp, 2 * nq, kk, lane, f0, f1);
+            mma3(acc[2 * nq], fp[kk], f0);
+            mma3(acc[2 * nq + 1], fp[kk], f1);
+          }
+        // Y^T = S R^^T + P1 C^T (+ V^T P^T once the v warps have stored V)
+        float yv[4][4] = {};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            FragB f0, f1;
+            rm_b2(Rh, 2 * np, kk, lane, f0, f1);
+            mma3(yv[2 * np], fs[kk], f0);
+            mma3(yv[2 * np + 1], fs[kk], f1);
+          }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            FragB f0, f1;
+            rm_b2(Cm, 2 * np, kk, lane, f0, f1);
+            mma3(yv[2 * np], fp[kk], f0);
+            mma3(yv[2 * np + 1], fp[kk], f1);
+          }
+        bsync<kBarN, 128>();  // V (operand) and N = V^T K' are in shared memory
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const FragA fv = rm_at(Vop, mt, kk, lane);
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            FragB f0, f1;
+            rm_b2(Pm, 2 * np, kk, lane, f0, f1);
+            if (kVExact) {
+              mma2(yv[2 * np], fv, f0);
+              mma2(yv[2 * np + 1], fv, f1);
+            } else {
+              mma3(yv[2 * np], fv, f0);
+              mma3(yv[2 * np + 1], fv, f1);
+            }
+          }
         }
-        bsync<kBarN, 128>();  // V^T K' is in shared memory
+        // S <- S o gamma_31 + P1 B' + N
         const float* GL = reinterpret_cast<const float*>(cb + LY::cGL);
 #pragma unroll
         for (int nj = 0; nj < 8; ++nj) {
@@ -231,6 +281,17 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
           S[nj][2] = fmaf(S[nj][2], gl.x, acc[nj][2] + nv.z);
           S[nj][3] = fmaf(S[nj][3], gl.y, acc[nj][3] + nv.w);
         }
+        // stage y as [t][i]
+        const int i0 = mt * 16 + g;
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj) {
+          const int t0 = nj * 8 + 2 * q;
+          ys[t0 * LY::kSY + i0] = yv[nj][0];
+          ys[(t0 + 1) * LY::kSY + i0] = yv[nj][1];
+          ys[t0 * LY::kSY + i0 + 8] = yv[nj][2];
+          ys[(t0 + 1) * LY::kSY + i0 + 8] = yv[nj][3];
+        }
+        barrive<kBarY, 128>();
       } else {
         // ---- token by token (decay too strong for the transition form); inputs from global memory
         float* FS = reinterpret_cast<float*>(sm + LY::oFS);
@@ -333,18 +394,14 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
   }
 
   if (warp < 4) {
-    // =============================================================== output warps
+    // =============================================================== v warps
     const int mt = warp - 2;
     const int ot = tid - 64;  // 0 .. 63
-    uint32_t* const pVT = reinterpret_cast<uint32_t*>(sm + LY::oVT);
-    const uint32_t* const pS = reinterpret_cast<const uint32_t*>(sm + LY::oS);
-    float* const nb = reinterpret_cast<float*>(sm + LY::oN);
-    float* const ys = reinterpret_cast<float*>(sm + LY::oY);
-    // v of this CTA's rows for chunk m into buffer m & 1 (rows past the chunk are not copied)
+    // v of this CTA's rows for chunk m into raw buffer m & 1 (steps outside the sequence zero)
     auto issue_v = [&](int m) {
       constexpr int VPR = kR * (int)sizeof(TV) / 16;
       constexpr int EPV = 16 / (int)sizeof(TV);
-      TV* dst = vbuf(m);
+      TV* dst = vraw(m);
       const int t0 = sub_start(m), nm = sub_len(m);
       for (int e = ot; e < nm * VPR; e += 64) {
         const int t = e / VPR, pc = e % VPR;
@@ -360,8 +417,7 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
     __syncthreads();  // chunk 0 prepared
 
     for (int n = 0; n < nsub; ++n) {
-      const unsigned char* cb = chain_buf(n);
-      const int slow = reinterpret_cast<const int*>(cb + LY::cMeta)[0] | reinterpret_cast<const int*>(cb + LY::cMeta)[1];
+      unsigned char* cb = chain_buf(n);
       const int tau0 = sub_start(n);
       const int nm = sub_len(n);
       if (n + 1 < nsub) {
@@ -370,36 +426,39 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
       } else {
         cp_async_wait<0>();
       }
-      bsync<kBarOut, 64>();  // v of chunk n has landed for both output warps
-      if (!slow) {
-        // V^T (rows i, columns t), steps past the chunk zero
+      bsync<kBarV, 64>();  // v of chunk n has landed for both v warps
+      if (!slow_flag(cb)) {
+        // V (rows t, columns i of this CTA) as an operand, steps past the chunk zero
         {
-          const TV* vb = vbuf(n);
-          for (int e = ot; e < 16 * kR; e += 64) {
-            const int tp = e >> 5, i = e & 31;
-            const int t0 = 2 * tp;
-            const float x0 = t0 < nm ? to_f32(vb[t0 * kR + i]) : 0.f;
-            const float x1 = t0 + 1 < nm ? to_f32(vb[(t0 + 1) * kR + i]) : 0.f;
-            if (kVExact)
-              pt_store_hi(pVT, i, t0, 2, x0, x1);
-            else
-              pt_store(pVT, pt_words(32, 32) / 2, i, t0, 2, x0, x1);
+          const TV* vb = vraw(n);
+          const int t = ot >> 1, c0 = (ot & 1) * 16;
+#pragma unroll
+          for (int h8 = 0; h8 < 2; ++h8) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = t < nm ? to_f32(vb[t * kR + c0 + 8 * h8 + u]) : 0.f;
+            rm_store8(Vop, t, c0 + 8 * h8, x);
           }
         }
-        bsync<kBarOut, 64>();
-        // N = V^T K' (this warp's 16 rows, all 64 columns), for the chain warps
+        bsync<kBarV, 64>();
+        // N = V^T K' (this warp's 16 rows i, all 64 columns), for the chain warps
         {
-          const uint32_t* pKpT = reinterpret_cast<const uint32_t*>(cb + LY::cKpT);
-          float acc[8][4];
-#pragma unroll
-          for (int nj = 0; nj < 8; ++nj) acc[nj][0] = acc[nj][1] = acc[nj][2] = acc[nj][3] = 0.f;
+          const RM Kp = cbuf_rm64(cb, LY::cKp);
+          float acc[8][4] = {};
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            const FragA fa = kVExact ? load_a_hi(pVT, 2, mt, kk, lane) : load_a(pVT, pt_words(32, 32) / 2, 2, mt, kk, lane);
+            const FragA fv = rm_at(Vop, mt, kk, lane);
 #pragma unroll
-            for (int nj = 0; nj < 8; ++nj) {
-              const FragB fb = load_b(pKpT, pt_words(64, 32) / 2, 2, nj, kk, lane);
-              if (kVExact) mma2(acc[nj], fa, fb); else mma3(acc[nj], fa, fb);
+            for (int nq = 0; nq < 4; ++nq) {
+              FragB f0, f1;
+              rm_bt2(Kp, 2 * nq, kk, lane, f0, f1);
+              if (kVExact) {
+                mma2(acc[2 * nq], fv, f0);
+                mma2(acc[2 * nq + 1], fv, f1);
+              } else {
+                mma3(acc[2 * nq], fv, f0);
+                mma3(acc[2 * nq + 1], fv, f1);
+              }
             }
           }
 #pragma unroll
@@ -408,41 +467,7 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
                 make_float4(acc[nj][0], acc[nj][1], acc[nj][2], acc[nj][3]);
         }
         barrive<kBarN, 128>();
-        bsync<kBarS, 128>();  // S of the chunk's start is in shared memory
-        // Y^T = S R'^T + V^T P^T: rows i of this warp, tokens t
-        {
-          const uint32_t* pRp = reinterpret_cast<const uint32_t*>(cb + LY::cRp);
-          const uint32_t* pP = reinterpret_cast<const uint32_t*>(cb + LY::cP);
-          float acc[4][4];
-#pragma unroll
-          for (int nj = 0; nj < 4; ++nj) acc[nj][0] = acc[nj][1] = acc[nj][2] = acc[nj][3] = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const FragA fa = load_a(pS, pt_words(32, 64) / 2, 4, mt, kk, lane);
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj) mma3(acc[nj], fa, load_b(pRp, pt_words(32, 64) / 2, 4, nj, kk, lane));
-          }
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const FragA fa = kVExact ? load_a_hi(pVT, 2, mt, kk, lane) : load_a(pVT, pt_words(32, 32) / 2, 2, mt, kk, lane);
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj) {
-              const FragB fb = load_b(pP, pt_words(32, 32) / 2, 2, nj, kk, lane);
-              if (kVExact) mma2(acc[nj], fa, fb); else mma3(acc[nj], fa, fb);
-            }
-          }
-          // stage as [t][i]
-          const int i0 = mt * 16 + g;
-#pragma unroll
-          for (int nj = 0; nj < 4; ++nj) {
-            const int t0 = nj * 8 + 2 * q;
-            ys[t0 * LY::kSY + i0] = acc[nj][0];
-            ys[(t0 + 1) * LY::kSY + i0] = acc[nj][1];
-            ys[t0 * LY::kSY + i0 + 8] = acc[nj][2];
-            ys[(t0 + 1) * LY::kSY + i0 + 8] = acc[nj][3];
-          }
-        }
-        bsync<kBarOut, 64>();
+        bsync<kBarY, 128>();  // y of the chunk is staged
         for (int e = ot; e < nm * (kR / 4); e += 64) {
           const int t = e >> 3, i = (e & 7) * 4;
           const float4 vy = *reinterpret_cast<const float4*>(ys + t * LY::kSY + i);
@@ -463,24 +488,13 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
   const int pt = tid - kFirstPrep;  // 0 .. 255
   const int pw = pt >> 5;           // 0 .. 7
   float* const G = reinterpret_cast<float*>(sm + LY::oG);
-  float* const MabT = reinterpret_cast<float*>(sm + LY::oG);
-  uint32_t* const pBt = reinterpret_cast<uint32_t*>(sm + LY::oBt);
-  uint32_t* const pKt = reinterpret_cast<uint32_t*>(sm + LY::oKt);
-  uint32_t* const pRh = reinterpret_cast<uint32_t*>(sm + LY::oRh);
-  uint32_t* const pAh = reinterpret_cast<uint32_t*>(sm + LY::oAh);
-  uint32_t* const pAhT = reinterpret_cast<uint32_t*>(sm + LY::oAhT);
-  uint32_t* const pBmT = reinterpret_cast<uint32_t*>(sm + LY::oBmT);
-  uint32_t* const pKmT = reinterpret_cast<uint32_t*>(sm + LY::oKmT);
-  uint32_t* const pMakT = reinterpret_cast<uint32_t*>(sm + LY::oMakT);
-  uint32_t* const pMrb = reinterpret_cast<uint32_t*>(sm + LY::oMrb);
-  uint32_t* const pMrk = reinterpret_cast<uint32_t*>(sm + LY::oMrk);
+  const RM Kt{bfp(sm, LY::oKt), 32 * kLD64, kLD64}, Bt{bfp(sm, LY::oBt), 32 * kLD64, kLD64};
+  const RM Mak{bfp(sm, LY::oMak), 32 * kLD32, kLD32}, Mrb{bfp(sm, LY::oMrb), 32 * kLD32, kLD32};
+  const RM Mrk{bfp(sm, LY::oMrk), 32 * kLD32, kLD32}, Tm{bfp(sm, LY::oT), 32 * kLD32, kLD32};
+  float* const Mab = reinterpret_cast<float*>(sm + LY::oMab);
   float* const TI = reinterpret_cast<float*>(sm + LY::oTI);
   float* const E = reinterpret_cast<float*>(sm + LY::oE);
-  uint32_t* const pTT = reinterpret_cast<uint32_t*>(sm + LY::oTT);
-  uint32_t* const pBpT = reinterpret_cast<uint32_t*>(sm + LY::oBpT);
-  uint32_t* const pC = reinterpret_cast<uint32_t*>(sm + LY::oC);
-  constexpr int H3232 = pt_words(32, 32) / 2, H3264 = pt_words(32, 64) / 2, H6432 = pt_words(64, 32) / 2,
-                H6464 = pt_words(64, 64) / 2;
+  constexpr int SM = LY::kSM;
 
   // cp.async copies of chunk m's w, k, a, b, r (rows past the chunk are not copied)
   auto issue_raw = [&](int m) {
@@ -507,7 +521,9 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
     cp_async_commit();
   };
 
-  auto prepare = [&](int m) {  // also issues the copy of chunk m + 1 once chunk m's inputs are consumed
+  // everything the chain needs for chunk m, into chain buffer m & 1 (its raw inputs have landed);
+  // issues the copy of chunk m + 1 once chunk m's inputs are consumed
+  auto prepare = [&](int m) {
     unsigned char* cb = chain_buf(m);
     int* meta = reinterpret_cast<int*>(cb + LY::cMeta);
     float* GL = reinterpret_cast<float*>(cb + LY::cGL);
@@ -517,6 +533,8 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
     const Tin* ra = raw + 2 * kL * kD;
     const Tin* rbv = raw + 3 * kL * kD;
     const Tin* rr = raw + 4 * kL * kD;
+    const RM Ah = cbuf_rm64(cb, LY::cAh), Rh = cbuf_rm64(cb, LY::cRh), Bp = cbuf_rm64(cb, LY::cBp);
+    const RM Kp = cbuf_rm64(cb, LY::cKp), Cm = cbuf_rm32(cb, LY::cC), Pm = cbuf_rm32(cb, LY::cP);
 
     // ---- S1a: gamma_t down each column; the token-by-token flag
     if (pt < kD) {
@@ -536,79 +554,79 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
     bsync<kBarPrep, kNP>();
     const bool slow = (meta[0] | meta[1]) != 0;
     if (!slow) {
-      // ---- S1b: row pairs (t, j): A^, R^, K~, B~
-      for (int e = pt; e < kL * (kD / 2); e += kNP) {
-        const int t = e >> 5, j = 2 * (e & 31);
-        const bool ok = t < nm;
-        const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
-        const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
-        const float ix = __frcp_rn(gt.x), iy = __frcp_rn(gt.y);
-        const float a0 = ok ? to_f32(ra[t * kD + j]) : 0.f, a1 = ok ? to_f32(ra[t * kD + j + 1]) : 0.f;
-        const float r0 = ok ? to_f32(rr[t * kD + j]) : 0.f, r1 = ok ? to_f32(rr[t * kD + j + 1]) : 0.f;
-        const float k0 = ok ? to_f32(rk[t * kD + j]) : 0.f, k1 = ok ? to_f32(rk[t * kD + j + 1]) : 0.f;
-        const float b0 = ok ? to_f32(rbv[t * kD + j]) : 0.f, b1 = ok ? to_f32(rbv[t * kD + j + 1]) : 0.f;
-        pt_store(pAh, H3264, t, j, 4, a0 * gp.x, a1 * gp.y);
-        pt_store(pRh, H3264, t, j, 4, r0 * gt.x, r1 * gt.y);
-        pt_store(pKt, H3264, t, j, 4, k0 * ix, k1 * iy);
-        pt_store(pBt, H3264, t, j, 4, b0 * ix, b1 * iy);
+      // ---- S1b: one (token, 8 columns) block per thread: A^, R^ (chain buffer), K~, B~
+      const int t = pt >> 3, c0 = (pt & 7) * 8;
+      const bool ok = t < nm;
+      float gt[8], gp[8], av[8], rv[8], kv[8], bv[8];
+      raw8(G + t * kD + c0, gt);
+      if (t > 0) {
+        raw8(G + (t - 1) * kD + c0, gp);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) gp[u] = 1.f;
       }
-      // ---- S1c: column pairs (t, t + 1; j): A^^T, B-^T, K-^T
-      for (int e = pt; e < (kL / 2) * kD; e += kNP) {
-        const int tp = e >> 6, j = e & 63;
-        const int t0 = 2 * tp, t1 = t0 + 1;
-        const float gl = G[(kL - 1) * kD + j];
-        const float g0 = G[t0 * kD + j], g1 = G[t1 * kD + j];
-        const float gp0 = t0 > 0 ? G[(t0 - 1) * kD + j] : 1.f;
-        const bool ok0 = t0 < nm, ok1 = t1 < nm;
-        const float a0 = ok0 ? to_f32(ra[t0 * kD + j]) : 0.f, a1 = ok1 ? to_f32(ra[t1 * kD + j]) : 0.f;
-        const float b0 = ok0 ? to_f32(rbv[t0 * kD + j]) : 0.f, b1 = ok1 ? to_f32(rbv[t1 * kD + j]) : 0.f;
-        const float k0 = ok0 ? to_f32(rk[t0 * kD + j]) : 0.f, k1 = ok1 ? to_f32(rk[t1 * kD + j]) : 0.f;
-        const float f0 = gl * __frcp_rn(g0), f1 = gl * __frcp_rn(g1);
-        pt_store(pAhT, H6432, j, t0, 2, a0 * gp0, a1 * g0);
-        pt_store(pBmT, H6432, j, t0, 2, b0 * f0, b1 * f1);
-        pt_store(pKmT, H6432, j, t0, 2, k0 * f0, k1 * f1);
+      raw8(ra + t * kD + c0, av);
+      raw8(rr + t * kD + c0, rv);
+      raw8(rk + t * kD + c0, kv);
+      raw8(rbv + t * kD + c0, bv);
+      float oa[8], orr[8], ok8[8], ob[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float ig = __fdividef(1.f, gt[u]);
+        oa[u] = ok ? av[u] * gp[u] : 0.f;
+        orr[u] = ok ? rv[u] * gt[u] : 0.f;
+        ok8[u] = ok ? kv[u] * ig : 0.f;
+        ob[u] = ok ? bv[u] * ig : 0.f;
       }
+      rm_store8(Ah, t, c0, oa);
+      rm_store8(Rh, t, c0, orr);
+      rm_store8(Kt, t, c0, ok8);
+      rm_store8(Bt, t, c0, ob);
     }
     bsync<kBarPrep, kNP>();  // raw is free: the next chunk is copied in while this one is prepared
     if (m + 1 < nsub) issue_raw(m + 1);
     if (slow) return;
 
-    // ---- S2: coupling products (m16 x n8 tiles, K = 64): M_ab^T = B~ A^^T and M_ak^T = K~ A^^T (rows t,
-    // columns s, kept s > t), M_rb = R^ B~^T and M_rk = R^ K~^T (kept s <= t).  Tiles wholly outside
-    // the kept triangle are stored as zeros (later products read them).
-    for (int job = pw; job < 32; job += 8) {
-      const int prod = job >> 3, mt = (job >> 2) & 1, nj = job & 3;
-      const bool upper = prod < 2;
-      const bool empty = upper ? (mt == 1 && nj < 2) : (mt == 0 && nj >= 2);
-      const uint32_t* X = prod == 0 ? pBt : (prod == 1 ? pKt : pRh);
-      const uint32_t* Y = prod <= 1 ? pAh : (prod == 2 ? pBt : pKt);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (!empty) {
+    // ---- S2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
+    // M_rk = tril(R^ K~^T): 16 jobs of (product, m-tile, pair of n-tiles), K = 64
+    for (int job = pw; job < 16; job += 8) {
+      const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
+      const bool strict = prod < 2;
+      float acc[2][4] = {};
+      if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
+        const RM& X = prod < 2 ? Ah : Rh;
+        const RM& Y = (prod & 1) ? Kt : Bt;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma3(acc, load_a(X, H3264, 4, mt, kk, lane), load_b(Y, H3264, 4, nj, kk, lane));
+        for (int kk = 0; kk < 4; ++kk) {
+          const FragA fa = rm_a(X, mt, kk, lane);
+          FragB f0, f1;
+          rm_b2(Y, 2 * np, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
       }
-      const int t0 = mt * 16 + g, s0 = nj * 8 + 2 * q;
-      float c[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = t0 + ((e >> 1) << 3), s = s0 + (e & 1);
-        const bool keep = upper ? (s > t) : (s <= t);
-        c[e] = keep ? acc[e] : 0.f;
-      }
-      if (prod == 0) {
-        *reinterpret_cast<float2*>(MabT + t0 * Lay<Tin, TV>::kSMab + s0) = make_float2(c[0], c[1]);
-        *reinterpret_cast<float2*>(MabT + (t0 + 8) * Lay<Tin, TV>::kSMab + s0) = make_float2(c[2], c[3]);
-      } else {
-        store_acc(prod == 1 ? pMakT : (prod == 2 ? pMrb : pMrk), H3232, 2, mt, nj, lane, c);
+      for (int h = 0; h < 2; ++h) {
+        const int nj = 2 * np + h;
+        const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+        float c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tt = tr + ((e >> 1) << 3), s = sc + (e & 1);
+          c[e] = (strict ? s < tt : s <= tt) ? acc[h][e] : 0.f;
+        }
+        if (prod == 0) {
+          *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+          *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
+        } else {
+          rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
+        }
       }
     }
     bsync<kBarPrep, kNP>();
 
     // ---- S3: T = (I - M_ab)^-1 (unit lower triangular) by blocks of 16: the diagonal blocks by forward
-    // substitution, one column per lane (lanes 0-15: T11, lanes 16-31: T22); M_ab[t][u] = M_ab^T[u][t]
-    constexpr int SM = Lay<Tin, TV>::kSMab;
-    constexpr int ST = Lay<Tin, TV>::kSTI;
+    // substitution, one column per lane (lanes 0-15: T11, lanes 16-31: T22), then T21 = T22 A21 T11
     if (pw == 0) {
       const int off = lane < 16 ? 0 : 16;
       const int c = lane & 15;
@@ -617,19 +635,18 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
       for (int t = 0; t < 16; ++t) {
         float acc = t == c ? 1.f : 0.f;
 #pragma unroll
-        for (int u = 0; u < t; ++u) acc = fmaf(MabT[(off + u) * SM + off + t], x[u], acc);
+        for (int u = 0; u < t; ++u) acc = fmaf(Mab[(off + t) * SM + off + u], x[u], acc);
         x[t] = acc;
       }
 #pragma unroll
-      for (int t = 0; t < 16; ++t) TI[(off + t) * ST + off + c] = x[t];
+      for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
     }
     bsync<kBarPrep, kNP>();
-    // E = A21 T11 (A21 = M_ab[16..31][0..15]), then T21 = T22 E
     {
       const int t = pt >> 4, s = pt & 15;
       float acc = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) acc = fmaf(MabT[u * SM + 16 + t], TI[u * ST + s], acc);
+      for (int u = 0; u < 16; ++u) acc = fmaf(Mab[(16 + t) * SM + u], TI[u * SM + s], acc);
       E[t * 16 + s] = acc;
     }
     bsync<kBarPrep, kNP>();
@@ -637,85 +654,102 @@ chain_kernel(int T, int H, int nchunks, ChainPtrs P) {
       const int t = pt >> 4, s = pt & 15;
       float acc = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * ST + 16 + u], E[u * 16 + s], acc);
-      TI[(16 + t) * ST + s] = acc;
+      for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * SM + 16 + u], E[u * 16 + s], acc);
+      TI[(16 + t) * SM + s] = acc;
     }
     bsync<kBarPrep, kNP>();
-    // T^T as pair tiles (rows s, columns t); T[t][s] = 0 for s > t
-    for (int e = pt; e < 32 * 16; e += kNP) {
-      const int s = e >> 4, t0 = 2 * (e & 15);
-      const float x0 = s <= t0 ? TI[t0 * ST + s] : 0.f;
-      const float x1 = s <= t0 + 1 ? TI[(t0 + 1) * ST + s] : 0.f;
-      pt_store(pTT, H3232, s, t0, 2, x0, x1);
+    if (pt < 128) {  // T as an operand (rows t, columns u), zero above the diagonal: 8 columns per thread
+      const int t = pt >> 2, u0 = (pt & 3) * 8;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = u0 + e <= t ? TI[t * SM + u0 + e] : 0.f;
+      rm_store8(Tm, t, u0, x);
     }
     bsync<kBarPrep, kNP>();
 
-    // ---- S4: B'^T = B-^T T (rows j, columns s, K = t) and C = M_rb T (rows t, columns s, K = u)
-    for (int job = pw; job < 24; job += 8) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (job < 16) {
-        const int mt = job >> 2, nj = job & 3;
+    // ---- S4: B' = (T^T B~) diag(gamma_31) (rows s, columns j; K = t) and C = M_rb T (rows t, columns s;
+    // K = u): 12 jobs of (product, m-tile, 2 n-tiles)
+    for (int job = pw; job < 12; job += 8) {
+      float acc[2][4] = {};
+      if (job < 8) {
+        const int mt = job >> 2, nq = job & 3;  // B' n-tiles 2nq, 2nq + 1
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          if (kk == 1 || nj < 2)  // T[t < 16][s >= 16] = 0
-            mma3(acc, load_a(pBmT, H6432, 2, mt, kk, lane), load_b(pTT, H3232, 2, nj, kk, lane));
-        store_acc(pBpT, H6432, 2, mt, nj, lane, acc);
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 1 && kk == 0) continue;  // T^T[s >= 16][t < 16] = 0
+          const FragA fa = rm_at(Tm, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Bt, 2 * nq, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 gl = *reinterpret_cast<const float2*>(GL + (2 * nq + h) * 8 + 2 * q);
+          acc[h][0] *= gl.x; acc[h][1] *= gl.y; acc[h][2] *= gl.x; acc[h][3] *= gl.y;
+          rm_store_acc(Bp, mt, 2 * nq + h, lane, acc[h]);
+        }
       } else {
-        const int mt = (job - 16) >> 2, nj = (job - 16) & 3;
+        const int mt = (job - 8) >> 1, np = (job - 8) & 1;  // C n-tiles 2np, 2np + 1
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          if ((kk == 1 || nj < 2) && (mt == 1 || kk == 0))  // M_rb[t < 16][u >= 16] = 0
-            mma3(acc, load_a(pMrb, H3232, 2, mt, kk, lane), load_b(pTT, H3232, 2, nj, kk, lane));
-        store_acc(pC, H3232, 2, mt, nj, lane, acc);
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 0 && kk == 1) continue;  // M_rb[t < 16][u >= 16] = 0
+          const FragA fa = rm_a(Mrb, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Tm, 2 * np, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
+        rm_store_acc(Cm, mt, 2 * np, lane, acc[0]);
+        rm_store_acc(Cm, mt, 2 * np + 1, lane, acc[1]);
       }
     }
     bsync<kBarPrep, kNP>();
 
-    // ---- S5 (into the chain buffer): M'^T = B'^T A^ (rows j, columns j'), K'^T = K-^T + B'^T M_ak (rows j,
-    // columns t), R' = R^ + C A^ (rows t, columns j), P = M_rk + C M_ak (rows t, columns s); K = 32 each
-    {
-      uint32_t* cMT = reinterpret_cast<uint32_t*>(cb + LY::cMT);
-      uint32_t* cKpT = reinterpret_cast<uint32_t*>(cb + LY::cKpT);
-      uint32_t* cRp = reinterpret_cast<uint32_t*>(cb + LY::cRp);
-      uint32_t* cP = reinterpret_cast<uint32_t*>(cb + LY::cP);
-      for (int job = pw; job < 72; job += 8) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (job < 32) {
-          const int mt = job >> 3, nj = job & 7;
+    // ---- S5: K' = K~ diag(gamma_31) + M_ak^T B' (rows t, columns j; K = s) and P = M_rk + C M_ak
+    // (rows t, columns s; K = u): 12 jobs
+    for (int job = pw; job < 12; job += 8) {
+      float acc[2][4] = {};
+      if (job < 8) {
+        const int mt = job >> 2, nq = job & 3;
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma3(acc, load_a(pBpT, H6432, 2, mt, kk, lane), load_b(pAhT, H6432, 2, nj, kk, lane));
-          store_acc(cMT, H6464, 4, mt, nj, lane, acc);
-        } else if (job < 48) {
-          const int mt = (job - 32) >> 2, nj = (job - 32) & 3;
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 1 && kk == 0) continue;  // M_ak^T[t >= 16][s < 16] = 0
+          const FragA fa = rm_at(Mak, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Bp, 2 * nq, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma3(acc, load_a(pBpT, H6432, 2, mt, kk, lane), load_b(pMakT, H3232, 2, nj, kk, lane));
-          float add[4];
-          load_acc_pos(pKmT, H6432, 2, mt, nj, lane, add);
+        for (int h = 0; h < 2; ++h) {
+          const int col = (2 * nq + h) * 8 + 2 * q;
+          const int tr = mt * 16 + g;
+          const float2 gl = *reinterpret_cast<const float2*>(GL + col);
+          const float2 k0 = rm_get2(Kt, tr, col), k8 = rm_get2(Kt, tr + 8, col);
+          acc[h][0] = fmaf(k0.x, gl.x, acc[h][0]);
+          acc[h][1] = fmaf(k0.y, gl.y, acc[h][1]);
+          acc[h][2] = fmaf(k8.x, gl.x, acc[h][2]);
+          acc[h][3] = fmaf(k8.y, gl.y, acc[h][3]);
+          rm_store_acc(Kp, mt, 2 * nq + h, lane, acc[h]);
+        }
+      } else {
+        const int mt = (job - 8) >> 1, np = (job - 8) & 1;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] += add[e];
-          store_acc(cKpT, H6432, 2, mt, nj, lane, acc);
-        } else if (job < 64) {
-          const int mt = (job - 48) >> 3, nj = (job - 48) & 7;
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 0 && kk == 1) continue;  // C[t < 16][u >= 16] = 0
+          const FragA fa = rm_a(Cm, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Mak, 2 * np, kk, lane, f0, f1);
+          mma3(acc[0], fa, f0);
+          mma3(acc[1], fa, f1);
+        }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma3(acc, load_a(pC, H3232, 2, mt, kk, lane), load_b(pAhT, H6432, 2, nj, kk, lane));
-          float add[4];
-          load_acc_pos(pRh, H3264, 4, mt, nj, lane, add);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] += add[e];
-          store_acc(cRp, H3264, 4, mt, nj, lane, acc);
-        } else {
-          const int mt = (job - 64) >> 2, nj = (job - 64) & 3;
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma3(acc, load_a(pC, H3232, 2, mt, kk, lane), load_b(pMakT, H3232, 2, nj, kk, lane));
-          float add[4];
-          load_acc_pos(pMrk, H3232, 2, mt, nj, lane, add);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] += add[e];
-          store_acc(cP, H3232, 2, mt, nj, lane, acc);
+        for (int h = 0; h < 2; ++h) {
+          const int col = (2 * np + h) * 8 + 2 * q;
+          const int tr = mt * 16 + g;
+          const float2 m0 = rm_get2(Mrk, tr, col), m8 = rm_get2(Mrk, tr + 8, col);
+          acc[h][0] += m0.x; acc[h][1] += m0.y; acc[h][2] += m8.x; acc[h][3] += m8.y;
+          rm_store_acc(Pm, mt, 2 * np + h, lane, acc[h]);
         }
       }
     }
@@ -745,7 +779,7 @@ cudaError_t launch_chain_t(int B, int T, int H, int nchunks, const ChainPtrs& P,
   using LY = Lay<Tin, TV>;
   static_assert(LY::kBytes <= 232448, "shared memory per CTA");
   auto kern = chain_kernel<Tin, GRAD>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kBytes);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)B * H * 2;
   kern<<<grid, kNT, LY::kBytes, stream>>>(T, H, nchunks, P);

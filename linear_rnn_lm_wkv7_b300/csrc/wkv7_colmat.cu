@@ -6,12 +6,12 @@
 // X_t the gradient w.r.t. the state after token t (including dy_t r_t^T) and S_t the state:
 //     dr_t = S_t^T dy_t,  dk_t = X_t^T v_t,  db_t = X_t^T sa_t,  da_t = S_{t-1}^T dsa_t,
 //     dw_t = colsum(X_t o S_{t-1}),  dsa_t = X_t b_t,  X_{t-1} = X_t diag(w_t) + dsa_t a_t^T + dy_{t-1} r_{t-1}^T.
-// The walk (the transition-chain kernel run backwards) leaves X at every chunk end and dv, dh0.
+// The walk over the chunks (wkv7_ops.cu) leaves G at every chunk end (the gradient w.r.t. the state
+// after the chunk from every later token, X_e = G + dy_{n-1} r_{n-1}^T) and dh0.
 //
 // Matrix form of one chunk of n tokens (t = 0..31, steps past n padded with w = 1 and zeros), from S0
-// (the state before the chunk), X_e (X at its last token) and S_e (the state after it), with gamma,
-// A^, R^, K~, B~, M_ab, M_ak, M_rb and T = (I - M_ab)^-1 as in the transition-chain kernel and
-// Xb = (X_e - dy_{n-1} r_{n-1}^T) diag(gamma_{n-1}) (the gradient from later tokens, decayed):
+// (the state before the chunk), G and S_e (the state after it), with gamma, A^, R^, K~, B~, M_ab, M_ak,
+// M_rb, M_rk and T = (I - M_ab)^-1 as in the transition-chain kernels and Xb = G diag(gamma_{n-1}):
 //     SA  = T U,    U = A^ S0^T + M_ak V                      (rows t: sa_t, recomputed)
 //     DSA = T^T W,  W = B~ Xb^T + M_rb^T DY                   (rows t: dsa_t)
 //     L1 = tril(DY V^T), L2 = tril(DY SA^T), L3 = tril(DSA V^T, -1), L4 = tril(DSA SA^T, -1)
@@ -19,14 +19,15 @@
 //     DA = Gamma_- o (DSA S0 + L3 K~ + L4 B~)                 (Gamma_- row t = gamma_{t-1})
 //     DK = Gamma^-1 o (V  Xb + L3^T A^ + L1^T R^)
 //     DB = Gamma^-1 o (SA Xb + L4^T A^ + L2^T R^)
+//     DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY                  (rows t: dv_t)
 // (X_t diag(gamma_t) and S_t diag(1/gamma_t) unrolled over the chunk: every column sum above becomes a
 // dot of the chunk's own vectors, masked to the tokens before or after t).  dw follows per column
-// from Z_t = colsum(X_t o S_t): Z_{n-1} = colsum(X_e o S_e), w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
+// from Z_t = colsum(X_t o S_t): Z_{n-1} = colsum(G o S_e) + r_{n-1} o dr_{n-1}, w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
 // Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1}.  No state is divided by w.
 //
 // A chunk whose gamma_31 falls below 1e-20 in some column (or is not finite), or that has some w_t
 // below 1/32 (where dividing w_t o dw_t by w_t would cost digits), takes the exact token-by-token
-// column passes instead (sa and dsa by their own recurrences, then wkv7_colpass.cuh).
+// column passes instead (sa, dsa and dv by their own recurrences, then wkv7_colpass.cuh).
 //
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation; operands are stored once, row-major, split into bf16 hi and lo, and read with
@@ -75,29 +76,31 @@ struct Lay {
   static constexpr int kRawIn = 6 * kL * kD * (int)sizeof(Tin);
   static constexpr int oDyRaw = oRaw + kRawIn;
   static constexpr int kRawEnd = oDyRaw + kL * kD * 4;
-  // ... then U, W, M_ak, M_rb, T, M_ab (fp32), TI, E; then L1..L4 over U and W
-  static constexpr int oU = oB;
-  static constexpr int oW = oU + rm_bytes(32, kLD64);
-  static constexpr int oMak = oW + rm_bytes(32, kLD64);
-  static constexpr int oMrb = oMak + rm_bytes(32, kLD32);
+  // ... then M_ak, M_rk, M_rb, T, U, W, M_ab (fp32), TI, E; then L1..L4 over U, W and M_ab
+  static constexpr int oMak = oB;
+  static constexpr int oMrk = oMak + rm_bytes(32, kLD32);
+  static constexpr int oMrb = oMrk + rm_bytes(32, kLD32);
   static constexpr int oT = oMrb + rm_bytes(32, kLD32);
+  static constexpr int oU = oT + rm_bytes(32, kLD32);
+  static constexpr int oW = oU + rm_bytes(32, kLD64);
   static constexpr int kSM = 36;
-  static constexpr int oMab = oT + rm_bytes(32, kLD32);         // float [32][36]
+  static constexpr int oMab = oW + rm_bytes(32, kLD64);         // float [32][36]
   static constexpr int oTI = oMab + 32 * kSM * 4;               // float [32][36]
   static constexpr int oE = oTI + 32 * kSM * 4;                 // float [16][16]
   static constexpr int kPhaseEnd = oE + 16 * 16 * 4;
-  static constexpr int oL = oB;                                 // L1..L4 (32 x 32 each)
-  static_assert(oL + 4 * rm_bytes(32, kLD32) <= oT, "L1..L4 fit over U, W, M_ak, M_rb");
+  static constexpr int oL = oU;                                 // L1..L4 (32 x 32 each)
+  static_assert(oL + 4 * rm_bytes(32, kLD32) <= oTI, "L1..L4 fit over U, W and M_ab");
   static constexpr int kBytes = (kRawEnd > kPhaseEnd ? kRawEnd : kPhaseEnd);
-  // ---- fallback (token-by-token column passes): fp32 [32][64] sa, dsa, v over A^ .. R^
+  // ---- fallback (token-by-token column passes): fp32 [32][64] sa, dsa, v and X_e [64][64] over A^ .. S0
   static constexpr int oFSa = oAh;
   static constexpr int oFDsa = oFSa + kL * kD * 4;
   static constexpr int oFV = oFDsa + kL * kD * 4;
-  static_assert(oFV + kL * kD * 4 <= oS0, "fallback arrays fit over A^ .. R^");
-  // ---- output staging over A^ .. Xb (after the last products): DR, DA, DK, DB, then r o dr, a o da,
+  static constexpr int oFXe = oFV + kL * kD * 4;
+  static_assert(oFXe + kD * kD * 4 <= oXb, "fallback arrays fit over A^ .. S0");
+  // ---- output staging over A^ .. Xb (after the last products): DR, DA, DK, DB, DV, then r o dr, a o da,
   // k o dk, b o db, fp32 [32][64] each
   static constexpr int oStage = oAh;
-  static_assert(oStage + 8 * kL * kD * 4 <= oV, "staging fits over A^ .. Xb");
+  static_assert(oStage + 9 * kL * kD * 4 <= oV, "staging fits over A^ .. Xb");
 };
 
 template <typename Tin>
@@ -106,7 +109,8 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
               const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
               const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
               const float* __restrict__ dy, const float* __restrict__ xck, float* __restrict__ dr,
-              float* __restrict__ dw, float* __restrict__ dk, float* __restrict__ da, float* __restrict__ db) {
+              float* __restrict__ dw, float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ da,
+              float* __restrict__ db) {
   using LY = Lay<Tin>;
   constexpr bool kVExact = sizeof(Tin) == 2;
   extern __shared__ float4 smem4[];
@@ -124,7 +128,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   const int n = min(kL, T - t0);
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
-  const float* xend = xck + ((size_t)bh * nchunks + ci) * kD * kD;
+  const float* gend = xck + ((size_t)bh * nchunks + ci) * kD * kD;  // G: the gradient from later tokens
   const float* send = h_ckpt + ((size_t)bh * nchunks + ci) * kD * kD;
   const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
                            : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
@@ -149,6 +153,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   const RM SA{bfp(LY::oSA), 32 * kLD64, kLD64}, DSA{bfp(LY::oDSA), 32 * kLD64, kLD64};
   const RM U{bfp(LY::oU), 32 * kLD64, kLD64}, W{bfp(LY::oW), 32 * kLD64, kLD64};
   const RM Mak{bfp(LY::oMak), 32 * kLD32, kLD32}, Mrb{bfp(LY::oMrb), 32 * kLD32, kLD32};
+  const RM Mrk{bfp(LY::oMrk), 32 * kLD32, kLD32};
   const RM Tm{bfp(LY::oT), 32 * kLD32, kLD32};
   const RM L1{bfp(LY::oL), 32 * kLD32, kLD32}, L2{bfp(LY::oL + rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
   const RM L3{bfp(LY::oL + 2 * rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
@@ -158,7 +163,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   float* E = reinterpret_cast<float*>(sm + LY::oE);
   constexpr int SM = LY::kSM;
 
-  // ---- P0: the chunk's inputs (rows past n are not copied); colsum(X_e o S_e) partials meanwhile
+  // ---- P0: the chunk's inputs (rows past n are not copied); colsum(G o S_e) partials meanwhile
   {
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
     constexpr int EPC = 16 / (int)sizeof(Tin);
@@ -177,7 +182,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     const int j = tid & 63, part = tid >> 6;
     float z = 0.f;
 #pragma unroll 4
-    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(__ldg(xend + i * kD + j), __ldg(send + i * kD + j), z);
+    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(__ldg(gend + i * kD + j), __ldg(send + i * kD + j), z);
     ZP[part * 64 + j] = z;
     cp_async_wait<0>();
   }
@@ -222,16 +227,25 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         for (int j = 0; j < 64; ++j)
           Sr[j] = fmaf(Sr[j], to_f32(rw[t * kD + j]), fmaf(vi, to_f32(rk[t * kD + j]), s * to_f32(rbv[t * kD + j])));
       }
-    } else if (tid < 128) {  // dsa_t = X_t b_t, row tid - 64, X walked down from X_e
+    } else if (tid < 128) {  // dsa_t = X_t b_t and dv_t = X_t k_t, row tid - 64, X walked down from X_e
       const int i = tid - 64;
+      float* fxe = reinterpret_cast<float*>(sm + LY::oFXe);
       float Xr[64];
+      const float dl = dyr[(n - 1) * kD + i];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) Xr[j] = __ldg(xend + i * kD + j);
+      for (int j = 0; j < 64; ++j) {
+        Xr[j] = fmaf(dl, to_f32(rr[(n - 1) * kD + j]), __ldg(gend + i * kD + j));
+        fxe[i * kD + j] = Xr[j];
+      }
       for (int t = n - 1; t >= 0; --t) {
-        float s = 0.f;
+        float s = 0.f, sv = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) s = fmaf(Xr[j], to_f32(rbv[t * kD + j]), s);
+        for (int j = 0; j < 64; ++j) {
+          s = fmaf(Xr[j], to_f32(rbv[t * kD + j]), s);
+          sv = fmaf(Xr[j], to_f32(rk[t * kD + j]), sv);
+        }
         fdsa[t * kD + i] = s;
+        dv[base + (size_t)(t0 + t) * tstride + i] = sv;
         const float e = t > 0 ? dyr[(t - 1) * kD + i] : 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
@@ -242,7 +256,8 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     }
     __syncthreads();
     if (tid < 64)
-      colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv, xend, s0, dr, dw, dk, da, db);
+      colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv,
+                           reinterpret_cast<const float*>(sm + LY::oFXe), s0, dr, dw, dk, da, db);
     return;
   }
 
@@ -266,28 +281,26 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     if (kVExact) rm_store_hi(Vm, t, j, v0, v1); else rm_store(Vm, t, j, v0, v1);
     rm_store(DY, t, j, d0, d1);
   }
-  // S0 and Xb = (X_e - dy_{n-1} r_{n-1}^T) diag(gamma_{n-1}) (rows i, columns j)
+  // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
   for (int e = tid; e < kD * (kD / 2); e += kNT) {
     const int i = e >> 5, j = 2 * (e & 31);
     const float2 s = s0 != nullptr ? __ldg(reinterpret_cast<const float2*>(s0 + i * kD + j)) : make_float2(0.f, 0.f);
     rm_store(S0, i, j, s.x, s.y);
-    const float2 x = __ldg(reinterpret_cast<const float2*>(xend + i * kD + j));
+    const float2 x = __ldg(reinterpret_cast<const float2*>(gend + i * kD + j));
     const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
-    const float dl = dyr[(n - 1) * kD + i];
-    const float rl0 = to_f32(rr[(n - 1) * kD + j]), rl1 = to_f32(rr[(n - 1) * kD + j + 1]);
-    rm_store(Xb, i, j, fmaf(-dl, rl0, x.x) * gl.x, fmaf(-dl, rl1, x.y) * gl.y);
+    rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
   }
   __syncthreads();
 
-  // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T); 12 jobs of
-  // (product, m-tile, pair of n-tiles), K = 64
-  for (int job = warp; job < 12; job += 8) {
+  // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
+  // M_rk = tril(R^ K~^T); 16 jobs of (product, m-tile, pair of n-tiles), K = 64
+  for (int job = warp; job < 16; job += 8) {
     const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
     const bool strict = prod < 2;
     float acc[2][4] = {};
     if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
       const RM& X = prod < 2 ? Ah : Rh;
-      const RM& Y = prod == 1 ? Kt : Bt;
+      const RM& Y = (prod & 1) ? Kt : Bt;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const FragA fa = rm_a(X, mt, kk, lane);
@@ -311,7 +324,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
         *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
       } else {
-        rm_store_acc(prod == 1 ? Mak : Mrb, mt, nj, lane, c);
+        rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
       }
     }
   }
@@ -447,62 +460,93 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   }
   __syncthreads();
 
-  // ---- P7: DR, DA, DK, DB (rows t, columns j): 16 jobs of (product, m-tile, 4 n-tiles), each a K = 64
-  // product with S0 / Xb plus the masked K = 64 product; held in registers until every warp is done
-  float res[2][4][4];
+  // ---- P7: DR, DA, DK, DB, DV (rows t, columns j or i): 20 jobs of (product, m-tile, 4 n-tiles), each a
+  // K = 64 product with S0 / Xb plus the masked products; held in registers until every warp is done
+  float res[3][4][4];
 #pragma unroll
-  for (int rep = 0; rep < 2; ++rep) {
+  for (int rep = 0; rep < 3; ++rep) {
     const int job = warp + 8 * rep;
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
     float (&acc)[4][4] = res[rep];
 #pragma unroll
     for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-    const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
-    const RM& B1 = prod < 2 ? S0 : Xb;
-    const bool exactA = kVExact && prod == 2;
+    if (job >= 20) continue;
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
+    if (prod < 4) {
+      const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
+      const RM& B1 = prod < 2 ? S0 : Xb;
+      const bool exactA = kVExact && prod == 2;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
 #pragma unroll
-      for (int p2 = 0; p2 < 2; ++p2) {
-        FragB f0, f1;
-        rm_bt2(B1, 4 * nh + 2 * p2, kk, lane, f0, f1);
-        if (exactA) {
-          mma2(acc[2 * p2], fa, f0);
-          mma2(acc[2 * p2 + 1], fa, f1);
-        } else {
+        for (int p2 = 0; p2 < 2; ++p2) {
+          FragB f0, f1;
+          rm_bt2(B1, 4 * nh + 2 * p2, kk, lane, f0, f1);
+          if (exactA) {
+            mma2(acc[2 * p2], fa, f0);
+            mma2(acc[2 * p2 + 1], fa, f1);
+          } else {
+            mma3(acc[2 * p2], fa, f0);
+            mma3(acc[2 * p2 + 1], fa, f1);
+          }
+        }
+      }
+      // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
+      // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int blk = kq >> 1, kk = kq & 1;
+        const bool lowerA = prod < 2;
+        if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
+        const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
+        const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
+        const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          FragB f0, f1;
+          rm_bt2(BB, 4 * nh + 2 * p2, kk, lane, f0, f1);
           mma3(acc[2 * p2], fa, f0);
           mma3(acc[2 * p2 + 1], fa, f1);
         }
       }
-    }
-    // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
-    // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
+    } else {
+      // DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY (rows t, columns i)
 #pragma unroll
-    for (int kq = 0; kq < 4; ++kq) {
-      const int blk = kq >> 1, kk = kq & 1;
-      const bool lowerA = prod < 2;
-      if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
-      const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
-      const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
-      const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(Kt, mt, kk, lane);
 #pragma unroll
-      for (int p2 = 0; p2 < 2; ++p2) {
-        FragB f0, f1;
-        rm_bt2(BB, 4 * nh + 2 * p2, kk, lane, f0, f1);
-        mma3(acc[2 * p2], fa, f0);
-        mma3(acc[2 * p2 + 1], fa, f1);
+        for (int p2 = 0; p2 < 2; ++p2) {
+          FragB f0, f1;
+          rm_b2(Xb, 4 * nh + 2 * p2, kk, lane, f0, f1);
+          mma3(acc[2 * p2], fa, f0);
+          mma3(acc[2 * p2 + 1], fa, f1);
+        }
+      }
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int blk = kq >> 1, kk = kq & 1;
+        if (mt == 1 && kk == 0) continue;  // M_ak^T, M_rk^T upper triangular
+        const FragA fa = rm_at(blk ? Mrk : Mak, mt, kk, lane);
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          FragB f0, f1;
+          rm_bt2(blk ? DY : DSA, 4 * nh + 2 * p2, kk, lane, f0, f1);
+          mma3(acc[2 * p2], fa, f0);
+          mma3(acc[2 * p2 + 1], fa, f1);
+        }
       }
     }
   }
   __syncthreads();  // every operand has been read: stage over A^ .. Xb
   float* stage = reinterpret_cast<float*>(sm + LY::oStage);
 #pragma unroll
-  for (int rep = 0; rep < 2; ++rep) {
+  for (int rep = 0; rep < 3; ++rep) {
     const int job = warp + 8 * rep;
+    if (job >= 20) continue;
     const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
     float* st = stage + prod * kL * kD;
-    float* sp = stage + (4 + prod) * kL * kD;  // times its own input (r, a, k, b) for the dw recurrence
+    // DR, DA, DK, DB times their own input (r, a, k, b) for the dw recurrence
+    float* sp = stage + (5 + (prod & 3)) * kL * kD;
     const Tin* inp = prod == 0 ? r : (prod == 1 ? a : (prod == 2 ? k : b));
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
@@ -515,30 +559,34 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         float2 sc;
         if (prod == 0) sc = gt;
         else if (prod == 1) sc = gp;
-        else sc = make_float2(__frcp_rn(gt.x), __frcp_rn(gt.y));
+        else if (prod < 4) sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
+        else sc = make_float2(1.f, 1.f);
         const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
         *reinterpret_cast<float2*>(st + t * kD + j) = o;
-        float2 in = make_float2(0.f, 0.f);
-        if (t < n) {
-          const size_t gi = base + (size_t)(t0 + t) * tstride + j;
-          in = make_float2(to_f32(inp[gi]), to_f32(inp[gi + 1]));
+        if (prod < 4) {
+          float2 in = make_float2(0.f, 0.f);
+          if (t < n) {
+            const size_t gi = base + (size_t)(t0 + t) * tstride + j;
+            in = make_float2(to_f32(inp[gi]), to_f32(inp[gi + 1]));
+          }
+          *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
         }
-        *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
       }
     }
   }
   __syncthreads();
 
-  // ---- P8: write dr, da, dk, db; dw by the column recurrence of Z_t = colsum(X_t o S_t)
+  // ---- P8: write dr, da, dk, db, dv; dw by the column recurrence of Z_t = colsum(X_t o S_t)
   {
     const float* sDR = stage;
     const float* sDA = stage + kL * kD;
     const float* sDK = stage + 2 * kL * kD;
     const float* sDB = stage + 3 * kL * kD;
-    const float* sRDR = stage + 4 * kL * kD;
-    const float* sADA = stage + 5 * kL * kD;
-    const float* sKDK = stage + 6 * kL * kD;
-    const float* sBDB = stage + 7 * kL * kD;
+    const float* sDV = stage + 4 * kL * kD;
+    const float* sRDR = stage + 5 * kL * kD;
+    const float* sADA = stage + 6 * kL * kD;
+    const float* sKDK = stage + 7 * kL * kD;
+    const float* sBDB = stage + 8 * kL * kD;
     for (int e = tid; e < n * (kD / 4); e += kNT) {
       const int t = e >> 4, c = (e & 15) * 4;
       const size_t o = base + (size_t)(t0 + t) * tstride + c;
@@ -546,10 +594,12 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
       *reinterpret_cast<float4*>(da + o) = *reinterpret_cast<const float4*>(sDA + t * kD + c);
       *reinterpret_cast<float4*>(dk + o) = *reinterpret_cast<const float4*>(sDK + t * kD + c);
       *reinterpret_cast<float4*>(db + o) = *reinterpret_cast<const float4*>(sDB + t * kD + c);
+      *reinterpret_cast<float4*>(dv + o) = *reinterpret_cast<const float4*>(sDV + t * kD + c);
     }
     if (tid < kD) {
       const int j = tid;
-      float Z = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j];
+      // Z_{n-1} = colsum(X_e o S_e) with X_e = G + dy_{n-1} r_{n-1}^T: the r_{n-1} o dr_{n-1} term
+      float Z = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * kD + j];
       for (int t = n - 1; t >= 0; --t) {
         const float wdw = Z - sKDK[t * kD + j] - sBDB[t * kD + j];
         dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
@@ -569,8 +619,8 @@ cudaError_t launch_colmat_t(const BwdArgs& p, const float* xck_ws, cudaStream_t 
   const unsigned grid = (unsigned)p.B * p.H * p.nchunks;
   kern<<<grid, kNT, LY::kBytes, stream>>>(p.T, p.H, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
                                           (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
-                                          (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, xck_ws, p.dr, p.dw, p.dk, p.da,
-                                          p.db);
+                                          (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, xck_ws, p.dr, p.dw, p.dk, p.dv,
+                                          p.da, p.db);
   return cudaGetLastError();
 }
 

@@ -55,12 +55,12 @@ __device__ __forceinline__ float col1(const Tin* p) {
 // quarters' reads of a token's row vector are 64 contiguous bytes.  Row pair p starts at prow(r0, p).
 __device__ __forceinline__ int prow(int r0, int p) { return 16 * (p >> 1) + r0 + 2 * (p & 1); }
 
-// the thread's row pairs (p < kRP) of columns c0 .. c0+3 of a row-major 64 x 64 fp32 matrix
+// the thread's row pairs (p < kRP) of columns c0 .. c0+3 of a row-major 64 x 64 fp32 matrix (global or shared)
 __device__ __forceinline__ void load_block(const float* __restrict__ m, int r0, int c0, float2 (&o)[kRP][kCT]) {
 #pragma unroll
   for (int p = 0; p < kRP; ++p) {
-    const float4 e = __ldg(reinterpret_cast<const float4*>(m + (size_t)prow(r0, p) * kD + c0));
-    const float4 f = __ldg(reinterpret_cast<const float4*>(m + (size_t)(prow(r0, p) + 1) * kD + c0));
+    const float4 e = *reinterpret_cast<const float4*>(m + (size_t)prow(r0, p) * kD + c0);
+    const float4 f = *reinterpret_cast<const float4*>(m + (size_t)(prow(r0, p) + 1) * kD + c0);
     o[p][0] = make_float2(e.x, f.x);
     o[p][1] = make_float2(e.y, f.y);
     o[p][2] = make_float2(e.z, f.z);
@@ -167,8 +167,8 @@ __device__ __forceinline__ void sweep_b(float2 (&M)[kRP][kCT], const float* rq, 
 
 // The two passes over one chunk of n tokens on 64 threads (tid < 64).  Shared memory holds the chunk's
 // raw inputs cols (Tin [6][32][64]: w, k, a, b, r, v, rows 0..n-1) and fp32 [32][64] sa, dsa, dy and
-// v widened; xend (X at the chunk's last token) and s0 (the state before the chunk, or null for zeros)
-// are read from global memory.  Writes dr, dw, dk, da, db at tokens t0..t0+n-1 (element
+// v widened; xend (X at the chunk's last token, row-major 64 x 64, global or shared memory) and s0 (the
+// state before the chunk, global, or null for zeros).  Writes dr, dw, dk, da, db at tokens t0..t0+n-1 (element
 // base + t*tstride + column).
 template <typename Tin>
 __device__ __forceinline__ void passes(int tid, int n, int t0, size_t base, size_t tstride, const Tin* cols,
@@ -294,7 +294,7 @@ __device__ __forceinline__ void passes(int tid, int n, int t0, size_t base, size
           float2 X[kCT];
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
-            const float4 e = __ldg(reinterpret_cast<const float4*>(xend + (size_t)(prow(r0, p) + hr) * kD + c0));
+            const float4 e = *reinterpret_cast<const float4*>(xend + (size_t)(prow(r0, p) + hr) * kD + c0);
             const float ev[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
             for (int c = 0; c < kCT; ++c) (hr ? X[c].y : X[c].x) = ev[c];

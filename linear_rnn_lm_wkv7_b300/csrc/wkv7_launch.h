@@ -73,12 +73,21 @@ cudaError_t launch_gwalk_chunked(const BwdArgs& a, float* dsa_ws, float* xck_ws,
 // (B,H,C,D,D), dh0
 cudaError_t launch_forward_transition(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_gwalk_transition(const BwdArgs& a, float* xck_ws, cudaStream_t stream);
-// the column gradients dr, dw, dk, da, db of every 32-token chunk in matrix form, from the walk's X at
-// the chunk ends (xck_ws), the checkpoints and the inputs (no saved sa)
-cudaError_t launch_colgrad_matrix(const BwdArgs& a, const float* xck_ws, cudaStream_t stream);
-// the two-phase backward by the transition walk and the matrix column gradients (chunk == 32); workspace
-// as launch_backward_two_phase
+// the transition operands of every 32-token chunk (B', K', C, P, gamma_31, flag; transition_ops_bytes()
+// bytes, 256-byte aligned), the forward chain reading them, and the backward's walk over the same chunks
+// writing G (the gradient w.r.t. the state after each chunk from every later token) into g_ends (B,H,C,D,D)
+size_t transition_ops_bytes(int B, int T, int H);
+cudaError_t launch_transition_ops(const FwdArgs& a, unsigned char* ops, cudaStream_t stream);
+cudaError_t launch_forward_from_ops(const FwdArgs& a, const unsigned char* ops, cudaStream_t stream);
+cudaError_t launch_walk_from_ops(const BwdArgs& a, const unsigned char* ops, float* g_ends, cudaStream_t stream);
+// the column gradients dr, dw, dk, dv, da, db of every 32-token chunk in matrix form, from G at the chunk
+// ends, the checkpoints and the inputs (no saved sa)
+cudaError_t launch_colgrad_matrix(const BwdArgs& a, const float* g_ends, cudaStream_t stream);
+// the backward without a saved sa at chunk 32: operands, walk, matrix column gradients; the workspace holds
+// the operands then G at the chunk ends
 cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, cudaStream_t stream);
+// bytes of the forward's workspace (the transition operands)
+size_t forward_workspace_bytes(int B, int T, int H, int chunk);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace wkv7

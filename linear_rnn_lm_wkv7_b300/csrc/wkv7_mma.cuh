@@ -52,9 +52,10 @@ struct FragB {
   uint32_t h[2], l[2];
 };
 
+// (not volatile: the instruction only reads registers and writes its accumulator, so the compiler may
+// interleave independent accumulators -- a product's three passes into one accumulator are dependent)
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -171,11 +172,13 @@ __device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const __nv_bfloat16* p) 
   if (TRANS)
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
+                 : "r"(a)
+                 : "memory");
   else
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
+                 : "r"(a)
+                 : "memory");
 }
 
 struct RM {
@@ -240,6 +243,21 @@ __device__ __forceinline__ void rm_store_acc(const RM& x, int mt, int nj, int la
   const int r = mt * 16 + (lane >> 2), col = nj * 8 + 2 * (lane & 3);
   rm_store(x, r, col, c[0], c[1]);
   rm_store(x, r + 8, col, c[2], c[3]);
+}
+// 8 split values to row r, columns c..c+7 (c a multiple of 8): two 16-byte stores
+__device__ __forceinline__ void rm_store8(const RM& x, int r, int c, const float (&v)[8]) {
+  uint4 h, l;
+  split2(v[0], v[1], h.x, l.x);
+  split2(v[2], v[3], h.y, l.y);
+  split2(v[4], v[5], h.z, l.z);
+  split2(v[6], v[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(x.p + r * x.ld + c) = h;
+  *reinterpret_cast<uint4*>(x.p + x.lo + r * x.ld + c) = l;
+}
+// fp32 values (hi + lo) at (r, c), (r, c + 1)
+__device__ __forceinline__ float2 rm_get2(const RM& x, int r, int c) {
+  return join2(*reinterpret_cast<const uint32_t*>(x.p + r * x.ld + c),
+               *reinterpret_cast<const uint32_t*>(x.p + x.lo + r * x.ld + c));
 }
 // d += A B for split A and an exact-bf16 B (hi only)
 __device__ __forceinline__ void mma2b(float (&d)[4], const FragA& a, const FragB& b) {

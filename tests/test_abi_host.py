@@ -47,7 +47,7 @@ def test_num_chunks_and_version():
 
 def fwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None):
     p = list(ALIGNED[:11]) if ptrs is None else ptrs
-    return wkv7.lib.wkv7_forward(B, T, H, D, chunk, dt, *p, None)
+    return wkv7.lib.wkv7_forward(B, T, H, D, chunk, dt, *p, None, 0, None)
 
 
 def bwd(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None, ws=None, ws_bytes=0):
@@ -122,13 +122,28 @@ def test_decode_validation(i):
 
 def test_workspace_size_query():
     n = wkv7.backward_workspace_size(12, 1024, 6, 64, 32)
+    # at chunk 32: the larger of the two-phase layout (dsa, then X at every chunk end) and the transition
+    # layout (25088 bytes of operands per chunk, then G at every chunk end)
     dsa = 12 * 1024 * 6 * 64 * 4
     xck = 12 * 6 * 32 * 64 * 64 * 4
-    assert n == (dsa + 255) // 256 * 256 + xck
+    ops = 12 * 6 * 32 * 25088
+    assert n == max((dsa + 255) // 256 * 256 + xck, (ops + 255) // 256 * 256 + xck)
+    assert wkv7.backward_workspace_size(2, 64, 3, 64, 16) == (2 * 64 * 3 * 64 * 4 + 255) // 256 * 256 + 2 * 3 * 4 * 64 * 64 * 4
+    assert wkv7.forward_workspace_size(12, 1024, 6, 64, 32) == ops
+    assert wkv7.forward_workspace_size(12, 1024, 6, 64, 16) == 0
     assert wkv7.backward_workspace_size(1, 0, 1, 64, 32) == 0
     with pytest.raises(wkv7.WKV7Error):
         wkv7.backward_workspace_size(1, 32, 1, 32, 32)      # D != 64
     assert wkv7.lib.wkv7_backward_workspace_size(1, 32, 1, 64, 32, None) == 1
+    assert wkv7.lib.wkv7_forward_workspace_size(1, 32, 1, 64, 32, None) == 1
+
+
+def test_forward_rejects_small_or_misaligned_workspace():
+    # without sa (index 10) a workspace selects the transition operands: it is checked before any launch
+    need = wkv7.forward_workspace_size(2, 64, 3, 64, 32)
+    p = list(ALIGNED[:10]) + [None]
+    assert wkv7.lib.wkv7_forward(2, 64, 3, 64, 32, 0, *p, P(0x100000), need - 1, None) == 7
+    assert wkv7.lib.wkv7_forward(2, 64, 3, 64, 32, 0, *p, P(0x100000 + 128), need, None) == 3
 
 
 def test_backward_rejects_small_or_misaligned_workspace():
