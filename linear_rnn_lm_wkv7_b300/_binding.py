@@ -5,7 +5,8 @@ checked, outputs are allocated with torch when the caller passes none, and the
 raw device pointers plus the current CUDA stream go to the C entry points.
 Every step of the recurrence runs in the library's kernels; there is no other
 implementation behind these functions.  If libwkv7.so is missing the import
-fails.
+fails.  WKV7_LIBRARY, if set, names another build of the same library to load
+(e.g. libwkv7_debug.so, the build with device-side bounds checks).
 """
 from __future__ import annotations
 
@@ -13,7 +14,7 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIBRARY_PATH = os.path.join(PKG, "libwkv7.so")
+LIBRARY_PATH = os.environ.get("WKV7_LIBRARY") or os.path.join(PKG, "libwkv7.so")
 
 F32 = 0
 BF16 = 1

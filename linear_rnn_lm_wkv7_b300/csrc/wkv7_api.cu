@@ -123,10 +123,7 @@ int forward_impl(bool sequential, int B, int T, int H, int D, int chunk, int in_
   if (workspace != nullptr && chunk == 32 && p.sa == nullptr && T > 0) {
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
     if (workspace_bytes < wkv7::forward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
-    unsigned char* ops = static_cast<unsigned char*>(workspace);
-    cudaError_t err = wkv7::launch_transition_ops(p, ops, st_);
-    if (err != cudaSuccess) return record_cuda(err);
-    return record_cuda(wkv7::launch_forward_from_ops(p, ops, st_));
+    return record_cuda(wkv7::launch_xop_forward(p, workspace, 0, st_));
   }
   return record_cuda(wkv7::launch_forward(p, st_));
 }

@@ -433,35 +433,24 @@ size_t two_phase_bytes(int B, int T, int H, int chunk) {
   const size_t xck = (size_t)B * H * C * kD * kD * 4;
   return (dsa + 255) / 256 * 256 + xck;
 }
-// the transition backward (chunk 32): the operands then G at every chunk end
-size_t transition_bytes(int B, int T, int H) {
-  const size_t C = T > 0 ? (size_t)((T + 31) / 32) : 0;
-  return (transition_ops_bytes(B, T, H) + 255) / 256 * 256 + (size_t)B * H * C * kD * kD * 4;
-}
 }  // namespace
 
 size_t backward_workspace_bytes(int B, int T, int H, int chunk) {
   const size_t a = two_phase_bytes(B, T, H, chunk);
   if (chunk != 32) return a;
-  const size_t b = transition_bytes(B, T, H);
+  const size_t b = xop_workspace_bytes(B, T, H);
   return a > b ? a : b;
 }
 
 size_t forward_workspace_bytes(int B, int T, int H, int chunk) {
-  return chunk == 32 ? transition_ops_bytes(B, T, H) : 0;
+  return chunk == 32 ? xop_workspace_bytes(B, T, H) : 0;
 }
 
 cudaError_t launch_backward_transition(const BwdArgs& p, void* workspace, cudaStream_t stream) {
-  unsigned char* ops = static_cast<unsigned char*>(workspace);
-  float* g_ends = reinterpret_cast<float*>(ops + (transition_ops_bytes(p.B, p.T, p.H) + 255) / 256 * 256);
-  FwdArgs f;
-  f.B = p.B; f.T = p.T; f.H = p.H; f.chunk = p.chunk; f.nchunks = p.nchunks; f.bf16 = p.bf16; f.in = p.in;
-  f.h0 = p.h0; f.y = nullptr; f.h_ckpt = nullptr; f.hT = nullptr; f.sa = nullptr;
-  cudaError_t err = launch_transition_ops(f, ops, stream);
+  ChunkEnds ends;
+  cudaError_t err = launch_xop_walk(p, workspace, 0, &ends, stream);
   if (err != cudaSuccess) return err;
-  err = launch_walk_from_ops(p, ops, g_ends, stream);
-  if (err != cudaSuccess) return err;
-  return launch_colgrad_matrix(p, g_ends, stream);
+  return launch_colgrad_matrix(p, ends, stream);
 }
 
 cudaError_t launch_backward_two_phase(const BwdArgs& p, void* workspace, cudaStream_t stream) {

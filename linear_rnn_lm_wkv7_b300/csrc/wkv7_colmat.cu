@@ -31,7 +31,7 @@
 //
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation; operands are stored once, row-major, split into bf16 hi and lo, and read with
-// ldmatrix (.trans for the transposed uses).  Mapping: one CTA of 8 warps per (head, chunk).
+// ldmatrix (.trans for the transposed uses).  Mapping: one CTA of 16 warps per (head, chunk).
 #include <type_traits>
 
 #include "wkv7_colpass.cuh"
@@ -46,6 +46,7 @@ using namespace mma;
 
 constexpr int kL = 32;
 constexpr int kNT = 256;
+constexpr int kNW = kNT / 32;
 constexpr int kLD64 = 72;  // row stride (bf16 elements) of 64-wide operands
 constexpr int kLD32 = 40;  // of 32-wide operands
 constexpr float kMinGamma = 1e-20f;
@@ -58,8 +59,9 @@ struct Lay {
   // ---- long-lived
   static constexpr int oG = 0;                                  // float [32][64] gamma
   static constexpr int oZP = oG + 32 * 64 * 4;                  // float [4][64] colsum partials
-  static constexpr int oMeta = oZP + 4 * 64 * 4;                // int [4]
-  static constexpr int oWc = oMeta + 16 + 240;                  // float [32][64] w (1 past n)
+  static constexpr int oBT = oZP + 4 * 64 * 4;                  // float [4][64] block totals of the scans
+  static constexpr int oMeta = oBT + 4 * 64 * 4;                // int [8]
+  static constexpr int oWc = oMeta + 256;                       // float [32][64] w (1 past n)
   static constexpr int oAh = oWc + 32 * 64 * 4;
   static constexpr int oBt = oAh + rm_bytes(32, kLD64);
   static constexpr int oKt = oBt + rm_bytes(32, kLD64);
@@ -90,17 +92,19 @@ struct Lay {
   static constexpr int kPhaseEnd = oE + 16 * 16 * 4;
   static constexpr int oL = oU;                                 // L1..L4 (32 x 32 each)
   static_assert(oL + 4 * rm_bytes(32, kLD32) <= oTI, "L1..L4 fit over U, W and M_ab");
-  static constexpr int kBytes = (kRawEnd > kPhaseEnd ? kRawEnd : kPhaseEnd);
-  // ---- fallback (token-by-token column passes): fp32 [32][64] sa, dsa, v and X_e [64][64] over A^ .. S0
-  static constexpr int oFSa = oAh;
-  static constexpr int oFDsa = oFSa + kL * kD * 4;
-  static constexpr int oFV = oFDsa + kL * kD * 4;
-  static constexpr int oFXe = oFV + kL * kD * 4;
-  static_assert(oFXe + kD * kD * 4 <= oXb, "fallback arrays fit over A^ .. S0");
-  // ---- output staging over A^ .. Xb (after the last products): DR, DA, DK, DB, DV, then r o dr, a o da,
-  // k o dk, b o db, fp32 [32][64] each
+  static constexpr int kMain = (kRawEnd > kPhaseEnd ? kRawEnd : kPhaseEnd);
+  // ---- fp32 S0 and G [64][64] staged by cp.async (through P1b); then r, a, k, b [32][64] (Tin) for the
+  // output stage.  S_e [64][64] fp32 is staged over SA and DSA (first written in P5).
+  static constexpr int oS0f = (kMain + 127) / 128 * 128;
+  static constexpr int oGf = oS0f + kD * kD * 4;
+  static constexpr int oIn = oS0f;
+  static constexpr int oSef = oSA;
+  static_assert(oSef + kD * kD * 4 <= oB, "S_e fits over SA and DSA");
+  static_assert(4 * kL * kD * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
+  static constexpr int kBytes = oGf + kD * kD * 4;
+  // ---- r o dr, a o da, k o dk, b o db, fp32 [32][64] each, over A^ .. (after the last products)
   static constexpr int oStage = oAh;
-  static_assert(oStage + 9 * kL * kD * 4 <= oV, "staging fits over A^ .. Xb");
+  static_assert(oStage + 4 * kL * kD * 4 <= oV, "dw terms fit over A^ .. Xb");
 };
 
 template <typename Tin>
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(kNT, 1)
 colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
               const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
               const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
-              const float* __restrict__ dy, const float* __restrict__ xck, float* __restrict__ dr,
+              const float* __restrict__ dy, const float* __restrict__ xck, int* __restrict__ flags, size_t xck_stride,
+              float* __restrict__ dr,
               float* __restrict__ dw, float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ da,
               float* __restrict__ db) {
   using LY = Lay<Tin>;
@@ -128,7 +133,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   const int n = min(kL, T - t0);
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
-  const float* gend = xck + ((size_t)bh * nchunks + ci) * kD * kD;  // G: the gradient from later tokens
+  const float* gend = xck + ((size_t)bh * nchunks + ci) * xck_stride;  // G: the gradient from later tokens
   const float* send = h_ckpt + ((size_t)bh * nchunks + ci) * kD * kD;
   const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
                            : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
@@ -163,7 +168,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   float* E = reinterpret_cast<float*>(sm + LY::oE);
   constexpr int SM = LY::kSM;
 
-  // ---- P0: the chunk's inputs (rows past n are not copied); colsum(G o S_e) partials meanwhile
+  // ---- P0: the chunk's inputs (rows past n are not copied) in one cp.async group, S0, G and S_e in a second
   {
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
     constexpr int EPC = 16 / (int)sizeof(Tin);
@@ -179,39 +184,559 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
       cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
     }
     cp_async_commit();
-    const int j = tid & 63, part = tid >> 6;
-    float z = 0.f;
-#pragma unroll 4
-    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(__ldg(gend + i * kD + j), __ldg(send + i * kD + j), z);
-    ZP[part * 64 + j] = z;
-    cp_async_wait<0>();
+    float* s0f = reinterpret_cast<float*>(sm + LY::oS0f);
+    float* gf = reinterpret_cast<float*>(sm + LY::oGf);
+    float* sef = reinterpret_cast<float*>(sm + LY::oSef);
+    for (int e = tid; e < kD * kD / 4; e += kNT) {
+      if (s0 != nullptr) cp_async16(s0f + 4 * e, s0 + 4 * e);
+      cp_async16(gf + 4 * e, gend + 4 * e);
+      cp_async16(sef + 4 * e, send + 4 * e);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();  // the inputs
   }
   __syncthreads();
 
-  // ---- P1a: gamma down each column; the fallback flag
-  if (tid < kD) {
-    const int j = tid;
-    float gm = 1.f;
+  // ---- P1a: gamma_t down each column as a scan (4 blocks of 8 tokens per column); the fallback flag
+  float* BT = reinterpret_cast<float*>(sm + LY::oBT);
+  {  // threads 0-255 (whole warps): column j, tokens 8 blk .. 8 blk + 7
+    const int j = tid & 63, blk = tid >> 6;
+    const bool act = tid < 256;
+    float loc[8];
+    float p = 1.f;
     bool bad = false;
-#pragma unroll 8
-    for (int t = 0; t < kL; ++t) {
-      const float wt = t < n ? to_f32(rw[t * kD + j]) : 1.f;
-      bad |= !(wt >= kWMin);
-      gm *= wt;
-      G[t * kD + j] = gm;
-      Wc[t * kD + j] = wt;
+    if (act) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = 8 * blk + u;
+        const float wt = t < n ? to_f32(rw[t * kD + j]) : 1.f;
+        bad |= !(wt >= kWMin);
+        p *= wt;
+        loc[u] = p;
+        Wc[t * kD + j] = wt;
+      }
+      BT[blk * 64 + j] = p;
     }
-    bad |= !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+    __syncthreads();
+    if (act) {
+      float pre = 1.f;
+      for (int q2 = 0; q2 < blk; ++q2) pre *= BT[q2 * 64 + j];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) G[(8 * blk + u) * kD + j] = pre * loc[u];
+      if (blk == 3) {
+        const float gm = pre * p;
+        bad |= !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+      }
+    }
     const unsigned any = __ballot_sync(0xffffffffu, bad);
-    if (lane == 0) meta[warp] = any != 0u;
+    if (lane == 0 && warp < 8) meta[warp] = any != 0u;
   }
   __syncthreads();
-  if ((meta[0] | meta[1]) != 0) {
-    // ================= fallback: sa and dsa by their per-token recurrences, then the exact column passes
+  {  // chunks with tiny decays are left to colfb_kernel (token by token); the flag tells it which
+    const bool flagged = (meta[0] | meta[1] | meta[2] | meta[3] | meta[4] | meta[5] | meta[6] | meta[7]) != 0;
+    if (tid == 0) flags[((size_t)bh * nchunks + ci) * xck_stride] = flagged ? 1 : 0;
+    if (flagged) {
+      cp_async_wait<0>();
+      return;
+    }
+  }
+
+  // ---- P1b: operands, one (token, 8 columns) block per thread: A^, R^, K~, B~, V, DY (steps past n zero)
+  if (tid < 256) {
+    const int t = tid >> 3, c0 = (tid & 7) * 8;
+    const bool ok = t < n;
+    float gt[8], gp[8], av[8], rv8[8], kv[8], bv[8], vv[8], dv8[8];
+    raw8(G + t * kD + c0, gt);
+    if (t > 0) {
+      raw8(G + (t - 1) * kD + c0, gp);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) gp[u] = 1.f;
+    }
+    raw8(ra + t * kD + c0, av);
+    raw8(rr + t * kD + c0, rv8);
+    raw8(rk + t * kD + c0, kv);
+    raw8(rbv + t * kD + c0, bv);
+    raw8(rv + t * kD + c0, vv);
+    raw8(dyr + t * kD + c0, dv8);
+    float oa[8], orr[8], ok8[8], ob[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float ig = __frcp_rn(gt[u]);
+      oa[u] = ok ? av[u] * gp[u] : 0.f;
+      orr[u] = ok ? rv8[u] * gt[u] : 0.f;
+      ok8[u] = ok ? kv[u] * ig : 0.f;
+      ob[u] = ok ? bv[u] * ig : 0.f;
+      vv[u] = ok ? vv[u] : 0.f;
+      dv8[u] = ok ? dv8[u] : 0.f;
+    }
+    rm_store8(Ah, t, c0, oa);
+    rm_store8(Rh, t, c0, orr);
+    rm_store8(Kt, t, c0, ok8);
+    rm_store8(Bt, t, c0, ob);
+    if (kVExact) rm_store8_hi(Vm, t, c0, vv); else rm_store8(Vm, t, c0, vv);
+    rm_store8(DY, t, c0, dv8);
+  }
+  cp_async_wait<0>();  // S0, G, S_e
+  __syncthreads();
+  if (tid < 256) {  // colsum(G o S_e) partials: 4 row blocks of 16 per column
+    const float* gf = reinterpret_cast<const float*>(sm + LY::oGf);
+    const float* sef = reinterpret_cast<const float*>(sm + LY::oSef);
+    const int j = tid & 63, part = tid >> 6;
+    float z = 0.f;
+#pragma unroll
+    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(gf[i * kD + j], sef[i * kD + j], z);
+    ZP[part * 64 + j] = z;
+  }
+  // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
+  {
+    const float* s0f = reinterpret_cast<const float*>(sm + LY::oS0f);
+    const float* gf = reinterpret_cast<const float*>(sm + LY::oGf);
+#pragma unroll 4
+    for (int e = tid; e < kD * (kD / 2); e += kNT) {
+      const int i = e >> 5, j = 2 * (e & 31);
+      const float2 s = s0 != nullptr ? *reinterpret_cast<const float2*>(s0f + i * kD + j) : make_float2(0.f, 0.f);
+      rm_store(S0, i, j, s.x, s.y);
+      const float2 x = *reinterpret_cast<const float2*>(gf + i * kD + j);
+      const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
+      rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
+    }
+  }
+  __syncthreads();
+  {  // r, a, k, b again (for the dw recurrence at the end) over the dead S0 / G staging
+    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    Tin* in4 = reinterpret_cast<Tin*>(sm + LY::oIn);
+    const Tin* srcs[4] = {r, a, k, b};
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4)
+      for (int e = tid; e < n * CPR; e += kNT) {
+        const int tt = e / CPR, pc = e % CPR;
+        cp_async16(in4 + (s4 * kL + tt) * kD + pc * EPC, srcs[s4] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+      }
+    cp_async_commit();
+  }
+
+  // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
+  // M_rk = tril(R^ K~^T); 16 jobs of (product, m-tile, pair of n-tiles), K = 64
+  // warp w forms jobs w and w + 8 together: the same tile of (M_ab, M_rb) or (M_ak, M_rk), sharing B~ or K~
+  static_assert(kNW == 8, "job pairing assumes 8 warps");
+  {
+    const int prodA = warp >> 2, mt = (warp >> 1) & 1, np = warp & 1;  // prodB = prodA + 2
+    float acc[2][2][4] = {};
+    if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
+      const RM& Y = (prodA & 1) ? Kt : Bt;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa0 = rm_a(Ah, mt, kk, lane), fa1 = rm_a(Rh, mt, kk, lane);
+        FragB fb[2];
+        rm_b2(Y, 2 * np, kk, lane, fb[0], fb[1]);
+        mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
+      }
+    }
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+      const int prod = prodA + 2 * jb;
+      const bool strict = prod < 2;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nj = 2 * np + h;
+        const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+        float c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = tr + ((e >> 1) << 3), s2 = sc + (e & 1);
+          c[e] = (strict ? s2 < t : s2 <= t) ? acc[jb][h][e] : 0.f;
+        }
+        if (prod == 0) {
+          *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+          *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
+        } else {
+          rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- P3 || P4: warp 0 solves the diagonal blocks of T = (I - M_ab)^-1 (forward substitution, one column
+  // per lane: lanes 0-15 T11, lanes 16-31 T22); the other warps form U = A^ S0^T + M_ak V and
+  // W = B~ Xb^T + M_rb^T DY (rows t, columns i): 16 jobs of (product, m-tile, 4 n-tiles)
+  if (warp == 0) {
+    const int off = lane < 16 ? 0 : 16;
+    const int c = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float acc = t == c ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) acc = fmaf(Mab[(off + t) * SM + off + u], x[u], acc);
+      x[t] = acc;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
+    __syncwarp();
+    {  // T21 = T22 A21 T11 (A21 = M_ab[16..31][0..15]) on tensor cores, transposed:
+       // E^T = T11^T A21^T, then T21^T = E^T T22^T (rows s, columns t)
+      auto ld2 = [&](const float* p0, const float* p1, uint32_t& hw, uint32_t& lw) { split2(*p0, *p1, hw, lw); };
+      FragA fa;  // T11^T: A[s][u] = T11[u][s]
+      ld2(TI + (2 * q) * SM + g, TI + (2 * q + 1) * SM + g, fa.h[0], fa.l[0]);
+      ld2(TI + (2 * q) * SM + g + 8, TI + (2 * q + 1) * SM + g + 8, fa.h[1], fa.l[1]);
+      ld2(TI + (2 * q + 8) * SM + g, TI + (2 * q + 9) * SM + g, fa.h[2], fa.l[2]);
+      ld2(TI + (2 * q + 8) * SM + g + 8, TI + (2 * q + 9) * SM + g + 8, fa.h[3], fa.l[3]);
+      FragB fb[2];  // A21^T: B[u][t] = A21[t][u]
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float* row = Mab + (16 + nt * 8 + g) * SM;
+        ld2(row + 2 * q, row + 2 * q + 1, fb[nt].h[0], fb[nt].l[0]);
+        ld2(row + 2 * q + 8, row + 2 * q + 9, fb[nt].h[1], fb[nt].l[1]);
+      }
+      float et[2][4] = {};
+      mma3n<2>(et, fa, fb);
+      const FragA fe = frag_from_acc(et[0], et[1]);  // E^T as an A operand (rows s, k = t')
+      FragB fc[2];  // T22^T: B[t'][t] = T22[t][t']
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float* row = TI + (16 + nt * 8 + g) * SM + 16;
+        ld2(row + 2 * q, row + 2 * q + 1, fc[nt].h[0], fc[nt].l[0]);
+        ld2(row + 2 * q + 8, row + 2 * q + 9, fc[nt].h[1], fc[nt].l[1]);
+      }
+      float tt[2][4] = {};
+      mma3n<2>(tt, fe, fc);
+      __syncwarp();
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {  // T21[t][s] from T21^T (rows s = g, g + 8; columns t = 8 nt + 2q, + 1)
+        const int t = nt * 8 + 2 * q;
+        TI[(16 + t) * SM + g] = tt[nt][0];
+        TI[(17 + t) * SM + g] = tt[nt][1];
+        TI[(16 + t) * SM + g + 8] = tt[nt][2];
+        TI[(17 + t) * SM + g + 8] = tt[nt][3];
+      }
+    }
+  } else {
+    for (int job = warp - 1; job < 16; job += kNW - 1) {
+      const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1
+      float acc[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(prod == 0 ? Ah : Bt, mt, kk, lane);
+        FragB f0, f1;
+        rm_b2(prod == 0 ? S0 : Xb, 2 * nq, kk, lane, f0, f1);
+        {
+          const FragB fb2[2] = {f0, f1};
+          mma3n<2>(acc, fa, fb2);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (prod == 0) {  // M_ak V: V is B[k = u][n = i] = V[u][i]
+          const FragA fa = rm_a(Mak, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Vm, 2 * nq, kk, lane, f0, f1, !kVExact);
+          if (kVExact) {
+            mma2b(acc[0], fa, f0);
+            mma2b(acc[1], fa, f1);
+          } else {
+            {
+              const FragB fb2[2] = {f0, f1};
+              mma3n<2>(acc, fa, fb2);
+            }
+          }
+        } else {  // M_rb^T DY
+          const FragA fa = rm_at(Mrb, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(DY, 2 * nq, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+      }
+      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq, lane, acc[0]);
+      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq + 1, lane, acc[1]);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < 32 * 16; e += kNT) {  // T (rows t, columns u), zero above the diagonal
+    const int t = e >> 4, u = 2 * (e & 15);
+    rm_store(Tm, t, u, u <= t ? TI[t * SM + u] : 0.f, u + 1 <= t ? TI[t * SM + u + 1] : 0.f);
+  }
+  __syncthreads();
+
+  // ---- P5: SA = T U, DSA = T^T W (rows t, columns i; K = 32); 16 jobs (product, m-tile, 4 n-tiles)
+  {  // warp w: SA and DSA at the same tile (m-tile, 2 n-tiles)
+    const int mt = (warp >> 2) & 1, nq = warp & 3;
+    float acc[2][2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const bool on0 = !(mt == 0 && kk == 1), on1 = !(mt == 1 && kk == 0);  // T lower, T^T upper
+      FragB fb0[2], fb1[2];
+      rm_bt2(U, 2 * nq, kk, lane, fb0[0], fb0[1]);
+      rm_bt2(W, 2 * nq, kk, lane, fb1[0], fb1[1]);
+      const FragA fa0 = rm_a(Tm, mt, kk, lane), fa1 = rm_at(Tm, mt, kk, lane);
+      if (on0 && on1)
+        mma3n_two<2>(acc[0], fa0, fb0, acc[1], fa1, fb1);
+      else if (on0)
+        mma3n<2>(acc[0], fa0, fb0);
+      else
+        mma3n<2>(acc[1], fa1, fb1);
+    }
+    rm_store_acc(SA, mt, 2 * nq, lane, acc[0][0]);
+    rm_store_acc(SA, mt, 2 * nq + 1, lane, acc[0][1]);
+    rm_store_acc(DSA, mt, 2 * nq, lane, acc[1][0]);
+    rm_store_acc(DSA, mt, 2 * nq + 1, lane, acc[1][1]);
+  }
+  __syncthreads();
+
+  // ---- P6: L1 = tril(DY V^T), L2 = tril(DY SA^T), L3 = tril(DSA V^T, -1), L4 = tril(DSA SA^T, -1) (over U, W)
+  {  // warp w: (L1, L3) or (L2, L4) at the same tile, sharing V or SA
+    const int prodA = warp >> 2, mt = (warp >> 1) & 1, np = warp & 1;  // prodB = prodA + 2
+    const bool exactB = kVExact && prodA == 0;
+    float acc[2][2][4] = {};
+    if (!(mt == 0 && np == 1)) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa0 = rm_a(DY, mt, kk, lane), fa1 = rm_a(DSA, mt, kk, lane);
+        FragB fb[2];
+        rm_b2(prodA ? SA : Vm, 2 * np, kk, lane, fb[0], fb[1], !exactB);
+        if (exactB)
+          mma2b_two<2>(acc[0], fa0, acc[1], fa1, fb);
+        else
+          mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
+      }
+    }
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+      const int prod = prodA + 2 * jb;
+      const bool strict = prod >= 2;
+      const RM& Lx = prod == 0 ? L1 : (prod == 1 ? L2 : (prod == 2 ? L3 : L4));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nj = 2 * np + h;
+        float c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = mt * 16 + g + ((e >> 1) << 3), s2 = nj * 8 + 2 * q + (e & 1);
+          c[e] = (strict ? s2 < t : s2 <= t) ? acc[jb][h][e] : 0.f;
+        }
+        rm_store_acc(Lx, mt, nj, lane, c);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- P7: DR, DA, DK, DB, DV (rows t, columns j or i): 20 jobs of (product, m-tile, 4 n-tiles), each a
+  // K = 64 product with S0 / Xb plus the masked products; held in registers until every warp is done
+  constexpr int kRep = (20 + kNW - 1) / kNW;  // output jobs per warp
+  float res[kRep][4][4];
+#pragma unroll
+  for (int rep = 0; rep < kRep; ++rep) {
+    const int job = warp + kNW * rep;
+    float (&acc)[4][4] = res[rep];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+    if (job >= 20) continue;
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
+    if (prod < 4) {
+      const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
+      const RM& B1 = prod < 2 ? S0 : Xb;
+      const bool exactA = kVExact && prod == 2;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
+        FragB fb[4];
+        rm_bt2(B1, 4 * nh, kk, lane, fb[0], fb[1]);
+        rm_bt2(B1, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+        if (exactA)
+          mma2n<4>(acc, fa, fb);
+        else
+          mma3n<4>(acc, fa, fb);
+      }
+      // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
+      // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int blk = kq >> 1, kk = kq & 1;
+        const bool lowerA = prod < 2;
+        if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
+        const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
+        const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
+        const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
+        FragB fb[4];
+        rm_bt2(BB, 4 * nh, kk, lane, fb[0], fb[1]);
+        rm_bt2(BB, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+        mma3n<4>(acc, fa, fb);
+      }
+    } else {
+      // DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY (rows t, columns i)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const FragA fa = rm_a(Kt, mt, kk, lane);
+        FragB fb[4];
+        rm_b2(Xb, 4 * nh, kk, lane, fb[0], fb[1]);
+        rm_b2(Xb, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+        mma3n<4>(acc, fa, fb);
+      }
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int blk = kq >> 1, kk = kq & 1;
+        if (mt == 1 && kk == 0) continue;  // M_ak^T, M_rk^T upper triangular
+        const FragA fa = rm_at(blk ? Mrk : Mak, mt, kk, lane);
+        FragB fb[4];
+        rm_bt2(blk ? DY : DSA, 4 * nh, kk, lane, fb[0], fb[1]);
+        rm_bt2(blk ? DY : DSA, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+        mma3n<4>(acc, fa, fb);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every operand has been read: stage over A^ .. Xb
+  // ---- outputs: dr, da, dk, db (scaled by Gamma, Gamma_-, 1/Gamma) and dv straight from the accumulators;
+  // r o dr, a o da, k o dk, b o db into shared memory (over A^ ..) for dw
+  float* terms = reinterpret_cast<float*>(sm + LY::oStage);
+  const Tin* in4 = reinterpret_cast<const Tin*>(sm + LY::oIn);
+#pragma unroll
+  for (int rep = 0; rep < kRep; ++rep) {
+    const int job = warp + kNW * rep;
+    if (job >= 20) continue;
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
+    float* outp = prod == 0 ? dr : (prod == 1 ? da : (prod == 2 ? dk : (prod == 3 ? db : dv)));
+    float* sp = terms + (prod & 3) * kL * kD;
+    const Tin* inp = in4 + (prod & 3) * kL * kD;  // r, a, k, b
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int j = (4 * nh + x) * 8 + 2 * q;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int t = mt * 16 + g + 8 * hr;
+        const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+        const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
+        float2 sc;
+        if (prod == 0) sc = gt;
+        else if (prod == 1) sc = gp;
+        else if (prod < 4) sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
+        else sc = make_float2(1.f, 1.f);
+        const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
+        if (t < n) *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) = o;
+        if (prod < 4) {
+          float2 in = make_float2(0.f, 0.f);
+          if (t < n) in = make_float2(to_f32(inp[t * kD + j]), to_f32(inp[t * kD + j + 1]));
+          *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- P8: dw per column from Z_t = colsum(X_t o S_t) (X_t: the gradient w.r.t. the state after token t):
+  //   Z_{n-1} = colsum(G o S_e) + r_{n-1} o dr_{n-1},   w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
+  //   Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1} = Z_t + D_t,
+  // so Z_t = Z_{n-1} + sum_{s = t+1}^{n-1} D_s, a suffix sum: 4 blocks of 8 tokens per column.
+  {
+    const float* sRDR = terms;
+    const float* sADA = terms + kL * kD;
+    const float* sKDK = terms + 2 * kL * kD;
+    const float* sBDB = terms + 3 * kL * kD;
+    const int j = tid & 63, blk = tid >> 6;  // threads 0-255
+    const bool act = tid < 256;
+    float dsum[8];  // sum of D_s over this block's tokens s > t
+    float tot = 0.f;
+    if (act) {
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        const int t = 8 * blk + u;
+        dsum[u] = tot;
+        if (t >= 1 && t < n) tot += sADA[t * kD + j] + sRDR[(t - 1) * kD + j] - sKDK[t * kD + j] - sBDB[t * kD + j];
+      }
+      BT[blk * 64 + j] = tot;
+    }
+    __syncthreads();
+    if (!act) return;
+    float later = 0.f;
+    for (int q2 = blk + 1; q2 < 4; ++q2) later += BT[q2 * 64 + j];
+    const float zn = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * kD + j];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = 8 * blk + u;
+      if (t < n) {
+        const float wdw = zn + later + dsum[u] - sKDK[t * kD + j] - sBDB[t * kD + j];
+        dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
+      }
+    }
+  }
+}
+
+// The token-by-token column passes for the chunks colmat_kernel flagged (some w_t below 1/32, or gamma_31
+// below 1e-20 or not finite): sa and dsa by their per-token recurrences, dv from X, then the exact column
+// passes of wkv7_colpass.cuh.  A persistent grid reads every chunk's flag and skips the others.
+template <typename Tin>
+struct FbLay {
+  static constexpr int oRaw = 0;  // w, k, a, b, r, v [32][64] Tin
+  static constexpr int kRawIn = 6 * kL * kD * (int)sizeof(Tin);
+  static constexpr int oDyRaw = oRaw + kRawIn;  // dy fp32 [32][64]
+  static constexpr int oFSa = oDyRaw + kL * kD * 4;
+  static constexpr int oFDsa = oFSa + kL * kD * 4;
+  static constexpr int oFV = oFDsa + kL * kD * 4;
+  static constexpr int oFXe = oFV + kL * kD * 4;  // X_e fp32 [64][64]
+  static constexpr int kBytes = oFXe + kD * kD * 4;
+};
+constexpr int kNTF = 128;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kNTF)
+colfb_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
+             const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
+             const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
+             const float* __restrict__ dy, const float* __restrict__ xck, const int* __restrict__ flags,
+             size_t xck_stride, float* __restrict__ dr, float* __restrict__ dw, float* __restrict__ dk,
+             float* __restrict__ dv, float* __restrict__ da, float* __restrict__ db) {
+  using LY = FbLay<Tin>;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+  const int tid = threadIdx.x;
+  Tin* raw = reinterpret_cast<Tin*>(sm + LY::oRaw);
+  const Tin* rw = raw;
+  const Tin* rk = raw + kL * kD;
+  const Tin* ra = raw + 2 * kL * kD;
+  const Tin* rbv = raw + 3 * kL * kD;
+  const Tin* rr = raw + 4 * kL * kD;
+  const Tin* rv = raw + 5 * kL * kD;
+  float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
+  const size_t tstride = (size_t)H * kD;
+  for (int job = blockIdx.x; job < total; job += gridDim.x) {
+    if (flags[(size_t)job * xck_stride] == 0) continue;
+    const int ci = job % nchunks;
+    const int bh = job / nchunks;
+    const int bi = bh / H;
+    const int hi = bh - bi * H;
+    const int t0 = ci * kL;
+    const int n = min(kL, T - t0);
+    const size_t base = ((size_t)bi * T * H + hi) * kD;
+    const float* gend = xck + (size_t)job * xck_stride;
+    const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
+                             : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
+    {
+      constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+      constexpr int EPC = 16 / (int)sizeof(Tin);
+      const Tin* srcs[6] = {w, k, a, b, r, v};
+#pragma unroll
+      for (int s6 = 0; s6 < 6; ++s6)
+        for (int e = tid; e < n * CPR; e += kNTF) {
+          const int tt = e / CPR, pc = e % CPR;
+          cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+        }
+      for (int e = tid; e < n * (kD / 4); e += kNTF) {
+        const int tt = e / (kD / 4), pc = e % (kD / 4);
+        cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
+    __syncthreads();
     float* fsa = reinterpret_cast<float*>(sm + LY::oFSa);
     float* fdsa = reinterpret_cast<float*>(sm + LY::oFDsa);
     float* fv = reinterpret_cast<float*>(sm + LY::oFV);
-    for (int e = tid; e < n * kD; e += kNT) fv[e] = to_f32(rv[e]);
+    for (int e = tid; e < n * kD; e += kNTF) fv[e] = to_f32(rv[e]);
     if (tid < 64) {  // sa_t = S_{t-1} a_t, row tid, the state run up from S0
       const int i = tid;
       float Sr[64];
@@ -258,377 +783,41 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     if (tid < 64)
       colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv,
                            reinterpret_cast<const float*>(sm + LY::oFXe), s0, dr, dw, dk, da, db);
-    return;
-  }
-
-  // ---- P1b: operands.  Row pairs (t, j): A^, R^, K~, B~, V, DY (steps past n zero)
-  for (int e = tid; e < kL * (kD / 2); e += kNT) {
-    const int t = e >> 5, j = 2 * (e & 31);
-    const bool ok = t < n;
-    const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
-    const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
-    const float ix = __frcp_rn(gt.x), iy = __frcp_rn(gt.y);
-    const float a0 = ok ? to_f32(ra[t * kD + j]) : 0.f, a1 = ok ? to_f32(ra[t * kD + j + 1]) : 0.f;
-    const float r0 = ok ? to_f32(rr[t * kD + j]) : 0.f, r1 = ok ? to_f32(rr[t * kD + j + 1]) : 0.f;
-    const float k0 = ok ? to_f32(rk[t * kD + j]) : 0.f, k1 = ok ? to_f32(rk[t * kD + j + 1]) : 0.f;
-    const float b0 = ok ? to_f32(rbv[t * kD + j]) : 0.f, b1 = ok ? to_f32(rbv[t * kD + j + 1]) : 0.f;
-    const float v0 = ok ? to_f32(rv[t * kD + j]) : 0.f, v1 = ok ? to_f32(rv[t * kD + j + 1]) : 0.f;
-    const float d0 = ok ? dyr[t * kD + j] : 0.f, d1 = ok ? dyr[t * kD + j + 1] : 0.f;
-    rm_store(Ah, t, j, a0 * gp.x, a1 * gp.y);
-    rm_store(Rh, t, j, r0 * gt.x, r1 * gt.y);
-    rm_store(Kt, t, j, k0 * ix, k1 * iy);
-    rm_store(Bt, t, j, b0 * ix, b1 * iy);
-    if (kVExact) rm_store_hi(Vm, t, j, v0, v1); else rm_store(Vm, t, j, v0, v1);
-    rm_store(DY, t, j, d0, d1);
-  }
-  // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
-  for (int e = tid; e < kD * (kD / 2); e += kNT) {
-    const int i = e >> 5, j = 2 * (e & 31);
-    const float2 s = s0 != nullptr ? __ldg(reinterpret_cast<const float2*>(s0 + i * kD + j)) : make_float2(0.f, 0.f);
-    rm_store(S0, i, j, s.x, s.y);
-    const float2 x = __ldg(reinterpret_cast<const float2*>(gend + i * kD + j));
-    const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
-    rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
-  }
-  __syncthreads();
-
-  // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
-  // M_rk = tril(R^ K~^T); 16 jobs of (product, m-tile, pair of n-tiles), K = 64
-  for (int job = warp; job < 16; job += 8) {
-    const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
-    const bool strict = prod < 2;
-    float acc[2][4] = {};
-    if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
-      const RM& X = prod < 2 ? Ah : Rh;
-      const RM& Y = (prod & 1) ? Kt : Bt;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = rm_a(X, mt, kk, lane);
-        FragB f0, f1;
-        rm_b2(Y, 2 * np, kk, lane, f0, f1);
-        mma3(acc[0], fa, f0);
-        mma3(acc[1], fa, f1);
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int nj = 2 * np + h;
-      const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
-      float c[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = tr + ((e >> 1) << 3), s = sc + (e & 1);
-        c[e] = (strict ? s < t : s <= t) ? acc[h][e] : 0.f;
-      }
-      if (prod == 0) {
-        *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
-        *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
-      } else {
-        rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- P3 || P4: warp 0 solves the diagonal blocks of T = (I - M_ab)^-1 (forward substitution, one column
-  // per lane: lanes 0-15 T11, lanes 16-31 T22); warps 1-7 form U = A^ S0^T + M_ak V and
-  // W = B~ Xb^T + M_rb^T DY (rows t, columns i): 16 jobs of (product, m-tile, 4 n-tiles)
-  if (warp == 0) {
-    const int off = lane < 16 ? 0 : 16;
-    const int c = lane & 15;
-    float x[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float acc = t == c ? 1.f : 0.f;
-#pragma unroll
-      for (int u = 0; u < t; ++u) acc = fmaf(Mab[(off + t) * SM + off + u], x[u], acc);
-      x[t] = acc;
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
-  } else {
-    for (int job = warp - 1; job < 16; job += 7) {
-      const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1
-      float acc[2][4] = {};
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = rm_a(prod == 0 ? Ah : Bt, mt, kk, lane);
-        FragB f0, f1;
-        rm_b2(prod == 0 ? S0 : Xb, 2 * nq, kk, lane, f0, f1);
-        mma3(acc[0], fa, f0);
-        mma3(acc[1], fa, f1);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        if (prod == 0) {  // M_ak V: V is B[k = u][n = i] = V[u][i]
-          const FragA fa = rm_a(Mak, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(Vm, 2 * nq, kk, lane, f0, f1, !kVExact);
-          if (kVExact) {
-            mma2b(acc[0], fa, f0);
-            mma2b(acc[1], fa, f1);
-          } else {
-            mma3(acc[0], fa, f0);
-            mma3(acc[1], fa, f1);
-          }
-        } else {  // M_rb^T DY
-          const FragA fa = rm_at(Mrb, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(DY, 2 * nq, kk, lane, f0, f1);
-          mma3(acc[0], fa, f0);
-          mma3(acc[1], fa, f1);
-        }
-      }
-      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq, lane, acc[0]);
-      rm_store_acc(prod == 0 ? U : W, mt, 2 * nq + 1, lane, acc[1]);
-    }
-  }
-  __syncthreads();
-  {  // E = A21 T11, then T21 = T22 E (A21 = M_ab[16..31][0..15])
-    const int t = tid >> 4, s = tid & 15;
-    float acc = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) acc = fmaf(Mab[(16 + t) * SM + u], TI[u * SM + s], acc);
-    E[t * 16 + s] = acc;
-  }
-  __syncthreads();
-  {
-    const int t = tid >> 4, s = tid & 15;
-    float acc = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * SM + 16 + u], E[u * 16 + s], acc);
-    TI[(16 + t) * SM + s] = acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < 32 * 16; e += kNT) {  // T (rows t, columns u), zero above the diagonal
-    const int t = e >> 4, u = 2 * (e & 15);
-    rm_store(Tm, t, u, u <= t ? TI[t * SM + u] : 0.f, u + 1 <= t ? TI[t * SM + u + 1] : 0.f);
-  }
-  __syncthreads();
-
-  // ---- P5: SA = T U, DSA = T^T W (rows t, columns i; K = 32); 16 jobs (product, m-tile, 4 n-tiles)
-  for (int job = warp; job < 16; job += 8) {
-    const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;
-    float acc[2][4] = {};
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      if (prod == 0 ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // T lower, T^T upper
-      const FragA fa = prod == 0 ? rm_a(Tm, mt, kk, lane) : rm_at(Tm, mt, kk, lane);
-      FragB f0, f1;
-      rm_bt2(prod == 0 ? U : W, 2 * nq, kk, lane, f0, f1);
-      mma3(acc[0], fa, f0);
-      mma3(acc[1], fa, f1);
-    }
-    rm_store_acc(prod == 0 ? SA : DSA, mt, 2 * nq, lane, acc[0]);
-    rm_store_acc(prod == 0 ? SA : DSA, mt, 2 * nq + 1, lane, acc[1]);
-  }
-  __syncthreads();
-
-  // ---- P6: L1 = tril(DY V^T), L2 = tril(DY SA^T), L3 = tril(DSA V^T, -1), L4 = tril(DSA SA^T, -1) (over U, W)
-  for (int job = warp; job < 16; job += 8) {
-    const int prod = job >> 2, mt = (job >> 1) & 1, np = job & 1;
-    const bool strict = prod >= 2;
-    const bool exactB = kVExact && (prod == 0 || prod == 2);
-    float acc[2][4] = {};
-    if (!(mt == 0 && np == 1)) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = rm_a(prod < 2 ? DY : DSA, mt, kk, lane);
-        FragB f0, f1;
-        rm_b2((prod & 1) ? SA : Vm, 2 * np, kk, lane, f0, f1, !exactB);
-        if (exactB) {
-          mma2b(acc[0], fa, f0);
-          mma2b(acc[1], fa, f1);
-        } else {
-          mma3(acc[0], fa, f0);
-          mma3(acc[1], fa, f1);
-        }
-      }
-    }
-    const RM& Lx = prod == 0 ? L1 : (prod == 1 ? L2 : (prod == 2 ? L3 : L4));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int nj = 2 * np + h;
-      float c[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = mt * 16 + g + ((e >> 1) << 3), s = nj * 8 + 2 * q + (e & 1);
-        c[e] = (strict ? s < t : s <= t) ? acc[h][e] : 0.f;
-      }
-      rm_store_acc(Lx, mt, nj, lane, c);
-    }
-  }
-  __syncthreads();
-
-  // ---- P7: DR, DA, DK, DB, DV (rows t, columns j or i): 20 jobs of (product, m-tile, 4 n-tiles), each a
-  // K = 64 product with S0 / Xb plus the masked products; held in registers until every warp is done
-  float res[3][4][4];
-#pragma unroll
-  for (int rep = 0; rep < 3; ++rep) {
-    const int job = warp + 8 * rep;
-    float (&acc)[4][4] = res[rep];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-    if (job >= 20) continue;
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
-    if (prod < 4) {
-      const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
-      const RM& B1 = prod < 2 ? S0 : Xb;
-      const bool exactA = kVExact && prod == 2;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          FragB f0, f1;
-          rm_bt2(B1, 4 * nh + 2 * p2, kk, lane, f0, f1);
-          if (exactA) {
-            mma2(acc[2 * p2], fa, f0);
-            mma2(acc[2 * p2 + 1], fa, f1);
-          } else {
-            mma3(acc[2 * p2], fa, f0);
-            mma3(acc[2 * p2 + 1], fa, f1);
-          }
-        }
-      }
-      // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
-      // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int blk = kq >> 1, kk = kq & 1;
-        const bool lowerA = prod < 2;
-        if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
-        const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
-        const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
-        const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          FragB f0, f1;
-          rm_bt2(BB, 4 * nh + 2 * p2, kk, lane, f0, f1);
-          mma3(acc[2 * p2], fa, f0);
-          mma3(acc[2 * p2 + 1], fa, f1);
-        }
-      }
-    } else {
-      // DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY (rows t, columns i)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = rm_a(Kt, mt, kk, lane);
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          FragB f0, f1;
-          rm_b2(Xb, 4 * nh + 2 * p2, kk, lane, f0, f1);
-          mma3(acc[2 * p2], fa, f0);
-          mma3(acc[2 * p2 + 1], fa, f1);
-        }
-      }
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int blk = kq >> 1, kk = kq & 1;
-        if (mt == 1 && kk == 0) continue;  // M_ak^T, M_rk^T upper triangular
-        const FragA fa = rm_at(blk ? Mrk : Mak, mt, kk, lane);
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          FragB f0, f1;
-          rm_bt2(blk ? DY : DSA, 4 * nh + 2 * p2, kk, lane, f0, f1);
-          mma3(acc[2 * p2], fa, f0);
-          mma3(acc[2 * p2 + 1], fa, f1);
-        }
-      }
-    }
-  }
-  __syncthreads();  // every operand has been read: stage over A^ .. Xb
-  float* stage = reinterpret_cast<float*>(sm + LY::oStage);
-#pragma unroll
-  for (int rep = 0; rep < 3; ++rep) {
-    const int job = warp + 8 * rep;
-    if (job >= 20) continue;
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
-    float* st = stage + prod * kL * kD;
-    // DR, DA, DK, DB times their own input (r, a, k, b) for the dw recurrence
-    float* sp = stage + (5 + (prod & 3)) * kL * kD;
-    const Tin* inp = prod == 0 ? r : (prod == 1 ? a : (prod == 2 ? k : b));
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int j = (4 * nh + x) * 8 + 2 * q;
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int t = mt * 16 + g + 8 * hr;
-        const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
-        const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
-        float2 sc;
-        if (prod == 0) sc = gt;
-        else if (prod == 1) sc = gp;
-        else if (prod < 4) sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
-        else sc = make_float2(1.f, 1.f);
-        const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
-        *reinterpret_cast<float2*>(st + t * kD + j) = o;
-        if (prod < 4) {
-          float2 in = make_float2(0.f, 0.f);
-          if (t < n) {
-            const size_t gi = base + (size_t)(t0 + t) * tstride + j;
-            in = make_float2(to_f32(inp[gi]), to_f32(inp[gi + 1]));
-          }
-          *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- P8: write dr, da, dk, db, dv; dw by the column recurrence of Z_t = colsum(X_t o S_t)
-  {
-    const float* sDR = stage;
-    const float* sDA = stage + kL * kD;
-    const float* sDK = stage + 2 * kL * kD;
-    const float* sDB = stage + 3 * kL * kD;
-    const float* sDV = stage + 4 * kL * kD;
-    const float* sRDR = stage + 5 * kL * kD;
-    const float* sADA = stage + 6 * kL * kD;
-    const float* sKDK = stage + 7 * kL * kD;
-    const float* sBDB = stage + 8 * kL * kD;
-    for (int e = tid; e < n * (kD / 4); e += kNT) {
-      const int t = e >> 4, c = (e & 15) * 4;
-      const size_t o = base + (size_t)(t0 + t) * tstride + c;
-      *reinterpret_cast<float4*>(dr + o) = *reinterpret_cast<const float4*>(sDR + t * kD + c);
-      *reinterpret_cast<float4*>(da + o) = *reinterpret_cast<const float4*>(sDA + t * kD + c);
-      *reinterpret_cast<float4*>(dk + o) = *reinterpret_cast<const float4*>(sDK + t * kD + c);
-      *reinterpret_cast<float4*>(db + o) = *reinterpret_cast<const float4*>(sDB + t * kD + c);
-      *reinterpret_cast<float4*>(dv + o) = *reinterpret_cast<const float4*>(sDV + t * kD + c);
-    }
-    if (tid < kD) {
-      const int j = tid;
-      // Z_{n-1} = colsum(X_e o S_e) with X_e = G + dy_{n-1} r_{n-1}^T: the r_{n-1} o dr_{n-1} term
-      float Z = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * kD + j];
-      for (int t = n - 1; t >= 0; --t) {
-        const float wdw = Z - sKDK[t * kD + j] - sBDB[t * kD + j];
-        dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
-        Z = wdw + sADA[t * kD + j] + (t > 0 ? sRDR[(t - 1) * kD + j] : 0.f);
-      }
-    }
+    __syncthreads();  // the next flagged chunk reuses the buffers
   }
 }
 
 template <typename Tin>
-cudaError_t launch_colmat_t(const BwdArgs& p, const float* xck_ws, cudaStream_t stream) {
+cudaError_t launch_colmat_t(const BwdArgs& p, const ChunkEnds& ends, cudaStream_t stream) {
   using LY = Lay<Tin>;
+  using FL = FbLay<Tin>;
   static_assert(LY::kBytes <= 232448, "shared memory per CTA");
   auto kern = colmat_kernel<Tin>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
   if (err != cudaSuccess) return err;
-  const unsigned grid = (unsigned)p.B * p.H * p.nchunks;
-  kern<<<grid, kNT, LY::kBytes, stream>>>(p.T, p.H, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w,
-                                          (const Tin*)p.in.k, (const Tin*)p.in.v, (const Tin*)p.in.a,
-                                          (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, xck_ws, p.dr, p.dw, p.dk, p.dv,
-                                          p.da, p.db);
+  const int total = p.B * p.H * p.nchunks;
+  kern<<<(unsigned)total, kNT, LY::kBytes, stream>>>(
+      p.T, p.H, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
+      (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, p.dr, p.dw, p.dk,
+      p.dv, p.da, p.db);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  auto fkern = colfb_kernel<Tin>;
+  err = cudaFuncSetAttribute(fkern, cudaFuncAttributeMaxDynamicSharedMemorySize, FL::kBytes);
+  if (err != cudaSuccess) return err;
+  const int grid = min(total, 2 * num_sms());
+  fkern<<<(unsigned)grid, kNTF, FL::kBytes, stream>>>(
+      p.T, p.H, p.nchunks, total, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
+      (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, p.dr, p.dw, p.dk,
+      p.dv, p.da, p.db);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_colgrad_matrix(const BwdArgs& p, const float* xck_ws, cudaStream_t stream) {
+cudaError_t launch_colgrad_matrix(const BwdArgs& p, const ChunkEnds& ends, cudaStream_t stream) {
   if (p.nchunks == 0) return cudaSuccess;
-  return p.bf16 ? launch_colmat_t<__nv_bfloat16>(p, xck_ws, stream) : launch_colmat_t<float>(p, xck_ws, stream);
+  return p.bf16 ? launch_colmat_t<__nv_bfloat16>(p, ends, stream) : launch_colmat_t<float>(p, ends, stream);
 }
 
 }  // namespace wkv7

@@ -73,18 +73,25 @@ cudaError_t launch_gwalk_chunked(const BwdArgs& a, float* dsa_ws, float* xck_ws,
 // (B,H,C,D,D), dh0
 cudaError_t launch_forward_transition(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_gwalk_transition(const BwdArgs& a, float* xck_ws, cudaStream_t stream);
-// the transition operands of every 32-token chunk (B', K', C, P, gamma_31, flag; transition_ops_bytes()
-// bytes, 256-byte aligned), the forward chain reading them, and the backward's walk over the same chunks
-// writing G (the gradient w.r.t. the state after each chunk from every later token) into g_ends (B,H,C,D,D)
-size_t transition_ops_bytes(int B, int T, int H);
-cudaError_t launch_transition_ops(const FwdArgs& a, unsigned char* ops, cudaStream_t stream);
-cudaError_t launch_forward_from_ops(const FwdArgs& a, const unsigned char* ops, cudaStream_t stream);
-cudaError_t launch_walk_from_ops(const BwdArgs& a, const unsigned char* ops, float* g_ends, cudaStream_t stream);
+// the chunk operators (wkv7_xop.cu): a workspace of xop_workspace_bytes() bytes, 256-byte aligned (a status
+// word, then one 40 KB operator block per (head, chunk)).  The forward: operators, then the chain writing y,
+// h_ckpt and hT.  The walk: operators, then the chain writing G (the gradient w.r.t. the state after each
+// chunk from every later token) over the blocks (returned as g_ends with a stride of g_stride floats per
+// chunk) and dh0.  rows = state rows per chain CTA (16, 32 or 64; 0 picks by the head count).
+size_t xop_workspace_bytes(int B, int T, int H);
+cudaError_t launch_xop_forward(const FwdArgs& a, void* workspace, int rows, cudaStream_t stream);
+// what the walk leaves per chunk c of head bh (at (bh * C + c) * stride from each pointer): G, and one int
+// of scratch for the column kernels
+struct ChunkEnds {
+  const float* g;
+  int* flags;
+  size_t stride;
+};
+cudaError_t launch_xop_walk(const BwdArgs& a, void* workspace, int rows, ChunkEnds* ends, cudaStream_t stream);
 // the column gradients dr, dw, dk, dv, da, db of every 32-token chunk in matrix form, from G at the chunk
-// ends, the checkpoints and the inputs (no saved sa)
-cudaError_t launch_colgrad_matrix(const BwdArgs& a, const float* g_ends, cudaStream_t stream);
-// the backward without a saved sa at chunk 32: operands, walk, matrix column gradients; the workspace holds
-// the operands then G at the chunk ends
+// ends, the checkpoints and the inputs (no saved sa); chunks with tiny decays token by token
+cudaError_t launch_colgrad_matrix(const BwdArgs& a, const ChunkEnds& ends, cudaStream_t stream);
+// the backward without a saved sa at chunk 32: operators, walk, matrix column gradients
 cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, cudaStream_t stream);
 // bytes of the forward's workspace (the transition operands)
 size_t forward_workspace_bytes(int B, int T, int H, int chunk);

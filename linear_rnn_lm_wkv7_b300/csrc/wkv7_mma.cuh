@@ -210,6 +210,13 @@ __device__ __forceinline__ FragA rm_at(const RM& x, int mt, int kk, int lane) {
   ldsm4<true>(f.l, x.p + x.lo + off);
   return f;
 }
+__device__ __forceinline__ FragA rm_at_hi(const RM& x, int mt, int kk, int lane) {
+  const int off = (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + mt * 16 + ((lane >> 3) & 1) * 8;
+  FragA f;
+  ldsm4<true>(f.h, x.p + off);
+  f.l[0] = f.l[1] = f.l[2] = f.l[3] = 0u;
+  return f;
+}
 // B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = X[n][k] (a product "times X^T")
 __device__ __forceinline__ void rm_b2(const RM& x, int nt, int kk, int lane, FragB& b0, FragB& b1, bool with_lo = true) {
   const int off = (nt * 8 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + kk * 16 + ((lane >> 3) & 1) * 8;
@@ -258,6 +265,73 @@ __device__ __forceinline__ void rm_store8(const RM& x, int r, int c, const float
 __device__ __forceinline__ float2 rm_get2(const RM& x, int r, int c) {
   return join2(*reinterpret_cast<const uint32_t*>(x.p + r * x.ld + c),
                *reinterpret_cast<const uint32_t*>(x.p + x.lo + r * x.ld + c));
+}
+// fp32 value (hi + lo) at (r, c)
+__device__ __forceinline__ float rm_get1(const RM& x, int r, int c) {
+  return __bfloat162float(x.p[r * x.ld + c]) + __bfloat162float(x.p[x.lo + r * x.ld + c]);
+}
+// 8 values to row r, columns c..c+7 of an exact-bf16 operand (hi only): one 16-byte store
+__device__ __forceinline__ void rm_store8_hi(const RM& x, int r, int c, const float (&v)[8]) {
+  uint4 h;
+  h.x = pack_bf16(v[0], v[1]);
+  h.y = pack_bf16(v[2], v[3]);
+  h.z = pack_bf16(v[4], v[5]);
+  h.w = pack_bf16(v[6], v[7]);
+  *reinterpret_cast<uint4*>(x.p + r * x.ld + c) = h;
+}
+// d[i] += A B[i] for split A and B, i < N: the three bf16 passes each over all N accumulators, so that
+// dependent mma into one accumulator are N instructions apart
+template <int N>
+__device__ __forceinline__ void mma3n(float (&d)[N][4], const FragA& a, const FragB (&b)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) mma16816(d[i], a.l, b[i].h[0], b[i].h[1]);
+#pragma unroll
+  for (int i = 0; i < N; ++i) mma16816(d[i], a.h, b[i].l[0], b[i].l[1]);
+#pragma unroll
+  for (int i = 0; i < N; ++i) mma16816(d[i], a.h, b[i].h[0], b[i].h[1]);
+}
+// ... for an exact-bf16 A (hi only)
+template <int N>
+__device__ __forceinline__ void mma2n(float (&d)[N][4], const FragA& a, const FragB (&b)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) mma16816(d[i], a.h, b[i].l[0], b[i].l[1]);
+#pragma unroll
+  for (int i = 0; i < N; ++i) mma16816(d[i], a.h, b[i].h[0], b[i].h[1]);
+}
+// two products at once, d0[i] += A0 B0[i] and d1[i] += A1 B1[i] (all split), pass by pass over both
+template <int N>
+__device__ __forceinline__ void mma3n_two(float (&d0)[N][4], const FragA& a0, const FragB (&b0)[N], float (&d1)[N][4],
+                                          const FragA& a1, const FragB (&b1)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.l, b0[i].h[0], b0[i].h[1]);
+    mma16816(d1[i], a1.l, b1[i].h[0], b1[i].h[1]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.h, b0[i].l[0], b0[i].l[1]);
+    mma16816(d1[i], a1.h, b1[i].l[0], b1[i].l[1]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.h, b0[i].h[0], b0[i].h[1]);
+    mma16816(d1[i], a1.h, b1[i].h[0], b1[i].h[1]);
+  }
+}
+// ... with an exact-bf16 B (hi only) shared by both: d0[i] += A0 B[i], d1[i] += A1 B[i]
+template <int N>
+__device__ __forceinline__ void mma2b_two(float (&d0)[N][4], const FragA& a0, float (&d1)[N][4], const FragA& a1,
+                                          const FragB (&b)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.l, b[i].h[0], b[i].h[1]);
+    mma16816(d1[i], a1.l, b[i].h[0], b[i].h[1]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.h, b[i].h[0], b[i].h[1]);
+    mma16816(d1[i], a1.h, b[i].h[0], b[i].h[1]);
+  }
 }
 // d += A B for split A and an exact-bf16 B (hi only)
 __device__ __forceinline__ void mma2b(float (&d)[4], const FragA& a, const FragB& b) {

@@ -1,0 +1,1008 @@
+// WKV7 on sm_103a as chunk operators: every 32-token chunk's transition operator at once (a parallel
+// kernel over all heads and chunks), then a short serial chain per head that applies them.
+//
+// Recurrence ("RWKV-7 Pretraining on Apple Silicon (MLX)", section "Metal kernel architecture",
+// Forward and Backward listings), per head, state S (rows i = value, columns j = key):
+//     sa_t = S_{t-1} a_t;   S_t = S_{t-1} diag(w_t) + v_t k_t^T + sa_t b_t^T = S_{t-1} M_t + v_t k_t^T;
+//     y_t = S_t r_t,        M_t = diag(w_t) + a_t b_t^T.
+// Over a chunk of n <= 32 tokens from the state S_c before it, with A_{<=t} = M_0 .. M_t:
+//     S_t = S_c A_{<=t} + U_{<=t},   U_{<=t} = sum_{s<=t} v_s k_s^T M_{s+1} .. M_t
+//     S_end = S_c A_c + U_c          (A_c = A_{<=n-1}, U_c = U_{<=n-1})
+//     Y_c^T = S_c Q_c + Y_intra^T    (column t of Q_c: A_{<=t} r_t; row t of Y_intra: U_{<=t} r_t)
+// and the backward's state gradient (G: w.r.t. the state after the chunk, from every later token)
+//     G_prev = G A_c^T + E_c,        E_c = DY^T Q_c^T   (row t of DY: dy_t).
+// The operators in closed form (gamma_t = w_0 o .. o w_t per column, gamma_L = gamma_31, steps past n
+// padded with w = 1 and zero inputs):
+//     A^_t = a_t o gamma_{t-1},  R^_t = r_t o gamma_t,  K~_t = k_t / gamma_t,  B~_t = b_t / gamma_t,
+//     M_ab = tril(A^ B~^T, -1), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T), M_rk = tril(R^ K~^T),
+//     T = (I - M_ab)^-1,  B' = (T^T B~) diag(gamma_L),  C = M_rb T,
+//     K' = K~ diag(gamma_L) + M_ak^T B',  P = M_rk + C M_ak,
+//     A_c = diag(gamma_L) + A^^T B',  U_c = V^T K',  Q_c = (R^ + C A^)^T,  Y_intra = P V.
+// (Unrolled over the chunk, sa is coupled through the unit lower-triangular system I - M_ab; T
+// eliminates it.)  A chunk whose gamma_L falls below 1e-20 in some column, or is not finite, forms the
+// same operators token by token instead (rows of A_c and U_c run the recurrence from I and 0), which
+// divides by nothing.
+//
+// xop_prep_kernel: one CTA per (head, chunk), all chunks at once; writes A_c, Q_c (bf16 hi + lo), and
+// U_c (forward; Y_intra into y) or E_c (backward), per chunk, into an operator block.
+// xop_chain_kernel: one CTA per (head, block of R state rows); a producer warp streams the chunks'
+// operator blocks into a ring of shared-memory stages with cp.async.bulk (one mbarrier per stage and
+// direction); R / 16 chain warps hold 16 state rows each as mma accumulators and apply
+//     forward: y_c += S Q_c;  S = S A_c + U_c  (checkpoint after every chunk)
+//     walk:    G_c written;   G = G A_c^T + E_c (G_c over E_c's block; dh0 at the end).
+// Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
+// fp32 accumulation (wkv7_mma.cuh).  Waits are bounded in time: past the limit a kernel sets the status
+// word and returns.
+#include "wkv7_device.cuh"
+#include "wkv7_launch.h"
+#include "wkv7_mma.cuh"
+
+namespace wkv7 {
+namespace {
+
+using namespace mma;
+
+constexpr int kL = 32;
+constexpr int kLD64 = 72;
+constexpr int kLD32 = 40;
+constexpr float kMinGamma = 1e-20f;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
+
+// ---- per-chunk operator block (bytes).  A_c and Q_c: bf16 hi array then lo array, rows unpadded, the
+// 16-byte pieces of row j permuted (piece p stored at p ^ (j & 7) for A, p ^ ((j >> 1) & 3) for Q) so
+// that ldmatrix reads of eight rows hit eight distinct bank groups.  X: U_c or E_c (fp32) in mma
+// accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4]; the walk overwrites it with G in
+// plain row-major order (the same 4 KB per 16 rows).
+constexpr int kXA = 0;
+constexpr int kXQ = 16384;
+constexpr int kXX = 24576;
+constexpr int kXBytes = 40960;
+constexpr int kXHead = 256;  // status word(s) before the first block
+
+__host__ __device__ __forceinline__ int swz_a(int j, int jp) { return j * 64 + (((jp >> 3) ^ (j & 7)) << 3) + (jp & 7); }
+__host__ __device__ __forceinline__ int swz_q(int j, int t) {
+  return j * 32 + (((t >> 3) ^ ((j >> 1) & 3)) << 3) + (t & 7);
+}
+// index (floats) of element (i, j) of a 64 x 64 matrix in mma accumulator order
+__host__ __device__ __forceinline__ int frag_idx(int i, int j) {
+  const int r = i & 15, c = j & 7;
+  const int lane = (r & 7) * 4 + (c >> 1);
+  const int e = (r >> 3) * 2 + (c & 1);
+  return ((((i >> 4) * 8 + (j >> 3)) * 32 + lane) << 2) + e;
+}
+
+__host__ __device__ constexpr int rmb(int rows, int ld) { return 2 * rows * ld * 2; }
+
+// ======================================================================================= prep
+
+constexpr int kNTP = 256;
+
+template <typename Tin, bool BWD>
+struct XPrepLay {
+  // region X: raw inputs + gamma first, then the coupling matrices
+  static constexpr int kRawN = BWD ? 4 : 6;  // w, a, b, r (, k, v)
+  static constexpr int kRaw = kRawN * kL * kD * (int)sizeof(Tin);
+  static constexpr int oRaw = 0;
+  static constexpr int oDyRaw = kRaw;  // backward: dy fp32 [32][64]
+  static constexpr int oG = oDyRaw + (BWD ? kL * kD * 4 : 0);
+  static constexpr int kXa = oG + kL * kD * 4;
+  static constexpr int kSM = 36;
+  static constexpr int oMab = 0;                        // fp32 [32][36]
+  static constexpr int oTI = oMab + 32 * kSM * 4;       // fp32 [32][36]
+  static constexpr int oE = oTI + 32 * kSM * 4;         // fp32 [16][16]
+  static constexpr int oMak = oE + 16 * 16 * 4;         // RM 32 x 32 each
+  static constexpr int oMrb = oMak + rmb(32, kLD32);
+  static constexpr int oMrk = oMrb + rmb(32, kLD32);
+  static constexpr int oT = oMrk + rmb(32, kLD32);
+  static constexpr int kXb = oT + rmb(32, kLD32);
+  static constexpr int kX = ((kXa > kXb ? kXa : kXb) + 127) / 128 * 128;
+  // long-lived operands
+  static constexpr int oAh = kX;
+  static constexpr int oRh = oAh + rmb(32, kLD64);
+  static constexpr int oBt = oRh + rmb(32, kLD64);  // B~, then K' (forward)
+  static constexpr int oKt = oBt + rmb(32, kLD64);  // K~ (forward) or DY (backward)
+  static constexpr int oV = oKt + rmb(32, kLD64);   // V (forward; hi only for bf16 inputs)
+  static constexpr int kV = BWD ? 0 : (sizeof(Tin) == 2 ? 32 * kLD64 * 2 : rmb(32, kLD64));
+  static constexpr int oBp = oV + kV;
+  static constexpr int oC = oBp + rmb(32, kLD64);
+  static constexpr int oP = oC + rmb(32, kLD32);  // P (forward) or Q as RM [64 j][32 t] (backward)
+  static constexpr int kP = BWD ? rmb(64, kLD32) : rmb(32, kLD32);
+  static constexpr int oGL = oP + kP;  // fp32 [64], then int [4]
+  static constexpr int kBytes = oGL + 64 * 4 + 16;
+  // token-by-token path: q_t as fp32 [64 j][33] over A^
+  static constexpr int oQf = oAh;
+  static_assert(64 * 33 * 4 <= rmb(32, kLD64), "q_t fit over A^");
+};
+
+template <typename Tin, bool BWD>
+__global__ void __launch_bounds__(kNTP)
+xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
+                const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
+                const Tin* __restrict__ b, const float* __restrict__ dy, unsigned char* __restrict__ ops,
+                float* __restrict__ y, unsigned* __restrict__ status) {
+  using LY = XPrepLay<Tin, BWD>;
+  constexpr int SM = LY::kSM;
+  constexpr bool kVExact = sizeof(Tin) == 2;
+  extern __shared__ float4 smem4[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
+  const int ci = blockIdx.x % nchunks;
+  const int bh = blockIdx.x / nchunks;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int t0 = ci * kL;
+  const int nm = min(kL, T - t0);
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
+  __nv_bfloat16* gA = reinterpret_cast<__nv_bfloat16*>(blk + kXA);
+  __nv_bfloat16* gQ = reinterpret_cast<__nv_bfloat16*>(blk + kXQ);
+  float* gX = reinterpret_cast<float*>(blk + kXX);
+  if (blockIdx.x == 0 && tid == 0 && status != nullptr) *status = 0u;
+
+  auto bfp = [&](int off) { return reinterpret_cast<__nv_bfloat16*>(sm + off); };
+  const RM Ah{bfp(LY::oAh), 32 * kLD64, kLD64}, Rh{bfp(LY::oRh), 32 * kLD64, kLD64};
+  const RM Bt{bfp(LY::oBt), 32 * kLD64, kLD64}, Kt{bfp(LY::oKt), 32 * kLD64, kLD64};
+  const RM Kp = Bt, DYm = Kt;
+  const RM Vm{bfp(LY::oV), kVExact ? 0 : 32 * kLD64, kLD64};
+  const RM Bp{bfp(LY::oBp), 32 * kLD64, kLD64};
+  const RM Cm{bfp(LY::oC), 32 * kLD32, kLD32};
+  const RM Pm{bfp(LY::oP), 32 * kLD32, kLD32};
+  const RM Qs{bfp(LY::oP), 64 * kLD32, kLD32};
+  const RM Mak{bfp(LY::oMak), 32 * kLD32, kLD32}, Mrb{bfp(LY::oMrb), 32 * kLD32, kLD32};
+  const RM Mrk{bfp(LY::oMrk), 32 * kLD32, kLD32}, Tm{bfp(LY::oT), 32 * kLD32, kLD32};
+  float* G = reinterpret_cast<float*>(sm + LY::oG);
+  float* GL = reinterpret_cast<float*>(sm + LY::oGL);
+  int* meta = reinterpret_cast<int*>(sm + LY::oGL + 256);
+  Tin* raw = reinterpret_cast<Tin*>(sm + LY::oRaw);
+  const Tin* rw = raw;
+  const Tin* ra = raw + kL * kD;
+  const Tin* rbv = raw + 2 * kL * kD;
+  const Tin* rr = raw + 3 * kL * kD;
+  const Tin* rk = raw + 4 * kL * kD;
+  const Tin* rv = raw + 5 * kL * kD;
+  float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
+  float* Mab = reinterpret_cast<float*>(sm + LY::oMab);
+  float* TI = reinterpret_cast<float*>(sm + LY::oTI);
+  float* E = reinterpret_cast<float*>(sm + LY::oE);
+
+  {  // the chunk's inputs (rows past the chunk are not copied)
+    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+    constexpr int EPC = 16 / (int)sizeof(Tin);
+    const Tin* srcs[6] = {w, a, b, r, k, v};
+#pragma unroll
+    for (int s6 = 0; s6 < LY::kRawN; ++s6)
+      for (int e = tid; e < nm * CPR; e += kNTP) {
+        const int t = e / CPR, pc = e % CPR;
+        cp_async16(raw + (s6 * kL + t) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + t) * tstride + pc * EPC);
+      }
+    if (BWD)
+      for (int e = tid; e < nm * (kD / 4); e += kNTP) {
+        const int t = e >> 4, pc = e & 15;
+        cp_async16(dyr + t * kD + pc * 4, dy + base + (size_t)(t0 + t) * tstride + pc * 4);
+      }
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+
+  if (tid < kD) {  // gamma_t down each column; the token-by-token flag
+    const int j = tid;
+    float gm = 1.f;
+#pragma unroll 8
+    for (int t = 0; t < kL; ++t) {
+      const float wt = t < nm ? to_f32(rw[t * kD + j]) : 1.f;
+      gm *= wt;
+      G[t * kD + j] = gm;
+    }
+    GL[j] = gm;
+    const bool bad = !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+    const unsigned any = __ballot_sync(0xffffffffu, bad);
+    if (lane == 0) meta[warp] = any != 0u;
+  }
+  __syncthreads();
+
+  if ((meta[0] | meta[1]) != 0) {
+    // ======== token by token: rows j of A_c from e_j (threads 0-63), rows i of U_c from 0 (64-127, forward)
+    float* Qf = reinterpret_cast<float*>(sm + LY::oQf);
+    if (tid < 64) {
+      const int j = tid;
+      float x[64];
+#pragma unroll
+      for (int u = 0; u < 64; ++u) x[u] = u == j ? 1.f : 0.f;
+      for (int t = 0; t < nm; ++t) {
+        float d = 0.f;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) d = fmaf(x[u], to_f32(ra[t * kD + u]), d);
+        float qv = 0.f;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          x[u] = fmaf(x[u], to_f32(rw[t * kD + u]), d * to_f32(rbv[t * kD + u]));
+          qv = fmaf(x[u], to_f32(rr[t * kD + u]), qv);
+        }
+        Qf[j * 33 + t] = qv;
+      }
+      for (int t = nm; t < kL; ++t) Qf[j * 33 + t] = 0.f;
+#pragma unroll
+      for (int p8 = 0; p8 < 8; ++p8) {
+        uint4 h, l;
+        split2(x[p8 * 8 + 0], x[p8 * 8 + 1], h.x, l.x);
+        split2(x[p8 * 8 + 2], x[p8 * 8 + 3], h.y, l.y);
+        split2(x[p8 * 8 + 4], x[p8 * 8 + 5], h.z, l.z);
+        split2(x[p8 * 8 + 6], x[p8 * 8 + 7], h.w, l.w);
+        *reinterpret_cast<uint4*>(gA + swz_a(j, p8 * 8)) = h;
+        *reinterpret_cast<uint4*>(gA + 4096 + swz_a(j, p8 * 8)) = l;
+      }
+    } else if (!BWD && tid < 128) {
+      const int i = tid - 64;
+      float u8[64];
+#pragma unroll
+      for (int u = 0; u < 64; ++u) u8[u] = 0.f;
+      for (int t = 0; t < nm; ++t) {
+        float d = 0.f;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) d = fmaf(u8[u], to_f32(ra[t * kD + u]), d);
+        const float vi = to_f32(rv[t * kD + i]);
+        float yv = 0.f;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          u8[u] = fmaf(u8[u], to_f32(rw[t * kD + u]), fmaf(vi, to_f32(rk[t * kD + u]), d * to_f32(rbv[t * kD + u])));
+          yv = fmaf(u8[u], to_f32(rr[t * kD + u]), yv);
+        }
+        y[base + (size_t)(t0 + t) * tstride + i] = yv;
+      }
+#pragma unroll
+      for (int u = 0; u < 64; ++u) gX[frag_idx(i, u)] = u8[u];
+    }
+    __syncthreads();
+    if (!BWD) {
+      for (int e = tid; e < 64 * 4; e += kNTP) {  // Q_c rows j, 8 tokens per piece
+        const int j = e >> 2, p4 = e & 3;
+        const float* src = Qf + j * 33 + p4 * 8;
+        uint4 h, l;
+        split2(src[0], src[1], h.x, l.x);
+        split2(src[2], src[3], h.y, l.y);
+        split2(src[4], src[5], h.z, l.z);
+        split2(src[6], src[7], h.w, l.w);
+        *reinterpret_cast<uint4*>(gQ + swz_q(j, p4 * 8)) = h;
+        *reinterpret_cast<uint4*>(gQ + 2048 + swz_q(j, p4 * 8)) = l;
+      }
+    } else {
+      for (int e = tid; e < 64 * 64; e += kNTP) {  // E_c[i][j] = sum_t dy_t[i] q_t[j]
+        const int i = e >> 6, j = e & 63;
+        float s = 0.f;
+        for (int t = 0; t < nm; ++t) s = fmaf(dyr[t * kD + i], Qf[j * 33 + t], s);
+        gX[frag_idx(i, j)] = s;
+      }
+    }
+    return;
+  }
+
+  {  // one (token, 8 columns) block per thread: A^, R^, B~, and K~, V (forward) or DY (backward)
+    const int t = tid >> 3, c0 = (tid & 7) * 8;
+    const bool ok = t < nm;
+    float gt[8], gp[8], av[8], rv8[8], bv[8];
+    raw8(G + t * kD + c0, gt);
+    if (t > 0) {
+      raw8(G + (t - 1) * kD + c0, gp);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) gp[u] = 1.f;
+    }
+    raw8(ra + t * kD + c0, av);
+    raw8(rr + t * kD + c0, rv8);
+    raw8(rbv + t * kD + c0, bv);
+    float oa[8], orr[8], ob[8], ig[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      ig[u] = __fdividef(1.f, gt[u]);
+      oa[u] = ok ? av[u] * gp[u] : 0.f;
+      orr[u] = ok ? rv8[u] * gt[u] : 0.f;
+      ob[u] = ok ? bv[u] * ig[u] : 0.f;
+    }
+    rm_store8(Ah, t, c0, oa);
+    rm_store8(Rh, t, c0, orr);
+    rm_store8(Bt, t, c0, ob);
+    if (!BWD) {
+      float kv[8], vv[8], ok8[8];
+      raw8(rk + t * kD + c0, kv);
+      raw8(rv + t * kD + c0, vv);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ok8[u] = ok ? kv[u] * ig[u] : 0.f;
+        vv[u] = ok ? vv[u] : 0.f;
+      }
+      rm_store8(Kt, t, c0, ok8);
+      if (kVExact) rm_store8_hi(Vm, t, c0, vv); else rm_store8(Vm, t, c0, vv);
+    } else {
+      float d8[8];
+      raw8(dyr + t * kD + c0, d8);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) d8[u] = ok ? d8[u] : 0.f;
+      rm_store8(DYm, t, c0, d8);
+    }
+  }
+  __syncthreads();  // raw inputs and gamma consumed: the coupling matrices reuse their space
+
+  // M_ab = tril(A^ B~^T, -1) (fp32), M_rb = tril(R^ B~^T), and (forward) M_ak = tril(A^ K~^T, -1),
+  // M_rk = tril(R^ K~^T)
+  {
+    constexpr int NP = BWD ? 2 : 4;
+    for (int job = warp; job < NP * 4; job += 8) {
+      const int prod = BWD ? 2 * (job >> 2) : (job >> 2);
+      const int mt = (job >> 1) & 1, np = job & 1;
+      const bool strict = prod < 2;
+      float acc[2][4] = {};
+      if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
+        const RM& X = prod < 2 ? Ah : Rh;
+        const RM& Y = (prod & 1) ? Kt : Bt;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const FragA fa = rm_a(X, mt, kk, lane);
+          FragB f0, f1;
+          rm_b2(Y, 2 * np, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nj = 2 * np + h;
+        const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+        float c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tt = tr + ((e >> 1) << 3), s = sc + (e & 1);
+          c[e] = (strict ? s < tt : s <= tt) ? acc[h][e] : 0.f;
+        }
+        if (prod == 0) {
+          *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+          *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
+        } else {
+          rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // T = (I - M_ab)^-1 by blocks of 16: diagonal blocks by forward substitution (one column per lane),
+  // then T21 = T22 A21 T11
+  if (warp == 0) {
+    const int off = lane < 16 ? 0 : 16;
+    const int c = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float acc = t == c ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) acc = fmaf(Mab[(off + t) * SM + off + u], x[u], acc);
+      x[t] = acc;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
+  }
+  __syncthreads();
+  {
+    const int t = tid >> 4, s = tid & 15;
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc = fmaf(Mab[(16 + t) * SM + u], TI[u * SM + s], acc);
+    E[t * 16 + s] = acc;
+  }
+  __syncthreads();
+  {
+    const int t = tid >> 4, s = tid & 15;
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * SM + 16 + u], E[u * 16 + s], acc);
+    TI[(16 + t) * SM + s] = acc;
+  }
+  __syncthreads();
+  if (tid < 128) {
+    const int t = tid >> 2, u0 = (tid & 3) * 8;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = u0 + e <= t ? TI[t * SM + u0 + e] : 0.f;
+    rm_store8(Tm, t, u0, x);
+  }
+  __syncthreads();
+
+  // B' = (T^T B~) diag(gamma_L) and C = M_rb T
+  for (int job = warp; job < 12; job += 8) {
+    float acc[2][4] = {};
+    if (job < 8) {
+      const int mt = job >> 2, nq = job & 3;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (mt == 1 && kk == 0) continue;
+        const FragA fa = rm_at(Tm, mt, kk, lane);
+        FragB f0, f1;
+        rm_bt2(Bt, 2 * nq, kk, lane, f0, f1);
+        {
+          const FragB fb2[2] = {f0, f1};
+          mma3n<2>(acc, fa, fb2);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 gl = *reinterpret_cast<const float2*>(GL + (2 * nq + h) * 8 + 2 * q);
+        acc[h][0] *= gl.x; acc[h][1] *= gl.y; acc[h][2] *= gl.x; acc[h][3] *= gl.y;
+      }
+      rm_store_acc(Bp, mt, 2 * nq, lane, acc[0]);
+      rm_store_acc(Bp, mt, 2 * nq + 1, lane, acc[1]);
+    } else {
+      const int mt = (job - 8) >> 1, np = (job - 8) & 1;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        if (mt == 0 && kk == 1) continue;
+        const FragA fa = rm_a(Mrb, mt, kk, lane);
+        FragB f0, f1;
+        rm_bt2(Tm, 2 * np, kk, lane, f0, f1);
+        {
+          const FragB fb2[2] = {f0, f1};
+          mma3n<2>(acc, fa, fb2);
+        }
+      }
+      rm_store_acc(Cm, mt, 2 * np, lane, acc[0]);
+      rm_store_acc(Cm, mt, 2 * np + 1, lane, acc[1]);
+    }
+  }
+  __syncthreads();
+
+  // A_c = diag(gamma_L) + A^^T B' and Q_c = R^^T + A^^T C^T (rows j); forward: K' = K~ diag(gamma_L) +
+  // M_ak^T B' (over B~) and P = M_rk + C M_ak
+  {
+    constexpr int NJ = BWD ? 24 : 36;
+    for (int job = warp; job < NJ; job += 8) {
+      float acc[2][4] = {};
+      if (job < 16) {
+        const int mt = job >> 2, p = job & 3;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const FragA fa = rm_at(Ah, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Bp, 2 * p, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int jr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
+          if (jr == col) acc[h][0] += GL[col];
+          if (jr == col + 1) acc[h][1] += GL[col + 1];
+          if (jr + 8 == col) acc[h][2] += GL[col];
+          if (jr + 8 == col + 1) acc[h][3] += GL[col + 1];
+          uint32_t hw, lw;
+          split2(acc[h][0], acc[h][1], hw, lw);
+          *reinterpret_cast<uint32_t*>(gA + swz_a(jr, col)) = hw;
+          *reinterpret_cast<uint32_t*>(gA + 4096 + swz_a(jr, col)) = lw;
+          split2(acc[h][2], acc[h][3], hw, lw);
+          *reinterpret_cast<uint32_t*>(gA + swz_a(jr + 8, col)) = hw;
+          *reinterpret_cast<uint32_t*>(gA + 4096 + swz_a(jr + 8, col)) = lw;
+        }
+      } else if (job < 24) {
+        const int mt = (job - 16) >> 1, p = (job - 16) & 1;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          if (p == 0 && kk == 1) continue;  // C[t][s] = 0 for s > t
+          const FragA fa = rm_at(Ah, mt, kk, lane);
+          FragB f0, f1;
+          rm_b2(Cm, 2 * p, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int jr = mt * 16 + g, tc = (2 * p + h) * 8 + 2 * q;
+          acc[h][0] += rm_get1(Rh, tc, jr);
+          acc[h][1] += rm_get1(Rh, tc + 1, jr);
+          acc[h][2] += rm_get1(Rh, tc, jr + 8);
+          acc[h][3] += rm_get1(Rh, tc + 1, jr + 8);
+          if (BWD) {
+            rm_store_acc(Qs, mt, 2 * p + h, lane, acc[h]);
+          } else {
+            uint32_t hw, lw;
+            split2(acc[h][0], acc[h][1], hw, lw);
+            *reinterpret_cast<uint32_t*>(gQ + swz_q(jr, tc)) = hw;
+            *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr, tc)) = lw;
+            split2(acc[h][2], acc[h][3], hw, lw);
+            *reinterpret_cast<uint32_t*>(gQ + swz_q(jr + 8, tc)) = hw;
+            *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr + 8, tc)) = lw;
+          }
+        }
+      } else if (job < 32) {
+        const int mt = (job - 24) >> 2, nq = (job - 24) & 3;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 1 && kk == 0) continue;
+          const FragA fa = rm_at(Mak, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Bp, 2 * nq, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+        // K~ is read here for the last time and K' written over B~ (read for the last time by B')
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = (2 * nq + h) * 8 + 2 * q;
+          const int tr = mt * 16 + g;
+          const float2 gl = *reinterpret_cast<const float2*>(GL + col);
+          const float2 k0 = rm_get2(Kt, tr, col), k8 = rm_get2(Kt, tr + 8, col);
+          acc[h][0] = fmaf(k0.x, gl.x, acc[h][0]);
+          acc[h][1] = fmaf(k0.y, gl.y, acc[h][1]);
+          acc[h][2] = fmaf(k8.x, gl.x, acc[h][2]);
+          acc[h][3] = fmaf(k8.y, gl.y, acc[h][3]);
+          rm_store_acc(Kp, mt, 2 * nq + h, lane, acc[h]);
+        }
+      } else {
+        const int mt = (job - 32) >> 1, np = (job - 32) & 1;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 0 && kk == 1) continue;
+          const FragA fa = rm_a(Cm, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Mak, 2 * np, kk, lane, f0, f1);
+          {
+            const FragB fb2[2] = {f0, f1};
+            mma3n<2>(acc, fa, fb2);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = (2 * np + h) * 8 + 2 * q;
+          const int tr = mt * 16 + g;
+          const float2 m0 = rm_get2(Mrk, tr, col), m8 = rm_get2(Mrk, tr + 8, col);
+          acc[h][0] += m0.x; acc[h][1] += m0.y; acc[h][2] += m8.x; acc[h][3] += m8.y;
+          rm_store_acc(Pm, mt, 2 * np + h, lane, acc[h]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  if (!BWD) {
+    // U_c = V^T K' (rows i, mma accumulator order) and Y_intra = P V (rows t, into y)
+    for (int job = warp; job < 24; job += 8) {
+      float acc[2][4] = {};
+      if (job < 16) {
+        const int mt = job >> 2, p = job & 3;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          FragB f0, f1;
+          rm_bt2(Kp, 2 * p, kk, lane, f0, f1);
+          if (kVExact) {
+            const FragA fa = rm_at_hi(Vm, mt, kk, lane);
+            mma2(acc[0], fa, f0);
+            mma2(acc[1], fa, f1);
+          } else {
+            const FragA fa = rm_at(Vm, mt, kk, lane);
+            {
+              const FragB fb2[2] = {f0, f1};
+              mma3n<2>(acc, fa, fb2);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
+              make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+      } else {
+        const int mt = (job - 16) >> 2, p = (job - 16) & 3;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          if (mt == 0 && kk == 1) continue;  // P lower triangular
+          const FragA fa = rm_a(Pm, mt, kk, lane);
+          FragB f0, f1;
+          rm_bt2(Vm, 2 * p, kk, lane, f0, f1, !kVExact);
+          if (kVExact) {
+            mma2b(acc[0], fa, f0);
+            mma2b(acc[1], fa, f1);
+          } else {
+            {
+              const FragB fb2[2] = {f0, f1};
+              mma3n<2>(acc, fa, fb2);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int tr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
+          if (tr < nm)
+            *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr) * tstride + col) = make_float2(acc[h][0], acc[h][1]);
+          if (tr + 8 < nm)
+            *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr + 8) * tstride + col) =
+                make_float2(acc[h][2], acc[h][3]);
+        }
+      }
+    }
+  } else {
+    // E_c = DY^T Q_c^T (rows i, mma accumulator order)
+    for (int job = warp; job < 16; job += 8) {
+      const int mt = job >> 2, p = job & 3;
+      float acc[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const FragA fa = rm_at(DYm, mt, kk, lane);
+        FragB f0, f1;
+        rm_b2(Qs, 2 * p, kk, lane, f0, f1);
+        {
+          const FragB fb2[2] = {f0, f1};
+          mma3n<2>(acc, fa, fb2);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
+            make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    }
+  }
+}
+
+// ====================================================================================== chain
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// wait for the phase of parity `parity` to complete; false once kWaitNs have passed
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - start > kWaitNs) return false;
+  return true;
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16) completing on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// B fragments (n-tiles nt, nt + 1; k-tile kk) of A_c for S A_c: B[k = j][n = j'] = A_c[j][j']
+__device__ __forceinline__ void ld_a_fwd(const __nv_bfloat16* sA, int nt, int kk, int lane, FragB& b0, FragB& b1) {
+  const int j = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const __nv_bfloat16* p = sA + j * 64 + (((nt + (lane >> 4)) ^ (lane & 7)) << 3);
+  uint32_t h[4], l[4];
+  ldsm4<true>(h, p);
+  ldsm4<true>(l, p + 4096);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+// ... of A_c^T for G A_c^T: B[k = j'][n = j] = A_c[j][j']
+__device__ __forceinline__ void ld_a_walk(const __nv_bfloat16* sA, int nt, int kk, int lane, FragB& b0, FragB& b1) {
+  const int j = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
+  const __nv_bfloat16* p = sA + j * 64 + (((2 * kk + ((lane >> 3) & 1)) ^ (lane & 7)) << 3);
+  uint32_t h[4], l[4];
+  ldsm4<false>(h, p);
+  ldsm4<false>(l, p + 4096);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+// ... of Q_c for S Q_c: B[k = j][n = t] = Q_c[j][t]
+__device__ __forceinline__ void ld_q_fwd(const __nv_bfloat16* sQ, int nt, int kk, int lane, FragB& b0, FragB& b1) {
+  const int j = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const __nv_bfloat16* p = sQ + j * 32 + (((nt + (lane >> 4)) ^ ((j >> 1) & 3)) << 3);
+  uint32_t h[4], l[4];
+  ldsm4<true>(h, p);
+  ldsm4<true>(l, p + 2048);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+
+constexpr int kNS = 3;  // stages in flight
+
+template <int R, bool WALK>
+struct Stage {
+  static constexpr int kNW = R / 16;                             // chain warps
+  static constexpr int oA = 0;                                   // A_c (16 KB), then Q_c (forward, 8 KB)
+  static constexpr int kAQ = WALK ? 16384 : 24576;
+  static constexpr int oX = kAQ;                                 // this CTA's rows of U_c / E_c
+  static constexpr int oY = oX + kNW * 4096;                     // forward: y rows [32 t][R + 4]
+  static constexpr int kYL = R + 4;
+  static constexpr int kBytes = oY + (WALK ? 0 : 32 * kYL * 4);
+  static constexpr int kSmem = 128 + kNS * kBytes;
+  static_assert(kBytes % 128 == 0, "stage alignment");
+};
+
+template <int R, bool WALK>
+__global__ void __launch_bounds__((R / 16 + 1) * 32)
+xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, const float* __restrict__ s0,
+                 float* __restrict__ y, float* __restrict__ ck, size_t ck_stride, float* __restrict__ sT,
+                 unsigned* __restrict__ status) {
+  // forward: s0 = h0 (or null), y (Y_intra in, y out), ck = h_ckpt (or null; ck_stride = 4096 floats),
+  // sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X (ck_stride = kXBytes / 4),
+  // sT = dh0.
+  using ST = Stage<R, WALK>;
+  constexpr int NW = ST::kNW;
+  constexpr int NB = 64 / R;
+  extern __shared__ float4 smem4[];
+  unsigned char* smc = reinterpret_cast<unsigned char*>(smem4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smc);
+  uint64_t* empty = full + kNS;
+  auto stage = [&](int s) { return smc + 128 + s * ST::kBytes; };
+  const int bh = blockIdx.x / NB, rb = blockIdx.x - (blockIdx.x / NB) * NB;
+  const int bi = bh / H, hi = bh - bi * H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t tstride = (size_t)H * kD;
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const unsigned char* hops = ops + (size_t)bh * nchunks * kXBytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ================= producer: chunk n into stage n % kNS once the chain warps have released it
+    int issued = 0;
+    bool ok = true;
+    for (int n = 0; n < nchunks; ++n) {
+      const int c = WALK ? nchunks - 1 - n : n;
+      const int s = n % kNS;
+      // every lane observes the release; the warp agrees on the outcome (a time limit could split it)
+      if (n >= kNS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((n / kNS) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int nm = min(kL, T - c * kL);
+      unsigned char* st = stage(s);
+      const unsigned char* src = hops + (size_t)c * kXBytes;
+      if (lane == 0) {
+        mbar_expect_tx(&full[s], ST::kAQ + NW * 4096 + (WALK ? 0 : nm * R * 4));
+        bulk_g2s(st + ST::oA, src + kXA, ST::kAQ, &full[s]);
+        bulk_g2s(st + ST::oX, src + kXX + rb * NW * 4096, NW * 4096, &full[s]);
+      }
+      __syncwarp();
+      if (!WALK && lane < nm)
+        bulk_g2s(st + ST::oY + lane * ST::kYL * 4, y + base + (size_t)(c * kL + lane) * tstride + rb * R, R * 4,
+                 &full[s]);
+      issued = n + 1;
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(status, 1u);
+      // the copies already issued land before the CTA may exit
+      for (int m = max(0, issued - kNS); m < issued; ++m) mbar_wait(&full[m % kNS], (m / kNS) & 1);
+    }
+    return;
+  }
+
+  // =================== chain warp: state rows rb * R + 16 warp + (g, g + 8)
+  const int g = lane >> 2, q = lane & 3;
+  const int lrow = warp * 16 + g;  // row within the CTA's block
+  const int row = rb * R + lrow;
+  const size_t sbase = (size_t)bh * kD * kD;
+  float S[8][4];
+#pragma unroll
+  for (int nj = 0; nj < 8; ++nj) {
+    if (s0 != nullptr) {
+      const float2 x0 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)row * kD + nj * 8 + 2 * q));
+      const float2 x8 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)(row + 8) * kD + nj * 8 + 2 * q));
+      S[nj][0] = x0.x; S[nj][1] = x0.y; S[nj][2] = x8.x; S[nj][3] = x8.y;
+    } else {
+      S[nj][0] = S[nj][1] = S[nj][2] = S[nj][3] = 0.f;
+    }
+  }
+  auto store_rows = [&](float* dst) {
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj) {
+      *reinterpret_cast<float2*>(dst + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
+      *reinterpret_cast<float2*>(dst + (size_t)(row + 8) * kD + nj * 8 + 2 * q) = make_float2(S[nj][2], S[nj][3]);
+    }
+  };
+
+  for (int n = 0; n < nchunks; ++n) {
+    const int c = WALK ? nchunks - 1 - n : n;
+    const int s = n % kNS;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (n / kNS) & 1))) {
+      if (lane == 0) atomicOr(status, 1u);
+      return;
+    }
+    const unsigned char* st = stage(s);
+    const __nv_bfloat16* sA = reinterpret_cast<const __nv_bfloat16*>(st + ST::oA);
+    // the walk's G before this chunk (its X block has been read into the stage: safe to overwrite)
+    if (WALK && ck != nullptr) store_rows(ck + ((size_t)bh * nchunks + c) * ck_stride);
+    // S = S A_c + U_c (forward) or G = G A_c^T + E_c (walk); the forward also y_c^T += S Q_c (rows i,
+    // columns t).  Per k-step the three bf16 passes go over all accumulators in turn, so that dependent
+    // mma into one accumulator are 8 (walk) or 12 (forward) instructions apart.
+    const int nm = min(kL, T - c * kL);
+    const float* ys = reinterpret_cast<const float*>(st + ST::oY);
+    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(st + kXQ);
+    float acc[8][4], ya[4][4];
+    const float4* xs = reinterpret_cast<const float4*>(st + ST::oX) + warp * 8 * 32 + lane;
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj) {
+      const float4 u = xs[nj * 32];
+      acc[nj][0] = u.x; acc[nj][1] = u.y; acc[nj][2] = u.z; acc[nj][3] = u.w;
+    }
+    if (!WALK) {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int tc = nt * 8 + 2 * q;
+        ya[nt][0] = ys[tc * ST::kYL + lrow];
+        ya[nt][1] = ys[(tc + 1) * ST::kYL + lrow];
+        ya[nt][2] = ys[tc * ST::kYL + lrow + 8];
+        ya[nt][3] = ys[(tc + 1) * ST::kYL + lrow + 8];
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const FragA fa = frag_from_acc(S[2 * kk], S[2 * kk + 1]);
+      FragB fb[8], fq[4];
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        if (WALK)
+          ld_a_walk(sA, 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
+        else
+          ld_a_fwd(sA, 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
+      }
+      if (!WALK) {
+        ld_q_fwd(sQ, 0, kk, lane, fq[0], fq[1]);
+        ld_q_fwd(sQ, 2, kk, lane, fq[2], fq[3]);
+      }
+#pragma unroll
+      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.l, fb[nj].h[0], fb[nj].h[1]);
+      if (!WALK)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.l, fq[nt].h[0], fq[nt].h[1]);
+#pragma unroll
+      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.h, fb[nj].l[0], fb[nj].l[1]);
+      if (!WALK)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.h, fq[nt].l[0], fq[nt].l[1]);
+#pragma unroll
+      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.h, fb[nj].h[0], fb[nj].h[1]);
+      if (!WALK)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.h, fq[nt].h[0], fq[nt].h[1]);
+    }
+    if (!WALK) {
+      float* yo = y + base + (size_t)(c * kL) * tstride;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int tc = nt * 8 + 2 * q;
+        if (tc < nm) {
+          yo[(size_t)tc * tstride + row] = ya[nt][0];
+          yo[(size_t)tc * tstride + row + 8] = ya[nt][2];
+        }
+        if (tc + 1 < nm) {
+          yo[(size_t)(tc + 1) * tstride + row] = ya[nt][1];
+          yo[(size_t)(tc + 1) * tstride + row + 8] = ya[nt][3];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int nj = 0; nj < 8; ++nj)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S[nj][e] = acc[nj][e];
+    if (!WALK && ck != nullptr) store_rows(ck + ((size_t)bh * nchunks + c) * ck_stride);
+  }
+  if (sT != nullptr) store_rows(sT + sbase);
+}
+
+template <typename Tin, bool BWD>
+cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* ops, unsigned* status,
+                          cudaStream_t stream) {
+  using LY = XPrepLay<Tin, BWD>;
+  static_assert(LY::kBytes <= 232448, "shared memory per CTA");
+  auto kern = xop_prep_kernel<Tin, BWD>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
+  if (err != cudaSuccess) return err;
+  const int B = BWD ? ba->B : fa->B, T = BWD ? ba->T : fa->T, H = BWD ? ba->H : fa->H;
+  const int C = BWD ? ba->nchunks : fa->nchunks;
+  const TokenInputs& in = BWD ? ba->in : fa->in;
+  const unsigned grid = (unsigned)B * H * C;
+  kern<<<grid, kNTP, LY::kBytes, stream>>>(T, H, C, (const Tin*)in.r, (const Tin*)in.w, (const Tin*)in.k,
+                                          (const Tin*)in.v, (const Tin*)in.a, (const Tin*)in.b,
+                                          BWD ? ba->dy : nullptr, ops, BWD ? nullptr : fa->y, status);
+  return cudaGetLastError();
+}
+
+template <int R, bool WALK>
+cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, const float* s0, float* y, float* ck,
+                           size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+  using ST = Stage<R, WALK>;
+  static_assert(ST::kSmem <= 232448, "shared memory per CTA");
+  auto kern = xop_chain_kernel<R, WALK>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ST::kSmem);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = (unsigned)B * H * (64 / R);
+  kern<<<grid, (R / 16 + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, s0, y, ck, ck_stride, sT, status);
+  return cudaGetLastError();
+}
+
+// state rows per chain CTA.  Every chain warp spends the same time per chunk whatever the split, while each
+// CTA reads the head's A_c and Q_c: whole heads (64 rows) read them once.
+#ifndef WKV7_CHAIN_ROWS
+#define WKV7_CHAIN_ROWS 64
+#endif
+int chain_rows(int /*heads*/) { return WKV7_CHAIN_ROWS; }
+
+template <bool WALK>
+cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned char* ops, const float* s0, float* y,
+                         float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+  switch (rows) {
+    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
+    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
+    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
+  }
+}
+
+}  // namespace
+
+size_t xop_workspace_bytes(int B, int T, int H) {
+  const size_t C = ((size_t)T + kL - 1) / kL;
+  return kXHead + (size_t)B * H * C * kXBytes;
+}
+
+cudaError_t launch_xop_forward(const FwdArgs& p, void* workspace, int rows, cudaStream_t stream) {
+  if (p.nchunks == 0) return cudaSuccess;
+  unsigned* status = static_cast<unsigned*>(workspace);
+  unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
+  cudaError_t err = p.bf16 ? launch_prep_t<__nv_bfloat16, false>(&p, nullptr, ops, status, stream)
+                           : launch_prep_t<float, false>(&p, nullptr, ops, status, stream);
+  if (err != cudaSuccess) return err;
+  if (rows == 0) rows = chain_rows(p.B * p.H);
+  return launch_chain<false>(rows, p.B, p.T, p.H, p.nchunks, ops, p.h0, p.y, p.h_ckpt, (size_t)kD * kD, p.hT, status,
+                             stream);
+}
+
+cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, int rows, ChunkEnds* ends, cudaStream_t stream) {
+  unsigned* status = static_cast<unsigned*>(workspace);
+  unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
+  ends->g = reinterpret_cast<const float*>(ops + kXX);
+  ends->flags = reinterpret_cast<int*>(ops + kXQ);  // Q_c's slot: the walk does not use it
+  ends->stride = kXBytes / 4;
+  if (p.nchunks > 0) {  // (no chunks: the chain only copies dhT to dh0)
+    cudaError_t err = p.bf16 ? launch_prep_t<__nv_bfloat16, true>(nullptr, &p, ops, status, stream)
+                             : launch_prep_t<float, true>(nullptr, &p, ops, status, stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (rows == 0) rows = chain_rows(p.B * p.H);
+  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, p.dhT, nullptr,
+                            reinterpret_cast<float*>(ops + kXX), kXBytes / 4, p.dh0, status, stream);
+}
+
+}  // namespace wkv7

@@ -122,16 +122,16 @@ def test_decode_validation(i):
 
 def test_workspace_size_query():
     n = wkv7.backward_workspace_size(12, 1024, 6, 64, 32)
-    # at chunk 32: the larger of the two-phase layout (dsa, then X at every chunk end) and the transition
-    # layout (25088 bytes of operands per chunk, then G at every chunk end)
+    # at chunk 32: the larger of the two-phase layout (dsa, then X at every chunk end) and the chunk-operator
+    # layout (a 256-byte status header, then a 40960-byte operator block per (head, chunk))
     dsa = 12 * 1024 * 6 * 64 * 4
     xck = 12 * 6 * 32 * 64 * 64 * 4
-    ops = 12 * 6 * 32 * 25088
-    assert n == max((dsa + 255) // 256 * 256 + xck, (ops + 255) // 256 * 256 + xck)
+    ops = 256 + 12 * 6 * 32 * 40960
+    assert n == max((dsa + 255) // 256 * 256 + xck, ops)
     assert wkv7.backward_workspace_size(2, 64, 3, 64, 16) == (2 * 64 * 3 * 64 * 4 + 255) // 256 * 256 + 2 * 3 * 4 * 64 * 64 * 4
     assert wkv7.forward_workspace_size(12, 1024, 6, 64, 32) == ops
     assert wkv7.forward_workspace_size(12, 1024, 6, 64, 16) == 0
-    assert wkv7.backward_workspace_size(1, 0, 1, 64, 32) == 0
+    assert wkv7.backward_workspace_size(1, 0, 1, 64, 32) == 256
     with pytest.raises(wkv7.WKV7Error):
         wkv7.backward_workspace_size(1, 32, 1, 32, 32)      # D != 64
     assert wkv7.lib.wkv7_backward_workspace_size(1, 32, 1, 64, 32, None) == 1
