@@ -5,7 +5,10 @@
 
 A step is one pass of the whole path on one batch of the 36M "debug" training
 shape (B=12, T=1024, H=6, D=64, bf16 inputs, fp32 state, chunk 32): wkv7_forward
-(y, checkpoints, hT) then wkv7_backward (dr, dw, dk, dv, da, db, dh0).  Inputs are
+(y, checkpoints, hT) then wkv7_backward (dr, dw, dk, dv, da, db, dh0), both with a
+workspace and without a saved sa (--path operators, the default; --path two-phase and
+--path single time the other backward paths).  other_configs adds the step time and
+step roofline fractions of the other training workloads.  Inputs are
 seeded synthetic draws (wkv7_inputs.py).  Under torchrun each rank runs its own
 independent batch (weak scaling, no collective on the data path); rank 0 prints
 one JSON line.
@@ -16,11 +19,9 @@ bounded sample of the same workload, in the same unit.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -54,14 +55,14 @@ def parse_args():
                    help="default: the debug training shape (the headline line); others for extra measurements")
     p.add_argument("--decode-batch", type=int, default=0,
                    help="decode workload only: number of sequences (default: the workload's 256)")
-    p.add_argument("--bwd", choices=["two-phase", "single"], default="two-phase",
-                   help="two-phase backward with a workspace (needs --sa saved), or the single-pass backward")
-    p.add_argument("--fwd", choices=["auto", "sequential"], default="auto",
-                   help="forward kernel: auto = 16-token sub-chunks where they apply, sequential = token by token")
+    p.add_argument("--path", choices=["operators", "two-phase", "single"], default="operators",
+                   help="operators: chunk-operator forward and backward with a workspace, no saved sa (the "
+                        "default); two-phase: forward saving sa, two-phase backward reading it; single: "
+                        "single-pass backward without a workspace")
     p.add_argument("--graph", choices=["on", "off"], default="on",
                    help="time the step as CUDA-graph replays (one graph per input set) instead of eager calls")
-    p.add_argument("--sa", choices=["saved", "recompute"], default="saved",
-                   help="backward reads the forward's saved sa, or recomputes it per chunk")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the step times of the other training workloads (other_configs in the line)")
     return p.parse_args()
 
 
@@ -97,29 +98,12 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback", {}
 
 
-def kernel_source_sha(names) -> str:
-    """sha256 of the given kernel file(s) (name or tuple, in order) then wkv7_device.cuh, 12 hex digits."""
-    names = (names,) if isinstance(names, str) else tuple(names)
-    h = hashlib.sha256()
-    for n in names + ("wkv7_device.cuh",):
-        with open(os.path.join(ROOT, "linear_rnn_lm_wkv7_b300", "csrc", n), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:12]
-
-
-def profiled_traffic(kernel: str, workload: str, src_sha: str):
-    """DRAM bytes per launch from profiles/dram_traffic.md, only if taken on the current source."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
-        return None
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[3] == src_sha:
-            try:
-                return float(cells[2])
-            except ValueError:
-                return None
-    return None
+def workload_config(wl) -> dict:
+    """The `config` object of both arms' lines: the workload alone (how the step runs is in `path`)."""
+    fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "D": wl.D, "chunk": wl.chunk, "inputs": wl.dtype,
+            "state": "fp32", "l2": f"{N_SETS} rotating input/output sets "
+                                   f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"}
 
 
 # ------------------------------------------------------------------------------ ranks
@@ -301,7 +285,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, wkv7_inputs.py)",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "D": wl.D, "chunk": wl.chunk},
+            "config": workload_config(wl),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -444,6 +428,122 @@ def run_decode(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+PATHS = {
+    # forward call, backward call and the kernels each launches (counted per step for gpu_launches)
+    "operators": {"forward": "wkv7_forward with a workspace, no sa: chunk-operator prep + chain",
+                  "backward": "wkv7_backward with a workspace, no sa: operator prep + walk + matrix column "
+                              "kernel + token-by-token companion (exits at once without flagged chunks)",
+                  "launches": 2 + 4},
+    "two-phase": {"forward": "wkv7_forward saving sa: 16-token sub-chunks (one wave) or token by token",
+                  "backward": "wkv7_backward with sa and a workspace: sub-chunk walk + column passes",
+                  "launches": 1 + 2},
+    "single": {"forward": "wkv7_forward saving sa: 16-token sub-chunks (one wave) or token by token",
+               "backward": "wkv7_backward without a workspace: single pass (rebuilds states dividing by w)",
+               "launches": 1 + 1},
+}
+
+
+def make_runner(wkv7, torch, dev, wl, path, n_sets):
+    """Input/output sets on the device and the step (forward then backward) of one path."""
+    B, T, H, D = wl.B, wl.T, wl.H, wl.D
+    C = wkv7.num_chunks(T, wl.chunk)
+    x = gen.full(wl)
+    host_in = {n: torch.from_numpy(x[n]).to(torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
+               for n in "rwkvab"}
+    host = {"in": host_in, "dy": torch.from_numpy(x["dy"]),
+            "h0": None if x["h0"] is None else torch.from_numpy(x["h0"]),
+            "dhT": None if x["dhT"] is None else torch.from_numpy(x["dhT"])}
+    del x
+    saved = path != "operators"
+    ws_bytes = 0
+    if path == "operators":
+        ws_bytes = max(wkv7.forward_workspace_size(B, T, H, D, wl.chunk), wkv7.backward_workspace_size(B, T, H, D, wl.chunk))
+    elif path == "two-phase":
+        ws_bytes = wkv7.backward_workspace_size(B, T, H, D, wl.chunk)
+
+    def make_set():
+        s = {n: host_in[n].to(dev) for n in "rwkvab"}
+        s["dy"] = host["dy"].to(dev)
+        s["h0"] = None if host["h0"] is None else host["h0"].to(dev)
+        s["dhT"] = None if host["dhT"] is None else host["dhT"].to(dev)
+        s["y"] = torch.empty((B, T, H, D), device=dev)
+        s["ck"] = torch.empty((B, H, C, D, D), device=dev)
+        s["hT"] = torch.empty((B, H, D, D), device=dev)
+        s["sa"] = torch.empty((B, T, H, D), device=dev) if saved else None
+        s["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+        s["g"] = [torch.empty((B, T, H, D), device=dev) for _ in range(6)] + [torch.empty((B, H, D, D), device=dev)]
+        return s
+
+    sets = [make_set() for _ in range(n_sets)]
+
+    def step(s, stream=None, ev=None):
+        ins = [s[n] for n in "rwkvab"]
+        if ev is not None:
+            ev[0].record(stream)
+        out = (s["y"], s["ck"], s["hT"]) + ((s["sa"],) if saved else ())
+        wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=out, save_sa=saved,
+                     workspace=s["ws"] if path == "operators" else None)
+        if ev is not None:
+            ev[1].record(stream)
+        wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"],
+                      workspace=s["ws"] if path != "single" else None, out=s["g"])
+        if ev is not None:
+            ev[2].record(stream)
+
+    return sets, step, host
+
+
+def capture_graphs(torch, dev, stream, sets, step):
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for s_ in sets:
+            step(s_)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = []
+    for s_ in sets:
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            step(s_)
+        graphs.append(g_)
+    return graphs
+
+
+def other_configs(wkv7, torch, dev, args, peaks, hbm, sms):
+    """Step time and step roofline fractions of the other training workloads (CUDA-graph replays)."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, wl in gen.WORKLOADS.items():
+        if wl.decode or name == args.workload or name.startswith("oracle"):
+            continue
+        try:
+            sets, step, _ = make_runner(wkv7, torch, dev, wl, args.path, 2)
+            graphs = capture_graphs(torch, dev, stream, sets, step)
+            for i in range(3):
+                graphs[i % 2].replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 10
+            e0.record(stream)
+            for i in range(n):
+                graphs[i % 2].replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
+            roof_s = max((fwd_b + bwd_b) / (hbm * 1e9), literal_flops(wl) / (fp32_peak_tflops(peaks, sms) * 1e12))
+            roof_d = max((fwd_b + bwd_b) / (hbm * 1e9), derived_flops(wl) / (fp32_peak_tflops(peaks, sms) * 1e12))
+            out[name] = {"B": wl.B, "T": wl.T, "H": wl.H, "ms_per_step": ms, "tokens_per_s": wl.B * wl.T / (ms / 1e3),
+                         "roofline_step_frac": roof_s / (ms / 1e3), "roofline_step_derived_frac": roof_d / (ms / 1e3),
+                         "launch": "CUDA graph replay (2 input sets)"}
+            del sets, graphs
+            torch.cuda.empty_cache()
+        except Exception as e:  # reported in the line
+            out[name] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import linear_rnn_lm_wkv7_b300 as wkv7
@@ -453,46 +553,9 @@ def run_ours(args, rank, world, local_rank):
     wl = gen.WORKLOADS[args.workload]
     if wl.decode:
         return run_decode(args, rank, world, local_rank)
-    saved = args.sa == "saved"
     B, T, H, D = wl.B, wl.T, wl.H, wl.D
-    C = wkv7.num_chunks(T, wl.chunk)
-
-    x = gen.full(wl)   # same seeded batch on every rank (each rank owns an independent replica)
-    host_in = {n: torch.from_numpy(x[n]).to(torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
-               for n in "rwkvab"}
-    host_dy = torch.from_numpy(x["dy"])
-    host_h0 = None if x["h0"] is None else torch.from_numpy(x["h0"])
-    host_dhT = None if x["dhT"] is None else torch.from_numpy(x["dhT"])
-
-    def make_set():
-        s = {n: host_in[n].to(dev) for n in "rwkvab"}
-        s["dy"] = host_dy.to(dev)
-        s["h0"] = None if host_h0 is None else host_h0.to(dev)
-        s["dhT"] = None if host_dhT is None else host_dhT.to(dev)
-        s["y"] = torch.empty((B, T, H, D), device=dev)
-        s["ck"] = torch.empty((B, H, C, D, D), device=dev)
-        s["hT"] = torch.empty((B, H, D, D), device=dev)
-        s["sa"] = torch.empty((B, T, H, D), device=dev)
-        s["ws"] = torch.empty(wkv7.backward_workspace_size(B, T, H, D, wl.chunk), dtype=torch.uint8, device=dev) \
-            if args.bwd == "two-phase" else None
-        s["g"] = [torch.empty((B, T, H, D), device=dev) for _ in range(6)] + [torch.empty((B, H, D, D), device=dev)]
-        return s
-
-    sets = [make_set() for _ in range(N_SETS)]
+    sets, step, host = make_runner(wkv7, torch, dev, wl, args.path, N_SETS)
     stream = torch.cuda.current_stream()
-
-    def step(s, ev=None):
-        ins = [s[n] for n in "rwkvab"]
-        if ev is not None:
-            ev[0].record(stream)
-        wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=(s["y"], s["ck"], s["hT"], s["sa"] if saved else None),
-                     kernel=args.fwd)
-        if ev is not None:
-            ev[1].record(stream)
-        wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"] if saved else None,
-                      workspace=s["ws"], out=s["g"])
-        if ev is not None:
-            ev[2].record(stream)
 
     for i in range(max(3, args.warmup)):
         step(sets[i % N_SETS])
@@ -509,13 +572,14 @@ def run_ours(args, rank, world, local_rank):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
+    # eager calls, CUDA events around each call (the per-call split)
     with ClockSampler(uuid) as clk:
         if dist:
             tdist.barrier()
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            step(sets[i % N_SETS], evs[i])
+            step(sets[i % N_SETS], stream, evs[i])
         stop.record(stream)
         torch.cuda.synchronize()
         if dist:
@@ -525,24 +589,11 @@ def run_ours(args, rank, world, local_rank):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
     # The same steps replayed from CUDA graphs (one per input set, captured once): the launches no
-    # longer wait on the host, which matters at shapes where a step takes less time on the GPU than
-    # the Python calls that issue it.  The per-kernel split above stays the eager one.
+    # longer wait on the host.  The per-call split above stays the eager one.
     launch = "eager"
     if args.graph == "on":
         try:
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                for s_ in sets:
-                    step(s_)
-            stream.wait_stream(side)
-            torch.cuda.synchronize()
-            graphs = []
-            for s_ in sets:
-                g_ = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_):
-                    step(s_)
-                graphs.append(g_)
+            graphs = capture_graphs(torch, dev, stream, sets, step)
             for i in range(max(3, args.warmup)):
                 graphs[i % N_SETS].replay()
             torch.cuda.synchronize()
@@ -559,6 +610,7 @@ def run_ours(args, rank, world, local_rank):
                     tdist.barrier()
             elapsed_ms = start.elapsed_time(stop)
             launch = f"CUDA graph replay ({N_SETS} graphs, one per input set)"
+            del graphs
         except Exception as e:  # capture refused: the eager timing stands, and the line says why
             launch = f"eager (graph capture failed: {type(e).__name__}: {str(e)[:160]})"
     clocks = clk.summary()
@@ -568,16 +620,15 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
     if args.e2e_steps > 0:
+        host_in, host_dy = host["in"], host["dy"]
         pin_in = {n: host_in[n].pin_memory() for n in "rwkvab"}
         pin_dy = host_dy.pin_memory()
         pin_y = torch.empty((B, T, H, D), pin_memory=True)
         pin_g = [torch.empty((B, T, H, D), pin_memory=True) for _ in range(6)] + \
                 [torch.empty((B, H, D, D), pin_memory=True)]
-        s = sets[0]
         h2d = sum(t.numel() * t.element_size() for t in pin_in.values()) + pin_dy.numel() * 4
         d2h = pin_y.numel() * 4 + sum(t.numel() * 4 for t in pin_g)
-
-        pin_st = {n: t.pin_memory() for n, t in (("h0", host_h0), ("dhT", host_dhT)) if t is not None}
+        pin_st = {n: t.pin_memory() for n, t in (("h0", host["h0"]), ("dhT", host["dhT"])) if t is not None}
         h2d += sum(t.numel() * 4 for t in pin_st.values())
 
         # Pipelined across steps like an input pipeline: step i's host->device copies, compute and
@@ -643,53 +694,51 @@ def run_ours(args, rank, world, local_rank):
 
     fwd_b, bwd_b = byte_counts(wl, 2 if wl.dtype == "bf16" else 4)
     hbm, peak_kind, peaks = measured_peaks()
-    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    # the two-phase backward's walk runs on the sub-chunk kernel: its traffic row is keyed by both files
-    bwd_name, bwd_src = ("wkv7_bwd_two_phase", ("wkv7_bwd2.cu", "wkv7_fwdc.cu")) if (saved and args.bwd == "two-phase") \
-        else ("wkv7_bwd", "wkv7_bwd.cu")
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    chunked = args.fwd == "auto" and wl.chunk % 16 == 0 and B * H * 2 <= sms
-    fwd_name, fwd_src = ("wkv7_fwd_chunked", "wkv7_fwdc.cu") if chunked else ("wkv7_fwd", "wkv7_fwd.cu")
-    dom = (bwd_name, bwd_b, b_ms, bwd_src) if b_ms >= f_ms else (fwd_name, fwd_b, f_ms, fwd_src)
+    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dom = ("wkv7_backward", bwd_b, b_ms) if b_ms >= f_ms else ("wkv7_forward", fwd_b, f_ms)
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
-    sha = kernel_source_sha(dom[3])
-    traffic = profiled_traffic(dom[0], wl.name, sha)
     step_s = elapsed_ms / 1e3 / args.steps
-    roof_s = max((fwd_b + bwd_b) / (hbm * 1e9), literal_flops(wl) / (fp32_peak_tflops(peaks) * 1e12))
-    roof_d = max((fwd_b + bwd_b) / (hbm * 1e9), derived_flops(wl) / (fp32_peak_tflops(peaks) * 1e12))
+    fp32 = fp32_peak_tflops(peaks, sms)
+    roof_s = max((fwd_b + bwd_b) / (hbm * 1e9), literal_flops(wl) / (fp32 * 1e12))
+    roof_d = max((fwd_b + bwd_b) / (hbm * 1e9), derived_flops(wl) / (fp32 * 1e12))
+    pth = PATHS[args.path]
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, wkv7_inputs.py)",
-        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "D": D, "chunk": wl.chunk, "inputs": wl.dtype,
-                   "state": "fp32", "sa": args.sa, "forward": fwd_name,
-                   "backward": args.bwd if args.sa == "saved" else "single",
-                   "launch": launch, "parallelism": f"replicas x{world} (independent batches, no collective)",
-                   "l2": f"{N_SETS} rotating input/output sets "
-                         f"({N_SETS * (fwd_b + bwd_b) / 1e9:.2f} GB touched per rotation > 126 MB L2)"},
-        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "config": workload_config(wl),
+        "path": {"name": args.path, "forward": pth["forward"], "backward": pth["backward"], "launch": launch,
+                 "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "roofline": {"bound": "hbm", "kernel": dom[0] + " (" + args.path + " path, one call)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": traffic, "algorithmic_bytes": dom[1], "avg_launch_ms": dom[2]},
+                     "traffic": None,
+                     "traffic_note": "DRAM bytes are not measured inside the run; ncu counts per kernel are in profiles/",
+                     "algorithmic_bytes": dom[1], "avg_launch_ms": dom[2]},
         "roofline_step": {"definition": "max(HBM bytes / peak BW, 8*D^2 FLOP per head-token / FP32 peak) / step time",
-                          "bytes": fwd_b + bwd_b, "roofline_ms": roof_s * 1e3, "frac": roof_s / step_s},
+                          "bytes": fwd_b + bwd_b, "roofline_ms": roof_s * 1e3, "frac": roof_s / step_s,
+                          "fp32_peak_tflops": fp32},
         "roofline_step_derived": {"definition": "max(HBM bytes / peak BW, 28*D^2 FLOP per head-token / FP32 peak) "
                                                 "/ step time", "flops": derived_flops(wl),
                                   "roofline_ms": roof_d * 1e3, "frac": roof_d / step_s},
-        "kernels_ms": {fwd_name: f_ms, bwd_name: b_ms, "timing": "eager calls, CUDA events around each"},
+        "calls_ms": {"wkv7_forward": f_ms, "wkv7_backward": b_ms, "timing": "eager calls, CUDA events around each"},
         "clocks": clocks,
-        "gpu_launches": (3 if (saved and args.bwd == "two-phase") else 2) * args.steps,
+        "gpu_launches": pth["launches"] * args.steps,
         "e2e": e2e,
     }
+    if world == 1 and not args.no_other_configs:
+        line["other_configs"] = other_configs(wkv7, torch, dev, args, peaks, hbm, sms)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
-def fp32_peak_tflops(peaks: dict) -> float:
-    """FP32 CUDA-core peak: 148 SMs x 128 FMA lanes x 2 FLOP x max SM clock."""
+def fp32_peak_tflops(peaks: dict, sms: int) -> float:
+    """FP32 CUDA-core peak: SMs x 128 FMA lanes x 2 FLOP x max SM clock."""
     mhz = float(peaks.get("sm_max_mhz", 2032.0)) if peaks else 2032.0
-    return 148 * 128 * 2 * mhz * 1e6 / 1e12
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def main():

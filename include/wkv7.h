@@ -29,9 +29,14 @@
  *     states, y and every gradient are fp32.  w is the decay multiplier, not its
  *     log, and must be > 0 where the backward divides by it.
  *   - Every pointer is a DEVICE pointer on the current CUDA device (memory the
- *     caller owns; the library allocates, frees and keeps nothing), 16-byte
- *     aligned.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
- *     default stream) and is asynchronous: no call synchronises the device.
+ *     caller owns), 16-byte aligned.  The library calls no allocator and keeps
+ *     no device memory of its own, with one exception: the fixed scratch array of
+ *     wkv7_backward_noalloc (WKV7_NOALLOC_SCRATCH_BYTES, compiled into the
+ *     library), which the CUDA runtime reserves on a device when the library's
+ *     device code is loaded there (its first use on the device under the default
+ *     lazy module loading) until the process exits.  Work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and is asynchronous: no
+ *     call synchronises the device (except wkv7_debug_status).
  *   - D must be 64.  1 <= chunk <= 32.  B, H >= 1, T >= 0.
  *   - Outputs are fully overwritten (never accumulated into).  Outputs must not
  *     alias inputs or each other, except the in-place decode state.
@@ -58,8 +63,8 @@ typedef enum {
     WKV7_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned */
     WKV7_ERR_DTYPE = 4,    /* in_dtype is not WKV7_F32 / WKV7_BF16 */
     WKV7_ERR_CUDA = 5,     /* the CUDA runtime reported an error at launch */
-    WKV7_ERR_TIMEOUT = 6,  /* a bounded device-side wait gave up (reserved) */
-    WKV7_ERR_WORKSPACE = 7, /* the backward's workspace is smaller than wkv7_backward_workspace_size */
+    WKV7_ERR_TIMEOUT = 6,  /* a bounded device-side wait gave up (the workspace status word) */
+    WKV7_ERR_WORKSPACE = 7, /* a workspace is smaller than its *_workspace_size */
     WKV7_ERR_SCRATCH_LIMIT = 8 /* wkv7_backward_noalloc: needs more than WKV7_NOALLOC_SCRATCH_BYTES */
 } wkv7_status;
 
@@ -80,13 +85,18 @@ int wkv7_num_chunks(int T, int chunk);
  *           selects the two-phase backward that reads it.
  *   workspace, workspace_bytes
  *           device scratch of at least wkv7_forward_workspace_size() bytes, 256-byte
- *           aligned, owned by the caller; or NULL / 0.  Used at chunk == 32 without sa:
- *           every 32-token chunk's transition operands are formed at once into it (a
- *           chunk-parallel kernel), then one kernel runs the chain over the chunks reading
- *           them.  Without it, the same chain runs with the operands formed inside the
- *           chain kernel, one chunk ahead (slower).  With sa (or chunk != 32): 16-token
- *           sub-chunks when chunk % 16 == 0 and the B*H*2 row blocks fit one wave of SMs,
- *           else token by token.
+ *           aligned, owned by the caller; or NULL / 0.  Used at chunk == 32 without sa
+ *           (the chunk-operator forward): a parallel kernel forms every 32-token chunk's
+ *           transition operator (S_end = S_start A_c + U_c, and the chunk's y from S_start)
+ *           into it, 40960 bytes per (head, chunk) after a 256-byte header, and writes the
+ *           chunk-internal part of y; then one short chain per head applies them.  The
+ *           header's first 4 bytes hold a status word: 0 after a call that completed
+ *           normally; non-zero (WKV7_ERR_TIMEOUT) when a bounded wait inside the chain gave
+ *           up (2 s), in which case the outputs are invalid.  Reading it is the caller's
+ *           choice (it needs the stream synchronised).  Without a workspace at chunk 32 (no
+ *           sa) the operators are formed inside the chain kernel, one chunk ahead (slower).
+ *           With sa (or chunk != 32): 16-token sub-chunks when chunk % 16 == 0 and the B*H*2
+ *           row blocks fit one wave of SMs, else token by token.
  * Results of every path agree with the token-by-token definition to ~1e-5 relative.
  * Source: Forward listing of "Metal kernel architecture" (see top of file).
  */
@@ -96,8 +106,8 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const float *h0, float *y, float *h_ckpt, float *hT, float *sa,
                  void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes; 0 when chunk != 32);
- * returns a wkv7_status (the same size checks as wkv7_forward). */
+/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 40960 per (head,
+ * chunk) at chunk 32, 0 otherwise; returns a wkv7_status (the same size checks as wkv7_forward). */
 int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
 /*
@@ -124,15 +134,17 @@ int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
  *   workspace, workspace_bytes
  *           device scratch of at least wkv7_backward_workspace_size() bytes, 256-byte
  *           aligned, owned by the caller and reused freely between calls; or NULL / 0.
- *           With a workspace and no sa at chunk == 32 (the transition backward): every
- *           32-token chunk's transition operands are formed at once; one pass over the chunks,
- *           last to first, carries the state gradient G (w.r.t. the state after a chunk, from
- *           every later token) back through the transposed transitions, writing G at each
- *           chunk end into the workspace, and dh0; then every chunk forms dr, dw, dk, dv, da, db
- *           at once in matrix form from the state before it (h_ckpt[c-1], or h0), G and the
- *           state after it, recomputing sa -- no state is divided by w.  Chunks whose decays
- *           are too strong for the matrix form (some w < 1/32, or a 32-token decay product
- *           below 1e-20) take the exact token-by-token passes.  Results ~1e-5 of exact.
+ *           With a workspace and no sa at chunk == 32 (the chunk-operator backward): a
+ *           parallel kernel forms every chunk's transposed transition operator A_c^T and the
+ *           chunk's dy contribution E_c into the workspace (the forward's layout); one short
+ *           chain per head, last chunk to first, carries the state gradient G (w.r.t. the
+ *           state after a chunk, from every later token) back through them, writing G at each
+ *           chunk end over E_c, and dh0; then every chunk forms dr, dw, dk, dv, da, db at once
+ *           in matrix form on tensor cores from the state before it (h_ckpt[c-1], or h0), G and
+ *           the state after it, recomputing sa -- no state is divided by w.  Chunks whose
+ *           decays are too strong for the matrix form (some w < 1/32, or a 32-token decay
+ *           product below 1e-20) take the exact token-by-token passes.  Results ~1e-5 of
+ *           exact.  The workspace header's status word is as in wkv7_forward.
  *           With a workspace and sa: the two-phase backward -- one pass over the sequence walks
  *           the state gradient (16 tokens per step in the closed form when chunk % 16 == 0 and
  *           the B*H*2 row blocks fit one wave of SMs, else token by token), then every chunk's
@@ -156,11 +168,12 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
                   float *dr, float *dw, float *dk, float *dv, float *da, float *db,
                   float *dh0, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace the two-phase backward needs for these sizes (written to *bytes);
- * returns a wkv7_status (the same size checks as wkv7_backward). */
+/* Bytes of workspace wkv7_backward uses for these sizes (written to *bytes): at chunk 32 the larger of
+ * the two-phase layout and the chunk-operator layout, else the two-phase one; returns a wkv7_status (the
+ * same size checks as wkv7_backward). */
 int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
-/* Bytes of device scratch the library owns for wkv7_backward_noalloc (128 MiB). */
+/* Bytes of device scratch the library owns for wkv7_backward_noalloc (128 MiB; see the conventions above). */
 #define WKV7_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 
 /*
@@ -174,12 +187,15 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *
  * library until the process exits.  There is no counterpart of this in the source pages:
  * it is a packaging of the same computation as wkv7_backward with a workspace.
  *
- *   Arguments, layouts and results: as wkv7_backward, with `sa` required (the forward's
- *   saved sa) and no workspace.  Problems whose wkv7_backward_workspace_size exceeds
- *   WKV7_NOALLOC_SCRATCH_BYTES return WKV7_ERR_SCRATCH_LIMIT (B12 T1024 H6 needs ~96 MB;
+ *   Arguments, layouts and results: as wkv7_backward with a workspace, the same dispatch and
+ *   bit-identical results; `sa` is required off 32-token chunks (there only the two-phase
+ *   backward, which reads it, applies).  Problems whose wkv7_backward_workspace_size exceeds
+ *   WKV7_NOALLOC_SCRATCH_BYTES return WKV7_ERR_SCRATCH_LIMIT (B12 T1024 H6 needs ~94 MB;
  *   use wkv7_backward with a workspace for larger ones).
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   and caches it; make that first call before capturing a stream on that device.
+ *   Each call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress), so a device reset between calls is harmless.  The first call on
+ *   a device may load the library's device code there (lazy loading: that reserves the
+ *   array); make it before capturing a stream on that device.
  *   All calls share the one array and it keeps the previous call's contents; nothing in
  *   it needs clearing (each call writes every scratch value before reading it).  Calls
  *   whose work overlaps on the GPU (different streams, or different host threads) race on
@@ -206,6 +222,19 @@ int wkv7_decode(int B, int H, int D, int in_dtype, float *state,
                 float *y, void *stream);
 
 /* Static text for a wkv7_status value. */
+/* ---- device-side index checks (no counterpart in the pages: a stand-in for a memory checker)
+ * A library built with WKV7_DEBUG_CHECKS (build.py --debug: libwkv7_debug.so) checks the indices its
+ * kernels derive (shared-memory operand rows and columns, global rows, tile and block indices) and,
+ * instead of making an out-of-range access, records it in a status word of the kernel's source file and
+ * skips the access (or reads a safe address); no kernel traps.
+ *   wkv7_debug_status: synchronizes the device, then ORs and clears every file's word into *word: 0 = no
+ *     failed check since the last call; bit 0 an operand helper, bit 1 the chunk-operator prep, bit 2 its
+ *     chain, bit 3 the matrix column kernel, bit 4 its token-by-token companion, bit 5 other kernels.
+ *     Release builds write 0.  WKV7_ERR_ARG for a NULL word; WKV7_ERR_CUDA if the device reports an error.
+ *   wkv7_debug_enabled: 1 for a debug build, else 0. */
+int wkv7_debug_status(unsigned *word);
+int wkv7_debug_enabled(void);
+
 const char *wkv7_strerror(int status);
 
 /* Text of the last CUDA error seen by this library on the calling thread ("" if none). */

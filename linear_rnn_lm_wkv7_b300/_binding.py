@@ -37,6 +37,8 @@ SIGNATURES = {
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
     "wkv7_backward_noalloc": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
     "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
+    "wkv7_debug_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "wkv7_debug_enabled": (_I, []),
     "wkv7_strerror": (ctypes.c_char_p, [_I]),
     "wkv7_last_cuda_error": (ctypes.c_char_p, []),
     "wkv7_version": (_I, []),
@@ -254,3 +256,15 @@ def decode(state, r, w, k, v, a, b, y=None, stream=None):
                          _stream(stream))
     _check(st, "wkv7_decode")
     return y
+
+
+def debug_enabled() -> bool:
+    """True when the loaded library is the build with device-side index checks."""
+    return bool(lib.wkv7_debug_enabled())
+
+
+def debug_status() -> int:
+    """OR of the failed device-side index checks since the last call (0 = none; always 0 in release builds)."""
+    w = ctypes.c_uint(0)
+    _check(lib.wkv7_debug_status(ctypes.byref(w)), "wkv7_debug_status")
+    return w.value

@@ -188,6 +188,32 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t* 
   return WKV7_OK;
 }
 
+int wkv7_debug_status(unsigned* word) {
+  if (word == nullptr) return WKV7_ERR_ARG;
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return record_cuda(err);
+  int (*const readers[])(unsigned*) = {wkv7::debug_word_xop,   wkv7::debug_word_colmat, wkv7::debug_word_fwd,
+                                       wkv7::debug_word_fwdc,  wkv7::debug_word_chain,  wkv7::debug_word_bwd,
+                                       wkv7::debug_word_bwd2,  wkv7::debug_word_decode};
+  unsigned all = 0;
+  for (auto rd : readers) {
+    unsigned v = 0;
+    const int e = rd(&v);
+    if (e != 0) return record_cuda(static_cast<cudaError_t>(e));
+    all |= v;
+  }
+  *word = all;
+  return WKV7_OK;
+}
+
+int wkv7_debug_enabled(void) {
+#ifdef WKV7_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 int wkv7_decode(int B, int H, int D, int in_dtype, float* state, const void* r, const void* w, const void* k,
                 const void* v, const void* a, const void* b, float* y, void* stream) {
   int st = check_sizes(B, 1, H, D, 1);

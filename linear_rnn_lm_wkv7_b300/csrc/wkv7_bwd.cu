@@ -580,4 +580,6 @@ cudaError_t launch_backward(const BwdArgs& p, cudaStream_t stream) {
   return p.bf16 ? launch_bwd_t<__nv_bfloat16, false>(p, stream) : launch_bwd_t<float, false>(p, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_bwd)
+
 }  // namespace wkv7

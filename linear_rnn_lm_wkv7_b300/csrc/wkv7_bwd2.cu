@@ -461,4 +461,6 @@ cudaError_t launch_backward_two_phase(const BwdArgs& p, void* workspace, cudaStr
                 : launch_bwd2_t<float>(p, dsa_ws, xck_ws, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_bwd2)
+
 }  // namespace wkv7

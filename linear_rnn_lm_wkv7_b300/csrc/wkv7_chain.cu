@@ -800,4 +800,6 @@ cudaError_t launch_gwalk_transition(const BwdArgs& p, float* xck_ws, cudaStream_
                 : launch_chain_t<float, true>(p.B, p.T, p.H, p.nchunks, P, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_chain)
+
 }  // namespace wkv7

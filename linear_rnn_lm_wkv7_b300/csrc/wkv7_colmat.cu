@@ -215,7 +215,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         loc[u] = p;
         Wc[t * kD + j] = wt;
       }
-      BT[blk * 64 + j] = p;
+      if (WKV7_IN(blk, 4, dbg::kColmat)) BT[blk * 64 + j] = p;
     }
     __syncthreads();
     if (act) {
@@ -234,7 +234,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   __syncthreads();
   {  // chunks with tiny decays are left to colfb_kernel (token by token); the flag tells it which
     const bool flagged = (meta[0] | meta[1] | meta[2] | meta[3] | meta[4] | meta[5] | meta[6] | meta[7]) != 0;
-    if (tid == 0) flags[((size_t)bh * nchunks + ci) * xck_stride] = flagged ? 1 : 0;
+    if (tid == 0 && WKV7_IN(ci, nchunks, dbg::kColmat)) flags[((size_t)bh * nchunks + ci) * xck_stride] = flagged ? 1 : 0;
     if (flagged) {
       cp_async_wait<0>();
       return;
@@ -286,7 +286,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     float z = 0.f;
 #pragma unroll
     for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(gf[i * kD + j], sef[i * kD + j], z);
-    ZP[part * 64 + j] = z;
+    if (WKV7_IN(part, 4, dbg::kColmat)) ZP[part * 64 + j] = z;
   }
   // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
   {
@@ -617,7 +617,8 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         else if (prod < 4) sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
         else sc = make_float2(1.f, 1.f);
         const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
-        if (t < n) *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) = o;
+        if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
+          *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) = o;
         if (prod < 4) {
           float2 in = make_float2(0.f, 0.f);
           if (t < n) in = make_float2(to_f32(inp[t * kD + j]), to_f32(inp[t * kD + j + 1]));
@@ -648,7 +649,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         dsum[u] = tot;
         if (t >= 1 && t < n) tot += sADA[t * kD + j] + sRDR[(t - 1) * kD + j] - sKDK[t * kD + j] - sBDB[t * kD + j];
       }
-      BT[blk * 64 + j] = tot;
+      if (WKV7_IN(blk, 4, dbg::kColmat)) BT[blk * 64 + j] = tot;
     }
     __syncthreads();
     if (!act) return;
@@ -658,7 +659,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int t = 8 * blk + u;
-      if (t < n) {
+      if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat)) {
         const float wdw = zn + later + dsum[u] - sKDK[t * kD + j] - sBDB[t * kD + j];
         dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
       }
@@ -704,7 +705,7 @@ colfb_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, co
   float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
   const size_t tstride = (size_t)H * kD;
   for (int job = blockIdx.x; job < total; job += gridDim.x) {
-    if (flags[(size_t)job * xck_stride] == 0) continue;
+    if (!WKV7_IN(job, total, dbg::kColfb) || flags[(size_t)job * xck_stride] == 0) continue;
     const int ci = job % nchunks;
     const int bh = job / nchunks;
     const int bi = bh / H;
@@ -814,6 +815,8 @@ cudaError_t launch_colmat_t(const BwdArgs& p, const ChunkEnds& ends, cudaStream_
 }
 
 }  // namespace
+
+WKV7_DEBUG_READER(debug_word_colmat)
 
 cudaError_t launch_colgrad_matrix(const BwdArgs& p, const ChunkEnds& ends, cudaStream_t stream) {
   if (p.nchunks == 0) return cudaSuccess;

@@ -87,4 +87,6 @@ cudaError_t launch_decode(const DecodeArgs& p, cudaStream_t stream) {
   return p.bf16 ? launch_decode_t<__nv_bfloat16>(p, stream) : launch_decode_t<float>(p, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_decode)
+
 }  // namespace wkv7

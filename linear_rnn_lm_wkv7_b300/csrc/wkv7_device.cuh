@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "wkv7_debug.cuh"
+
 namespace wkv7 {
 
 constexpr int kD = 64;  // head size: the state is kD x kD fp32

@@ -333,4 +333,6 @@ cudaError_t launch_forward(const FwdArgs& p, cudaStream_t stream) {
   return launch_forward_sequential(p, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_fwd)
+
 }  // namespace wkv7

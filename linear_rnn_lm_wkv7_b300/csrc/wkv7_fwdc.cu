@@ -790,4 +790,6 @@ cudaError_t launch_gwalk_chunked(const BwdArgs& p, float* dsa_ws, float* xck_ws,
                 : launch_fwdc_t<float, true>(p.B, p.T, p.H, p.chunk, p.nchunks, P, stream);
 }
 
+WKV7_DEBUG_READER(debug_word_fwdc)
+
 }  // namespace wkv7

@@ -97,4 +97,14 @@ cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, cudaSt
 size_t forward_workspace_bytes(int B, int T, int H, int chunk);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// debug builds: each source file's device status word, read and cleared (release builds: 0)
+int debug_word_xop(unsigned* out);
+int debug_word_colmat(unsigned* out);
+int debug_word_fwd(unsigned* out);
+int debug_word_fwdc(unsigned* out);
+int debug_word_chain(unsigned* out);
+int debug_word_bwd(unsigned* out);
+int debug_word_bwd2(unsigned* out);
+int debug_word_decode(unsigned* out);
+
 }  // namespace wkv7

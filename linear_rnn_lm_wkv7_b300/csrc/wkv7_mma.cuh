@@ -20,6 +20,8 @@
 // is stored as an operand of the next product by its own lane with no shuffle.
 #pragma once
 
+#include "wkv7_debug.cuh"
+
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -187,16 +189,31 @@ struct RM {
   int ld;
 };
 
+// element offset of (r, c) for an access of w elements from column c.  Rows: lo / ld (lo = 0: a hi-only
+// array, rows unchecked); columns: ld - 8 (every array pads its rows by 8).  Debug builds record an
+// out-of-range access and use offset 0 instead.
+__device__ __forceinline__ int rm_off(const RM& x, int r, int c, int w) {
+#ifdef WKV7_DEBUG_CHECKS
+  const int rows = x.lo > 0 ? x.lo / x.ld : (1 << 30);
+  if (!WKV7_IN(r, rows, dbg::kOperand) || !WKV7_IN(c, x.ld - 8, dbg::kOperand) ||
+      !WKV7_IN(c + w - 1, x.ld - 8, dbg::kOperand))
+    return 0;
+#else
+  (void)w;
+#endif
+  return r * x.ld + c;
+}
+
 // A fragment (m-tile mt, k-tile kk) of X[m][k]
 __device__ __forceinline__ FragA rm_a(const RM& x, int mt, int kk, int lane) {
-  const int off = (mt * 16 + (lane & 15)) * x.ld + kk * 16 + (lane >> 4) * 8;
+  const int off = rm_off(x, mt * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8, 8);
   FragA f;
   ldsm4<false>(f.h, x.p + off);
   ldsm4<false>(f.l, x.p + x.lo + off);
   return f;
 }
 __device__ __forceinline__ FragA rm_a_hi(const RM& x, int mt, int kk, int lane) {
-  const int off = (mt * 16 + (lane & 15)) * x.ld + kk * 16 + (lane >> 4) * 8;
+  const int off = rm_off(x, mt * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8, 8);
   FragA f;
   ldsm4<false>(f.h, x.p + off);
   f.l[0] = f.l[1] = f.l[2] = f.l[3] = 0u;
@@ -204,14 +221,14 @@ __device__ __forceinline__ FragA rm_a_hi(const RM& x, int mt, int kk, int lane) 
 }
 // A fragment (mt, kk) of X^T, i.e. A[m][k] = X[k][m]
 __device__ __forceinline__ FragA rm_at(const RM& x, int mt, int kk, int lane) {
-  const int off = (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + mt * 16 + ((lane >> 3) & 1) * 8;
+  const int off = rm_off(x, kk * 16 + (lane & 7) + ((lane >> 4) << 3), mt * 16 + ((lane >> 3) & 1) * 8, 8);
   FragA f;
   ldsm4<true>(f.h, x.p + off);
   ldsm4<true>(f.l, x.p + x.lo + off);
   return f;
 }
 __device__ __forceinline__ FragA rm_at_hi(const RM& x, int mt, int kk, int lane) {
-  const int off = (kk * 16 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + mt * 16 + ((lane >> 3) & 1) * 8;
+  const int off = rm_off(x, kk * 16 + (lane & 7) + ((lane >> 4) << 3), mt * 16 + ((lane >> 3) & 1) * 8, 8);
   FragA f;
   ldsm4<true>(f.h, x.p + off);
   f.l[0] = f.l[1] = f.l[2] = f.l[3] = 0u;
@@ -219,7 +236,7 @@ __device__ __forceinline__ FragA rm_at_hi(const RM& x, int mt, int kk, int lane)
 }
 // B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = X[n][k] (a product "times X^T")
 __device__ __forceinline__ void rm_b2(const RM& x, int nt, int kk, int lane, FragB& b0, FragB& b1, bool with_lo = true) {
-  const int off = (nt * 8 + (lane & 7) + ((lane >> 4) << 3)) * x.ld + kk * 16 + ((lane >> 3) & 1) * 8;
+  const int off = rm_off(x, nt * 8 + (lane & 7) + ((lane >> 4) << 3), kk * 16 + ((lane >> 3) & 1) * 8, 8);
   uint32_t h[4], l[4] = {0u, 0u, 0u, 0u};
   ldsm4<false>(h, x.p + off);
   if (with_lo) ldsm4<false>(l, x.p + x.lo + off);
@@ -228,7 +245,7 @@ __device__ __forceinline__ void rm_b2(const RM& x, int nt, int kk, int lane, Fra
 }
 // B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = X[k][n] (a product "times X")
 __device__ __forceinline__ void rm_bt2(const RM& x, int nt, int kk, int lane, FragB& b0, FragB& b1, bool with_lo = true) {
-  const int off = (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * x.ld + nt * 8 + (lane >> 4) * 8;
+  const int off = rm_off(x, kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, nt * 8 + (lane >> 4) * 8, 8);
   uint32_t h[4], l[4] = {0u, 0u, 0u, 0u};
   ldsm4<true>(h, x.p + off);
   if (with_lo) ldsm4<true>(l, x.p + x.lo + off);
@@ -239,11 +256,12 @@ __device__ __forceinline__ void rm_bt2(const RM& x, int nt, int kk, int lane, Fr
 __device__ __forceinline__ void rm_store(const RM& x, int r, int c, float a, float b) {
   uint32_t hi, lo;
   split2(a, b, hi, lo);
-  *reinterpret_cast<uint32_t*>(x.p + r * x.ld + c) = hi;
-  *reinterpret_cast<uint32_t*>(x.p + x.lo + r * x.ld + c) = lo;
+  const int off = rm_off(x, r, c, 2);
+  *reinterpret_cast<uint32_t*>(x.p + off) = hi;
+  *reinterpret_cast<uint32_t*>(x.p + x.lo + off) = lo;
 }
 __device__ __forceinline__ void rm_store_hi(const RM& x, int r, int c, float a, float b) {
-  *reinterpret_cast<uint32_t*>(x.p + r * x.ld + c) = pack_bf16(a, b);
+  *reinterpret_cast<uint32_t*>(x.p + rm_off(x, r, c, 2)) = pack_bf16(a, b);
 }
 // accumulator tile (mt, nj) of a result into X
 __device__ __forceinline__ void rm_store_acc(const RM& x, int mt, int nj, int lane, const float (&c)[4]) {
@@ -258,17 +276,19 @@ __device__ __forceinline__ void rm_store8(const RM& x, int r, int c, const float
   split2(v[2], v[3], h.y, l.y);
   split2(v[4], v[5], h.z, l.z);
   split2(v[6], v[7], h.w, l.w);
-  *reinterpret_cast<uint4*>(x.p + r * x.ld + c) = h;
-  *reinterpret_cast<uint4*>(x.p + x.lo + r * x.ld + c) = l;
+  const int off = rm_off(x, r, c, 8);
+  *reinterpret_cast<uint4*>(x.p + off) = h;
+  *reinterpret_cast<uint4*>(x.p + x.lo + off) = l;
 }
 // fp32 values (hi + lo) at (r, c), (r, c + 1)
 __device__ __forceinline__ float2 rm_get2(const RM& x, int r, int c) {
-  return join2(*reinterpret_cast<const uint32_t*>(x.p + r * x.ld + c),
-               *reinterpret_cast<const uint32_t*>(x.p + x.lo + r * x.ld + c));
+  const int off = rm_off(x, r, c, 2);
+  return join2(*reinterpret_cast<const uint32_t*>(x.p + off), *reinterpret_cast<const uint32_t*>(x.p + x.lo + off));
 }
 // fp32 value (hi + lo) at (r, c)
 __device__ __forceinline__ float rm_get1(const RM& x, int r, int c) {
-  return __bfloat162float(x.p[r * x.ld + c]) + __bfloat162float(x.p[x.lo + r * x.ld + c]);
+  const int off = rm_off(x, r, c, 1);
+  return __bfloat162float(x.p[off]) + __bfloat162float(x.p[x.lo + off]);
 }
 // 8 values to row r, columns c..c+7 of an exact-bf16 operand (hi only): one 16-byte store
 __device__ __forceinline__ void rm_store8_hi(const RM& x, int r, int c, const float (&v)[8]) {
@@ -277,7 +297,7 @@ __device__ __forceinline__ void rm_store8_hi(const RM& x, int r, int c, const fl
   h.y = pack_bf16(v[2], v[3]);
   h.z = pack_bf16(v[4], v[5]);
   h.w = pack_bf16(v[6], v[7]);
-  *reinterpret_cast<uint4*>(x.p + r * x.ld + c) = h;
+  *reinterpret_cast<uint4*>(x.p + rm_off(x, r, c, 8)) = h;
 }
 // d[i] += A B[i] for split A and B, i < N: the three bf16 passes each over all N accumulators, so that
 // dependent mma into one accumulator are N instructions apart

@@ -1,14 +1,13 @@
 // wkv7_backward_noalloc: the two-phase backward with its scratch in a fixed array that
 // the library itself owns, for callers that cannot hand the library device memory.
 //
-// The scratch is one file-scope __device__ array.  Loading the library reserves it on
-// every GPU that loads it, for as long as the process lives.  In host code the array's
-// name is only a host-side stand-in for the device symbol, never a device address, so
-// its device address is looked up with cudaGetSymbolAddress -- once per device, on the
-// first call made with that device current -- and that address is what the kernels get.
+// The scratch is one file-scope __device__ array.  The CUDA runtime reserves it on a device when this
+// file's device code is loaded there (at the library's first use on that device under lazy module loading,
+// the default; when the library loads under eager loading) and keeps it until the process exits.  In host
+// code the array's name is only a host-side stand-in for the device symbol, never a device address, so its
+// device address is looked up with cudaGetSymbolAddress on every call, on the current device: a device that
+// was reset (cudaDeviceReset) gets the address of the array reloaded there, never a stale one.
 #include <stdint.h>
-
-#include <mutex>
 
 #include "wkv7.h"
 #include "wkv7_launch.h"
@@ -17,25 +16,13 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_backward_scratch[WKV7_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// device address of g_backward_scratch on the current device (looked up once per device)
+// device address of g_backward_scratch on the current device
 int scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t err = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_backward_scratch);
   if (err != cudaSuccess) return wkv7::record_cuda_status(err);
-  if (dev < 0 || dev >= kMaxDevices) return WKV7_ERR_ARG;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_backward_scratch);
-    if (err != cudaSuccess) return wkv7::record_cuda_status(err);
-    if (p == nullptr) return WKV7_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  if (p == nullptr) return WKV7_ERR_CUDA;
+  *out = p;
   return WKV7_OK;
 }
 

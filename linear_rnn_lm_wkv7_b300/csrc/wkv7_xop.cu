@@ -596,8 +596,9 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
-              make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+          if (WKV7_IN((mt * 8 + 2 * p + h) * 32 + lane, 1024, dbg::kXopPrep))
+            reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
+                make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
       } else {
         const int mt = (job - 16) >> 2, p = (job - 16) & 3;
 #pragma unroll
@@ -619,9 +620,9 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int tr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
-          if (tr < nm)
+          if (tr < nm && WKV7_IN(t0 + tr, T, dbg::kXopPrep) && WKV7_IN(col + 1, kD, dbg::kXopPrep))
             *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr) * tstride + col) = make_float2(acc[h][0], acc[h][1]);
-          if (tr + 8 < nm)
+          if (tr + 8 < nm && WKV7_IN(t0 + tr + 8, T, dbg::kXopPrep))
             *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr + 8) * tstride + col) =
                 make_float2(acc[h][2], acc[h][3]);
         }
@@ -644,8 +645,9 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
-            make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        if (WKV7_IN((mt * 8 + 2 * p + h) * 32 + lane, 1024, dbg::kXopPrep))
+          reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
+              make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
     }
   }
 }
@@ -794,7 +796,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
         bulk_g2s(st + ST::oX, src + kXX + rb * NW * 4096, NW * 4096, &full[s]);
       }
       __syncwarp();
-      if (!WALK && lane < nm)
+      if (!WALK && lane < nm && WKV7_IN(c * kL + lane, T, dbg::kXopChain) && WKV7_IN(rb * R + R - 1, kD, dbg::kXopChain))
         bulk_g2s(st + ST::oY + lane * ST::kYL * 4, y + base + (size_t)(c * kL + lane) * tstride + rb * R, R * 4,
                  &full[s]);
       issued = n + 1;
@@ -824,6 +826,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     }
   }
   auto store_rows = [&](float* dst) {
+    if (!WKV7_IN(row + 8, kD, dbg::kXopChain)) return;
 #pragma unroll
     for (int nj = 0; nj < 8; ++nj) {
       *reinterpret_cast<float2*>(dst + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
@@ -971,6 +974,8 @@ cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned ch
 }
 
 }  // namespace
+
+WKV7_DEBUG_READER(debug_word_xop)
 
 size_t xop_workspace_bytes(int B, int T, int H) {
   const size_t C = ((size_t)T + kL - 1) / kL;

@@ -111,3 +111,26 @@ def test_cpu_baseline_reports_pool_and_single_thread():
     cb = bench.cpu_baseline(gen.WORKLOADS["oracle_b1_t128_h2"], 0.2)
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+
+
+def test_reference_arm_config_is_the_workload_config():
+    """Both arms print the same `config` object for the same workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import wkv7_inputs as gen
+
+    class A:
+        workload = "oracle_b1_t128_h2"
+        steps = 1
+        warmup = 0
+
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(A, rank=0, world=1)
+    line = json.loads(buf.getvalue())
+    assert line["config"] == bench.workload_config(gen.WORKLOADS["oracle_b1_t128_h2"])
+
+
+def test_bench_reads_no_markdown():
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert ".md" not in src

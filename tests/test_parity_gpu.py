@@ -305,17 +305,18 @@ def test_backward_is_deterministic(wkv7, mode):
         assert np.array_equal(ga, gb)
 
 
-def test_backward_without_sa_is_the_two_phase_path(wkv7):
-    """The backward called without the forward's sa (the plain forward's outputs only) and with a workspace
-    gives the same gradients as with sa: at chunk 32 the column gradients recompute sa themselves."""
+def test_backward_paths_agree(wkv7):
+    """The backward without the forward's sa (the chunk-operator path: operators, walk, matrix column
+    gradients) and with it (the two-phase path) are different kernels computing the same gradients;
+    they agree to ~1e-5 (each is checked against the oracle in the workload tests)."""
     x = gen.random_small(10, B=2, T=96, H=3, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
     ins = [dev(x[n], "bf16") for n in "rwkvab"]
     h0 = dev32(x["h0"])
     y, ck, hT, sa = wkv7.forward(*ins, h0, save_sa=True, kernel="sequential")
     g1 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=sa)
     g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=None, workspace="auto")
-    for p_, q_ in zip(g1, g2):
-        assert torch.equal(p_, q_)
+    for name, p_, q_ in zip(("dr", "dw", "dk", "dv", "da", "db", "dh0"), g1, g2):
+        assert rel(host(q_), host(p_).astype(np.float64)) <= 5e-5, name
 
 
 def test_explicit_workspace_and_too_small_workspace(wkv7):
