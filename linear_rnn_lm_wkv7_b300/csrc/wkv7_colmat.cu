@@ -376,43 +376,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
 #pragma unroll
     for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
     __syncwarp();
-    {  // T21 = T22 A21 T11 (A21 = M_ab[16..31][0..15]) on tensor cores, transposed:
-       // E^T = T11^T A21^T, then T21^T = E^T T22^T (rows s, columns t)
-      auto ld2 = [&](const float* p0, const float* p1, uint32_t& hw, uint32_t& lw) { split2(*p0, *p1, hw, lw); };
-      FragA fa;  // T11^T: A[s][u] = T11[u][s]
-      ld2(TI + (2 * q) * SM + g, TI + (2 * q + 1) * SM + g, fa.h[0], fa.l[0]);
-      ld2(TI + (2 * q) * SM + g + 8, TI + (2 * q + 1) * SM + g + 8, fa.h[1], fa.l[1]);
-      ld2(TI + (2 * q + 8) * SM + g, TI + (2 * q + 9) * SM + g, fa.h[2], fa.l[2]);
-      ld2(TI + (2 * q + 8) * SM + g + 8, TI + (2 * q + 9) * SM + g + 8, fa.h[3], fa.l[3]);
-      FragB fb[2];  // A21^T: B[u][t] = A21[t][u]
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float* row = Mab + (16 + nt * 8 + g) * SM;
-        ld2(row + 2 * q, row + 2 * q + 1, fb[nt].h[0], fb[nt].l[0]);
-        ld2(row + 2 * q + 8, row + 2 * q + 9, fb[nt].h[1], fb[nt].l[1]);
-      }
-      float et[2][4] = {};
-      mma3n<2>(et, fa, fb);
-      const FragA fe = frag_from_acc(et[0], et[1]);  // E^T as an A operand (rows s, k = t')
-      FragB fc[2];  // T22^T: B[t'][t] = T22[t][t']
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float* row = TI + (16 + nt * 8 + g) * SM + 16;
-        ld2(row + 2 * q, row + 2 * q + 1, fc[nt].h[0], fc[nt].l[0]);
-        ld2(row + 2 * q + 8, row + 2 * q + 9, fc[nt].h[1], fc[nt].l[1]);
-      }
-      float tt[2][4] = {};
-      mma3n<2>(tt, fe, fc);
-      __syncwarp();
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {  // T21[t][s] from T21^T (rows s = g, g + 8; columns t = 8 nt + 2q, + 1)
-        const int t = nt * 8 + 2 * q;
-        TI[(16 + t) * SM + g] = tt[nt][0];
-        TI[(17 + t) * SM + g] = tt[nt][1];
-        TI[(16 + t) * SM + g + 8] = tt[nt][2];
-        TI[(17 + t) * SM + g + 8] = tt[nt][3];
-      }
-    }
+    tri_inverse_t21(Mab, TI, SM, lane);  // T21 = T22 A21 T11 (A21 = M_ab[16..31][0..15])
   } else {
     for (int job = warp - 1; job < 16; job += kNW - 1) {
       const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1

@@ -338,6 +338,21 @@ __device__ __forceinline__ void mma3n_two(float (&d0)[N][4], const FragA& a0, co
     mma16816(d1[i], a1.h, b1[i].h[0], b1[i].h[1]);
   }
 }
+// ... with exact-bf16 A0, A1 (hi only) and a split B shared by both: d0[i] += A0 B[i], d1[i] += A1 B[i]
+template <int N>
+__device__ __forceinline__ void mma2n_two(float (&d0)[N][4], const FragA& a0, float (&d1)[N][4], const FragA& a1,
+                                          const FragB (&b)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.h, b[i].l[0], b[i].l[1]);
+    mma16816(d1[i], a1.h, b[i].l[0], b[i].l[1]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mma16816(d0[i], a0.h, b[i].h[0], b[i].h[1]);
+    mma16816(d1[i], a1.h, b[i].h[0], b[i].h[1]);
+  }
+}
 // ... with an exact-bf16 B (hi only) shared by both: d0[i] += A0 B[i], d1[i] += A1 B[i]
 template <int N>
 __device__ __forceinline__ void mma2b_two(float (&d0)[N][4], const FragA& a0, float (&d1)[N][4], const FragA& a1,
@@ -353,6 +368,48 @@ __device__ __forceinline__ void mma2b_two(float (&d0)[N][4], const FragA& a0, fl
     mma16816(d1[i], a1.h, b[i].h[0], b[i].h[1]);
   }
 }
+// The off-diagonal block of T = (I - M)^-1 for a strictly lower 32 x 32 M (fp32, row stride sm) once the
+// diagonal blocks T11, T22 are in TI (fp32, stride sm): T21 = T22 M21 T11, formed by one warp on tensor
+// cores in transposed form (E^T = T11^T M21^T, then T21^T = E^T T22^T) and written into TI rows 16-31,
+// columns 0-15.  Every lane of the warp calls it.
+__device__ __forceinline__ void tri_inverse_t21(const float* M, float* TI, int sm, int lane) {
+  const int g = lane >> 2, q = lane & 3;
+  auto ld2 = [&](const float* p0, const float* p1, uint32_t& hw, uint32_t& lw) { split2(*p0, *p1, hw, lw); };
+  FragA fa;  // T11^T: A[s][u] = T11[u][s]
+  ld2(TI + (2 * q) * sm + g, TI + (2 * q + 1) * sm + g, fa.h[0], fa.l[0]);
+  ld2(TI + (2 * q) * sm + g + 8, TI + (2 * q + 1) * sm + g + 8, fa.h[1], fa.l[1]);
+  ld2(TI + (2 * q + 8) * sm + g, TI + (2 * q + 9) * sm + g, fa.h[2], fa.l[2]);
+  ld2(TI + (2 * q + 8) * sm + g + 8, TI + (2 * q + 9) * sm + g + 8, fa.h[3], fa.l[3]);
+  FragB fb[2];  // M21^T: B[u][t] = M[16 + t][u]
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const float* row = M + (16 + nt * 8 + g) * sm;
+    ld2(row + 2 * q, row + 2 * q + 1, fb[nt].h[0], fb[nt].l[0]);
+    ld2(row + 2 * q + 8, row + 2 * q + 9, fb[nt].h[1], fb[nt].l[1]);
+  }
+  float et[2][4] = {};
+  mma3n<2>(et, fa, fb);
+  const FragA fe = frag_from_acc(et[0], et[1]);  // E^T as an A operand (rows s, k = t')
+  FragB fc[2];  // T22^T: B[t'][t] = T22[t][t']
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const float* row = TI + (16 + nt * 8 + g) * sm + 16;
+    ld2(row + 2 * q, row + 2 * q + 1, fc[nt].h[0], fc[nt].l[0]);
+    ld2(row + 2 * q + 8, row + 2 * q + 9, fc[nt].h[1], fc[nt].l[1]);
+  }
+  float tt[2][4] = {};
+  mma3n<2>(tt, fe, fc);
+  __syncwarp();
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {  // T21[t][s] from T21^T (rows s = g, g + 8; columns t = 8 nt + 2q, + 1)
+    const int t = nt * 8 + 2 * q;
+    TI[(16 + t) * sm + g] = tt[nt][0];
+    TI[(17 + t) * sm + g] = tt[nt][1];
+    TI[(16 + t) * sm + g + 8] = tt[nt][2];
+    TI[(17 + t) * sm + g + 8] = tt[nt][3];
+  }
+}
+
 // d += A B for split A and an exact-bf16 B (hi only)
 __device__ __forceinline__ void mma2b(float (&d)[4], const FragA& a, const FragB& b) {
   mma16816(d, a.l, b.h[0], b.h[1]);

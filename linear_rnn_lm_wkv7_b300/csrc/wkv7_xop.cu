@@ -107,15 +107,16 @@ struct XPrepLay {
   static constexpr int oC = oBp + rmb(32, kLD64);
   static constexpr int oP = oC + rmb(32, kLD32);  // P (forward) or Q as RM [64 j][32 t] (backward)
   static constexpr int kP = BWD ? rmb(64, kLD32) : rmb(32, kLD32);
-  static constexpr int oGL = oP + kP;  // fp32 [64], then int [4]
-  static constexpr int kBytes = oGL + 64 * 4 + 16;
+  static constexpr int oGL = oP + kP;  // fp32 [64], then int [8]
+  static constexpr int oBT = oGL + 64 * 4 + 32;  // fp32 [4][64]: block products of the gamma scan
+  static constexpr int kBytes = oBT + 4 * 64 * 4;
   // token-by-token path: q_t as fp32 [64 j][33] over A^
   static constexpr int oQf = oAh;
   static_assert(64 * 33 * 4 <= rmb(32, kLD64), "q_t fit over A^");
 };
 
 template <typename Tin, bool BWD>
-__global__ void __launch_bounds__(kNTP)
+__global__ void __launch_bounds__(kNTP, 2)  // two CTAs per SM (bf16 inputs: ~93 KB of shared memory each)
 xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
                 const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
                 const Tin* __restrict__ b, const float* __restrict__ dy, unsigned char* __restrict__ ops,
@@ -167,7 +168,6 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
   float* Mab = reinterpret_cast<float*>(sm + LY::oMab);
   float* TI = reinterpret_cast<float*>(sm + LY::oTI);
-  float* E = reinterpret_cast<float*>(sm + LY::oE);
 
   {  // the chunk's inputs (rows past the chunk are not copied)
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
@@ -189,23 +189,35 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   }
   __syncthreads();
 
-  if (tid < kD) {  // gamma_t down each column; the token-by-token flag
-    const int j = tid;
-    float gm = 1.f;
-#pragma unroll 8
-    for (int t = 0; t < kL; ++t) {
-      const float wt = t < nm ? to_f32(rw[t * kD + j]) : 1.f;
-      gm *= wt;
-      G[t * kD + j] = gm;
+  {  // gamma_t down each column as a scan: column j, tokens 8 blk .. 8 blk + 7; the token-by-token flag
+    float* BT = reinterpret_cast<float*>(sm + LY::oBT);
+    const int j = tid & 63, blk = tid >> 6;
+    float loc[8];
+    float p = 1.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = 8 * blk + u;
+      p *= t < nm ? to_f32(rw[t * kD + j]) : 1.f;
+      loc[u] = p;
     }
-    GL[j] = gm;
-    const bool bad = !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+    BT[blk * 64 + j] = p;
+    __syncthreads();
+    float pre = 1.f;
+    for (int q2 = 0; q2 < blk; ++q2) pre *= BT[q2 * 64 + j];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) G[(8 * blk + u) * kD + j] = pre * loc[u];
+    bool bad = false;
+    if (blk == 3) {
+      const float gm = pre * p;
+      GL[j] = gm;
+      bad = !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+    }
     const unsigned any = __ballot_sync(0xffffffffu, bad);
     if (lane == 0) meta[warp] = any != 0u;
   }
   __syncthreads();
 
-  if ((meta[0] | meta[1]) != 0) {
+  if ((meta[0] | meta[1] | meta[2] | meta[3] | meta[4] | meta[5] | meta[6] | meta[7]) != 0) {
     // ======== token by token: rows j of A_c from e_j (threads 0-63), rows i of U_c from 0 (64-127, forward)
     float* Qf = reinterpret_cast<float*>(sm + LY::oQf);
     if (tid < 64) {
@@ -328,43 +340,42 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   __syncthreads();  // raw inputs and gamma consumed: the coupling matrices reuse their space
 
   // M_ab = tril(A^ B~^T, -1) (fp32), M_rb = tril(R^ B~^T), and (forward) M_ak = tril(A^ K~^T, -1),
-  // M_rk = tril(R^ K~^T)
+  // M_rk = tril(R^ K~^T).  Warp w forms the same tile (m-tile (w >> 1) & 1, n-tiles 2 (w & 1) + 0, 1) of
+  // (M_ab, M_rb) (w < 4) or (M_ak, M_rk) (w >= 4, forward only), each pair sharing B~ or K~.
   {
-    constexpr int NP = BWD ? 2 : 4;
-    for (int job = warp; job < NP * 4; job += 8) {
-      const int prod = BWD ? 2 * (job >> 2) : (job >> 2);
-      const int mt = (job >> 1) & 1, np = job & 1;
-      const bool strict = prod < 2;
-      float acc[2][4] = {};
+    const int prodA = warp >> 2, mt = (warp >> 1) & 1, np = warp & 1;  // prodB = prodA + 2
+    if (!(BWD && prodA == 1)) {
+      float acc[2][2][4] = {};
       if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
-        const RM& X = prod < 2 ? Ah : Rh;
-        const RM& Y = (prod & 1) ? Kt : Bt;
+        const RM& Y = prodA ? Kt : Bt;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const FragA fa = rm_a(X, mt, kk, lane);
-          FragB f0, f1;
-          rm_b2(Y, 2 * np, kk, lane, f0, f1);
-          {
-            const FragB fb2[2] = {f0, f1};
-            mma3n<2>(acc, fa, fb2);
-          }
+          const FragA fa0 = rm_a(Ah, mt, kk, lane), fa1 = rm_a(Rh, mt, kk, lane);
+          FragB fb[2];
+          rm_b2(Y, 2 * np, kk, lane, fb[0], fb[1]);
+          mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
         }
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int nj = 2 * np + h;
-        const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
-        float c[4];
+      for (int jb = 0; jb < 2; ++jb) {
+        const int prod = prodA + 2 * jb;
+        const bool strict = prod < 2;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tt = tr + ((e >> 1) << 3), s = sc + (e & 1);
-          c[e] = (strict ? s < tt : s <= tt) ? acc[h][e] : 0.f;
-        }
-        if (prod == 0) {
-          *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
-          *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
-        } else {
-          rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
+        for (int h = 0; h < 2; ++h) {
+          const int nj = 2 * np + h;
+          const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+          float c[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tt = tr + ((e >> 1) << 3), s2 = sc + (e & 1);
+            c[e] = (strict ? s2 < tt : s2 <= tt) ? acc[jb][h][e] : 0.f;
+          }
+          if (prod == 0) {
+            *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+            *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
+          } else {
+            rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
+          }
         }
       }
     }
@@ -372,7 +383,7 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   __syncthreads();
 
   // T = (I - M_ab)^-1 by blocks of 16: diagonal blocks by forward substitution (one column per lane),
-  // then T21 = T22 A21 T11
+  // then T21 = T22 A21 T11 on tensor cores, all on warp 0
   if (warp == 0) {
     const int off = lane < 16 ? 0 : 16;
     const int c = lane & 15;
@@ -386,22 +397,8 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
     }
 #pragma unroll
     for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
-  }
-  __syncthreads();
-  {
-    const int t = tid >> 4, s = tid & 15;
-    float acc = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) acc = fmaf(Mab[(16 + t) * SM + u], TI[u * SM + s], acc);
-    E[t * 16 + s] = acc;
-  }
-  __syncthreads();
-  {
-    const int t = tid >> 4, s = tid & 15;
-    float acc = 0.f;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) acc = fmaf(TI[(16 + t) * SM + 16 + u], E[u * 16 + s], acc);
-    TI[(16 + t) * SM + s] = acc;
+    __syncwarp();
+    tri_inverse_t21(Mab, TI, SM, lane);
   }
   __syncthreads();
   if (tid < 128) {
@@ -456,82 +453,80 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   __syncthreads();
 
   // A_c = diag(gamma_L) + A^^T B' and Q_c = R^^T + A^^T C^T (rows j); forward: K' = K~ diag(gamma_L) +
-  // M_ak^T B' (over B~) and P = M_rk + C M_ak
+  // M_ak^T B' (over B~) and P = M_rk + C M_ak.  Warp w: the A_c tiles (m-tiles w >> 2 and (w >> 2) + 2,
+  // n-tiles 2 (w & 3) + 0, 1; B' shared), then one Q_c tile, one K' tile and (w < 4) one P tile.
   {
-    constexpr int NJ = BWD ? 24 : 36;
-    for (int job = warp; job < NJ; job += 8) {
-      float acc[2][4] = {};
-      if (job < 16) {
-        const int mt = job >> 2, p = job & 3;
+    {
+      const int mt0 = warp >> 2, p = warp & 3;
+      float acc[2][2][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const FragA fa = rm_at(Ah, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(Bp, 2 * p, kk, lane, f0, f1);
-          {
-            const FragB fb2[2] = {f0, f1};
-            mma3n<2>(acc, fa, fb2);
-          }
-        }
+      for (int kk = 0; kk < 2; ++kk) {
+        FragB fb[2];
+        rm_bt2(Bp, 2 * p, kk, lane, fb[0], fb[1]);
+        const FragA fa0 = rm_at(Ah, mt0, kk, lane), fa1 = rm_at(Ah, mt0 + 2, kk, lane);
+        mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
+      }
+#pragma unroll
+      for (int jb = 0; jb < 2; ++jb)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int jr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
-          if (jr == col) acc[h][0] += GL[col];
-          if (jr == col + 1) acc[h][1] += GL[col + 1];
-          if (jr + 8 == col) acc[h][2] += GL[col];
-          if (jr + 8 == col + 1) acc[h][3] += GL[col + 1];
+          const int jr = (mt0 + 2 * jb) * 16 + g, col = (2 * p + h) * 8 + 2 * q;
+          float* c = acc[jb][h];
+          if (jr == col) c[0] += GL[col];
+          if (jr == col + 1) c[1] += GL[col + 1];
+          if (jr + 8 == col) c[2] += GL[col];
+          if (jr + 8 == col + 1) c[3] += GL[col + 1];
           uint32_t hw, lw;
-          split2(acc[h][0], acc[h][1], hw, lw);
+          split2(c[0], c[1], hw, lw);
           *reinterpret_cast<uint32_t*>(gA + swz_a(jr, col)) = hw;
           *reinterpret_cast<uint32_t*>(gA + 4096 + swz_a(jr, col)) = lw;
-          split2(acc[h][2], acc[h][3], hw, lw);
+          split2(c[2], c[3], hw, lw);
           *reinterpret_cast<uint32_t*>(gA + swz_a(jr + 8, col)) = hw;
           *reinterpret_cast<uint32_t*>(gA + 4096 + swz_a(jr + 8, col)) = lw;
         }
-      } else if (job < 24) {
-        const int mt = (job - 16) >> 1, p = (job - 16) & 1;
+    }
+    {  // Q_c: m-tile w >> 1, n-tiles 2 (w & 1) + 0, 1
+      const int mt = warp >> 1, p = warp & 1;
+      float acc[2][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          if (p == 0 && kk == 1) continue;  // C[t][s] = 0 for s > t
-          const FragA fa = rm_at(Ah, mt, kk, lane);
-          FragB f0, f1;
-          rm_b2(Cm, 2 * p, kk, lane, f0, f1);
-          {
-            const FragB fb2[2] = {f0, f1};
-            mma3n<2>(acc, fa, fb2);
-          }
-        }
+      for (int kk = 0; kk < 2; ++kk) {
+        if (p == 0 && kk == 1) continue;  // C[t][s] = 0 for s > t
+        const FragA fa = rm_at(Ah, mt, kk, lane);
+        FragB fb[2];
+        rm_b2(Cm, 2 * p, kk, lane, fb[0], fb[1]);
+        mma3n<2>(acc, fa, fb);
+      }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int jr = mt * 16 + g, tc = (2 * p + h) * 8 + 2 * q;
-          acc[h][0] += rm_get1(Rh, tc, jr);
-          acc[h][1] += rm_get1(Rh, tc + 1, jr);
-          acc[h][2] += rm_get1(Rh, tc, jr + 8);
-          acc[h][3] += rm_get1(Rh, tc + 1, jr + 8);
-          if (BWD) {
-            rm_store_acc(Qs, mt, 2 * p + h, lane, acc[h]);
-          } else {
-            uint32_t hw, lw;
-            split2(acc[h][0], acc[h][1], hw, lw);
-            *reinterpret_cast<uint32_t*>(gQ + swz_q(jr, tc)) = hw;
-            *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr, tc)) = lw;
-            split2(acc[h][2], acc[h][3], hw, lw);
-            *reinterpret_cast<uint32_t*>(gQ + swz_q(jr + 8, tc)) = hw;
-            *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr + 8, tc)) = lw;
-          }
+      for (int h = 0; h < 2; ++h) {
+        const int jr = mt * 16 + g, tc = (2 * p + h) * 8 + 2 * q;
+        acc[h][0] += rm_get1(Rh, tc, jr);
+        acc[h][1] += rm_get1(Rh, tc + 1, jr);
+        acc[h][2] += rm_get1(Rh, tc, jr + 8);
+        acc[h][3] += rm_get1(Rh, tc + 1, jr + 8);
+        if (BWD) {
+          rm_store_acc(Qs, mt, 2 * p + h, lane, acc[h]);
+        } else {
+          uint32_t hw, lw;
+          split2(acc[h][0], acc[h][1], hw, lw);
+          *reinterpret_cast<uint32_t*>(gQ + swz_q(jr, tc)) = hw;
+          *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr, tc)) = lw;
+          split2(acc[h][2], acc[h][3], hw, lw);
+          *reinterpret_cast<uint32_t*>(gQ + swz_q(jr + 8, tc)) = hw;
+          *reinterpret_cast<uint32_t*>(gQ + 2048 + swz_q(jr + 8, tc)) = lw;
         }
-      } else if (job < 32) {
-        const int mt = (job - 24) >> 2, nq = (job - 24) & 3;
+      }
+    }
+    if (!BWD) {
+      {  // K': m-tile w >> 2, n-tiles 2 (w & 3) + 0, 1
+        const int mt = warp >> 2, nq = warp & 3;
+        float acc[2][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           if (mt == 1 && kk == 0) continue;
           const FragA fa = rm_at(Mak, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(Bp, 2 * nq, kk, lane, f0, f1);
-          {
-            const FragB fb2[2] = {f0, f1};
-            mma3n<2>(acc, fa, fb2);
-          }
+          FragB fb[2];
+          rm_bt2(Bp, 2 * nq, kk, lane, fb[0], fb[1]);
+          mma3n<2>(acc, fa, fb);
         }
         // K~ is read here for the last time and K' written over B~ (read for the last time by B')
 #pragma unroll
@@ -546,18 +541,17 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
           acc[h][3] = fmaf(k8.y, gl.y, acc[h][3]);
           rm_store_acc(Kp, mt, 2 * nq + h, lane, acc[h]);
         }
-      } else {
-        const int mt = (job - 32) >> 1, np = (job - 32) & 1;
+      }
+      if (warp < 4) {  // P: m-tile w >> 1, n-tiles 2 (w & 1) + 0, 1
+        const int mt = warp >> 1, np = warp & 1;
+        float acc[2][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           if (mt == 0 && kk == 1) continue;
           const FragA fa = rm_a(Cm, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(Mak, 2 * np, kk, lane, f0, f1);
-          {
-            const FragB fb2[2] = {f0, f1};
-            mma3n<2>(acc, fa, fb2);
-          }
+          FragB fb[2];
+          rm_bt2(Mak, 2 * np, kk, lane, fb[0], fb[1]);
+          mma3n<2>(acc, fa, fb);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -572,82 +566,63 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   }
   __syncthreads();
 
-  if (!BWD) {
-    // U_c = V^T K' (rows i, mma accumulator order) and Y_intra = P V (rows t, into y)
-    for (int job = warp; job < 24; job += 8) {
-      float acc[2][4] = {};
-      if (job < 16) {
-        const int mt = job >> 2, p = job & 3;
+  // U_c = V^T K' (forward) or E_c = DY^T Q_c^T (backward), rows i in mma accumulator order: warp w forms
+  // m-tiles w >> 2 and (w >> 2) + 2 at n-tiles 2 (w & 3) + 0, 1 (sharing K' or Q_c); the forward then forms
+  // Y_intra = P V at m-tile w >> 2, n-tiles 2 (w & 3) + 0, 1 into y
+  {
+    const int mt0 = warp >> 2, p = warp & 3;
+    float acc[2][2][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          FragB f0, f1;
-          rm_bt2(Kp, 2 * p, kk, lane, f0, f1);
-          if (kVExact) {
-            const FragA fa = rm_at_hi(Vm, mt, kk, lane);
-            mma2(acc[0], fa, f0);
-            mma2(acc[1], fa, f1);
-          } else {
-            const FragA fa = rm_at(Vm, mt, kk, lane);
-            {
-              const FragB fb2[2] = {f0, f1};
-              mma3n<2>(acc, fa, fb2);
-            }
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (WKV7_IN((mt * 8 + 2 * p + h) * 32 + lane, 1024, dbg::kXopPrep))
-            reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
-                make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    for (int kk = 0; kk < 2; ++kk) {
+      FragB fb[2];
+      if (BWD) {
+        rm_b2(Qs, 2 * p, kk, lane, fb[0], fb[1]);
+        const FragA fa0 = rm_at(DYm, mt0, kk, lane), fa1 = rm_at(DYm, mt0 + 2, kk, lane);
+        mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
       } else {
-        const int mt = (job - 16) >> 2, p = (job - 16) & 3;
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          if (mt == 0 && kk == 1) continue;  // P lower triangular
-          const FragA fa = rm_a(Pm, mt, kk, lane);
-          FragB f0, f1;
-          rm_bt2(Vm, 2 * p, kk, lane, f0, f1, !kVExact);
-          if (kVExact) {
-            mma2b(acc[0], fa, f0);
-            mma2b(acc[1], fa, f1);
-          } else {
-            {
-              const FragB fb2[2] = {f0, f1};
-              mma3n<2>(acc, fa, fb2);
-            }
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int tr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
-          if (tr < nm && WKV7_IN(t0 + tr, T, dbg::kXopPrep) && WKV7_IN(col + 1, kD, dbg::kXopPrep))
-            *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr) * tstride + col) = make_float2(acc[h][0], acc[h][1]);
-          if (tr + 8 < nm && WKV7_IN(t0 + tr + 8, T, dbg::kXopPrep))
-            *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr + 8) * tstride + col) =
-                make_float2(acc[h][2], acc[h][3]);
+        rm_bt2(Kp, 2 * p, kk, lane, fb[0], fb[1]);
+        if (kVExact) {
+          const FragA fa0 = rm_at_hi(Vm, mt0, kk, lane), fa1 = rm_at_hi(Vm, mt0 + 2, kk, lane);
+          mma2n_two<2>(acc[0], fa0, acc[1], fa1, fb);
+        } else {
+          const FragA fa0 = rm_at(Vm, mt0, kk, lane), fa1 = rm_at(Vm, mt0 + 2, kk, lane);
+          mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
         }
       }
     }
-  } else {
-    // E_c = DY^T Q_c^T (rows i, mma accumulator order)
-    for (int job = warp; job < 16; job += 8) {
-      const int mt = job >> 2, p = job & 3;
-      float acc[2][4] = {};
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const FragA fa = rm_at(DYm, mt, kk, lane);
-        FragB f0, f1;
-        rm_b2(Qs, 2 * p, kk, lane, f0, f1);
-        {
-          const FragB fb2[2] = {f0, f1};
-          mma3n<2>(acc, fa, fb2);
-        }
+    for (int jb = 0; jb < 2; ++jb)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int idx = ((mt0 + 2 * jb) * 8 + 2 * p + h) * 32 + lane;
+        if (WKV7_IN(idx, 1024, dbg::kXopPrep))
+          reinterpret_cast<float4*>(gX)[idx] = make_float4(acc[jb][h][0], acc[jb][h][1], acc[jb][h][2], acc[jb][h][3]);
       }
+  }
+  if (!BWD) {
+    const int mt = warp >> 2, p = warp & 3;
+    float acc[2][4] = {};
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (WKV7_IN((mt * 8 + 2 * p + h) * 32 + lane, 1024, dbg::kXopPrep))
-          reinterpret_cast<float4*>(gX)[(mt * 8 + 2 * p + h) * 32 + lane] =
-              make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    for (int kk = 0; kk < 2; ++kk) {
+      if (mt == 0 && kk == 1) continue;  // P lower triangular
+      const FragA fa = rm_a(Pm, mt, kk, lane);
+      FragB fb[2];
+      rm_bt2(Vm, 2 * p, kk, lane, fb[0], fb[1], !kVExact);
+      if (kVExact) {
+        mma2b(acc[0], fa, fb[0]);
+        mma2b(acc[1], fa, fb[1]);
+      } else {
+        mma3n<2>(acc, fa, fb);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int tr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
+      if (tr < nm && WKV7_IN(t0 + tr, T, dbg::kXopPrep) && WKV7_IN(col + 1, kD, dbg::kXopPrep))
+        *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr) * tstride + col) = make_float2(acc[h][0], acc[h][1]);
+      if (tr + 8 < nm && WKV7_IN(t0 + tr + 8, T, dbg::kXopPrep))
+        *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr + 8) * tstride + col) =
+            make_float2(acc[h][2], acc[h][3]);
     }
   }
 }
