@@ -668,87 +668,99 @@ colfb_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, co
   const Tin* rv = raw + 5 * kL * kD;
   float* dyr = reinterpret_cast<float*>(sm + LY::oDyRaw);
   const size_t tstride = (size_t)H * kD;
-  for (int job = blockIdx.x; job < total; job += gridDim.x) {
-    if (!WKV7_IN(job, total, dbg::kColfb) || flags[(size_t)job * xck_stride] == 0) continue;
-    const int ci = job % nchunks;
-    const int bh = job / nchunks;
-    const int bi = bh / H;
-    const int hi = bh - bi * H;
-    const int t0 = ci * kL;
-    const int n = min(kL, T - t0);
-    const size_t base = ((size_t)bi * T * H + hi) * kD;
-    const float* gend = xck + (size_t)job * xck_stride;
-    const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
-                             : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
+  __shared__ int fl[kNTF];
+  // this CTA's chunks are blockIdx.x + gridDim.x * m; their flags are read kNTF at a time, in parallel
+  for (int m0 = 0; blockIdx.x + (size_t)gridDim.x * m0 < (size_t)total; m0 += kNTF) {
     {
-      constexpr int CPR = kD * (int)sizeof(Tin) / 16;
-      constexpr int EPC = 16 / (int)sizeof(Tin);
-      const Tin* srcs[6] = {w, k, a, b, r, v};
-#pragma unroll
-      for (int s6 = 0; s6 < 6; ++s6)
-        for (int e = tid; e < n * CPR; e += kNTF) {
-          const int tt = e / CPR, pc = e % CPR;
-          cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
-        }
-      for (int e = tid; e < n * (kD / 4); e += kNTF) {
-        const int tt = e / (kD / 4), pc = e % (kD / 4);
-        cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
+      const size_t jt = blockIdx.x + (size_t)gridDim.x * (m0 + tid);
+      fl[tid] = (jt < (size_t)total && flags[jt * xck_stride] != 0) ? 1 : 0;
     }
-    __syncthreads();
-    float* fsa = reinterpret_cast<float*>(sm + LY::oFSa);
-    float* fdsa = reinterpret_cast<float*>(sm + LY::oFDsa);
-    float* fv = reinterpret_cast<float*>(sm + LY::oFV);
-    for (int e = tid; e < n * kD; e += kNTF) fv[e] = to_f32(rv[e]);
-    if (tid < 64) {  // sa_t = S_{t-1} a_t, row tid, the state run up from S0
-      const int i = tid;
-      float Sr[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) Sr[j] = s0 != nullptr ? __ldg(s0 + i * kD + j) : 0.f;
-      for (int t = 0; t < n; ++t) {
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) s = fmaf(Sr[j], to_f32(ra[t * kD + j]), s);
-        fsa[t * kD + i] = s;
-        const float vi = to_f32(rv[t * kD + i]);
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-          Sr[j] = fmaf(Sr[j], to_f32(rw[t * kD + j]), fmaf(vi, to_f32(rk[t * kD + j]), s * to_f32(rbv[t * kD + j])));
-      }
-    } else if (tid < 128) {  // dsa_t = X_t b_t and dv_t = X_t k_t, row tid - 64, X walked down from X_e
-      const int i = tid - 64;
-      float* fxe = reinterpret_cast<float*>(sm + LY::oFXe);
-      float Xr[64];
-      const float dl = dyr[(n - 1) * kD + i];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        Xr[j] = fmaf(dl, to_f32(rr[(n - 1) * kD + j]), __ldg(gend + i * kD + j));
-        fxe[i * kD + j] = Xr[j];
-      }
-      for (int t = n - 1; t >= 0; --t) {
-        float s = 0.f, sv = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          s = fmaf(Xr[j], to_f32(rbv[t * kD + j]), s);
-          sv = fmaf(Xr[j], to_f32(rk[t * kD + j]), sv);
+    if (__syncthreads_or(fl[tid]) == 0) continue;
+    for (int m = 0; m < kNTF; ++m) {
+      if (fl[m] == 0) continue;
+      const int job = blockIdx.x + gridDim.x * (m0 + m);
+      if (!WKV7_IN(job, total, dbg::kColfb)) continue;
+      const int ci = job % nchunks;
+      const int bh = job / nchunks;
+      const int bi = bh / H;
+      const int hi = bh - bi * H;
+      const int t0 = ci * kL;
+      const int n = min(kL, T - t0);
+      const size_t base = ((size_t)bi * T * H + hi) * kD;
+      const float* gend = xck + (size_t)job * xck_stride;
+      const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
+                               : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
+      {
+        constexpr int CPR = kD * (int)sizeof(Tin) / 16;
+        constexpr int EPC = 16 / (int)sizeof(Tin);
+        const Tin* srcs[6] = {w, k, a, b, r, v};
+  #pragma unroll
+        for (int s6 = 0; s6 < 6; ++s6)
+          for (int e = tid; e < n * CPR; e += kNTF) {
+            const int tt = e / CPR, pc = e % CPR;
+            cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+          }
+        for (int e = tid; e < n * (kD / 4); e += kNTF) {
+          const int tt = e / (kD / 4), pc = e % (kD / 4);
+          cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
         }
-        fdsa[t * kD + i] = s;
-        dv[base + (size_t)(t0 + t) * tstride + i] = sv;
-        const float e = t > 0 ? dyr[(t - 1) * kD + i] : 0.f;
-#pragma unroll
+        cp_async_commit();
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      float* fsa = reinterpret_cast<float*>(sm + LY::oFSa);
+      float* fdsa = reinterpret_cast<float*>(sm + LY::oFDsa);
+      float* fv = reinterpret_cast<float*>(sm + LY::oFV);
+      for (int e = tid; e < n * kD; e += kNTF) fv[e] = to_f32(rv[e]);
+      if (tid < 64) {  // sa_t = S_{t-1} a_t, row tid, the state run up from S0
+        const int i = tid;
+        float Sr[64];
+  #pragma unroll
+        for (int j = 0; j < 64; ++j) Sr[j] = s0 != nullptr ? __ldg(s0 + i * kD + j) : 0.f;
+        for (int t = 0; t < n; ++t) {
+          float s = 0.f;
+  #pragma unroll
+          for (int j = 0; j < 64; ++j) s = fmaf(Sr[j], to_f32(ra[t * kD + j]), s);
+          fsa[t * kD + i] = s;
+          const float vi = to_f32(rv[t * kD + i]);
+  #pragma unroll
+          for (int j = 0; j < 64; ++j)
+            Sr[j] = fmaf(Sr[j], to_f32(rw[t * kD + j]), fmaf(vi, to_f32(rk[t * kD + j]), s * to_f32(rbv[t * kD + j])));
+        }
+      } else if (tid < 128) {  // dsa_t = X_t b_t and dv_t = X_t k_t, row tid - 64, X walked down from X_e
+        const int i = tid - 64;
+        float* fxe = reinterpret_cast<float*>(sm + LY::oFXe);
+        float Xr[64];
+        const float dl = dyr[(n - 1) * kD + i];
+  #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          const float rp = t > 0 ? to_f32(rr[(t - 1) * kD + j]) : 0.f;
-          Xr[j] = fmaf(Xr[j], to_f32(rw[t * kD + j]), fmaf(s, to_f32(ra[t * kD + j]), e * rp));
+          Xr[j] = fmaf(dl, to_f32(rr[(n - 1) * kD + j]), __ldg(gend + i * kD + j));
+          fxe[i * kD + j] = Xr[j];
+        }
+        for (int t = n - 1; t >= 0; --t) {
+          float s = 0.f, sv = 0.f;
+  #pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            s = fmaf(Xr[j], to_f32(rbv[t * kD + j]), s);
+            sv = fmaf(Xr[j], to_f32(rk[t * kD + j]), sv);
+          }
+          fdsa[t * kD + i] = s;
+          dv[base + (size_t)(t0 + t) * tstride + i] = sv;
+          const float e = t > 0 ? dyr[(t - 1) * kD + i] : 0.f;
+  #pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float rp = t > 0 ? to_f32(rr[(t - 1) * kD + j]) : 0.f;
+            Xr[j] = fmaf(Xr[j], to_f32(rw[t * kD + j]), fmaf(s, to_f32(ra[t * kD + j]), e * rp));
+          }
         }
       }
+      __syncthreads();
+      if (tid < 64)
+        colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv,
+                             reinterpret_cast<const float*>(sm + LY::oFXe), s0, dr, dw, dk, da, db);
+      __syncthreads();  // the next flagged chunk reuses the buffers
     }
-    __syncthreads();
-    if (tid < 64)
-      colpass::passes<Tin>(tid, n, t0, base, tstride, raw, fsa, fdsa, dyr, fv,
-                           reinterpret_cast<const float*>(sm + LY::oFXe), s0, dr, dw, dk, da, db);
-    __syncthreads();  // the next flagged chunk reuses the buffers
+    __syncthreads();  // fl is rewritten for the next kNTF chunks
   }
 }
 
