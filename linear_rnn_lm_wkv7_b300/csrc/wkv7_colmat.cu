@@ -6,8 +6,9 @@
 // X_t the gradient w.r.t. the state after token t (including dy_t r_t^T) and S_t the state:
 //     dr_t = S_t^T dy_t,  dk_t = X_t^T v_t,  db_t = X_t^T sa_t,  da_t = S_{t-1}^T dsa_t,
 //     dw_t = colsum(X_t o S_{t-1}),  dsa_t = X_t b_t,  X_{t-1} = X_t diag(w_t) + dsa_t a_t^T + dy_{t-1} r_{t-1}^T.
-// The walk over the chunks (wkv7_ops.cu) leaves G at every chunk end (the gradient w.r.t. the state
-// after the chunk from every later token, X_e = G + dy_{n-1} r_{n-1}^T) and dh0.
+// The walk over the chunks (wkv7_xop.cu) leaves G at every chunk end (the gradient w.r.t. the state
+// after the chunk from every later token, X_e = G + dy_{n-1} r_{n-1}^T; 64 x 64 fp32 in mma accumulator
+// order, acc_order in wkv7_mma.cuh) and dh0.
 //
 // Matrix form of one chunk of n tokens (t = 0..31, steps past n padded with w = 1 and zeros), from S0
 // (the state before the chunk), G and S_e (the state after it), with gamma, A^, R^, K~, B~, M_ab, M_ak,
@@ -109,7 +110,7 @@ struct Lay {
 
 template <typename Tin>
 __global__ void __launch_bounds__(kNT, 1)
-colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
+colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
               const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
               const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
               const float* __restrict__ dy, const float* __restrict__ xck, int* __restrict__ flags, size_t xck_stride,
@@ -121,22 +122,11 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   extern __shared__ float4 smem4[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
 
-  const int ci = blockIdx.x % nchunks;
-  const int bh = blockIdx.x / nchunks;
-  const int bi = bh / H;
-  const int hi = bh - bi * H;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int t0 = ci * kL;
-  const int n = min(kL, T - t0);
   const size_t tstride = (size_t)H * kD;
-  const size_t base = ((size_t)bi * T * H + hi) * kD;
-  const float* gend = xck + ((size_t)bh * nchunks + ci) * xck_stride;  // G: the gradient from later tokens
-  const float* send = h_ckpt + ((size_t)bh * nchunks + ci) * kD * kD;
-  const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
-                           : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
 
   float* G = reinterpret_cast<float*>(sm + LY::oG);
   float* Wc = reinterpret_cast<float*>(sm + LY::oWc);
@@ -168,33 +158,56 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   float* E = reinterpret_cast<float*>(sm + LY::oE);
   constexpr int SM = LY::kSM;
 
-  // ---- P0: the chunk's inputs (rows past n are not copied) in one cp.async group, S0, G and S_e in a second
-  {
+  // ---- P0: a chunk's inputs (rows past n are not copied) in one cp.async group, S0, G and S_e in a second.
+  // The CTA loops over chunks blockIdx.x, + gridDim.x, ...; the next chunk's groups are issued once the
+  // current chunk's raw, staging and SA / DSA regions are dead (after its output products).
+  auto issue = [&](int jb) {
+    const int ci_ = jb % nchunks, bh_ = jb / nchunks;
+    const int bi_ = bh_ / H, hi_ = bh_ - bi_ * H;
+    const int t0_ = ci_ * kL, n_ = min(kL, T - t0_);
+    const size_t base_ = ((size_t)bi_ * T * H + hi_) * kD;
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
     constexpr int EPC = 16 / (int)sizeof(Tin);
     const Tin* srcs[6] = {w, k, a, b, r, v};
 #pragma unroll
     for (int s6 = 0; s6 < 6; ++s6)
-      for (int e = tid; e < n * CPR; e += kNT) {
+      for (int e = tid; e < n_ * CPR; e += kNT) {
         const int tt = e / CPR, pc = e % CPR;
-        cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+        cp_async16(raw + (s6 * kL + tt) * kD + pc * EPC, srcs[s6] + base_ + (size_t)(t0_ + tt) * tstride + pc * EPC);
       }
-    for (int e = tid; e < n * (kD / 4); e += kNT) {
+    for (int e = tid; e < n_ * (kD / 4); e += kNT) {
       const int tt = e / (kD / 4), pc = e % (kD / 4);
-      cp_async16(dyr + tt * kD + pc * 4, dy + base + (size_t)(t0 + tt) * tstride + pc * 4);
+      cp_async16(dyr + tt * kD + pc * 4, dy + base_ + (size_t)(t0_ + tt) * tstride + pc * 4);
     }
     cp_async_commit();
+    const float* gend_ = xck + ((size_t)bh_ * nchunks + ci_) * xck_stride;
+    const float* send_ = h_ckpt + ((size_t)bh_ * nchunks + ci_) * kD * kD;
+    const float* s0_ = ci_ > 0 ? h_ckpt + ((size_t)bh_ * nchunks + ci_ - 1) * kD * kD
+                               : (h0 != nullptr ? h0 + (size_t)bh_ * kD * kD : nullptr);
     float* s0f = reinterpret_cast<float*>(sm + LY::oS0f);
     float* gf = reinterpret_cast<float*>(sm + LY::oGf);
     float* sef = reinterpret_cast<float*>(sm + LY::oSef);
     for (int e = tid; e < kD * kD / 4; e += kNT) {
-      if (s0 != nullptr) cp_async16(s0f + 4 * e, s0 + 4 * e);
-      cp_async16(gf + 4 * e, gend + 4 * e);
-      cp_async16(sef + 4 * e, send + 4 * e);
+      if (s0_ != nullptr) cp_async16(s0f + 4 * e, s0_ + 4 * e);
+      cp_async16(gf + 4 * e, gend_ + 4 * e);
+      cp_async16(sef + 4 * e, send_ + 4 * e);
     }
     cp_async_commit();
-    cp_async_wait<1>();  // the inputs
-  }
+  };
+  if (blockIdx.x < total) issue(blockIdx.x);
+
+  for (int job = blockIdx.x; job < total; job += gridDim.x) {
+  const int ci = job % nchunks;
+  const int bh = job / nchunks;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int t0 = ci * kL;
+  const int n = min(kL, T - t0);
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const float* s0 = ci > 0 ? h_ckpt + ((size_t)bh * nchunks + ci - 1) * kD * kD
+                           : (h0 != nullptr ? h0 + (size_t)bh * kD * kD : nullptr);
+  const int next = job + gridDim.x;
+  cp_async_wait<1>();  // this chunk's inputs
   __syncthreads();
 
   // ---- P1a: gamma_t down each column as a scan (4 blocks of 8 tokens per column); the fallback flag
@@ -237,7 +250,9 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     if (tid == 0 && WKV7_IN(ci, nchunks, dbg::kColmat)) flags[((size_t)bh * nchunks + ci) * xck_stride] = flagged ? 1 : 0;
     if (flagged) {
       cp_async_wait<0>();
-      return;
+      __syncthreads();  // every thread's copies have landed before the next chunk's land in the same places
+      if (next < total) issue(next);
+      continue;
     }
   }
 
@@ -285,7 +300,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
     const int j = tid & 63, part = tid >> 6;
     float z = 0.f;
 #pragma unroll
-    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(gf[i * kD + j], sef[i * kD + j], z);
+    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(gf[acc_order(i, j)], sef[i * kD + j], z);
     if (WKV7_IN(part, 4, dbg::kColmat)) ZP[part * 64 + j] = z;
   }
   // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
@@ -297,7 +312,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
       const int i = e >> 5, j = 2 * (e & 31);
       const float2 s = s0 != nullptr ? *reinterpret_cast<const float2*>(s0f + i * kD + j) : make_float2(0.f, 0.f);
       rm_store(S0, i, j, s.x, s.y);
-      const float2 x = *reinterpret_cast<const float2*>(gf + i * kD + j);
+      const float2 x = *reinterpret_cast<const float2*>(gf + acc_order(i, j));  // (i, j), (i, j + 1)
       const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
       rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
     }
@@ -593,6 +608,8 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
   }
   __syncthreads();
 
+  if (next < total) issue(next);  // raw, staging and SA / DSA regions are dead from here on
+
   // ---- P8: dw per column from Z_t = colsum(X_t o S_t) (X_t: the gradient w.r.t. the state after token t):
   //   Z_{n-1} = colsum(G o S_e) + r_{n-1} o dr_{n-1},   w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
   //   Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1} = Z_t + D_t,
@@ -616,7 +633,7 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
       if (WKV7_IN(blk, 4, dbg::kColmat)) BT[blk * 64 + j] = tot;
     }
     __syncthreads();
-    if (!act) return;
+    if (act) {
     float later = 0.f;
     for (int q2 = blk + 1; q2 < 4; ++q2) later += BT[q2 * 64 + j];
     const float zn = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * kD + j];
@@ -628,7 +645,9 @@ colmat_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* _
         dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
       }
     }
+    }
   }
+  }  // chunks
 }
 
 // The token-by-token column passes for the chunks colmat_kernel flagged (some w_t below 1/32, or gamma_31
@@ -734,7 +753,7 @@ colfb_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, co
         const float dl = dyr[(n - 1) * kD + i];
   #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          Xr[j] = fmaf(dl, to_f32(rr[(n - 1) * kD + j]), __ldg(gend + i * kD + j));
+          Xr[j] = fmaf(dl, to_f32(rr[(n - 1) * kD + j]), __ldg(gend + acc_order(i, j)));
           fxe[i * kD + j] = Xr[j];
         }
         for (int t = n - 1; t >= 0; --t) {
@@ -773,8 +792,9 @@ cudaError_t launch_colmat_t(const BwdArgs& p, const ChunkEnds& ends, cudaStream_
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
   if (err != cudaSuccess) return err;
   const int total = p.B * p.H * p.nchunks;
-  kern<<<(unsigned)total, kNT, LY::kBytes, stream>>>(
-      p.T, p.H, p.nchunks, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
+  const int grid = min(total, num_sms());  // one CTA per SM (shared memory), each looping over its chunks
+  kern<<<(unsigned)grid, kNT, LY::kBytes, stream>>>(
+      p.T, p.H, p.nchunks, total, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
       (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, p.dr, p.dw, p.dk,
       p.dv, p.da, p.db);
   err = cudaGetLastError();
@@ -782,8 +802,8 @@ cudaError_t launch_colmat_t(const BwdArgs& p, const ChunkEnds& ends, cudaStream_
   auto fkern = colfb_kernel<Tin>;
   err = cudaFuncSetAttribute(fkern, cudaFuncAttributeMaxDynamicSharedMemorySize, FL::kBytes);
   if (err != cudaSuccess) return err;
-  const int grid = min(total, 2 * num_sms());
-  fkern<<<(unsigned)grid, kNTF, FL::kBytes, stream>>>(
+  const int fgrid = min(total, 2 * num_sms());
+  fkern<<<(unsigned)fgrid, kNTF, FL::kBytes, stream>>>(
       p.T, p.H, p.nchunks, total, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
       (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, p.dr, p.dw, p.dk,
       p.dv, p.da, p.db);

@@ -410,6 +410,16 @@ __device__ __forceinline__ void tri_inverse_t21(const float* M, float* TI, int s
   }
 }
 
+// index (floats) of element (i, j) of a 64 x 64 fp32 matrix stored in mma accumulator order:
+// [m-tile i / 16][n-tile j / 8][lane][4], lane = 4 (i % 8) + (j % 8) / 2, slot 2 ((i % 16) / 8) + j % 2
+// (the order in which a warp's m16n8 accumulators leave or enter registers as one float4 per lane)
+__host__ __device__ __forceinline__ int acc_order(int i, int j) {
+  const int r = i & 15, c = j & 7;
+  const int lane = (r & 7) * 4 + (c >> 1);
+  const int e = (r >> 3) * 2 + (c & 1);
+  return ((((i >> 4) * 8 + (j >> 3)) * 32 + lane) << 2) + e;
+}
+
 // d += A B for split A and an exact-bf16 B (hi only)
 __device__ __forceinline__ void mma2b(float (&d)[4], const FragA& a, const FragB& b) {
   mma16816(d, a.l, b.h[0], b.h[1]);

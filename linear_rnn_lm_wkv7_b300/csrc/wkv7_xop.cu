@@ -29,7 +29,7 @@
 // operator blocks into a ring of shared-memory stages with cp.async.bulk (one mbarrier per stage and
 // direction); R / 16 chain warps hold 16 state rows each as mma accumulators and apply
 //     forward: y_c += S Q_c;  S = S A_c + U_c  (checkpoint after every chunk)
-//     walk:    G_c written;   G = G A_c^T + E_c (G_c over E_c's block; dh0 at the end).
+//     walk:    G_c written;   G = G A_c^T + E_c (G_c over E_c's block, accumulator order; dh0 at the end).
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation (wkv7_mma.cuh).  Waits are bounded in time: past the limit a kernel sets the status
 // word and returns.
@@ -51,8 +51,8 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up 
 // ---- per-chunk operator block (bytes).  A_c and Q_c: bf16 hi array then lo array, rows unpadded, the
 // 16-byte pieces of row j permuted (piece p stored at p ^ (j & 7) for A, p ^ ((j >> 1) & 3) for Q) so
 // that ldmatrix reads of eight rows hit eight distinct bank groups.  X: U_c or E_c (fp32) in mma
-// accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4]; the walk overwrites it with G in
-// plain row-major order (the same 4 KB per 16 rows).
+// accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4] (acc_order in wkv7_mma.cuh); the
+// walk overwrites it with G in the same order.
 constexpr int kXA = 0;
 constexpr int kXQ = 16384;
 constexpr int kXX = 24576;
@@ -62,13 +62,6 @@ constexpr int kXHead = 256;  // status word(s) before the first block
 __host__ __device__ __forceinline__ int swz_a(int j, int jp) { return j * 64 + (((jp >> 3) ^ (j & 7)) << 3) + (jp & 7); }
 __host__ __device__ __forceinline__ int swz_q(int j, int t) {
   return j * 32 + (((t >> 3) ^ ((j >> 1) & 3)) << 3) + (t & 7);
-}
-// index (floats) of element (i, j) of a 64 x 64 matrix in mma accumulator order
-__host__ __device__ __forceinline__ int frag_idx(int i, int j) {
-  const int r = i & 15, c = j & 7;
-  const int lane = (r & 7) * 4 + (c >> 1);
-  const int e = (r >> 3) * 2 + (c & 1);
-  return ((((i >> 4) * 8 + (j >> 3)) * 32 + lane) << 2) + e;
 }
 
 __host__ __device__ constexpr int rmb(int rows, int ld) { return 2 * rows * ld * 2; }
@@ -267,7 +260,7 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
         y[base + (size_t)(t0 + t) * tstride + i] = yv;
       }
 #pragma unroll
-      for (int u = 0; u < 64; ++u) gX[frag_idx(i, u)] = u8[u];
+      for (int u = 0; u < 64; ++u) gX[acc_order(i, u)] = u8[u];
     }
     __syncthreads();
     if (!BWD) {
@@ -287,7 +280,7 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
         const int i = e >> 6, j = e & 63;
         float s = 0.f;
         for (int t = 0; t < nm; ++t) s = fmaf(dyr[t * kD + i], Qf[j * 33 + t], s);
-        gX[frag_idx(i, j)] = s;
+        gX[acc_order(i, j)] = s;
       }
     }
     return;
@@ -724,8 +717,8 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
                  float* __restrict__ y, float* __restrict__ ck, size_t ck_stride, float* __restrict__ sT,
                  unsigned* __restrict__ status) {
   // forward: s0 = h0 (or null), y (Y_intra in, y out), ck = h_ckpt (or null; ck_stride = 4096 floats),
-  // sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X (ck_stride = kXBytes / 4),
-  // sT = dh0.
+  // sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X in accumulator order
+  // (ck_stride = kXBytes / 4), sT = dh0.
   using ST = Stage<R, WALK>;
   constexpr int NW = ST::kNW;
   constexpr int NB = 64 / R;
@@ -818,8 +811,12 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     }
     const unsigned char* st = stage(s);
     const __nv_bfloat16* sA = reinterpret_cast<const __nv_bfloat16*>(st + ST::oA);
-    // the walk's G before this chunk (its X block has been read into the stage: safe to overwrite)
-    if (WALK && ck != nullptr) store_rows(ck + ((size_t)bh * nchunks + c) * ck_stride);
+    // the walk's G before this chunk, over its E block (already read into the stage), in accumulator order
+    if (WALK && ck != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(ck + ((size_t)bh * nchunks + c) * ck_stride) + (rb * NW + warp) * 8 * 32 + lane;
+#pragma unroll
+      for (int nj = 0; nj < 8; ++nj) dst[nj * 32] = make_float4(S[nj][0], S[nj][1], S[nj][2], S[nj][3]);
+    }
     // S = S A_c + U_c (forward) or G = G A_c^T + E_c (walk); the forward also y_c^T += S Q_c (rows i,
     // columns t).  Per k-step the three bf16 passes go over all accumulators in turn, so that dependent
     // mma into one accumulator are 8 (walk) or 12 (forward) instructions apart.
