@@ -23,8 +23,9 @@
 // same operators token by token instead (rows of A_c and U_c run the recurrence from I and 0), which
 // divides by nothing.
 //
-// xop_prep_kernel: one CTA per (head, chunk), all chunks at once; writes A_c, Q_c (bf16 hi + lo), and
-// U_c (forward; Y_intra into y) or E_c (backward), per chunk, into an operator block.
+// xop_prep_kernel: all chunks at once, two CTAs per SM each looping over chunks (the next chunk's inputs
+// loaded during the current one's last products); writes A_c, Q_c (bf16 hi + lo), and U_c (forward;
+// Y_intra into y) or E_c (backward), per chunk, into an operator block.
 // xop_chain_kernel: one CTA per (head, block of R state rows); a producer warp streams the chunks'
 // operator blocks into a ring of shared-memory stages with cp.async.bulk (one mbarrier per stage and
 // direction); R / 16 chain warps hold 16 state rows each as mma accumulators and apply
@@ -110,7 +111,7 @@ struct XPrepLay {
 
 template <typename Tin, bool BWD>
 __global__ void __launch_bounds__(kNTP, 2)  // two CTAs per SM (bf16 inputs: ~93 KB of shared memory each)
-xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin* __restrict__ w,
+xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
                 const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
                 const Tin* __restrict__ b, const float* __restrict__ dy, unsigned char* __restrict__ ops,
                 float* __restrict__ y, unsigned* __restrict__ status) {
@@ -119,22 +120,11 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   constexpr bool kVExact = sizeof(Tin) == 2;
   extern __shared__ float4 smem4[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(smem4);
-  const int ci = blockIdx.x % nchunks;
-  const int bh = blockIdx.x / nchunks;
-  const int bi = bh / H;
-  const int hi = bh - bi * H;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int t0 = ci * kL;
-  const int nm = min(kL, T - t0);
   const size_t tstride = (size_t)H * kD;
-  const size_t base = ((size_t)bi * T * H + hi) * kD;
-  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
-  __nv_bfloat16* gA = reinterpret_cast<__nv_bfloat16*>(blk + kXA);
-  __nv_bfloat16* gQ = reinterpret_cast<__nv_bfloat16*>(blk + kXQ);
-  float* gX = reinterpret_cast<float*>(blk + kXX);
   if (blockIdx.x == 0 && tid == 0 && status != nullptr) *status = 0u;
 
   auto bfp = [&](int off) { return reinterpret_cast<__nv_bfloat16*>(sm + off); };
@@ -162,24 +152,46 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
   float* Mab = reinterpret_cast<float*>(sm + LY::oMab);
   float* TI = reinterpret_cast<float*>(sm + LY::oTI);
 
-  {  // the chunk's inputs (rows past the chunk are not copied)
+  // A chunk's inputs (rows past the chunk are not copied) by cp.async.  The CTA loops over chunks
+  // blockIdx.x, + gridDim.x, ...; the next chunk's inputs are issued once the current chunk's raw inputs
+  // and coupling matrices are dead (before its last products).
+  auto issue = [&](int jb) {
+    const int ci_ = jb % nchunks, bh_ = jb / nchunks;
+    const int bi_ = bh_ / H, hi_ = bh_ - bi_ * H;
+    const int t0_ = ci_ * kL, nm_ = min(kL, T - t0_);
+    const size_t base_ = ((size_t)bi_ * T * H + hi_) * kD;
     constexpr int CPR = kD * (int)sizeof(Tin) / 16;
     constexpr int EPC = 16 / (int)sizeof(Tin);
     const Tin* srcs[6] = {w, a, b, r, k, v};
 #pragma unroll
     for (int s6 = 0; s6 < LY::kRawN; ++s6)
-      for (int e = tid; e < nm * CPR; e += kNTP) {
+      for (int e = tid; e < nm_ * CPR; e += kNTP) {
         const int t = e / CPR, pc = e % CPR;
-        cp_async16(raw + (s6 * kL + t) * kD + pc * EPC, srcs[s6] + base + (size_t)(t0 + t) * tstride + pc * EPC);
+        cp_async16(raw + (s6 * kL + t) * kD + pc * EPC, srcs[s6] + base_ + (size_t)(t0_ + t) * tstride + pc * EPC);
       }
     if (BWD)
-      for (int e = tid; e < nm * (kD / 4); e += kNTP) {
+      for (int e = tid; e < nm_ * (kD / 4); e += kNTP) {
         const int t = e >> 4, pc = e & 15;
-        cp_async16(dyr + t * kD + pc * 4, dy + base + (size_t)(t0 + t) * tstride + pc * 4);
+        cp_async16(dyr + t * kD + pc * 4, dy + base_ + (size_t)(t0_ + t) * tstride + pc * 4);
       }
     cp_async_commit();
-    cp_async_wait<0>();
-  }
+  };
+  if (blockIdx.x < total) issue(blockIdx.x);
+
+  for (int job = blockIdx.x; job < total; job += gridDim.x) {
+  const int ci = job % nchunks;
+  const int bh = job / nchunks;
+  const int bi = bh / H;
+  const int hi = bh - bi * H;
+  const int t0 = ci * kL;
+  const int nm = min(kL, T - t0);
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
+  __nv_bfloat16* gA = reinterpret_cast<__nv_bfloat16*>(blk + kXA);
+  __nv_bfloat16* gQ = reinterpret_cast<__nv_bfloat16*>(blk + kXQ);
+  float* gX = reinterpret_cast<float*>(blk + kXX);
+  const int next = job + gridDim.x;
+  cp_async_wait<0>();
   __syncthreads();
 
   {  // gamma_t down each column as a scan: column j, tokens 8 blk .. 8 blk + 7; the token-by-token flag
@@ -283,7 +295,9 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
         gX[acc_order(i, j)] = s;
       }
     }
-    return;
+    __syncthreads();  // the raw inputs and dy are read
+    if (next < total) issue(next);
+    continue;
   }
 
   {  // one (token, 8 columns) block per thread: A^, R^, B~, and K~, V (forward) or DY (backward)
@@ -558,6 +572,7 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
     }
   }
   __syncthreads();
+  if (next < total) issue(next);  // the raw inputs and the coupling matrices are dead from here on
 
   // U_c = V^T K' (forward) or E_c = DY^T Q_c^T (backward), rows i in mma accumulator order: warp w forms
   // m-tiles w >> 2 and (w >> 2) + 2 at n-tiles 2 (w & 3) + 0, 1 (sharing K' or Q_c); the forward then forms
@@ -618,6 +633,7 @@ xop_prep_kernel(int T, int H, int nchunks, const Tin* __restrict__ r, const Tin*
             make_float2(acc[h][2], acc[h][3]);
     }
   }
+  }  // chunks
 }
 
 // ====================================================================================== chain
@@ -908,8 +924,9 @@ cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* o
   const int B = BWD ? ba->B : fa->B, T = BWD ? ba->T : fa->T, H = BWD ? ba->H : fa->H;
   const int C = BWD ? ba->nchunks : fa->nchunks;
   const TokenInputs& in = BWD ? ba->in : fa->in;
-  const unsigned grid = (unsigned)B * H * C;
-  kern<<<grid, kNTP, LY::kBytes, stream>>>(T, H, C, (const Tin*)in.r, (const Tin*)in.w, (const Tin*)in.k,
+  const int total = B * H * C;
+  const unsigned grid = (unsigned)min(total, 2 * num_sms());  // two CTAs per SM, each looping over its chunks
+  kern<<<grid, kNTP, LY::kBytes, stream>>>(T, H, C, total, (const Tin*)in.r, (const Tin*)in.w, (const Tin*)in.k,
                                           (const Tin*)in.v, (const Tin*)in.a, (const Tin*)in.b,
                                           BWD ? ba->dy : nullptr, ops, BWD ? nullptr : fa->y, status);
   return cudaGetLastError();
