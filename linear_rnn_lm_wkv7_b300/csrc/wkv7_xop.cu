@@ -945,12 +945,17 @@ cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops,
   return cudaGetLastError();
 }
 
-// state rows per chain CTA.  Every chain warp spends the same time per chunk whatever the split, while each
-// CTA reads the head's A_c and Q_c: whole heads (64 rows) read them once.
-#ifndef WKV7_CHAIN_ROWS
-#define WKV7_CHAIN_ROWS 64
+// state rows per chain CTA.  Two CTAs of 32 rows per head (the head's operators read twice) while they fit
+// one CTA per SM: measured faster than one 64-row CTA there (B12 T1024 H6 forward 115 vs 121 us, B4 T512
+// H12 54 vs 57 us); whole heads past that (B2 T4096 H64: 636 vs 678 us).  WKV7_CHAIN_ROWS fixes the choice.
+int chain_rows(int heads) {
+#ifdef WKV7_CHAIN_ROWS
+  (void)heads;
+  return WKV7_CHAIN_ROWS;
+#else
+  return 2 * heads <= num_sms() ? 32 : 64;
 #endif
-int chain_rows(int /*heads*/) { return WKV7_CHAIN_ROWS; }
+}
 
 template <bool WALK>
 cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned char* ops, const float* s0, float* y,
