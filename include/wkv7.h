@@ -173,6 +173,32 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype,
  * same size checks as wkv7_backward). */
 int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
+/*
+ * The chunk-operator backward that takes the transition operators from its forward instead of forming
+ * them again (the forward's operators of a chunk are the backward's: A_c, and Q_c for E_c = DY^T Q_c^T).
+ *   fwd_workspace, fwd_workspace_bytes
+ *           the workspace of the wkv7_forward call (chunk 32, no sa, with a workspace) that wrote
+ *           h_ckpt from these same r..b and h0, untouched since; at least
+ *           wkv7_forward_workspace_size() bytes, 256-byte aligned.  Required (WKV7_ERR_ARG if NULL).
+ *           It is this call's only scratch and is consumed: E_c, then G, replace the forward's U_c,
+ *           and flags replace Q_c, so a second backward needs the forward run again.  A workspace that
+ *           holds anything else gives meaningless gradients (nothing on the device can tell).
+ *   Every other argument, layout and result as wkv7_backward with a workspace and no sa; chunk must
+ *   be 32 (WKV7_ERR_SHAPE otherwise).  The first kernel only forms E_c (one product per chunk) where
+ *   wkv7_backward forms A_c, Q_c and E_c; the walk and the column gradients are the same kernels.
+ *   Chunks in closed form get the same A_c and E_c bit for bit, so the same gradients; chunks taken
+ *   token by token (tiny decays) get E_c from the split Q_c (~1e-6 relative difference).  The
+ *   workspace header's status word is as in wkv7_forward.
+ * Source: Backward listing of "Metal kernel architecture" (see top of file).
+ */
+int wkv7_backward_from_forward(int B, int T, int H, int D, int chunk, int in_dtype,
+                               const void *r, const void *w, const void *k,
+                               const void *v, const void *a, const void *b,
+                               const float *h0, const float *h_ckpt,
+                               const float *dy, const float *dhT,
+                               float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                               float *dh0, void *fwd_workspace, size_t fwd_workspace_bytes, void *stream);
+
 /* Bytes of device scratch the library owns for wkv7_backward_noalloc (128 MiB; see the conventions above). */
 #define WKV7_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 

@@ -35,6 +35,7 @@ SIGNATURES = {
     "wkv7_forward_sequential": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
     "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "wkv7_backward_from_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_noalloc": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P]),
     "wkv7_decode": (_I, [_I] * 4 + [_P] + [_P] * 6 + [_P] + [_P]),
     "wkv7_debug_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
@@ -239,6 +240,39 @@ def backward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, chunk: int = 32, need_d
                            *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, sa, dy, dhT)),
                            *map(_ptr, grads), _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "wkv7_backward")
+    return tuple(grads)
+
+
+def backward_from_forward(r, w, k, v, a, b, h0, h_ckpt, dy, dhT=None, *, workspace, need_dh0: bool = True,
+                          out=None, stream=None):
+    """The chunk-operator backward (chunk 32) reusing the transition operators that `forward` left in
+    `workspace` (the uint8 tensor passed to that forward, which ran on these same inputs and h0 and
+    wrote h_ckpt).  The workspace is consumed: a second backward needs the forward again.  Returns
+    (dr, dw, dk, dv, da, db, dh0) as `backward` does."""
+    torch = _torch()
+    B, T, H, D = r.shape
+    where = "wkv7.backward_from_forward"
+    _check_inputs((r, w, k, v, a, b), (B, T, H, D), where)
+    C = num_chunks(T, 32)
+    dev = r.device
+    _check_f32(h0, (B, H, D, D), "h0", where, dev)
+    _check_f32(h_ckpt, (B, H, C, D, D), "h_ckpt", where, dev)
+    _check_f32(dy, (B, T, H, D), "dy", where, dev)
+    _check_f32(dhT, (B, H, D, D), "dhT", where, dev)
+    if workspace is None or workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError(f"{where}: workspace must be the contiguous uint8 tensor the forward used")
+    if out is not None:
+        grads = list(out)
+    else:
+        grads = [torch.empty((B, T, H, D), dtype=torch.float32, device=dev) for _ in range(6)]
+        grads.append(torch.empty((B, H, D, D), dtype=torch.float32, device=dev) if need_dh0 else None)
+    for name, g in zip(("dr", "dw", "dk", "dv", "da", "db"), grads[:6]):
+        _check_f32(g, (B, T, H, D), name, where, dev)
+    _check_f32(grads[6], (B, H, D, D), "dh0", where, dev)
+    st = lib.wkv7_backward_from_forward(B, T, H, D, 32, _in_dtype(r),
+                                        *map(_ptr, (r, w, k, v, a, b, h0, h_ckpt, dy, dhT)),
+                                        *map(_ptr, grads), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "wkv7_backward_from_forward")
     return tuple(grads)
 
 

@@ -151,11 +151,12 @@ int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t* b
   return WKV7_OK;
 }
 
-int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
-                  const void* k, const void* v, const void* a, const void* b, const float* h0,
-                  const float* h_ckpt, const float* sa, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
-                  float* dv, float* da, float* db, float* dh0, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+namespace {
+// the argument checks and BwdArgs shared by wkv7_backward and wkv7_backward_from_forward
+int backward_args(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w, const void* k,
+                  const void* v, const void* a, const void* b, const float* h0, const float* h_ckpt,
+                  const float* sa, const float* dy, const float* dhT, float* dr, float* dw, float* dk, float* dv,
+                  float* da, float* db, float* dh0, wkv7::BwdArgs* p) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;
   if ((st = check_dtype(in_dtype))) return st;
@@ -164,20 +165,48 @@ int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const voi
   } else if ((st = check_ptrs({}, {h0, dhT, dh0}))) {
     return st;
   }
+  p->B = B; p->T = T; p->H = H; p->chunk = chunk; p->nchunks = wkv7_num_chunks(T, chunk);
+  p->bf16 = in_dtype == WKV7_BF16;
+  p->in = {r, w, k, v, a, b};
+  p->h0 = h0; p->h_ckpt = h_ckpt; p->sa = T > 0 ? sa : nullptr; p->dy = dy; p->dhT = dhT;
+  p->dr = dr; p->dw = dw; p->dk = dk; p->dv = dv; p->da = da; p->db = db; p->dh0 = dh0;
+  return WKV7_OK;
+}
+}  // namespace
+
+int wkv7_backward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                  const void* k, const void* v, const void* a, const void* b, const float* h0,
+                  const float* h_ckpt, const float* sa, const float* dy, const float* dhT, float* dr, float* dw, float* dk,
+                  float* dv, float* da, float* db, float* dh0, void* workspace, size_t workspace_bytes,
+                  void* stream) {
   wkv7::BwdArgs p;
-  p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
-  p.bf16 = in_dtype == WKV7_BF16;
-  p.in = {r, w, k, v, a, b};
-  p.h0 = h0; p.h_ckpt = h_ckpt; p.sa = T > 0 ? sa : nullptr; p.dy = dy; p.dhT = dhT;
-  p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.dh0 = dh0;
+  const int st = backward_args(B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, h_ckpt, sa, dy, dhT, dr, dw, dk,
+                               dv, da, db, dh0, &p);
+  if (st) return st;
   if (workspace != nullptr && (chunk == 32 || p.sa != nullptr)) {
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
     if (workspace_bytes < wkv7::backward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
     const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-    return record_cuda(p.sa == nullptr ? wkv7::launch_backward_transition(p, workspace, st_)
+    return record_cuda(p.sa == nullptr ? wkv7::launch_backward_transition(p, workspace, false, st_)
                                        : wkv7::launch_backward_two_phase(p, workspace, st_));
   }
   return record_cuda(wkv7::launch_backward(p, static_cast<cudaStream_t>(stream)));
+}
+
+int wkv7_backward_from_forward(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                               const void* k, const void* v, const void* a, const void* b, const float* h0,
+                               const float* h_ckpt, const float* dy, const float* dhT, float* dr, float* dw,
+                               float* dk, float* dv, float* da, float* db, float* dh0, void* fwd_workspace,
+                               size_t fwd_workspace_bytes, void* stream) {
+  wkv7::BwdArgs p;
+  const int st = backward_args(B, T, H, D, chunk, in_dtype, r, w, k, v, a, b, h0, h_ckpt, nullptr, dy, dhT, dr, dw,
+                               dk, dv, da, db, dh0, &p);
+  if (st) return st;
+  if (chunk != 32) return WKV7_ERR_SHAPE;
+  if (fwd_workspace == nullptr) return WKV7_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) return WKV7_ERR_ALIGN;
+  if (fwd_workspace_bytes < wkv7::forward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
+  return record_cuda(wkv7::launch_backward_transition(p, fwd_workspace, true, static_cast<cudaStream_t>(stream)));
 }
 
 int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t* bytes) {

@@ -446,9 +446,9 @@ size_t forward_workspace_bytes(int B, int T, int H, int chunk) {
   return chunk == 32 ? xop_workspace_bytes(B, T, H) : 0;
 }
 
-cudaError_t launch_backward_transition(const BwdArgs& p, void* workspace, cudaStream_t stream) {
+cudaError_t launch_backward_transition(const BwdArgs& p, void* workspace, bool from_forward, cudaStream_t stream) {
   ChunkEnds ends;
-  cudaError_t err = launch_xop_walk(p, workspace, 0, &ends, stream);
+  cudaError_t err = launch_xop_walk(p, workspace, from_forward, 0, &ends, stream);
   if (err != cudaSuccess) return err;
   return launch_colgrad_matrix(p, ends, stream);
 }

@@ -87,12 +87,15 @@ struct ChunkEnds {
   int* flags;
   size_t stride;
 };
-cudaError_t launch_xop_walk(const BwdArgs& a, void* workspace, int rows, ChunkEnds* ends, cudaStream_t stream);
+// from_forward: the blocks already hold the forward's A_c and Q_c (the same inputs); only E_c is formed
+cudaError_t launch_xop_walk(const BwdArgs& a, void* workspace, bool from_forward, int rows, ChunkEnds* ends,
+                            cudaStream_t stream);
 // the column gradients dr, dw, dk, dv, da, db of every 32-token chunk in matrix form, from G at the chunk
 // ends, the checkpoints and the inputs (no saved sa); chunks with tiny decays token by token
 cudaError_t launch_colgrad_matrix(const BwdArgs& a, const ChunkEnds& ends, cudaStream_t stream);
-// the backward without a saved sa at chunk 32: operators, walk, matrix column gradients
-cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, cudaStream_t stream);
+// the backward without a saved sa at chunk 32: operators (or, from_forward, E_c beside the forward's
+// operators), walk, matrix column gradients
+cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, bool from_forward, cudaStream_t stream);
 // bytes of the forward's workspace (the transition operands)
 size_t forward_workspace_bytes(int B, int T, int H, int chunk);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -65,6 +65,6 @@ extern "C" int wkv7_backward_noalloc(int B, int T, int H, int D, int chunk, int 
   // written earlier in the same call (the walk writes each chunk-end state gradient, and each dsa when
   // the column pass reads them, before the column pass runs): nothing to clear
   const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-  return wkv7::record_cuda_status(p.sa == nullptr ? wkv7::launch_backward_transition(p, scratch, st_)
+  return wkv7::record_cuda_status(p.sa == nullptr ? wkv7::launch_backward_transition(p, scratch, false, st_)
                                                   : wkv7::launch_backward_two_phase(p, scratch, st_));
 }

@@ -967,6 +967,68 @@ cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned ch
   }
 }
 
+// ================================================================================ E_c from the forward
+
+constexpr int kNTE = 128;
+
+// B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = Q_c[n][k] (rows j, tokens t) from an
+// operator block's Q_c copied as is (hi then lo, pieces permuted as swz_q)
+__device__ __forceinline__ void q_b2(const __nv_bfloat16* sq, int nt, int kk, int lane, FragB& b0, FragB& b1) {
+  const int j = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
+  const int t = kk * 16 + ((lane >> 3) & 1) * 8;
+  const int off = swz_q(j, t);
+  uint32_t h[4], l[4];
+  ldsm4<false>(h, sq + off);
+  ldsm4<false>(l, sq + 2048 + off);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+
+// E_c = DY^T Q_c^T of every chunk from the Q_c that the forward left in the operator blocks: one CTA per
+// chunk, warp w forms rows 16 w .. 16 w + 15 (all 64 columns) and writes them over U_c in accumulator
+// order.  A_c stays as the forward wrote it.  DY is split as the backward's operator kernel splits it and
+// the products run in the same order, so E_c of a closed-form chunk is the same as that kernel's.
+__global__ void __launch_bounds__(kNTE)
+xop_e_kernel(int T, int H, int nchunks, const float* __restrict__ dy, unsigned char* __restrict__ ops,
+             unsigned* __restrict__ status) {
+  __shared__ __align__(128) __nv_bfloat16 sQ[2 * 64 * 32];
+  __shared__ __align__(128) __nv_bfloat16 sDY[2 * kL * kLD64];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int job = blockIdx.x;
+  const int ci = job % nchunks, bh = job / nchunks;
+  const int bi = bh / H, hi = bh - bi * H;
+  const int t0 = ci * kL, nm = min(kL, T - t0);
+  const size_t base = ((size_t)bi * T * H + hi) * kD;
+  const size_t tstride = (size_t)H * kD;
+  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
+  if (job == 0 && tid == 0 && status != nullptr) *status = 0u;
+  for (int e = tid; e < 512; e += kNTE) cp_async16(sQ + e * 8, blk + kXQ + e * 16);
+  cp_async_commit();
+  const RM DYm{sDY, kL * kLD64, kLD64};
+  for (int e = tid; e < kL * (kD / 4); e += kNTE) {  // rows t, four columns per thread and step
+    const int t = e >> 4, c = (e & 15) * 4;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < nm && WKV7_IN(t0 + t, T, dbg::kXopPrep))
+      x = *reinterpret_cast<const float4*>(dy + base + (size_t)(t0 + t) * tstride + c);
+    rm_store(DYm, t, c, x.x, x.y);
+    rm_store(DYm, t, c + 2, x.z, x.w);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  float acc[8][4] = {};
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const FragA fa = rm_at(DYm, warp, kk, lane);
+    FragB fb[8];
+#pragma unroll
+    for (int np = 0; np < 4; ++np) q_b2(sQ, 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
+    mma3n<8>(acc, fa, fb);
+  }
+  float4* gX = reinterpret_cast<float4*>(blk + kXX);
+#pragma unroll
+  for (int nj = 0; nj < 8; ++nj) gX[(warp * 8 + nj) * 32 + lane] = make_float4(acc[nj][0], acc[nj][1], acc[nj][2], acc[nj][3]);
+}
+
 }  // namespace
 
 WKV7_DEBUG_READER(debug_word_xop)
@@ -988,15 +1050,22 @@ cudaError_t launch_xop_forward(const FwdArgs& p, void* workspace, int rows, cuda
                              stream);
 }
 
-cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, int rows, ChunkEnds* ends, cudaStream_t stream) {
+cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward, int rows, ChunkEnds* ends,
+                            cudaStream_t stream) {
   unsigned* status = static_cast<unsigned*>(workspace);
   unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
   ends->g = reinterpret_cast<const float*>(ops + kXX);
   ends->flags = reinterpret_cast<int*>(ops + kXQ);  // Q_c's slot: the walk does not use it
   ends->stride = kXBytes / 4;
   if (p.nchunks > 0) {  // (no chunks: the chain only copies dhT to dh0)
-    cudaError_t err = p.bf16 ? launch_prep_t<__nv_bfloat16, true>(nullptr, &p, ops, status, stream)
-                             : launch_prep_t<float, true>(nullptr, &p, ops, status, stream);
+    cudaError_t err;
+    if (from_forward) {
+      xop_e_kernel<<<(unsigned)(p.B * p.H * p.nchunks), kNTE, 0, stream>>>(p.T, p.H, p.nchunks, p.dy, ops, status);
+      err = cudaGetLastError();
+    } else {
+      err = p.bf16 ? launch_prep_t<__nv_bfloat16, true>(nullptr, &p, ops, status, stream)
+                   : launch_prep_t<float, true>(nullptr, &p, ops, status, stream);
+    }
     if (err != cudaSuccess) return err;
   }
   if (rows == 0) rows = chain_rows(p.B * p.H);

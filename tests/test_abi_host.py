@@ -170,3 +170,35 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 32, 1, 64)
     with pytest.raises(ValueError):
         wkv7.forward(x, x, x, x, x, x)
+
+
+def bwd_ff(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None, ws=P(0x100000), ws_bytes=None):
+    p = list(ALIGNED[:17]) if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = wkv7.forward_workspace_size(B, T, H, 64, 32) if D == 64 and B > 0 and H > 0 and T >= 0 else 0
+    return wkv7.lib.wkv7_backward_from_forward(B, T, H, D, chunk, dt, *p, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=32), 2), (dict(chunk=0), 2), (dict(chunk=16), 2), (dict(chunk=64), 2), (dict(B=0), 1),
+    (dict(T=-1), 1), (dict(dt=2), 4),
+])
+def test_backward_from_forward_rejects_bad_sizes(kw, status):
+    assert bwd_ff(**kw) == status
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4, 5, 7, 8, 10, 11, 12, 13, 14, 15])
+def test_backward_from_forward_requires(i):
+    # r..b, h_ckpt, dy and the six gradients are required; h0 (6), dhT (9) and dh0 (16) may be NULL
+    p = list(ALIGNED[:17])
+    p[i] = None
+    assert bwd_ff(ptrs=p) == 1
+    p[i] = MISALIGNED
+    assert bwd_ff(ptrs=p) == 3
+
+
+def test_backward_from_forward_needs_the_forward_workspace():
+    need = wkv7.forward_workspace_size(2, 64, 3, 64, 32)
+    assert bwd_ff(ws=None, ws_bytes=need) == 1
+    assert bwd_ff(ws=P(0x100000), ws_bytes=need - 1) == 7
+    assert bwd_ff(ws=P(0x100000 + 128), ws_bytes=need) == 3

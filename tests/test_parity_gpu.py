@@ -83,13 +83,22 @@ FWD = ["transition", "subchunk", "sequential"]
 
 # backward paths: "two_phase" (a workspace: at chunk 32 the transition walk + matrix column gradients,
 # otherwise the two-phase backward with the forward's saved sa), the single pass reading the saved sa,
-# the single pass recomputing sa per chunk
-MODES = ["two_phase", "single_saved_sa", "single_recompute"]
+# the single pass recomputing sa per chunk, and "from_forward" (chunk 32: wkv7_backward_from_forward on
+# the operators the transition forward left in its workspace)
+MODES = ["two_phase", "single_saved_sa", "single_recompute", "from_forward"]
 
 
 def run_gpu(wkv7, x, dtype, chunk=32, mode="two_phase", fwd="transition"):
     ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
+    if mode == "from_forward":
+        assert fwd == "transition" and chunk == 32, "the operators come from the chunk-32 transition forward"
+        B, T, H, _ = ins[0].shape
+        ws = torch.empty(wkv7.forward_workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
+        y, ck, hT = wkv7.forward(*ins, h0, workspace=ws)
+        grads = wkv7.backward_from_forward(*ins, h0, ck, dev32(x["dy"]), dev32(x.get("dhT")), workspace=ws)
+        torch.cuda.synchronize()
+        return host(y), host(ck), host(hT), [host(g) for g in grads], None
     if fwd == "transition":
         y, ck, hT = wkv7.forward(*ins, h0, chunk=chunk)
         sa = None
@@ -162,8 +171,8 @@ def workload_ref(name):
 
 
 @pytest.mark.parametrize("fwd,mode", [("transition", "two_phase"), ("transition", "single_recompute"),
-                                      ("subchunk", "two_phase"), ("subchunk", "single_saved_sa"),
-                                      ("sequential", "two_phase")])
+                                      ("transition", "from_forward"), ("subchunk", "two_phase"),
+                                      ("subchunk", "single_saved_sa"), ("sequential", "two_phase")])
 @pytest.mark.parametrize("name", ["oracle_b1_t128_h2", "debug_b12_t1024_h6", "m100_b4_t512_h12"])
 def test_workload_parity_full(wkv7, name, fwd, mode):
     wl = gen.WORKLOADS[name]
@@ -178,6 +187,13 @@ def test_workload_parity_wide7b_every_head(wkv7, fwd):
     wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
     x, ref = workload_ref("wide7b_b2_t4096_h64")
     check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "two_phase", fwd), wl.chunk, ref=ref)
+
+
+def test_workload_parity_wide7b_from_forward_every_head(wkv7):
+    """The backward on the forward's operators, 7B-width slice, all 128 heads."""
+    wl = gen.WORKLOADS["wide7b_b2_t4096_h64"]
+    x, ref = workload_ref("wide7b_b2_t4096_h64")
+    check(x, run_gpu(wkv7, x, wl.dtype, wl.chunk, "from_forward", "transition"), wl.chunk, ref=ref)
 
 
 def test_workload_parity_wide7b_single_pass_sampled_heads(wkv7):
@@ -228,6 +244,8 @@ def test_edge_shapes(wkv7, dtype, B, T, H, chunk):
         for mode in MODES:
             if (fwd == "sequential" and mode != "two_phase") or (fwd == "transition" and mode == "single_saved_sa"):
                 continue
+            if mode == "from_forward" and (fwd != "transition" or chunk != 32):
+                continue
             check(x, run_gpu(wkv7, x, dtype, chunk, mode, fwd), chunk, ref=ref)
 
 
@@ -266,6 +284,7 @@ def test_strong_decay_backward_two_phase(wkv7, dtype, lo, hi):
     ref = oracle_ref(x, 32)
     for fwd in ("transition", "subchunk"):
         check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd), 32, ref=ref)
+    check(x, run_gpu(wkv7, x, dtype, 32, "from_forward", "transition"), 32, ref=ref)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -282,6 +301,7 @@ def test_zero_and_vanishing_decay_two_phase(wkv7, dtype):
     ref = oracle_ref(x, 32)
     for fwd in FWD:
         check(x, run_gpu(wkv7, x, dtype, 32, "two_phase", fwd), 32, ref=ref)
+    check(x, run_gpu(wkv7, x, dtype, 32, "from_forward", "transition"), 32, ref=ref)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -290,7 +310,8 @@ def test_many_heads(wkv7, dtype):
     x = gen.random_small(77, B=3, T=45, H=26, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
     heads = [(0, 0), (1, 13), (2, 25)]
     ref = oracle_ref(x, 32, heads)
-    for fwd, mode in (("transition", "two_phase"), ("transition", "single_recompute"), ("subchunk", "single_saved_sa")):
+    for fwd, mode in (("transition", "two_phase"), ("transition", "single_recompute"), ("subchunk", "single_saved_sa"),
+                      ("transition", "from_forward")):
         check(x, run_gpu(wkv7, x, dtype, 32, mode, fwd), 32, heads=heads, ref=ref)
 
 
@@ -317,6 +338,36 @@ def test_backward_paths_agree(wkv7):
     g2 = wkv7.backward(*ins, h0, ck, dev32(x["dy"]), dev32(x["dhT"]), sa=None, workspace="auto")
     for name, p_, q_ in zip(("dr", "dw", "dk", "dv", "da", "db", "dh0"), g1, g2):
         assert rel(host(q_), host(p_).astype(np.float64)) <= 5e-5, name
+
+
+@pytest.mark.parametrize("decay", ["workload", "strong"])
+def test_backward_from_forward_equals_backward(wkv7, decay):
+    """wkv7_backward_from_forward on the forward's operators against wkv7_backward forming them again: the
+    same A_c and E_c on closed-form chunks, so the same gradients bit for bit; with strong decays (chunks
+    taken token by token, whose E_c comes from the split Q_c) within 1e-5."""
+    if decay == "workload":
+        x = gen.random_small(12, B=3, T=200, H=4, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
+    else:
+        x = strong_decay(4245, "bf16", 0.005, 0.05)
+    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    h0, dy, dhT = dev32(x["h0"]), dev32(x["dy"]), dev32(x["dhT"])
+    B, T, H, _ = ins[0].shape
+    ws = torch.empty(wkv7.forward_workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
+    y, ck, hT = wkv7.forward(*ins, h0, workspace=ws)
+    g1 = wkv7.backward(*ins, h0, ck, dy, dhT, workspace="auto")
+    g2 = wkv7.backward_from_forward(*ins, h0, ck, dy, dhT, workspace=ws)
+    for name, p_, q_ in zip(("dr", "dw", "dk", "dv", "da", "db", "dh0"), g1, g2):
+        if decay == "workload":
+            assert torch.equal(p_, q_), name
+        else:
+            assert rel(host(q_), host(p_)) <= 1e-5, name
+    # the workspace is consumed: the forward's U_c and Q_c are gone, so it is refilled before a second call
+    y2, ck2, _ = wkv7.forward(*ins, h0, workspace=ws)
+    g3 = wkv7.backward_from_forward(*ins, h0, ck2, dy, dhT, workspace=ws)
+    for p_, q_ in zip(g2, g3):
+        assert torch.equal(p_, q_)
+    with pytest.raises(wkv7.WKV7Error):
+        wkv7.backward_from_forward(*ins, h0, ck, dy, dhT, workspace=ws[: ws.numel() - 256])
 
 
 def test_explicit_workspace_and_too_small_workspace(wkv7):
@@ -381,6 +432,9 @@ def test_zero_tokens(wkv7):
     y, ck, hT = wkv7.forward(e, e, e, e, e, e, h0)
     assert torch.equal(hT, h0) and ck.numel() == 0
     grads = wkv7.backward(e, e, e, e, e, e, h0, ck, e, dhT)
+    assert torch.equal(grads[6], dhT)
+    ws = torch.empty(wkv7.forward_workspace_size(B, 0, H), dtype=torch.uint8, device="cuda")
+    grads = wkv7.backward_from_forward(e, e, e, e, e, e, h0, ck, e, dhT, workspace=ws)
     assert torch.equal(grads[6], dhT)
 
 
