@@ -5,9 +5,10 @@
 
 A step is one pass of the whole path on one batch of the 36M "debug" training
 shape (B=12, T=1024, H=6, D=64, bf16 inputs, fp32 state, chunk 32): wkv7_forward
-(y, checkpoints, hT) then wkv7_backward (dr, dw, dk, dv, da, db, dh0), both with a
-workspace and without a saved sa (--path operators, the default; --path two-phase and
---path single time the other backward paths).  other_configs adds the step time and
+(y, checkpoints, hT) with a workspace, then wkv7_backward_from_forward (dr, dw, dk,
+dv, da, db, dh0) on the operators that forward left in it (--path operators, the
+default; --path operators-reform has wkv7_backward form them again, --path two-phase
+and --path single time the other backward paths).  other_configs adds the step time and
 step roofline fractions of the other training workloads.  Inputs are
 seeded synthetic draws (wkv7_inputs.py).  Under torchrun each rank runs its own
 independent batch (weak scaling, no collective on the data path); rank 0 prints
@@ -55,10 +56,11 @@ def parse_args():
                    help="default: the debug training shape (the headline line); others for extra measurements")
     p.add_argument("--decode-batch", type=int, default=0,
                    help="decode workload only: number of sequences (default: the workload's 256)")
-    p.add_argument("--path", choices=["operators", "two-phase", "single"], default="operators",
-                   help="operators: chunk-operator forward and backward with a workspace, no saved sa (the "
-                        "default); two-phase: forward saving sa, two-phase backward reading it; single: "
-                        "single-pass backward without a workspace")
+    p.add_argument("--path", choices=list(PATHS), default="operators",
+                   help="operators: chunk-operator forward with a workspace, then the backward on the operators "
+                        "it left there (the default); operators-reform: the backward forms them again "
+                        "(wkv7_backward with a workspace, no sa); two-phase: forward saving sa, two-phase "
+                        "backward reading it; single: single-pass backward without a workspace")
     p.add_argument("--graph", choices=["on", "off"], default="on",
                    help="time the step as CUDA-graph replays (one graph per input set) instead of eager calls")
     p.add_argument("--no-other-configs", action="store_true",
@@ -431,9 +433,14 @@ def run_decode(args, rank, world, local_rank):
 PATHS = {
     # forward call, backward call and the kernels each launches (counted per step for gpu_launches)
     "operators": {"forward": "wkv7_forward with a workspace, no sa: chunk-operator prep + chain",
-                  "backward": "wkv7_backward with a workspace, no sa: operator prep + walk + matrix column "
-                              "kernel + token-by-token companion (exits at once without flagged chunks)",
+                  "backward": "wkv7_backward_from_forward on the forward's workspace: E_c kernel + walk + matrix "
+                              "column kernel + token-by-token companion (exits at once without flagged chunks)",
+                  "backward_call": "wkv7_backward_from_forward",
                   "launches": 2 + 4},
+    "operators-reform": {"forward": "wkv7_forward with a workspace, no sa: chunk-operator prep + chain",
+                         "backward": "wkv7_backward with a workspace, no sa: operator prep + walk + matrix column "
+                                     "kernel + token-by-token companion",
+                         "launches": 2 + 4},
     "two-phase": {"forward": "wkv7_forward saving sa: 16-token sub-chunks (one wave) or token by token",
                   "backward": "wkv7_backward with sa and a workspace: sub-chunk walk + column passes",
                   "launches": 1 + 2},
@@ -454,9 +461,12 @@ def make_runner(wkv7, torch, dev, wl, path, n_sets):
             "h0": None if x["h0"] is None else torch.from_numpy(x["h0"]),
             "dhT": None if x["dhT"] is None else torch.from_numpy(x["dhT"])}
     del x
-    saved = path != "operators"
+    operators = path.startswith("operators")
+    saved = not operators
     ws_bytes = 0
     if path == "operators":
+        ws_bytes = wkv7.forward_workspace_size(B, T, H, D, wl.chunk)
+    elif path == "operators-reform":
         ws_bytes = max(wkv7.forward_workspace_size(B, T, H, D, wl.chunk), wkv7.backward_workspace_size(B, T, H, D, wl.chunk))
     elif path == "two-phase":
         ws_bytes = wkv7.backward_workspace_size(B, T, H, D, wl.chunk)
@@ -482,11 +492,14 @@ def make_runner(wkv7, torch, dev, wl, path, n_sets):
             ev[0].record(stream)
         out = (s["y"], s["ck"], s["hT"]) + ((s["sa"],) if saved else ())
         wkv7.forward(*ins, s["h0"], chunk=wl.chunk, out=out, save_sa=saved,
-                     workspace=s["ws"] if path == "operators" else None)
+                     workspace=s["ws"] if operators else None)
         if ev is not None:
             ev[1].record(stream)
-        wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"],
-                      workspace=s["ws"] if path != "single" else None, out=s["g"])
+        if path == "operators":
+            wkv7.backward_from_forward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], workspace=s["ws"], out=s["g"])
+        else:
+            wkv7.backward(*ins, s["h0"], s["ck"], s["dy"], s["dhT"], chunk=wl.chunk, sa=s["sa"],
+                          workspace=s["ws"] if path != "single" else None, out=s["g"])
         if ev is not None:
             ev[2].record(stream)
 
@@ -696,13 +709,14 @@ def run_ours(args, rank, world, local_rank):
     hbm, peak_kind, peaks = measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    dom = ("wkv7_backward", bwd_b, b_ms) if b_ms >= f_ms else ("wkv7_forward", fwd_b, f_ms)
+    pth = PATHS[args.path]
+    bwd_call = pth.get("backward_call", "wkv7_backward")
+    dom = (bwd_call, bwd_b, b_ms) if b_ms >= f_ms else ("wkv7_forward", fwd_b, f_ms)
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     step_s = elapsed_ms / 1e3 / args.steps
     fp32 = fp32_peak_tflops(peaks, sms)
     roof_s = max((fwd_b + bwd_b) / (hbm * 1e9), literal_flops(wl) / (fp32 * 1e12))
     roof_d = max((fwd_b + bwd_b) / (hbm * 1e9), derived_flops(wl) / (fp32 * 1e12))
-    pth = PATHS[args.path]
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -723,7 +737,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline_step_derived": {"definition": "max(HBM bytes / peak BW, 28*D^2 FLOP per head-token / FP32 peak) "
                                                 "/ step time", "flops": derived_flops(wl),
                                   "roofline_ms": roof_d * 1e3, "frac": roof_d / step_s},
-        "calls_ms": {"wkv7_forward": f_ms, "wkv7_backward": b_ms, "timing": "eager calls, CUDA events around each"},
+        "calls_ms": {"wkv7_forward": f_ms, bwd_call: b_ms, "timing": "eager calls, CUDA events around each"},
         "clocks": clocks,
         "gpu_launches": pth["launches"] * args.steps,
         "e2e": e2e,
