@@ -53,11 +53,20 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up 
 // 16-byte pieces of row j permuted (piece p stored at p ^ (j & 7) for A, p ^ ((j >> 1) & 3) for Q) so
 // that ldmatrix reads of eight rows hit eight distinct bank groups.  X: U_c or E_c (fp32) in mma
 // accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4] (acc_order in wkv7_mma.cuh); the
-// walk overwrites it with G in the same order.
+// walk overwrites it with G in the same order.  Y (forward): Y_intra^T (rows i, columns t; fp32) in the
+// same order [i / 16][t / 8][lane][4], so that a chain CTA fetches its rows' part in one copy.
 constexpr int kXA = 0;
 constexpr int kXQ = 16384;
 constexpr int kXX = 24576;
-constexpr int kXBytes = 40960;
+constexpr int kXY = 40960;
+constexpr int kXBytes = 49152;
+
+// index (floats) of element (i, t) of a 64 x 32 fp32 matrix in mma accumulator order
+__host__ __device__ __forceinline__ int acc_order32(int i, int t) {
+  const int lane = (i & 7) * 4 + ((t & 7) >> 1);
+  const int e = ((i >> 3) & 1) * 2 + (t & 1);
+  return ((((i >> 4) * 4 + (t >> 3)) * 32 + lane) << 2) + e;
+}
 constexpr int kXHead = 256;  // status word(s) before the first block
 
 __host__ __device__ __forceinline__ int swz_a(int j, int jp) { return j * 64 + (((jp >> 3) ^ (j & 7)) << 3) + (jp & 7); }
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kNTP, 2)  // two CTAs per SM (bf16 inputs: ~93
 xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
                 const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
                 const Tin* __restrict__ b, const float* __restrict__ dy, unsigned char* __restrict__ ops,
-                float* __restrict__ y, unsigned* __restrict__ status) {
+                unsigned* __restrict__ status) {
   using LY = XPrepLay<Tin, BWD>;
   constexpr int SM = LY::kSM;
   constexpr bool kVExact = sizeof(Tin) == 2;
@@ -181,15 +190,13 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
   for (int job = blockIdx.x; job < total; job += gridDim.x) {
   const int ci = job % nchunks;
   const int bh = job / nchunks;
-  const int bi = bh / H;
-  const int hi = bh - bi * H;
   const int t0 = ci * kL;
   const int nm = min(kL, T - t0);
-  const size_t base = ((size_t)bi * T * H + hi) * kD;
   unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
   __nv_bfloat16* gA = reinterpret_cast<__nv_bfloat16*>(blk + kXA);
   __nv_bfloat16* gQ = reinterpret_cast<__nv_bfloat16*>(blk + kXQ);
   float* gX = reinterpret_cast<float*>(blk + kXX);
+  float* gY = reinterpret_cast<float*>(blk + kXY);
   const int next = job + gridDim.x;
   cp_async_wait<0>();
   __syncthreads();
@@ -269,8 +276,9 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
           u8[u] = fmaf(u8[u], to_f32(rw[t * kD + u]), fmaf(vi, to_f32(rk[t * kD + u]), d * to_f32(rbv[t * kD + u])));
           yv = fmaf(u8[u], to_f32(rr[t * kD + u]), yv);
         }
-        y[base + (size_t)(t0 + t) * tstride + i] = yv;
+        gY[acc_order32(i, t)] = yv;
       }
+      for (int t = nm; t < kL; ++t) gY[acc_order32(i, t)] = 0.f;
 #pragma unroll
       for (int u = 0; u < 64; ++u) gX[acc_order(i, u)] = u8[u];
     }
@@ -607,30 +615,25 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
           reinterpret_cast<float4*>(gX)[idx] = make_float4(acc[jb][h][0], acc[jb][h][1], acc[jb][h][2], acc[jb][h][3]);
       }
   }
-  if (!BWD) {
-    const int mt = warp >> 2, p = warp & 3;
+  if (!BWD) {  // Y_intra^T = V^T P^T (rows i, columns t): m-tile w >> 1, t n-tiles 2 (w & 1) + 0, 1
+    const int mt = warp >> 1, p = warp & 1;
     float acc[2][4] = {};
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
-      if (mt == 0 && kk == 1) continue;  // P lower triangular
-      const FragA fa = rm_a(Pm, mt, kk, lane);
+      if (kk > p) continue;  // P[t][s] = 0 for s > t
+      const FragA fa = kVExact ? rm_at_hi(Vm, mt, kk, lane) : rm_at(Vm, mt, kk, lane);  // A[i][s] = V[s][i]
       FragB fb[2];
-      rm_bt2(Vm, 2 * p, kk, lane, fb[0], fb[1], !kVExact);
-      if (kVExact) {
-        mma2b(acc[0], fa, fb[0]);
-        mma2b(acc[1], fa, fb[1]);
-      } else {
+      rm_b2(Pm, 2 * p, kk, lane, fb[0], fb[1]);  // B[s][t] = P[t][s]
+      if (kVExact)
+        mma2n<2>(acc, fa, fb);
+      else
         mma3n<2>(acc, fa, fb);
-      }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int tr = mt * 16 + g, col = (2 * p + h) * 8 + 2 * q;
-      if (tr < nm && WKV7_IN(t0 + tr, T, dbg::kXopPrep) && WKV7_IN(col + 1, kD, dbg::kXopPrep))
-        *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr) * tstride + col) = make_float2(acc[h][0], acc[h][1]);
-      if (tr + 8 < nm && WKV7_IN(t0 + tr + 8, T, dbg::kXopPrep))
-        *reinterpret_cast<float2*>(y + base + (size_t)(t0 + tr + 8) * tstride + col) =
-            make_float2(acc[h][2], acc[h][3]);
+      const int idx = (mt * 4 + 2 * p + h) * 32 + lane;
+      if (WKV7_IN(idx, 512, dbg::kXopPrep))
+        reinterpret_cast<float4*>(gY)[idx] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
     }
   }
   }  // chunks
@@ -714,21 +717,32 @@ __device__ __forceinline__ void ld_q_fwd(const __nv_bfloat16* sQ, int nt, int kk
 
 constexpr int kNS = 3;  // stages in flight
 
+// One chain CTA holds R state rows of a head: R / 16 row blocks of 16 rows, each split by columns between
+// two warps (column half 0: columns 0-31, half 1: 32-63) so that a CTA keeps every SM sub-partition's
+// tensor pipe busy.  A product over the state's columns (S A_c, S Q_c) needs the whole row block as its A
+// operand: each warp forms the fragments of its own half from its accumulators and trades them with its
+// partner once per chunk through shared memory (double-buffered by chunk parity, one named barrier per
+// pair and chunk).
 template <int R, bool WALK>
 struct Stage {
-  static constexpr int kNW = R / 16;                             // chain warps
+  static constexpr int kRB = R / 16;                             // row blocks
+  static constexpr int kNW = 2 * kRB;                            // chain warps
   static constexpr int oA = 0;                                   // A_c (16 KB), then Q_c (forward, 8 KB)
   static constexpr int kAQ = WALK ? 16384 : 24576;
   static constexpr int oX = kAQ;                                 // this CTA's rows of U_c / E_c
-  static constexpr int oY = oX + kNW * 4096;                     // forward: y rows [32 t][R + 4]
-  static constexpr int kYL = R + 4;
-  static constexpr int kBytes = oY + (WALK ? 0 : 32 * kYL * 4);
-  static constexpr int kSmem = 128 + kNS * kBytes;
+  static constexpr int kX = kRB * 4096;
+  static constexpr int oY = oX + kX;                             // forward: this CTA's rows of Y_intra^T
+  static constexpr int kY = WALK ? 0 : kRB * 2048;
+  static constexpr int kBytes = oY + kY;
+  static constexpr int oFlag = 64;                               // int [2][kNW] after the mbarriers
+  static constexpr int oXch = 128 + kNS * kBytes;                // uint4 [2][kNW][4][32]
+  static constexpr int kSmem = oXch + 2 * kNW * 4 * 32 * 16;
   static_assert(kBytes % 128 == 0, "stage alignment");
+  static_assert(2 * kNS * 8 <= oFlag && oFlag + 2 * kNW * 4 <= 128, "barriers and flags fit the header");
 };
 
 template <int R, bool WALK>
-__global__ void __launch_bounds__((R / 16 + 1) * 32)
+__global__ void __launch_bounds__((2 * R / 16 + 1) * 32)
 xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, const float* __restrict__ s0,
                  float* __restrict__ y, float* __restrict__ ck, size_t ck_stride, float* __restrict__ sT,
                  unsigned* __restrict__ status) {
@@ -742,6 +756,8 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
   unsigned char* smc = reinterpret_cast<unsigned char*>(smem4);
   uint64_t* full = reinterpret_cast<uint64_t*>(smc);
   uint64_t* empty = full + kNS;
+  int* okf = reinterpret_cast<int*>(smc + ST::oFlag);
+  uint4* xch = reinterpret_cast<uint4*>(smc + ST::oXch);
   auto stage = [&](int s) { return smc + 128 + s * ST::kBytes; };
   const int bh = blockIdx.x / NB, rb = blockIdx.x - (blockIdx.x / NB) * NB;
   const int bi = bh / H, hi = bh - bi * H;
@@ -775,14 +791,12 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
       unsigned char* st = stage(s);
       const unsigned char* src = hops + (size_t)c * kXBytes;
       if (lane == 0) {
-        mbar_expect_tx(&full[s], ST::kAQ + NW * 4096 + (WALK ? 0 : nm * R * 4));
+        mbar_expect_tx(&full[s], ST::kAQ + ST::kX + ST::kY);
         bulk_g2s(st + ST::oA, src + kXA, ST::kAQ, &full[s]);
-        bulk_g2s(st + ST::oX, src + kXX + rb * NW * 4096, NW * 4096, &full[s]);
+        bulk_g2s(st + ST::oX, src + kXX + rb * ST::kX, ST::kX, &full[s]);
+        if (!WALK) bulk_g2s(st + ST::oY, src + kXY + rb * ST::kY, ST::kY, &full[s]);
       }
       __syncwarp();
-      if (!WALK && lane < nm && WKV7_IN(c * kL + lane, T, dbg::kXopChain) && WKV7_IN(rb * R + R - 1, kD, dbg::kXopChain))
-        bulk_g2s(st + ST::oY + lane * ST::kYL * 4, y + base + (size_t)(c * kL + lane) * tstride + rb * R, R * 4,
-                 &full[s]);
       issued = n + 1;
     }
     if (!ok) {
@@ -793,17 +807,19 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     return;
   }
 
-  // =================== chain warp: state rows rb * R + 16 warp + (g, g + 8)
+  // =================== chain warp: state rows rb * R + 16 pair + (g, g + 8), columns 32 half + ..
+  const int pair = warp >> 1, half = warp & 1;
   const int g = lane >> 2, q = lane & 3;
-  const int lrow = warp * 16 + g;  // row within the CTA's block
+  const int lrow = pair * 16 + g;  // row within the CTA's block
   const int row = rb * R + lrow;
   const size_t sbase = (size_t)bh * kD * kD;
-  float S[8][4];
+  float S[4][4];  // n-tiles 4 half + 0 .. 3
 #pragma unroll
-  for (int nj = 0; nj < 8; ++nj) {
+  for (int nj = 0; nj < 4; ++nj) {
+    const int col = (4 * half + nj) * 8 + 2 * q;
     if (s0 != nullptr) {
-      const float2 x0 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)row * kD + nj * 8 + 2 * q));
-      const float2 x8 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)(row + 8) * kD + nj * 8 + 2 * q));
+      const float2 x0 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)row * kD + col));
+      const float2 x8 = __ldg(reinterpret_cast<const float2*>(s0 + sbase + (size_t)(row + 8) * kD + col));
       S[nj][0] = x0.x; S[nj][1] = x0.y; S[nj][2] = x8.x; S[nj][3] = x8.y;
     } else {
       S[nj][0] = S[nj][1] = S[nj][2] = S[nj][3] = 0.f;
@@ -812,86 +828,107 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
   auto store_rows = [&](float* dst) {
     if (!WKV7_IN(row + 8, kD, dbg::kXopChain)) return;
 #pragma unroll
-    for (int nj = 0; nj < 8; ++nj) {
-      *reinterpret_cast<float2*>(dst + (size_t)row * kD + nj * 8 + 2 * q) = make_float2(S[nj][0], S[nj][1]);
-      *reinterpret_cast<float2*>(dst + (size_t)(row + 8) * kD + nj * 8 + 2 * q) = make_float2(S[nj][2], S[nj][3]);
+    for (int nj = 0; nj < 4; ++nj) {
+      const int col = (4 * half + nj) * 8 + 2 * q;
+      *reinterpret_cast<float2*>(dst + (size_t)row * kD + col) = make_float2(S[nj][0], S[nj][1]);
+      *reinterpret_cast<float2*>(dst + (size_t)(row + 8) * kD + col) = make_float2(S[nj][2], S[nj][3]);
     }
   };
 
   for (int n = 0; n < nchunks; ++n) {
     const int c = WALK ? nchunks - 1 - n : n;
     const int s = n % kNS;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (n / kNS) & 1))) {
-      if (lane == 0) atomicOr(status, 1u);
+    const int par = n & 1;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (n / kNS) & 1));
+    // this warp's half of the chunk-start state as A fragments (k-tiles 2 half, 2 half + 1), handed to
+    // the partner; both warps of the pair learn whether either wait gave up, and leave together
+    FragA own[2] = {frag_from_acc(S[0], S[1]), frag_from_acc(S[2], S[3])};
+    {
+      uint4* xo = xch + ((par * NW + warp) * 4) * 32 + lane;
+      xo[0] = make_uint4(own[0].h[0], own[0].h[1], own[0].h[2], own[0].h[3]);
+      xo[32] = make_uint4(own[0].l[0], own[0].l[1], own[0].l[2], own[0].l[3]);
+      xo[64] = make_uint4(own[1].h[0], own[1].h[1], own[1].h[2], own[1].h[3]);
+      xo[96] = make_uint4(own[1].l[0], own[1].l[1], own[1].l[2], own[1].l[3]);
+      if (lane == 0) okf[par * NW + warp] = ok ? 1 : 0;
+    }
+    asm volatile("bar.sync %0, 64;\n" ::"r"(1 + pair) : "memory");
+    if (!ok || okf[par * NW + (warp ^ 1)] == 0) {
+      if (!ok && lane == 0) atomicOr(status, 1u);
       return;
+    }
+    FragA oth[2];
+    {
+      const uint4* xi = xch + ((par * NW + (warp ^ 1)) * 4) * 32 + lane;
+      const uint4 a0 = xi[0], a1 = xi[32], a2 = xi[64], a3 = xi[96];
+      oth[0].h[0] = a0.x; oth[0].h[1] = a0.y; oth[0].h[2] = a0.z; oth[0].h[3] = a0.w;
+      oth[0].l[0] = a1.x; oth[0].l[1] = a1.y; oth[0].l[2] = a1.z; oth[0].l[3] = a1.w;
+      oth[1].h[0] = a2.x; oth[1].h[1] = a2.y; oth[1].h[2] = a2.z; oth[1].h[3] = a2.w;
+      oth[1].l[0] = a3.x; oth[1].l[1] = a3.y; oth[1].l[2] = a3.z; oth[1].l[3] = a3.w;
     }
     const unsigned char* st = stage(s);
     const __nv_bfloat16* sA = reinterpret_cast<const __nv_bfloat16*>(st + ST::oA);
     // the walk's G before this chunk, over its E block (already read into the stage), in accumulator order
     if (WALK && ck != nullptr) {
-      float4* dst = reinterpret_cast<float4*>(ck + ((size_t)bh * nchunks + c) * ck_stride) + (rb * NW + warp) * 8 * 32 + lane;
+      float4* dst = reinterpret_cast<float4*>(ck + ((size_t)bh * nchunks + c) * ck_stride) +
+                    ((rb * ST::kRB + pair) * 8 + 4 * half) * 32 + lane;
 #pragma unroll
-      for (int nj = 0; nj < 8; ++nj) dst[nj * 32] = make_float4(S[nj][0], S[nj][1], S[nj][2], S[nj][3]);
+      for (int nj = 0; nj < 4; ++nj) dst[nj * 32] = make_float4(S[nj][0], S[nj][1], S[nj][2], S[nj][3]);
     }
-    // S = S A_c + U_c (forward) or G = G A_c^T + E_c (walk); the forward also y_c^T += S Q_c (rows i,
-    // columns t).  Per k-step the three bf16 passes go over all accumulators in turn, so that dependent
-    // mma into one accumulator are 8 (walk) or 12 (forward) instructions apart.
+    // S = S A_c + U_c (forward) or G = G A_c^T + E_c (walk) at this warp's columns; the forward also
+    // y_c^T += S Q_c at tokens 16 half .. 16 half + 15 (rows i, columns t).  The own k-tiles go first;
+    // per k-step the three bf16 passes go over all accumulators in turn, so that dependent mma into one
+    // accumulator are 4 (walk) or 6 (forward) instructions apart.
     const int nm = min(kL, T - c * kL);
-    const float* ys = reinterpret_cast<const float*>(st + ST::oY);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(st + kXQ);
-    float acc[8][4], ya[4][4];
-    const float4* xs = reinterpret_cast<const float4*>(st + ST::oX) + warp * 8 * 32 + lane;
+    float acc[4][4], ya[2][4];
+    const float4* xs = reinterpret_cast<const float4*>(st + ST::oX) + (pair * 8 + 4 * half) * 32 + lane;
 #pragma unroll
-    for (int nj = 0; nj < 8; ++nj) {
+    for (int nj = 0; nj < 4; ++nj) {
       const float4 u = xs[nj * 32];
       acc[nj][0] = u.x; acc[nj][1] = u.y; acc[nj][2] = u.z; acc[nj][3] = u.w;
     }
     if (!WALK) {
+      const float4* ys = reinterpret_cast<const float4*>(st + ST::oY) + (pair * 4 + 2 * half) * 32 + lane;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int tc = nt * 8 + 2 * q;
-        ya[nt][0] = ys[tc * ST::kYL + lrow];
-        ya[nt][1] = ys[(tc + 1) * ST::kYL + lrow];
-        ya[nt][2] = ys[tc * ST::kYL + lrow + 8];
-        ya[nt][3] = ys[(tc + 1) * ST::kYL + lrow + 8];
+      for (int nt = 0; nt < 2; ++nt) {
+        const float4 u = ys[nt * 32];
+        ya[nt][0] = u.x; ya[nt][1] = u.y; ya[nt][2] = u.z; ya[nt][3] = u.w;
       }
     }
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const FragA fa = frag_from_acc(S[2 * kk], S[2 * kk + 1]);
-      FragB fb[8], fq[4];
+    for (int ki = 0; ki < 4; ++ki) {
+      const int kk = (2 * half + ki) & 3;
+      const FragA& fa = ki < 2 ? own[ki] : oth[ki - 2];
+      FragB fb[4], fq[2];
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < 2; ++np) {
         if (WALK)
-          ld_a_walk(sA, 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
+          ld_a_walk(sA, 4 * half + 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
         else
-          ld_a_fwd(sA, 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
+          ld_a_fwd(sA, 4 * half + 2 * np, kk, lane, fb[2 * np], fb[2 * np + 1]);
       }
-      if (!WALK) {
-        ld_q_fwd(sQ, 0, kk, lane, fq[0], fq[1]);
-        ld_q_fwd(sQ, 2, kk, lane, fq[2], fq[3]);
-      }
+      if (!WALK) ld_q_fwd(sQ, 2 * half, kk, lane, fq[0], fq[1]);
 #pragma unroll
-      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.l, fb[nj].h[0], fb[nj].h[1]);
+      for (int nj = 0; nj < 4; ++nj) mma16816(acc[nj], fa.l, fb[nj].h[0], fb[nj].h[1]);
       if (!WALK)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.l, fq[nt].h[0], fq[nt].h[1]);
+        for (int nt = 0; nt < 2; ++nt) mma16816(ya[nt], fa.l, fq[nt].h[0], fq[nt].h[1]);
 #pragma unroll
-      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.h, fb[nj].l[0], fb[nj].l[1]);
+      for (int nj = 0; nj < 4; ++nj) mma16816(acc[nj], fa.h, fb[nj].l[0], fb[nj].l[1]);
       if (!WALK)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.h, fq[nt].l[0], fq[nt].l[1]);
+        for (int nt = 0; nt < 2; ++nt) mma16816(ya[nt], fa.h, fq[nt].l[0], fq[nt].l[1]);
 #pragma unroll
-      for (int nj = 0; nj < 8; ++nj) mma16816(acc[nj], fa.h, fb[nj].h[0], fb[nj].h[1]);
+      for (int nj = 0; nj < 4; ++nj) mma16816(acc[nj], fa.h, fb[nj].h[0], fb[nj].h[1]);
       if (!WALK)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma16816(ya[nt], fa.h, fq[nt].h[0], fq[nt].h[1]);
+        for (int nt = 0; nt < 2; ++nt) mma16816(ya[nt], fa.h, fq[nt].h[0], fq[nt].h[1]);
     }
     if (!WALK) {
       float* yo = y + base + (size_t)(c * kL) * tstride;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int tc = nt * 8 + 2 * q;
+      for (int nt = 0; nt < 2; ++nt) {
+        const int tc = (2 * half + nt) * 8 + 2 * q;
         if (tc < nm) {
           yo[(size_t)tc * tstride + row] = ya[nt][0];
           yo[(size_t)tc * tstride + row + 8] = ya[nt][2];
@@ -905,7 +942,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
-    for (int nj = 0; nj < 8; ++nj)
+    for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[nj][e] = acc[nj][e];
     if (!WALK && ck != nullptr) store_rows(ck + ((size_t)bh * nchunks + c) * ck_stride);
@@ -928,7 +965,7 @@ cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* o
   const unsigned grid = (unsigned)min(total, 2 * num_sms());  // two CTAs per SM, each looping over its chunks
   kern<<<grid, kNTP, LY::kBytes, stream>>>(T, H, C, total, (const Tin*)in.r, (const Tin*)in.w, (const Tin*)in.k,
                                           (const Tin*)in.v, (const Tin*)in.a, (const Tin*)in.b,
-                                          BWD ? ba->dy : nullptr, ops, BWD ? nullptr : fa->y, status);
+                                          BWD ? ba->dy : nullptr, ops, status);
   return cudaGetLastError();
 }
 
@@ -941,7 +978,7 @@ cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops,
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ST::kSmem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)B * H * (64 / R);
-  kern<<<grid, (R / 16 + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, s0, y, ck, ck_stride, sT, status);
+  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, s0, y, ck, ck_stride, sT, status);
   return cudaGetLastError();
 }
 
