@@ -88,8 +88,9 @@ int wkv7_num_chunks(int T, int chunk);
  *           aligned, owned by the caller; or NULL / 0.  Used at chunk == 32 without sa
  *           (the chunk-operator forward): a parallel kernel forms every 32-token chunk's
  *           transition operator (S_end = S_start A_c + U_c, and the chunk's y from S_start)
- *           into it, 49152 bytes per (head, chunk) after a 256-byte header, with the
- *           chunk-internal part of y; then one short chain per head applies them.  The
+ *           into it, 65536 bytes per (head, chunk) after a 256-byte header, with the
+ *           chunk-internal part of y and the coupling matrices a later
+ *           wkv7_backward_from_forward reuses; then one short chain per head applies them.  The
  *           header's first 4 bytes hold a status word: 0 after a call that completed
  *           normally; non-zero (WKV7_ERR_TIMEOUT) when a bounded wait inside the chain gave
  *           up (2 s), in which case the outputs are invalid.  Reading it is the caller's
@@ -106,7 +107,7 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const float *h0, float *y, float *h_ckpt, float *hT, float *sa,
                  void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 49152 per (head,
+/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 65536 per (head,
  * chunk) at chunk 32, 0 otherwise; returns a wkv7_status (the same size checks as wkv7_forward). */
 int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 
@@ -175,7 +176,9 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *
 
 /*
  * The chunk-operator backward that takes the transition operators from its forward instead of forming
- * them again (the forward's operators of a chunk are the backward's: A_c, and Q_c for E_c = DY^T Q_c^T).
+ * them again (the forward's operators of a chunk are the backward's: A_c, and Q_c for E_c = DY^T Q_c^T),
+ * and, with bf16 inputs, the coupling matrices M_ak, M_rb, M_rk and T = (I - M_ab)^-1 that the column
+ * gradients use.
  *   fwd_workspace, fwd_workspace_bytes
  *           the workspace of the wkv7_forward call (chunk 32, no sa, with a workspace) that wrote
  *           h_ckpt from these same r..b and h0, untouched since; at least
@@ -185,10 +188,11 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *
  *           holds anything else gives meaningless gradients (nothing on the device can tell).
  *   Every other argument, layout and result as wkv7_backward with a workspace and no sa; chunk must
  *   be 32 (WKV7_ERR_SHAPE otherwise).  The first kernel only forms E_c (one product per chunk) where
- *   wkv7_backward forms A_c, Q_c and E_c; the walk and the column gradients are the same kernels.
- *   Chunks in closed form get the same A_c and E_c bit for bit, so the same gradients; chunks taken
- *   token by token (tiny decays) get E_c from the split Q_c (~1e-6 relative difference).  The
- *   workspace header's status word is as in wkv7_forward.
+ *   wkv7_backward forms A_c, Q_c and E_c; the walk is the same kernel, and the column gradients skip
+ *   forming the coupling matrices.  The walk sees the same A_c and E_c as wkv7_backward's on chunks in
+ *   closed form (bit for bit); the matrices the forward formed differ from the column kernel's own in
+ *   rounding only, so the gradients agree with wkv7_backward's to ~1e-6 relative.  The workspace
+ *   header's status word is as in wkv7_forward.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).
  */
 int wkv7_backward_from_forward(int B, int T, int H, int D, int chunk, int in_dtype,

@@ -438,12 +438,12 @@ size_t two_phase_bytes(int B, int T, int H, int chunk) {
 size_t backward_workspace_bytes(int B, int T, int H, int chunk) {
   const size_t a = two_phase_bytes(B, T, H, chunk);
   if (chunk != 32) return a;
-  const size_t b = xop_workspace_bytes(B, T, H);
+  const size_t b = xop_workspace_bytes(B, T, H, false);
   return a > b ? a : b;
 }
 
 size_t forward_workspace_bytes(int B, int T, int H, int chunk) {
-  return chunk == 32 ? xop_workspace_bytes(B, T, H) : 0;
+  return chunk == 32 ? xop_workspace_bytes(B, T, H, true) : 0;
 }
 
 cudaError_t launch_backward_transition(const BwdArgs& p, void* workspace, bool from_forward, cudaStream_t stream) {

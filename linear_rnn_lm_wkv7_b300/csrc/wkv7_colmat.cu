@@ -103,18 +103,25 @@ struct Lay {
   static_assert(oSef + kD * kD * 4 <= oB, "S_e fits over SA and DSA");
   static_assert(4 * kL * kD * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
   static constexpr int kBytes = oGf + kD * kD * 4;
+  // ---- (matrices from the forward) M_ak, M_rb, M_rk, T, loaded with S0, G and S_e
+  static constexpr int oM = kBytes;
+  static constexpr int kBytesM = oM + 4 * rm_bytes(32, kLD32);
   // ---- r o dr, a o da, k o dk, b o db, fp32 [32][64] each, over A^ .. (after the last products)
   static constexpr int oStage = oAh;
   static_assert(oStage + 4 * kL * kD * 4 <= oV, "dw terms fit over A^ .. Xb");
 };
 
-template <typename Tin>
+// FM: M_ak, M_rb, M_rk and T come from the forward's operator blocks (`mats`, at the blocks' stride of
+// xck_stride floats) instead of being formed here (no M_ab, no inverse).  The forward formed them in
+// closed form for every chunk whose gamma_31 passes the same test as here (>= 1e-20 and finite), a
+// superset of the chunks this kernel takes in matrix form.
+template <typename Tin, bool FM>
 __global__ void __launch_bounds__(kNT, 1)
 colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
               const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
               const Tin* __restrict__ b, const float* __restrict__ h0, const float* __restrict__ h_ckpt,
               const float* __restrict__ dy, const float* __restrict__ xck, int* __restrict__ flags, size_t xck_stride,
-              float* __restrict__ dr,
+              const unsigned char* __restrict__ mats, float* __restrict__ dr,
               float* __restrict__ dw, float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ da,
               float* __restrict__ db) {
   using LY = Lay<Tin>;
@@ -147,9 +154,11 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   const RM Vm{bfp(LY::oV), 32 * kLD64, kLD64}, DY{bfp(LY::oDY), 32 * kLD64, kLD64};
   const RM SA{bfp(LY::oSA), 32 * kLD64, kLD64}, DSA{bfp(LY::oDSA), 32 * kLD64, kLD64};
   const RM U{bfp(LY::oU), 32 * kLD64, kLD64}, W{bfp(LY::oW), 32 * kLD64, kLD64};
-  const RM Mak{bfp(LY::oMak), 32 * kLD32, kLD32}, Mrb{bfp(LY::oMrb), 32 * kLD32, kLD32};
-  const RM Mrk{bfp(LY::oMrk), 32 * kLD32, kLD32};
-  const RM Tm{bfp(LY::oT), 32 * kLD32, kLD32};
+  constexpr int kRM32 = rm_bytes(32, kLD32);
+  const RM Mak{bfp(FM ? LY::oM : LY::oMak), 32 * kLD32, kLD32};
+  const RM Mrb{bfp(FM ? LY::oM + kRM32 : LY::oMrb), 32 * kLD32, kLD32};
+  const RM Mrk{bfp(FM ? LY::oM + 2 * kRM32 : LY::oMrk), 32 * kLD32, kLD32};
+  const RM Tm{bfp(FM ? LY::oM + 3 * kRM32 : LY::oT), 32 * kLD32, kLD32};
   const RM L1{bfp(LY::oL), 32 * kLD32, kLD32}, L2{bfp(LY::oL + rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
   const RM L3{bfp(LY::oL + 2 * rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
   const RM L4{bfp(LY::oL + 3 * rm_bytes(32, kLD32)), 32 * kLD32, kLD32};
@@ -191,6 +200,14 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       if (s0_ != nullptr) cp_async16(s0f + 4 * e, s0_ + 4 * e);
       cp_async16(gf + 4 * e, gend_ + 4 * e);
       cp_async16(sef + 4 * e, send_ + 4 * e);
+    }
+    if (FM) {  // (matrix, hi / lo, row, 16-byte piece): rows of 64 bytes into rows of kLD32 elements
+      const unsigned char* msrc = mats + ((size_t)bh_ * nchunks + ci_) * xck_stride * 4;
+      for (int e = tid; e < 4 * 2 * 32 * 4; e += kNT) {
+        const int m = e >> 8, hl = (e >> 7) & 1, rr = (e >> 2) & 31, pc = e & 3;
+        cp_async16(sm + LY::oM + m * kRM32 + hl * (32 * kLD32 * 2) + rr * (kLD32 * 2) + pc * 16,
+                   msrc + m * 4096 + hl * 2048 + rr * 64 + pc * 16);
+      }
     }
     cp_async_commit();
   };
@@ -332,6 +349,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     cp_async_commit();
   }
 
+  if constexpr (!FM) {  // (from the forward: loaded instead)
   // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
   // M_rk = tril(R^ K~^T); 16 jobs of (product, m-tile, pair of n-tiles), K = 64
   // warp w forms jobs w and w + 8 together: the same tile of (M_ab, M_rb) or (M_ak, M_rk), sharing B~ or K~
@@ -373,11 +391,13 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     }
   }
   __syncthreads();
+  }
 
   // ---- P3 || P4: warp 0 solves the diagonal blocks of T = (I - M_ab)^-1 (forward substitution, one column
   // per lane: lanes 0-15 T11, lanes 16-31 T22); the other warps form U = A^ S0^T + M_ak V and
   // W = B~ Xb^T + M_rb^T DY (rows t, columns i): 16 jobs of (product, m-tile, 4 n-tiles)
-  if (warp == 0) {
+  // (from the forward: T is loaded, and all eight warps form U and W)
+  if (!FM && warp == 0) {
     const int off = lane < 16 ? 0 : 16;
     const int c = lane & 15;
     float x[16];
@@ -393,7 +413,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     __syncwarp();
     tri_inverse_t21(Mab, TI, SM, lane);  // T21 = T22 A21 T11 (A21 = M_ab[16..31][0..15])
   } else {
-    for (int job = warp - 1; job < 16; job += kNW - 1) {
+    for (int job = FM ? warp : warp - 1; job < 16; job += FM ? kNW : kNW - 1) {
       const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1
       float acc[2][4] = {};
 #pragma unroll
@@ -436,11 +456,13 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     }
   }
   __syncthreads();
-  for (int e = tid; e < 32 * 16; e += kNT) {  // T (rows t, columns u), zero above the diagonal
-    const int t = e >> 4, u = 2 * (e & 15);
-    rm_store(Tm, t, u, u <= t ? TI[t * SM + u] : 0.f, u + 1 <= t ? TI[t * SM + u + 1] : 0.f);
+  if constexpr (!FM) {
+    for (int e = tid; e < 32 * 16; e += kNT) {  // T (rows t, columns u), zero above the diagonal
+      const int t = e >> 4, u = 2 * (e & 15);
+      rm_store(Tm, t, u, u <= t ? TI[t * SM + u] : 0.f, u + 1 <= t ? TI[t * SM + u + 1] : 0.f);
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- P5: SA = T U, DSA = T^T W (rows t, columns i; K = 32); 16 jobs (product, m-tile, 4 n-tiles)
   {  // warp w: SA and DSA at the same tile (m-tile, 2 n-tiles)
@@ -788,15 +810,22 @@ cudaError_t launch_colmat_t(const BwdArgs& p, const ChunkEnds& ends, cudaStream_
   using LY = Lay<Tin>;
   using FL = FbLay<Tin>;
   static_assert(LY::kBytes <= 232448, "shared memory per CTA");
-  auto kern = colmat_kernel<Tin>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes);
+  // the forward's matrices are taken where their region fits beside the rest (bf16 inputs); fp32 inputs
+  // (twice the raw staging) form them here
+  constexpr bool kFits = LY::kBytesM <= 232448;
+  const bool fm = kFits && ends.mats != nullptr;
+  auto kern = colmat_kernel<Tin, false>;
+  if constexpr (kFits)
+    if (fm) kern = colmat_kernel<Tin, true>;
+  const int smem = fm ? LY::kBytesM : LY::kBytes;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   const int total = p.B * p.H * p.nchunks;
   const int grid = min(total, num_sms());  // one CTA per SM (shared memory), each looping over its chunks
-  kern<<<(unsigned)grid, kNT, LY::kBytes, stream>>>(
+  kern<<<(unsigned)grid, kNT, smem, stream>>>(
       p.T, p.H, p.nchunks, total, (const Tin*)p.in.r, (const Tin*)p.in.w, (const Tin*)p.in.k, (const Tin*)p.in.v,
-      (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, p.dr, p.dw, p.dk,
-      p.dv, p.da, p.db);
+      (const Tin*)p.in.a, (const Tin*)p.in.b, p.h0, p.h_ckpt, p.dy, ends.g, ends.flags, ends.stride, ends.mats, p.dr,
+      p.dw, p.dk, p.dv, p.da, p.db);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   auto fkern = colfb_kernel<Tin>;

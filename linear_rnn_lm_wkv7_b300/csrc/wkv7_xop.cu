@@ -53,13 +53,17 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up 
 // 16-byte pieces of row j permuted (piece p stored at p ^ (j & 7) for A, p ^ ((j >> 1) & 3) for Q) so
 // that ldmatrix reads of eight rows hit eight distinct bank groups.  X: U_c or E_c (fp32) in mma
 // accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4] (acc_order in wkv7_mma.cuh); the
-// walk overwrites it with G in the same order.  Y (forward): Y_intra^T (rows i, columns t; fp32) in the
-// same order [i / 16][t / 8][lane][4], so that a chain CTA fetches its rows' part in one copy.
+// walk overwrites it with G in the same order.  The forward's blocks add Y: Y_intra^T (rows i, columns t;
+// fp32) in the same order [i / 16][t / 8][lane][4], so that a chain CTA fetches its rows' part in one
+// copy; and M: M_ak, M_rb, M_rk and T (4 KB each: bf16 hi rows then lo rows, 32 x 32, unpadded) for a
+// backward that reuses them.  A backward alone uses only A, Q and X.
 constexpr int kXA = 0;
 constexpr int kXQ = 16384;
 constexpr int kXX = 24576;
 constexpr int kXY = 40960;
-constexpr int kXBytes = 49152;
+constexpr int kXM = 49152;
+constexpr int kXBytesFwd = 65536;  // block stride of the forward's workspace
+constexpr int kXBytesBwd = 40960;  // ... of a backward's own
 
 // index (floats) of element (i, t) of a 64 x 32 fp32 matrix in mma accumulator order
 __host__ __device__ __forceinline__ int acc_order32(int i, int t) {
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kNTP, 2)  // two CTAs per SM (bf16 inputs: ~93
 xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, const Tin* __restrict__ w,
                 const Tin* __restrict__ k, const Tin* __restrict__ v, const Tin* __restrict__ a,
                 const Tin* __restrict__ b, const float* __restrict__ dy, unsigned char* __restrict__ ops,
-                unsigned* __restrict__ status) {
+                size_t bstride, unsigned* __restrict__ status) {
   using LY = XPrepLay<Tin, BWD>;
   constexpr int SM = LY::kSM;
   constexpr bool kVExact = sizeof(Tin) == 2;
@@ -192,7 +196,7 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
   const int bh = job / nchunks;
   const int t0 = ci * kL;
   const int nm = min(kL, T - t0);
-  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
+  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * bstride;
   __nv_bfloat16* gA = reinterpret_cast<__nv_bfloat16*>(blk + kXA);
   __nv_bfloat16* gQ = reinterpret_cast<__nv_bfloat16*>(blk + kXQ);
   float* gX = reinterpret_cast<float*>(blk + kXX);
@@ -577,6 +581,14 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
           rm_store_acc(Pm, mt, 2 * np + h, lane, acc[h]);
         }
       }
+      // M_ak, M_rb, M_rk and T into the block (rows of 64 bytes, hi then lo) for a backward that reuses them
+      unsigned char* gM = blk + kXM;
+      for (int e = tid; e < 4 * 2 * 32 * 4; e += kNTP) {  // (matrix, hi / lo, row, 16-byte piece)
+        const int m = e >> 8, hl = (e >> 7) & 1, rr = (e >> 2) & 31, pc = e & 3;
+        const int so = m == 0 ? LY::oMak : (m == 1 ? LY::oMrb : (m == 2 ? LY::oMrk : LY::oT));
+        *reinterpret_cast<uint4*>(gM + m * 4096 + hl * 2048 + rr * 64 + pc * 16) =
+            *reinterpret_cast<const uint4*>(sm + so + hl * (32 * kLD32 * 2) + rr * (kLD32 * 2) + pc * 16);
+      }
     }
   }
   __syncthreads();
@@ -743,12 +755,12 @@ struct Stage {
 
 template <int R, bool WALK>
 __global__ void __launch_bounds__((2 * R / 16 + 1) * 32)
-xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, const float* __restrict__ s0,
-                 float* __restrict__ y, float* __restrict__ ck, size_t ck_stride, float* __restrict__ sT,
-                 unsigned* __restrict__ status) {
+xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, size_t bstride,
+                 const float* __restrict__ s0, float* __restrict__ y, float* __restrict__ ck, size_t ck_stride,
+                 float* __restrict__ sT, unsigned* __restrict__ status) {
   // forward: s0 = h0 (or null), y (Y_intra in, y out), ck = h_ckpt (or null; ck_stride = 4096 floats),
   // sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X in accumulator order
-  // (ck_stride = kXBytes / 4), sT = dh0.
+  // (ck_stride = bstride / 4), sT = dh0.  bstride: bytes between operator blocks.
   using ST = Stage<R, WALK>;
   constexpr int NW = ST::kNW;
   constexpr int NB = 64 / R;
@@ -764,7 +776,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t tstride = (size_t)H * kD;
   const size_t base = ((size_t)bi * T * H + hi) * kD;
-  const unsigned char* hops = ops + (size_t)bh * nchunks * kXBytes;
+  const unsigned char* hops = ops + (size_t)bh * nchunks * bstride;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
@@ -789,7 +801,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
       }
       const int nm = min(kL, T - c * kL);
       unsigned char* st = stage(s);
-      const unsigned char* src = hops + (size_t)c * kXBytes;
+      const unsigned char* src = hops + (size_t)c * bstride;
       if (lane == 0) {
         mbar_expect_tx(&full[s], ST::kAQ + ST::kX + ST::kY);
         bulk_g2s(st + ST::oA, src + kXA, ST::kAQ, &full[s]);
@@ -951,7 +963,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
 }
 
 template <typename Tin, bool BWD>
-cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* ops, unsigned* status,
+cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* ops, size_t bstride, unsigned* status,
                           cudaStream_t stream) {
   using LY = XPrepLay<Tin, BWD>;
   static_assert(LY::kBytes <= 232448, "shared memory per CTA");
@@ -965,20 +977,20 @@ cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* o
   const unsigned grid = (unsigned)min(total, 2 * num_sms());  // two CTAs per SM, each looping over its chunks
   kern<<<grid, kNTP, LY::kBytes, stream>>>(T, H, C, total, (const Tin*)in.r, (const Tin*)in.w, (const Tin*)in.k,
                                           (const Tin*)in.v, (const Tin*)in.a, (const Tin*)in.b,
-                                          BWD ? ba->dy : nullptr, ops, status);
+                                          BWD ? ba->dy : nullptr, ops, bstride, status);
   return cudaGetLastError();
 }
 
 template <int R, bool WALK>
-cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, const float* s0, float* y, float* ck,
-                           size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0, float* y,
+                           float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
   using ST = Stage<R, WALK>;
   static_assert(ST::kSmem <= 232448, "shared memory per CTA");
   auto kern = xop_chain_kernel<R, WALK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ST::kSmem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)B * H * (64 / R);
-  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, s0, y, ck, ck_stride, sT, status);
+  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status);
   return cudaGetLastError();
 }
 
@@ -995,12 +1007,12 @@ int chain_rows(int heads) {
 }
 
 template <bool WALK>
-cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned char* ops, const float* s0, float* y,
-                         float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0,
+                         float* y, float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
   switch (rows) {
-    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
-    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
-    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, s0, y, ck, ck_stride, sT, status, stream);
+    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
+    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
+    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
   }
 }
 
@@ -1027,9 +1039,10 @@ __device__ __forceinline__ void q_b2(const __nv_bfloat16* sq, int nt, int kk, in
 // the products run in the same order, so E_c of a closed-form chunk is the same as that kernel's.
 __global__ void __launch_bounds__(kNTE)
 xop_e_kernel(int T, int H, int nchunks, const float* __restrict__ dy, unsigned char* __restrict__ ops,
-             unsigned* __restrict__ status) {
+             size_t bstride, unsigned* __restrict__ status) {
   __shared__ __align__(128) __nv_bfloat16 sQ[2 * 64 * 32];
   __shared__ __align__(128) __nv_bfloat16 sDY[2 * kL * kLD64];
+  __shared__ __align__(16) float sdy[kL * kD];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int job = blockIdx.x;
   const int ci = job % nchunks, bh = job / nchunks;
@@ -1037,20 +1050,25 @@ xop_e_kernel(int T, int H, int nchunks, const float* __restrict__ dy, unsigned c
   const int t0 = ci * kL, nm = min(kL, T - t0);
   const size_t base = ((size_t)bi * T * H + hi) * kD;
   const size_t tstride = (size_t)H * kD;
-  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * kXBytes;
+  unsigned char* blk = ops + ((size_t)bh * nchunks + ci) * bstride;
   if (job == 0 && tid == 0 && status != nullptr) *status = 0u;
+  // Q_c (8 KB) and the chunk's dy rows (fp32, 256 bytes each) in flight together
   for (int e = tid; e < 512; e += kNTE) cp_async16(sQ + e * 8, blk + kXQ + e * 16);
+  for (int e = tid; e < nm * (kD / 4); e += kNTE) {
+    const int t = e >> 4, c = (e & 15) * 4;
+    if (WKV7_IN(t0 + t, T, dbg::kXopPrep)) cp_async16(sdy + t * kD + c, dy + base + (size_t)(t0 + t) * tstride + c);
+  }
   cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
   const RM DYm{sDY, kL * kLD64, kLD64};
-  for (int e = tid; e < kL * (kD / 4); e += kNTE) {  // rows t, four columns per thread and step
+  for (int e = tid; e < kL * (kD / 4); e += kNTE) {  // split into hi + lo (rows past the chunk zero)
     const int t = e >> 4, c = (e & 15) * 4;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < nm && WKV7_IN(t0 + t, T, dbg::kXopPrep))
-      x = *reinterpret_cast<const float4*>(dy + base + (size_t)(t0 + t) * tstride + c);
+    if (t < nm) x = *reinterpret_cast<const float4*>(sdy + t * kD + c);
     rm_store(DYm, t, c, x.x, x.y);
     rm_store(DYm, t, c + 2, x.z, x.w);
   }
-  cp_async_wait<0>();
   __syncthreads();
   float acc[8][4] = {};
 #pragma unroll
@@ -1070,44 +1088,47 @@ xop_e_kernel(int T, int H, int nchunks, const float* __restrict__ dy, unsigned c
 
 WKV7_DEBUG_READER(debug_word_xop)
 
-size_t xop_workspace_bytes(int B, int T, int H) {
+size_t xop_workspace_bytes(int B, int T, int H, bool forward) {
   const size_t C = ((size_t)T + kL - 1) / kL;
-  return kXHead + (size_t)B * H * C * kXBytes;
+  return kXHead + (size_t)B * H * C * (forward ? kXBytesFwd : kXBytesBwd);
 }
 
 cudaError_t launch_xop_forward(const FwdArgs& p, void* workspace, int rows, cudaStream_t stream) {
   if (p.nchunks == 0) return cudaSuccess;
   unsigned* status = static_cast<unsigned*>(workspace);
   unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
-  cudaError_t err = p.bf16 ? launch_prep_t<__nv_bfloat16, false>(&p, nullptr, ops, status, stream)
-                           : launch_prep_t<float, false>(&p, nullptr, ops, status, stream);
+  cudaError_t err = p.bf16 ? launch_prep_t<__nv_bfloat16, false>(&p, nullptr, ops, kXBytesFwd, status, stream)
+                           : launch_prep_t<float, false>(&p, nullptr, ops, kXBytesFwd, status, stream);
   if (err != cudaSuccess) return err;
   if (rows == 0) rows = chain_rows(p.B * p.H);
-  return launch_chain<false>(rows, p.B, p.T, p.H, p.nchunks, ops, p.h0, p.y, p.h_ckpt, (size_t)kD * kD, p.hT, status,
-                             stream);
+  return launch_chain<false>(rows, p.B, p.T, p.H, p.nchunks, ops, kXBytesFwd, p.h0, p.y, p.h_ckpt, (size_t)kD * kD,
+                             p.hT, status, stream);
 }
 
 cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward, int rows, ChunkEnds* ends,
                             cudaStream_t stream) {
   unsigned* status = static_cast<unsigned*>(workspace);
   unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
+  const size_t bstride = from_forward ? kXBytesFwd : kXBytesBwd;
   ends->g = reinterpret_cast<const float*>(ops + kXX);
   ends->flags = reinterpret_cast<int*>(ops + kXQ);  // Q_c's slot: the walk does not use it
-  ends->stride = kXBytes / 4;
+  ends->stride = bstride / 4;
+  ends->mats = from_forward ? ops + kXM : nullptr;
   if (p.nchunks > 0) {  // (no chunks: the chain only copies dhT to dh0)
     cudaError_t err;
     if (from_forward) {
-      xop_e_kernel<<<(unsigned)(p.B * p.H * p.nchunks), kNTE, 0, stream>>>(p.T, p.H, p.nchunks, p.dy, ops, status);
+      xop_e_kernel<<<(unsigned)(p.B * p.H * p.nchunks), kNTE, 0, stream>>>(p.T, p.H, p.nchunks, p.dy, ops, bstride,
+                                                                             status);
       err = cudaGetLastError();
     } else {
-      err = p.bf16 ? launch_prep_t<__nv_bfloat16, true>(nullptr, &p, ops, status, stream)
-                   : launch_prep_t<float, true>(nullptr, &p, ops, status, stream);
+      err = p.bf16 ? launch_prep_t<__nv_bfloat16, true>(nullptr, &p, ops, bstride, status, stream)
+                   : launch_prep_t<float, true>(nullptr, &p, ops, bstride, status, stream);
     }
     if (err != cudaSuccess) return err;
   }
   if (rows == 0) rows = chain_rows(p.B * p.H);
-  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, p.dhT, nullptr,
-                            reinterpret_cast<float*>(ops + kXX), kXBytes / 4, p.dh0, status, stream);
+  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr,
+                            reinterpret_cast<float*>(ops + kXX), bstride / 4, p.dh0, status, stream);
 }
 
 }  // namespace wkv7
