@@ -527,7 +527,9 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   __syncthreads();
 
   // ---- P7: DR, DA, DK, DB, DV (rows t, columns j or i): 20 jobs of (product, m-tile, 4 n-tiles), each a
-  // K = 64 product with S0 / Xb plus the masked products; held in registers until every warp is done
+  // K = 64 product with S0 / Xb plus the masked products.  Each job's dr, da, dk, db (scaled by Gamma,
+  // Gamma_-, 1 / Gamma) or dv is written as soon as it is formed, so that the stores drain during the
+  // warp's later jobs; the scaled values stay in registers for the dw terms.
   constexpr int kRep = (20 + kNW - 1) / kNW;  // output jobs per warp
   float res[kRep][4][4];
 #pragma unroll
@@ -589,42 +591,51 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
         mma3n<4>(acc, fa, fb);
       }
     }
-  }
-  cp_async_wait<0>();
-  __syncthreads();  // every operand has been read: stage over A^ .. Xb
-  // ---- outputs: dr, da, dk, db (scaled by Gamma, Gamma_-, 1/Gamma) and dv straight from the accumulators;
-  // r o dr, a o da, k o dk, b o db into shared memory (over A^ ..) for dw
-  float* terms = reinterpret_cast<float*>(sm + LY::oStage);
-  const Tin* in4 = reinterpret_cast<const Tin*>(sm + LY::oIn);
-#pragma unroll
-  for (int rep = 0; rep < kRep; ++rep) {
-    const int job = warp + kNW * rep;
-    if (job >= 20) continue;
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
     float* outp = prod == 0 ? dr : (prod == 1 ? da : (prod == 2 ? dk : (prod == 3 ? db : dv)));
-    float* sp = terms + (prod & 3) * kL * kD;
-    const Tin* inp = in4 + (prod & 3) * kL * kD;  // r, a, k, b
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int j = (4 * nh + x) * 8 + 2 * q;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int t = mt * 16 + g + 8 * hr;
-        const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
-        const float2 gp = t > 0 ? *reinterpret_cast<const float2*>(G + (t - 1) * kD + j) : make_float2(1.f, 1.f);
-        float2 sc;
-        if (prod == 0) sc = gt;
-        else if (prod == 1) sc = gp;
-        else if (prod < 4) sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
-        else sc = make_float2(1.f, 1.f);
-        const float2 o = make_float2(res[rep][x][2 * hr] * sc.x, res[rep][x][2 * hr + 1] * sc.y);
-        if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
-          *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) = o;
-        if (prod < 4) {
-          float2 in = make_float2(0.f, 0.f);
-          if (t < n) in = make_float2(to_f32(inp[t * kD + j]), to_f32(inp[t * kD + j + 1]));
-          *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(o.x * in.x, o.y * in.y);
+        float2 sc = make_float2(1.f, 1.f);
+        if (prod == 0) {
+          sc = *reinterpret_cast<const float2*>(G + t * kD + j);
+        } else if (prod == 1) {
+          if (t > 0) sc = *reinterpret_cast<const float2*>(G + (t - 1) * kD + j);
+        } else if (prod < 4) {
+          const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+          sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
         }
+        acc[x][2 * hr] *= sc.x;
+        acc[x][2 * hr + 1] *= sc.y;
+        if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
+          *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) =
+              make_float2(acc[x][2 * hr], acc[x][2 * hr + 1]);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every operand has been read: stage over A^ .. Xb
+  // ---- r o dr, a o da, k o dk, b o db into shared memory (over A^ ..) for dw
+  float* terms = reinterpret_cast<float*>(sm + LY::oStage);
+  const Tin* in4 = reinterpret_cast<const Tin*>(sm + LY::oIn);
+#pragma unroll
+  for (int rep = 0; rep < kRep; ++rep) {
+    const int job = warp + kNW * rep;
+    if (job >= 16) continue;  // (jobs 16-19: dv)
+    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
+    float* sp = terms + prod * kL * kD;
+    const Tin* inp = in4 + prod * kL * kD;  // r, a, k, b
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int j = (4 * nh + x) * 8 + 2 * q;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int t = mt * 16 + g + 8 * hr;
+        float2 in = make_float2(0.f, 0.f);
+        if (t < n) in = make_float2(to_f32(inp[t * kD + j]), to_f32(inp[t * kD + j + 1]));
+        *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(res[rep][x][2 * hr] * in.x, res[rep][x][2 * hr + 1] * in.y);
       }
     }
   }
