@@ -107,6 +107,24 @@ int wkv7_forward(int B, int T, int H, int D, int chunk, int in_dtype,
                  const float *h0, float *y, float *h_ckpt, float *hT, float *sa,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * The chunk-operator forward with y written in bf16 (round to nearest even) instead of fp32.
+ *   y       (B,T,H,D) bf16 output (2 bytes per element), required when T > 0.
+ *   workspace, workspace_bytes
+ *           required (WKV7_ERR_ARG if NULL): as in wkv7_forward, and likewise usable by a
+ *           following wkv7_backward_from_forward.
+ *   chunk must be 32 (WKV7_ERR_SHAPE otherwise); there is no sa output.  Every other argument and
+ *   result as wkv7_forward.  The state, the checkpoints and hT stay fp32; y is the fp32 value that
+ *   wkv7_forward writes, rounded once to bf16 at the store (so it carries the bf16 rounding, a
+ *   relative error up to 2^-9 per element, on top of the forward's ~1e-5).
+ * Source: Forward listing of "Metal kernel architecture" (see top of file).
+ */
+int wkv7_forward_bf16_y(int B, int T, int H, int D, int chunk, int in_dtype,
+                        const void *r, const void *w, const void *k,
+                        const void *v, const void *a, const void *b,
+                        const float *h0, void *y, float *h_ckpt, float *hT,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 65536 per (head,
  * chunk) at chunk 32, 0 otherwise; returns a wkv7_status (the same size checks as wkv7_forward). */
 int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);

@@ -32,6 +32,7 @@ SIGNATURES = {
     "wkv7_num_chunks": (_I, [_I, _I]),
     "wkv7_forward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_forward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "wkv7_forward_bf16_y": (_I, [_I] * 6 + [_P] * 6 + [_P] * 4 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_forward_sequential": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P]),
     "wkv7_backward": (_I, [_I] * 6 + [_P] * 6 + [_P] * 5 + [_P] * 7 + [_P, ctypes.c_size_t] + [_P]),
     "wkv7_backward_workspace_size": (_I, [_I] * 5 + [ctypes.POINTER(ctypes.c_size_t)]),
@@ -143,7 +144,7 @@ def _check_f32(t, shape, name, where, dev):
 
 
 def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True, final_state: bool = True,
-            save_sa: bool = False, out=None, stream=None, kernel: str = "auto", workspace="auto"):
+            save_sa: bool = False, out=None, stream=None, kernel: str = "auto", workspace="auto", y_bf16: bool = False):
     """WKV7 forward.  r..b: (B, T, H, 64) float32/bfloat16 CUDA tensors; h0: (B, H, 64, 64) float32 or None.
 
     Returns (y, h_ckpt, hT): y (B,T,H,64) fp32; h_ckpt (B,H,C,64,64) fp32 (None when
@@ -153,7 +154,8 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
     (y, h_ckpt, hT, sa).  kernel="auto" is `wkv7_forward`; "sequential" is
     `wkv7_forward_sequential` (token by token).  workspace: "auto" (default) allocates the
     forward's scratch with torch when it uses one (chunk 32 without sa); a uint8 CUDA tensor of
-    at least forward_workspace_size() bytes is used as is; None runs without one.
+    at least forward_workspace_size() bytes is used as is; None runs without one.  y_bf16=True
+    returns y as bfloat16 (`wkv7_forward_bf16_y`: chunk 32, a workspace, no sa).
     """
     if kernel not in ("auto", "sequential"):
         raise ValueError(f"wkv7.forward: kernel must be 'auto' or 'sequential', got {kernel!r}")
@@ -166,12 +168,18 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
         y, ck, hT = out[:3]
         sa = out[3] if len(out) > 3 else None
     else:
-        y = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
+        y = torch.empty((B, T, H, D), dtype=torch.bfloat16 if y_bf16 else torch.float32, device=dev)
         ck = torch.empty((B, H, C, D, D), dtype=torch.float32, device=dev) if checkpoints else None
         hT = torch.empty((B, H, D, D), dtype=torch.float32, device=dev) if final_state else None
         sa = torch.empty((B, T, H, D), dtype=torch.float32, device=dev) if save_sa else None
     _check_f32(h0, (B, H, D, D), "h0", "wkv7.forward", dev)
-    _check_f32(y, (B, T, H, D), "y", "wkv7.forward", dev)
+    if y_bf16:
+        if kernel != "auto" or save_sa:
+            raise ValueError("wkv7.forward: y_bf16 is the chunk-operator forward (kernel 'auto', no sa)")
+        if y.dtype != torch.bfloat16 or tuple(y.shape) != (B, T, H, D) or not y.is_contiguous() or y.device != dev:
+            raise ValueError(f"wkv7.forward: y must be a contiguous bfloat16 {(B, T, H, D)} tensor on {dev}")
+    else:
+        _check_f32(y, (B, T, H, D), "y", "wkv7.forward", dev)
     _check_f32(ck, (B, H, C, D, D), "h_ckpt", "wkv7.forward", dev)
     _check_f32(hT, (B, H, D, D), "hT", "wkv7.forward", dev)
     _check_f32(sa, (B, T, H, D), "sa", "wkv7.forward", dev)
@@ -190,9 +198,17 @@ def forward(r, w, k, v, a, b, h0=None, chunk: int = 32, checkpoints: bool = True
             if workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
                 raise ValueError("wkv7.forward: workspace must be a contiguous uint8 tensor on the inputs' device")
             ws, ws_bytes = workspace, workspace.numel()
-        st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)),
-                              _ptr(ws), ws_bytes, _stream(stream))
-        _check(st, "wkv7_forward")
+        if y_bf16:
+            if ws is None:
+                ws_bytes = forward_workspace_size(B, T, H, D, chunk)
+                ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+            st = lib.wkv7_forward_bf16_y(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT)),
+                                         _ptr(ws), ws_bytes, _stream(stream))
+            _check(st, "wkv7_forward_bf16_y")
+        else:
+            st = lib.wkv7_forward(B, T, H, D, chunk, _in_dtype(r), *map(_ptr, (r, w, k, v, a, b, h0, y, ck, hT, sa)),
+                                  _ptr(ws), ws_bytes, _stream(stream))
+            _check(st, "wkv7_forward")
     if save_sa or (out is not None and len(out) > 3):
         return y, ck, hT, sa
     return y, ck, hT

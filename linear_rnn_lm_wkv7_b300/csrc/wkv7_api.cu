@@ -143,6 +143,31 @@ int wkv7_forward_sequential(int B, int T, int H, int D, int chunk, int in_dtype,
                       stream);
 }
 
+int wkv7_forward_bf16_y(int B, int T, int H, int D, int chunk, int in_dtype, const void* r, const void* w,
+                        const void* k, const void* v, const void* a, const void* b, const float* h0, void* y,
+                        float* h_ckpt, float* hT, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_sizes(B, T, H, D, chunk);
+  if (st) return st;
+  if ((st = check_dtype(in_dtype))) return st;
+  if (T > 0) {
+    if ((st = check_ptrs({r, w, k, v, a, b, y}, {h0, h_ckpt, hT}))) return st;
+  } else if ((st = check_ptrs({}, {h0, hT}))) {
+    return st;
+  }
+  if (chunk != 32) return WKV7_ERR_SHAPE;
+  if (workspace == nullptr) return WKV7_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return WKV7_ERR_ALIGN;
+  if (workspace_bytes < wkv7::forward_workspace_bytes(B, T, H, chunk)) return WKV7_ERR_WORKSPACE;
+  wkv7::FwdArgs p;
+  p.B = B; p.T = T; p.H = H; p.chunk = chunk; p.nchunks = wkv7_num_chunks(T, chunk);
+  p.bf16 = in_dtype == WKV7_BF16;
+  p.in = {r, w, k, v, a, b};
+  p.h0 = h0; p.y = static_cast<float*>(y); p.h_ckpt = h_ckpt; p.hT = hT; p.sa = nullptr; p.y_bf16 = true;
+  const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  if (T == 0) return record_cuda(wkv7::launch_forward(p, st_));  // hT = h0 (or zeros); y is empty
+  return record_cuda(wkv7::launch_xop_forward(p, workspace, 0, st_));
+}
+
 int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t* bytes) {
   int st = check_sizes(B, T, H, D, chunk);
   if (st) return st;

@@ -25,6 +25,7 @@ struct FwdArgs {
   float* h_ckpt;
   float* hT;
   float* sa;  // (B,T,H,D) fp32 sa_t per row, or null
+  bool y_bf16 = false;  // y holds bf16 values (the chunk-operator forward only)
 };
 
 struct BwdArgs {

@@ -756,10 +756,10 @@ struct Stage {
 template <int R, bool WALK>
 __global__ void __launch_bounds__((2 * R / 16 + 1) * 32)
 xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, size_t bstride,
-                 const float* __restrict__ s0, float* __restrict__ y, float* __restrict__ ck, size_t ck_stride,
-                 float* __restrict__ sT, unsigned* __restrict__ status) {
-  // forward: s0 = h0 (or null), y (Y_intra in, y out), ck = h_ckpt (or null; ck_stride = 4096 floats),
-  // sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X in accumulator order
+                 const float* __restrict__ s0, void* __restrict__ y, bool ybf, float* __restrict__ ck,
+                 size_t ck_stride, float* __restrict__ sT, unsigned* __restrict__ status) {
+  // forward: s0 = h0 (or null), y out (fp32, or bf16 rounded to nearest when ybf), ck = h_ckpt (or null;
+  // ck_stride = 4096 floats), sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X in accumulator order
   // (ck_stride = bstride / 4), sT = dh0.  bstride: bytes between operator blocks.
   using ST = Stage<R, WALK>;
   constexpr int NW = ST::kNW;
@@ -937,17 +937,24 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
         for (int nt = 0; nt < 2; ++nt) mma16816(ya[nt], fa.h, fq[nt].h[0], fq[nt].h[1]);
     }
     if (!WALK) {
-      float* yo = y + base + (size_t)(c * kL) * tstride;
+      const size_t yo = base + (size_t)(c * kL) * tstride;
+      auto put = [&](int t, int rr, float v) {
+        const size_t o = yo + (size_t)t * tstride + rr;
+        if (ybf)
+          static_cast<__nv_bfloat16*>(y)[o] = __float2bfloat16_rn(v);
+        else
+          static_cast<float*>(y)[o] = v;
+      };
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int tc = (2 * half + nt) * 8 + 2 * q;
         if (tc < nm) {
-          yo[(size_t)tc * tstride + row] = ya[nt][0];
-          yo[(size_t)tc * tstride + row + 8] = ya[nt][2];
+          put(tc, row, ya[nt][0]);
+          put(tc, row + 8, ya[nt][2]);
         }
         if (tc + 1 < nm) {
-          yo[(size_t)(tc + 1) * tstride + row] = ya[nt][1];
-          yo[(size_t)(tc + 1) * tstride + row + 8] = ya[nt][3];
+          put(tc + 1, row, ya[nt][1]);
+          put(tc + 1, row + 8, ya[nt][3]);
         }
       }
     }
@@ -982,15 +989,15 @@ cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* o
 }
 
 template <int R, bool WALK>
-cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0, float* y,
-                           float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0, void* y,
+                           bool ybf, float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
   using ST = Stage<R, WALK>;
   static_assert(ST::kSmem <= 232448, "shared memory per CTA");
   auto kern = xop_chain_kernel<R, WALK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ST::kSmem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)B * H * (64 / R);
-  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status);
+  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status);
   return cudaGetLastError();
 }
 
@@ -1008,11 +1015,12 @@ int chain_rows(int heads) {
 
 template <bool WALK>
 cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0,
-                         float* y, float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
+                         void* y, bool ybf, float* ck, size_t ck_stride, float* sT, unsigned* status,
+                         cudaStream_t stream) {
   switch (rows) {
-    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
-    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
-    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, bstride, s0, y, ck, ck_stride, sT, status, stream);
+    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
+    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
+    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
   }
 }
 
@@ -1101,8 +1109,8 @@ cudaError_t launch_xop_forward(const FwdArgs& p, void* workspace, int rows, cuda
                            : launch_prep_t<float, false>(&p, nullptr, ops, kXBytesFwd, status, stream);
   if (err != cudaSuccess) return err;
   if (rows == 0) rows = chain_rows(p.B * p.H);
-  return launch_chain<false>(rows, p.B, p.T, p.H, p.nchunks, ops, kXBytesFwd, p.h0, p.y, p.h_ckpt, (size_t)kD * kD,
-                             p.hT, status, stream);
+  return launch_chain<false>(rows, p.B, p.T, p.H, p.nchunks, ops, kXBytesFwd, p.h0, p.y, p.y_bf16, p.h_ckpt,
+                             (size_t)kD * kD, p.hT, status, stream);
 }
 
 cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward, int rows, ChunkEnds* ends,
@@ -1127,7 +1135,7 @@ cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward
     if (err != cudaSuccess) return err;
   }
   if (rows == 0) rows = chain_rows(p.B * p.H);
-  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr,
+  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr, false,
                             reinterpret_cast<float*>(ops + kXX), bstride / 4, p.dh0, status, stream);
 }
 

@@ -203,3 +203,34 @@ def test_backward_from_forward_needs_the_forward_workspace():
     assert bwd_ff(ws=None, ws_bytes=need) == 1
     assert bwd_ff(ws=P(0x100000), ws_bytes=need - 1) == 7
     assert bwd_ff(ws=P(0x100000 + 128), ws_bytes=need) == 3
+
+
+def fwd_b16(B=2, T=64, H=3, D=64, chunk=32, dt=0, ptrs=None, ws=P(0x100000), ws_bytes=None):
+    p = list(ALIGNED[:10]) if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = wkv7.forward_workspace_size(B, T, H, 64, 32) if D == 64 and B > 0 and H > 0 and T >= 0 else 0
+    return wkv7.lib.wkv7_forward_bf16_y(B, T, H, D, chunk, dt, *p, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=32), 2), (dict(chunk=16), 2), (dict(chunk=33), 2), (dict(B=0), 1), (dict(T=-1), 1), (dict(dt=2), 4),
+])
+def test_forward_bf16_y_rejects_bad_sizes(kw, status):
+    assert fwd_b16(**kw) == status
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4, 5, 7])
+def test_forward_bf16_y_requires_inputs_and_y(i):
+    # r..b (0-5) and y (7) are required; h0 (6), h_ckpt (8) and hT (9) may be NULL
+    p = list(ALIGNED[:10])
+    p[i] = None
+    assert fwd_b16(ptrs=p) == 1
+    p[i] = MISALIGNED
+    assert fwd_b16(ptrs=p) == 3
+
+
+def test_forward_bf16_y_needs_a_workspace():
+    need = wkv7.forward_workspace_size(2, 64, 3, 64, 32)
+    assert fwd_b16(ws=None, ws_bytes=need) == 1
+    assert fwd_b16(ws=P(0x100000), ws_bytes=need - 1) == 7
+    assert fwd_b16(ws=P(0x100000 + 128), ws_bytes=need) == 3

@@ -371,6 +371,39 @@ def test_backward_from_forward_equals_backward(wkv7, decay):
         wkv7.backward_from_forward(*ins, h0, ck, dy, dhT, workspace=ws[: ws.numel() - 256])
 
 
+TOL_Y_BF16 = 2.0 ** -8  # bf16 keeps 8 significant bits: one rounding is at most 2^-9 relative per element
+
+
+@pytest.mark.parametrize("name,shape", [("debug_b12_t1024_h6", None), ("ragged", (2, 33, 3)), ("m100_b4_t512_h12", None)])
+def test_forward_bf16_y(wkv7, name, shape):
+    """wkv7_forward_bf16_y: y is the fp32 forward's y rounded to bf16 (bit for bit), within the bf16 rounding of
+    the oracle (whole tensor and per row); checkpoints, hT and the operators left for the backward are the
+    fp32 forward's, so the backward on them gives the same gradients bit for bit."""
+    if shape is None:
+        wl = gen.WORKLOADS[name]
+        x, ref = workload_ref(name)
+    else:
+        B, T, H = shape
+        x = gen.random_small(31, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype="bf16")
+        ref = oracle_ref(x, 32)
+    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    h0 = dev32(x.get("h0"))
+    B, T, H, _ = ins[0].shape
+    ws1 = torch.empty(wkv7.forward_workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty_like(ws1)
+    y32, ck32, hT32 = wkv7.forward(*ins, h0, workspace=ws1)
+    y16, ck16, hT16 = wkv7.forward(*ins, h0, workspace=ws2, y_bf16=True)
+    assert y16.dtype == torch.bfloat16
+    assert torch.equal(y16, y32.to(torch.bfloat16))
+    assert torch.equal(ck16, ck32) and torch.equal(hT16, hT32)
+    assert_close("y_bf16", host(y16), ref["y"], TOL_Y_BF16, 1)
+    dy, dhT = dev32(x["dy"]), dev32(x.get("dhT"))
+    g1 = wkv7.backward_from_forward(*ins, h0, ck32, dy, dhT, workspace=ws1)
+    g2 = wkv7.backward_from_forward(*ins, h0, ck16, dy, dhT, workspace=ws2)
+    for p_, q_ in zip(g1, g2):
+        assert torch.equal(p_, q_)
+
+
 def test_explicit_workspace_and_too_small_workspace(wkv7):
     """A caller-owned workspace gives the same gradients as the automatic one; a smaller one is refused."""
     x = gen.random_small(9, B=2, T=70, H=3, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
