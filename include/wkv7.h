@@ -88,7 +88,7 @@ int wkv7_num_chunks(int T, int chunk);
  *           aligned, owned by the caller; or NULL / 0.  Used at chunk == 32 without sa
  *           (the chunk-operator forward): a parallel kernel forms every 32-token chunk's
  *           transition operator (S_end = S_start A_c + U_c, and the chunk's y from S_start)
- *           into it, 65536 bytes per (head, chunk) after a 256-byte header, with the
+ *           into it, 69632 bytes per (head, chunk) after a 256-byte header, with the
  *           chunk-internal part of y and the coupling matrices a later
  *           wkv7_backward_from_forward reuses; then one short chain per head applies them.  The
  *           header's first 4 bytes hold a status word: 0 after a call that completed
@@ -125,7 +125,7 @@ int wkv7_forward_bf16_y(int B, int T, int H, int D, int chunk, int in_dtype,
                         const float *h0, void *y, float *h_ckpt, float *hT,
                         void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 65536 per (head,
+/* Bytes of workspace wkv7_forward uses for these sizes (written to *bytes): 256 + 69632 per (head,
  * chunk) at chunk 32, 0 otherwise; returns a wkv7_status (the same size checks as wkv7_forward). */
 int wkv7_forward_workspace_size(int B, int T, int H, int D, int chunk, size_t *bytes);
 

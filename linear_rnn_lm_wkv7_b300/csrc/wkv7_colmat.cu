@@ -201,13 +201,9 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       cp_async16(gf + 4 * e, gend_ + 4 * e);
       cp_async16(sef + 4 * e, send_ + 4 * e);
     }
-    if (FM) {  // (matrix, hi / lo, row, 16-byte piece): rows of 64 bytes into rows of kLD32 elements
+    if (FM) {  // the four matrices in this kernel's operand layout (rows of kLD32 elements), as stored
       const unsigned char* msrc = mats + ((size_t)bh_ * nchunks + ci_) * xck_stride * 4;
-      for (int e = tid; e < 4 * 2 * 32 * 4; e += kNT) {
-        const int m = e >> 8, hl = (e >> 7) & 1, rr = (e >> 2) & 31, pc = e & 3;
-        cp_async16(sm + LY::oM + m * kRM32 + hl * (32 * kLD32 * 2) + rr * (kLD32 * 2) + pc * 16,
-                   msrc + m * 4096 + hl * 2048 + rr * 64 + pc * 16);
-      }
+      for (int e = tid; e < 4 * kRM32 / 16; e += kNT) cp_async16(sm + LY::oM + e * 16, msrc + e * 16);
     }
     cp_async_commit();
   };

@@ -55,14 +55,16 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up 
 // accumulator order [m-tile of 16 rows][n-tile of 8 columns][lane][4] (acc_order in wkv7_mma.cuh); the
 // walk overwrites it with G in the same order.  The forward's blocks add Y: Y_intra^T (rows i, columns t;
 // fp32) in the same order [i / 16][t / 8][lane][4], so that a chain CTA fetches its rows' part in one
-// copy; and M: M_ak, M_rb, M_rk and T (4 KB each: bf16 hi rows then lo rows, 32 x 32, unpadded) for a
+// copy; and M: M_ak, M_rb, M_rk and T (5 KB each: bf16 hi rows then lo rows, 32 x 32 in rows of 40
+// elements, the operand layout of shared memory, so that one bulk copy moves all four each way) for a
 // backward that reuses them.  A backward alone uses only A, Q and X.
 constexpr int kXA = 0;
 constexpr int kXQ = 16384;
 constexpr int kXX = 24576;
 constexpr int kXY = 40960;
 constexpr int kXM = 49152;
-constexpr int kXBytesFwd = 65536;  // block stride of the forward's workspace
+constexpr int kXMBytes = 20480;
+constexpr int kXBytesFwd = kXM + kXMBytes;  // block stride of the forward's workspace (68 KB)
 constexpr int kXBytesBwd = 40960;  // ... of a backward's own
 
 // index (floats) of element (i, t) of a 64 x 32 fp32 matrix in mma accumulator order
@@ -79,6 +81,19 @@ __host__ __device__ __forceinline__ int swz_q(int j, int t) {
 }
 
 __host__ __device__ constexpr int rmb(int rows, int ld) { return 2 * rows * ld * 2; }
+
+// shared -> global bulk copy (16-byte aligned addresses, size a multiple of 16), in the issuing thread's
+// bulk group; the generic-proxy writes it reads are made visible to the copy by fence_async_smem in every
+// writing thread before a barrier
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
+               "r"(static_cast<unsigned>(__cvta_generic_to_shared(ssrc))), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 // ======================================================================================= prep
 
@@ -469,7 +484,14 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
       rm_store_acc(Cm, mt, 2 * np + 1, lane, acc[1]);
     }
   }
+  if (!BWD) fence_async_smem();  // M_ak, M_rb, M_rk, T (written in earlier phases) for the bulk store below
   __syncthreads();
+  // (forward) M_ak, M_rb, M_rk and T, contiguous in shared memory, into the block for a backward that
+  // reuses them: one bulk copy, read by the end of this phase
+  static_assert(LY::oMrb == LY::oMak + rmb(32, kLD32) && LY::oMrk == LY::oMrb + rmb(32, kLD32) &&
+                    LY::oT == LY::oMrk + rmb(32, kLD32) && 4 * rmb(32, kLD32) == kXMBytes,
+                "the coupling matrices are one contiguous block");
+  if (!BWD && tid == 0) bulk_s2g(blk + kXM, sm + LY::oMak, kXMBytes);
 
   // A_c = diag(gamma_L) + A^^T B' and Q_c = R^^T + A^^T C^T (rows j); forward: K' = K~ diag(gamma_L) +
   // M_ak^T B' (over B~) and P = M_rk + C M_ak.  Warp w: the A_c tiles (m-tiles w >> 2 and (w >> 2) + 2,
@@ -581,16 +603,9 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
           rm_store_acc(Pm, mt, 2 * np + h, lane, acc[h]);
         }
       }
-      // M_ak, M_rb, M_rk and T into the block (rows of 64 bytes, hi then lo) for a backward that reuses them
-      unsigned char* gM = blk + kXM;
-      for (int e = tid; e < 4 * 2 * 32 * 4; e += kNTP) {  // (matrix, hi / lo, row, 16-byte piece)
-        const int m = e >> 8, hl = (e >> 7) & 1, rr = (e >> 2) & 31, pc = e & 3;
-        const int so = m == 0 ? LY::oMak : (m == 1 ? LY::oMrb : (m == 2 ? LY::oMrk : LY::oT));
-        *reinterpret_cast<uint4*>(gM + m * 4096 + hl * 2048 + rr * 64 + pc * 16) =
-            *reinterpret_cast<const uint4*>(sm + so + hl * (32 * kLD32 * 2) + rr * (kLD32 * 2) + pc * 16);
-      }
     }
   }
+  if (!BWD && tid == 0) bulk_wait_read_all();  // the bulk store has read the matrices
   __syncthreads();
   if (next < total) issue(next);  // the raw inputs and the coupling matrices are dead from here on
 
@@ -649,6 +664,7 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
     }
   }
   }  // chunks
+  if (!BWD && tid == 0) bulk_wait_all();  // the last bulk store has landed before the CTA exits
 }
 
 // ====================================================================================== chain

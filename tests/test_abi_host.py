@@ -124,13 +124,13 @@ def test_workspace_size_query():
     n = wkv7.backward_workspace_size(12, 1024, 6, 64, 32)
     # at chunk 32: the larger of the two-phase layout (dsa, then X at every chunk end) and the chunk-operator
     # layout (a 256-byte status header, then a 40960-byte operator block per (head, chunk)); the forward's
-    # blocks are 65536 bytes (they add y's chunk-internal part and the matrices a backward can reuse)
+    # blocks are 69632 bytes (they add y's chunk-internal part and the matrices a backward can reuse)
     dsa = 12 * 1024 * 6 * 64 * 4
     xck = 12 * 6 * 32 * 64 * 64 * 4
     ops = 256 + 12 * 6 * 32 * 40960
     assert n == max((dsa + 255) // 256 * 256 + xck, ops)
     assert wkv7.backward_workspace_size(2, 64, 3, 64, 16) == (2 * 64 * 3 * 64 * 4 + 255) // 256 * 256 + 2 * 3 * 4 * 64 * 64 * 4
-    assert wkv7.forward_workspace_size(12, 1024, 6, 64, 32) == 256 + 12 * 6 * 32 * 65536
+    assert wkv7.forward_workspace_size(12, 1024, 6, 64, 32) == 256 + 12 * 6 * 32 * 69632
     assert wkv7.forward_workspace_size(12, 1024, 6, 64, 16) == 0
     assert wkv7.backward_workspace_size(1, 0, 1, 64, 32) == 256
     with pytest.raises(wkv7.WKV7Error):
