@@ -522,91 +522,115 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   }
   __syncthreads();
 
-  // ---- P7: DR, DA, DK, DB, DV (rows t, columns j or i): 20 jobs of (product, m-tile, 4 n-tiles), each a
-  // K = 64 product with S0 / Xb plus the masked products.  Each job's dr, da, dk, db (scaled by Gamma,
-  // Gamma_-, 1 / Gamma) or dv is written as soon as it is formed, so that the stores drain during the
-  // warp's later jobs; the scaled values stay in registers for the dw terms.
-  constexpr int kRep = (20 + kNW - 1) / kNW;  // output jobs per warp
-  float res[kRep][4][4];
+  // ---- P7: DR, DA, DK, DB (rows t, columns j) at (m-tile, 4 n-tiles), in pairs that share their right
+  // operands -- warps 0-3: DR and DA (S0, then [K~; B~]), warps 4-7: DK and DB (Xb, then [A^; R^]) -- each a
+  // K = 64 product plus the masked products, the two accumulator sets pass-major; then DV (rows t, columns
+  // i) at (m-tile, 2 n-tiles), one per warp, so that every warp forms the same number of products.  Each
+  // gradient (dr, da, dk, db scaled by Gamma, Gamma_-, 1 / Gamma) is written as soon as formed, so that the
+  // stores drain during the warp's later products; the scaled values stay in registers for the dw terms.
+  static_assert(kNW == 8, "P7 job split assumes 8 warps");
+  float res[2][4][4];  // the pair's products 2 pg and 2 pg + 1 (0 dr, 1 da, 2 dk, 3 db)
+  const int pg = warp >> 2;
+  {
+    const int mt = (warp >> 1) & 1, nh = warp & 1;  // n-tiles 4nh .. 4nh + 3
 #pragma unroll
-  for (int rep = 0; rep < kRep; ++rep) {
-    const int job = warp + kNW * rep;
-    float (&acc)[4][4] = res[rep];
+    for (int rep = 0; rep < 2; ++rep)
 #pragma unroll
-    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-    if (job >= 20) continue;
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;  // n-tiles 4nh .. 4nh + 3
-    if (prod < 4) {
-      const RM& A1 = prod == 0 ? DY : (prod == 1 ? DSA : (prod == 2 ? Vm : SA));
-      const RM& B1 = prod < 2 ? S0 : Xb;
-      const bool exactA = kVExact && prod == 2;
+      for (int x = 0; x < 4; ++x) res[rep][x][0] = res[rep][x][1] = res[rep][x][2] = res[rep][x][3] = 0.f;
+    const RM& B1 = pg == 0 ? S0 : Xb;
+    const RM& A0 = pg == 0 ? DY : Vm;   // DR: DY S0, DK: V Xb
+    const RM& A1 = pg == 0 ? DSA : SA;  // DA: DSA S0, DB: SA Xb
+    const bool exact0 = kVExact && pg == 1;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = exactA ? rm_a_hi(A1, mt, kk, lane) : rm_a(A1, mt, kk, lane);
-        FragB fb[4];
-        rm_bt2(B1, 4 * nh, kk, lane, fb[0], fb[1]);
-        rm_bt2(B1, 4 * nh + 2, kk, lane, fb[2], fb[3]);
-        if (exactA)
-          mma2n<4>(acc, fa, fb);
-        else
-          mma3n<4>(acc, fa, fb);
-      }
-      // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
-      // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int blk = kq >> 1, kk = kq & 1;
-        const bool lowerA = prod < 2;
-        if (lowerA ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
-        const RM& LA = prod == 0 ? (blk ? L2 : L1) : prod == 1 ? (blk ? L4 : L3) : prod == 2 ? (blk ? L1 : L3) : (blk ? L2 : L4);
-        const RM& BB = lowerA ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
-        const FragA fa = lowerA ? rm_a(LA, mt, kk, lane) : rm_at(LA, mt, kk, lane);
-        FragB fb[4];
-        rm_bt2(BB, 4 * nh, kk, lane, fb[0], fb[1]);
-        rm_bt2(BB, 4 * nh + 2, kk, lane, fb[2], fb[3]);
-        mma3n<4>(acc, fa, fb);
-      }
-    } else {
-      // DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY (rows t, columns i)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const FragA fa = rm_a(Kt, mt, kk, lane);
-        FragB fb[4];
-        rm_b2(Xb, 4 * nh, kk, lane, fb[0], fb[1]);
-        rm_b2(Xb, 4 * nh + 2, kk, lane, fb[2], fb[3]);
-        mma3n<4>(acc, fa, fb);
-      }
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int blk = kq >> 1, kk = kq & 1;
-        if (mt == 1 && kk == 0) continue;  // M_ak^T, M_rk^T upper triangular
-        const FragA fa = rm_at(blk ? Mrk : Mak, mt, kk, lane);
-        FragB fb[4];
-        rm_bt2(blk ? DY : DSA, 4 * nh, kk, lane, fb[0], fb[1]);
-        rm_bt2(blk ? DY : DSA, 4 * nh + 2, kk, lane, fb[2], fb[3]);
-        mma3n<4>(acc, fa, fb);
+    for (int kk = 0; kk < 4; ++kk) {
+      FragB fb[4];
+      rm_bt2(B1, 4 * nh, kk, lane, fb[0], fb[1]);
+      rm_bt2(B1, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+      const FragA fa1 = rm_a(A1, mt, kk, lane);
+      if (exact0) {
+        const FragA fa0 = rm_a_hi(A0, mt, kk, lane);
+        mma2n<4>(res[0], fa0, fb);
+        mma3n<4>(res[1], fa1, fb);
+      } else {
+        const FragA fa0 = rm_a(A0, mt, kk, lane);
+        mma3n_two<4>(res[0], fa0, fb, res[1], fa1, fb);
       }
     }
-    float* outp = prod == 0 ? dr : (prod == 1 ? da : (prod == 2 ? dk : (prod == 3 ? db : dv)));
+    // masked part: K = 64 over (block, s); DR: [L1 | L2] [K~; B~], DA: [L3 | L4] [K~; B~],
+    // DK: [L3^T | L1^T] [A^; R^], DB: [L4^T | L2^T] [A^; R^]
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int j = (4 * nh + x) * 8 + 2 * q;
+    for (int kq = 0; kq < 4; ++kq) {
+      const int blk = kq >> 1, kk = kq & 1;
+      if (pg == 0 ? (mt == 0 && kk == 1) : (mt == 1 && kk == 0)) continue;  // zero tiles
+      const RM& BB = pg == 0 ? (blk ? Bt : Kt) : (blk ? Rh : Ah);
+      FragB fb[4];
+      rm_bt2(BB, 4 * nh, kk, lane, fb[0], fb[1]);
+      rm_bt2(BB, 4 * nh + 2, kk, lane, fb[2], fb[3]);
+      FragA fa0, fa1;
+      if (pg == 0) {
+        fa0 = rm_a(blk ? L2 : L1, mt, kk, lane);
+        fa1 = rm_a(blk ? L4 : L3, mt, kk, lane);
+      } else {
+        fa0 = rm_at(blk ? L1 : L3, mt, kk, lane);
+        fa1 = rm_at(blk ? L2 : L4, mt, kk, lane);
+      }
+      mma3n_two<4>(res[0], fa0, fb, res[1], fa1, fb);
+    }
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int prod = 2 * pg + rep;
+      float* outp = prod == 0 ? dr : (prod == 1 ? da : (prod == 2 ? dk : db));
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int j = (4 * nh + x) * 8 + 2 * q;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int t = mt * 16 + g + 8 * hr;
+          float2 sc = make_float2(1.f, 1.f);
+          if (prod == 0) {
+            sc = *reinterpret_cast<const float2*>(G + t * kD + j);
+          } else if (prod == 1) {
+            if (t > 0) sc = *reinterpret_cast<const float2*>(G + (t - 1) * kD + j);
+          } else {
+            const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+            sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
+          }
+          res[rep][x][2 * hr] *= sc.x;
+          res[rep][x][2 * hr + 1] *= sc.y;
+          if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
+            *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) =
+                make_float2(res[rep][x][2 * hr], res[rep][x][2 * hr + 1]);
+        }
+      }
+    }
+  }
+  {  // DV = K~ Xb^T + M_ak^T DSA + M_rk^T DY (rows t, columns i): m-tile w >> 2, n-tiles 2 (w & 3) + 0, 1
+    const int mt = warp >> 2, nq = warp & 3;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const FragA fa = rm_a(Kt, mt, kk, lane);
+      FragB fb[2];
+      rm_b2(Xb, 2 * nq, kk, lane, fb[0], fb[1]);
+      mma3n<2>(acc, fa, fb);
+    }
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {
+      const int blk = kq >> 1, kk = kq & 1;
+      if (mt == 1 && kk == 0) continue;  // M_ak^T, M_rk^T upper triangular
+      const FragA fa = rm_at(blk ? Mrk : Mak, mt, kk, lane);
+      FragB fb[2];
+      rm_bt2(blk ? DY : DSA, 2 * nq, kk, lane, fb[0], fb[1]);
+      mma3n<2>(acc, fa, fb);
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int i = (2 * nq + x) * 8 + 2 * q;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int t = mt * 16 + g + 8 * hr;
-        float2 sc = make_float2(1.f, 1.f);
-        if (prod == 0) {
-          sc = *reinterpret_cast<const float2*>(G + t * kD + j);
-        } else if (prod == 1) {
-          if (t > 0) sc = *reinterpret_cast<const float2*>(G + (t - 1) * kD + j);
-        } else if (prod < 4) {
-          const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
-          sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
-        }
-        acc[x][2 * hr] *= sc.x;
-        acc[x][2 * hr + 1] *= sc.y;
-        if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
-          *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) =
+        if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(i + 1, kD, dbg::kColmat))
+          *reinterpret_cast<float2*>(dv + base + (size_t)(t0 + t) * tstride + i) =
               make_float2(acc[x][2 * hr], acc[x][2 * hr + 1]);
       }
     }
@@ -617,10 +641,8 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   float* terms = reinterpret_cast<float*>(sm + LY::oStage);
   const Tin* in4 = reinterpret_cast<const Tin*>(sm + LY::oIn);
 #pragma unroll
-  for (int rep = 0; rep < kRep; ++rep) {
-    const int job = warp + kNW * rep;
-    if (job >= 16) continue;  // (jobs 16-19: dv)
-    const int prod = job >> 2, mt = (job >> 1) & 1, nh = job & 1;
+  for (int rep = 0; rep < 2; ++rep) {
+    const int prod = 2 * pg + rep, mt = (warp >> 1) & 1, nh = warp & 1;
     float* sp = terms + prod * kL * kD;
     const Tin* inp = in4 + prod * kL * kD;  // r, a, k, b
 #pragma unroll
