@@ -373,51 +373,34 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
   }
   __syncthreads();  // raw inputs and gamma consumed: the coupling matrices reuse their space
 
-  // M_ab = tril(A^ B~^T, -1) (fp32), M_rb = tril(R^ B~^T), and (forward) M_ak = tril(A^ K~^T, -1),
-  // M_rk = tril(R^ K~^T).  Warp w forms the same tile (m-tile (w >> 1) & 1, n-tiles 2 (w & 1) + 0, 1) of
-  // (M_ab, M_rb) (w < 4) or (M_ak, M_rk) (w >= 4, forward only), each pair sharing B~ or K~.
-  {
-    const int prodA = warp >> 2, mt = (warp >> 1) & 1, np = warp & 1;  // prodB = prodA + 2
-    if (!(BWD && prodA == 1)) {
-      float acc[2][2][4] = {};
-      if (!(mt == 0 && np == 1)) {  // rows 0-15 x columns 16-31: above the diagonal
-        const RM& Y = prodA ? Kt : Bt;
+  // M_ab = tril(A^ B~^T, -1) (fp32), the only coupling matrix T needs: warps 0-2, one of its three nonzero
+  // (m-tile, pair of n-tiles) each
+  if (warp < 3) {
+    const int mt = warp >= 1 ? 1 : 0, np = warp == 2 ? 1 : 0;  // (0, 0), (1, 0), (1, 1)
+    float acc[2][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const FragA fa0 = rm_a(Ah, mt, kk, lane), fa1 = rm_a(Rh, mt, kk, lane);
-          FragB fb[2];
-          rm_b2(Y, 2 * np, kk, lane, fb[0], fb[1]);
-          mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
-        }
-      }
+    for (int kk = 0; kk < 4; ++kk) {
+      const FragA fa = rm_a(Ah, mt, kk, lane);
+      FragB fb[2];
+      rm_b2(Bt, 2 * np, kk, lane, fb[0], fb[1]);
+      mma3n<2>(acc, fa, fb);
+    }
 #pragma unroll
-      for (int jb = 0; jb < 2; ++jb) {
-        const int prod = prodA + 2 * jb;
-        const bool strict = prod < 2;
+    for (int h = 0; h < 2; ++h) {
+      const int tr = mt * 16 + g, sc = (2 * np + h) * 8 + 2 * q;
+      float c[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int nj = 2 * np + h;
-          const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
-          float c[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tt = tr + ((e >> 1) << 3), s2 = sc + (e & 1);
-            c[e] = (strict ? s2 < tt : s2 <= tt) ? acc[jb][h][e] : 0.f;
-          }
-          if (prod == 0) {
-            *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
-            *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
-          } else {
-            rm_store_acc(prod == 1 ? Mak : (prod == 2 ? Mrb : Mrk), mt, nj, lane, c);
-          }
-        }
-      }
+      for (int e = 0; e < 4; ++e) c[e] = sc + (e & 1) < tr + ((e >> 1) << 3) ? acc[h][e] : 0.f;
+      *reinterpret_cast<float2*>(Mab + tr * SM + sc) = make_float2(c[0], c[1]);
+      *reinterpret_cast<float2*>(Mab + (tr + 8) * SM + sc) = make_float2(c[2], c[3]);
     }
   }
   __syncthreads();
 
-  // T = (I - M_ab)^-1 by blocks of 16: diagonal blocks by forward substitution (one column per lane),
-  // then T21 = T22 A21 T11 on tensor cores, all on warp 0
+  // T = (I - M_ab)^-1 by blocks of 16 on warp 0: diagonal blocks by forward substitution (one column per
+  // lane), then T21 = T22 A21 T11 on tensor cores.  Meanwhile warps 1-3 form (forward) M_ak = tril(A^ K~^T,
+  // -1) and M_rk = tril(R^ K~^T) at one nonzero tile each (sharing K~), warps 4-6 M_rb = tril(R^ B~^T), and
+  // warp 7 zeroes their blocks above the diagonal (rows 0-15, columns 16-31), which later products read.
   if (warp == 0) {
     const int off = lane < 16 ? 0 : 16;
     const int c = lane & 15;
@@ -433,6 +416,50 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
     for (int t = 0; t < 16; ++t) TI[(off + t) * SM + off + c] = x[t];
     __syncwarp();
     tri_inverse_t21(Mab, TI, SM, lane);
+  } else if (warp < 7) {
+    const bool kside = warp <= 3;  // (M_ak, M_rk) or M_rb
+    const int j = kside ? warp - 1 : warp - 4;
+    const int mt = j >= 1 ? 1 : 0, np = j == 2 ? 1 : 0;
+    if (!(BWD && kside)) {
+      float acc[2][2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        FragB fb[2];
+        rm_b2(kside ? Kt : Bt, 2 * np, kk, lane, fb[0], fb[1]);
+        const FragA fr = rm_a(Rh, mt, kk, lane);
+        if (kside) {
+          const FragA fa = rm_a(Ah, mt, kk, lane);
+          mma3n_two<2>(acc[0], fa, fb, acc[1], fr, fb);
+        } else {
+          mma3n<2>(acc[1], fr, fb);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nj = 2 * np + h;
+        const int tr = mt * 16 + g, sc = nj * 8 + 2 * q;
+        float c0[4], c1[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tt = tr + ((e >> 1) << 3), s2 = sc + (e & 1);
+          c0[e] = s2 < tt ? acc[0][h][e] : 0.f;   // M_ak: strictly below the diagonal
+          c1[e] = s2 <= tt ? acc[1][h][e] : 0.f;  // M_rk, M_rb: with the diagonal
+        }
+        if (kside) {
+          rm_store_acc(Mak, mt, nj, lane, c0);
+          rm_store_acc(Mrk, mt, nj, lane, c1);
+        } else {
+          rm_store_acc(Mrb, mt, nj, lane, c1);
+        }
+      }
+    }
+  } else {
+    for (int e = lane; e < 3 * 2 * 16 * 2; e += 32) {  // (matrix, hi / lo, row, 16-byte piece)
+      const int m = e >> 6, hl = (e >> 5) & 1, rr = (e >> 1) & 15, pc = e & 1;
+      const RM& X = m == 0 ? Mrb : (m == 1 ? Mak : Mrk);
+      if (BWD && m != 0) continue;
+      *reinterpret_cast<uint4*>(X.p + hl * X.lo + rm_off(X, rr, 16 + 8 * pc, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   __syncthreads();
   if (tid < 128) {
