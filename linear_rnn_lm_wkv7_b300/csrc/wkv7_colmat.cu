@@ -99,16 +99,21 @@ struct Lay {
   static constexpr int oS0f = (kMain + 127) / 128 * 128;
   static constexpr int oGf = oS0f + kD * kD * 4;
   static constexpr int oIn = oS0f;
+  // row stride (elements) of r, a, k, b there: padded for bf16 so that the rows of a warp's reads fall
+  // in distinct banks (fp32 rows fill the staging unpadded)
+  static constexpr int kIL = sizeof(Tin) == 2 ? kD + 8 : kD;
   static constexpr int oSef = oSA;
   static_assert(oSef + kD * kD * 4 <= oB, "S_e fits over SA and DSA");
-  static_assert(4 * kL * kD * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
+  static_assert(4 * kL * kIL * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
   static constexpr int kBytes = oGf + kD * kD * 4;
   // ---- (matrices from the forward) M_ak, M_rb, M_rk, T, loaded with S0, G and S_e
   static constexpr int oM = kBytes;
   static constexpr int kBytesM = oM + 4 * rm_bytes(32, kLD32);
-  // ---- r o dr, a o da, k o dk, b o db, fp32 [32][64] each, over A^ .. (after the last products)
+  // ---- r o dr, a o da, k o dk, b o db, fp32 [32][kTL] each, over A^ .. (after the last products); rows
+  // padded so that the eight rows of a warp's stores fall in distinct banks
+  static constexpr int kTL = kD + 8;
   static constexpr int oStage = oAh;
-  static_assert(oStage + 4 * kL * kD * 4 <= oV, "dw terms fit over A^ .. Xb");
+  static_assert(oStage + 4 * kL * kTL * 4 <= oV, "dw terms fit over A^ .. Xb");
 };
 
 // FM: M_ak, M_rb, M_rk and T come from the forward's operator blocks (`mats`, at the blocks' stride of
@@ -340,7 +345,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     for (int s4 = 0; s4 < 4; ++s4)
       for (int e = tid; e < n * CPR; e += kNT) {
         const int tt = e / CPR, pc = e % CPR;
-        cp_async16(in4 + (s4 * kL + tt) * kD + pc * EPC, srcs[s4] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
+        cp_async16(in4 + (s4 * kL + tt) * LY::kIL + pc * EPC, srcs[s4] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
       }
     cp_async_commit();
   }
@@ -643,8 +648,8 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
 #pragma unroll
   for (int rep = 0; rep < 2; ++rep) {
     const int prod = 2 * pg + rep, mt = (warp >> 1) & 1, nh = warp & 1;
-    float* sp = terms + prod * kL * kD;
-    const Tin* inp = in4 + prod * kL * kD;  // r, a, k, b
+    float* sp = terms + prod * kL * LY::kTL;
+    const Tin* inp = in4 + prod * kL * LY::kIL;  // r, a, k, b
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int j = (4 * nh + x) * 8 + 2 * q;
@@ -652,8 +657,14 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       for (int hr = 0; hr < 2; ++hr) {
         const int t = mt * 16 + g + 8 * hr;
         float2 in = make_float2(0.f, 0.f);
-        if (t < n) in = make_float2(to_f32(inp[t * kD + j]), to_f32(inp[t * kD + j + 1]));
-        *reinterpret_cast<float2*>(sp + t * kD + j) = make_float2(res[rep][x][2 * hr] * in.x, res[rep][x][2 * hr + 1] * in.y);
+        if (t < n) {
+          if constexpr (sizeof(Tin) == 2)
+            in = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(inp + t * LY::kIL + j));
+          else
+            in = *reinterpret_cast<const float2*>(inp + t * LY::kIL + j);
+        }
+        *reinterpret_cast<float2*>(sp + t * LY::kTL + j) =
+            make_float2(res[rep][x][2 * hr] * in.x, res[rep][x][2 * hr + 1] * in.y);
       }
     }
   }
@@ -666,10 +677,11 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   //   Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1} = Z_t + D_t,
   // so Z_t = Z_{n-1} + sum_{s = t+1}^{n-1} D_s, a suffix sum: 4 blocks of 8 tokens per column.
   {
+    constexpr int TL = LY::kTL;
     const float* sRDR = terms;
-    const float* sADA = terms + kL * kD;
-    const float* sKDK = terms + 2 * kL * kD;
-    const float* sBDB = terms + 3 * kL * kD;
+    const float* sADA = terms + kL * TL;
+    const float* sKDK = terms + 2 * kL * TL;
+    const float* sBDB = terms + 3 * kL * TL;
     const int j = tid & 63, blk = tid >> 6;  // threads 0-255
     const bool act = tid < 256;
     float dsum[8];  // sum of D_s over this block's tokens s > t
@@ -679,7 +691,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       for (int u = 7; u >= 0; --u) {
         const int t = 8 * blk + u;
         dsum[u] = tot;
-        if (t >= 1 && t < n) tot += sADA[t * kD + j] + sRDR[(t - 1) * kD + j] - sKDK[t * kD + j] - sBDB[t * kD + j];
+        if (t >= 1 && t < n) tot += sADA[t * TL + j] + sRDR[(t - 1) * TL + j] - sKDK[t * TL + j] - sBDB[t * TL + j];
       }
       if (WKV7_IN(blk, 4, dbg::kColmat)) BT[blk * 64 + j] = tot;
     }
@@ -687,12 +699,12 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     if (act) {
     float later = 0.f;
     for (int q2 = blk + 1; q2 < 4; ++q2) later += BT[q2 * 64 + j];
-    const float zn = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * kD + j];
+    const float zn = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * TL + j];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int t = 8 * blk + u;
       if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat)) {
-        const float wdw = zn + later + dsum[u] - sKDK[t * kD + j] - sBDB[t * kD + j];
+        const float wdw = zn + later + dsum[u] - sKDK[t * TL + j] - sBDB[t * TL + j];
         dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
       }
     }
