@@ -59,7 +59,7 @@ template <typename Tin>
 struct Lay {
   // ---- long-lived
   static constexpr int oG = 0;                                  // float [32][64] gamma
-  static constexpr int oZP = oG + 32 * 64 * 4;                  // float [4][64] colsum partials
+  static constexpr int oZP = oG + 32 * 64 * 4;                  // float [64] colsum(G o S_e) (room for 256)
   static constexpr int oBT = oZP + 4 * 64 * 4;                  // float [4][64] block totals of the scans
   static constexpr int oMeta = oBT + 4 * 64 * 4;                // int [8]
   static constexpr int oWc = oMeta + 256;                       // float [32][64] w (1 past n)
@@ -103,7 +103,8 @@ struct Lay {
   // in distinct banks (fp32 rows fill the staging unpadded)
   static constexpr int kIL = sizeof(Tin) == 2 ? kD + 8 : kD;
   static constexpr int oSef = oSA;
-  static_assert(oSef + kD * kD * 4 <= oB, "S_e fits over SA and DSA");
+  static constexpr int kSL = kD + 8;  // S_e row stride (floats): padded so a warp's rows fall in distinct banks
+  static_assert(oSef + kD * kSL * 4 <= oB, "S_e fits over SA and DSA");
   static_assert(4 * kL * kIL * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
   static constexpr int kBytes = oGf + kD * kD * 4;
   // ---- (matrices from the forward) M_ak, M_rb, M_rk, T, loaded with S0, G and S_e
@@ -204,7 +205,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     for (int e = tid; e < kD * kD / 4; e += kNT) {
       if (s0_ != nullptr) cp_async16(s0f + 4 * e, s0_ + 4 * e);
       cp_async16(gf + 4 * e, gend_ + 4 * e);
-      cp_async16(sef + 4 * e, send_ + 4 * e);
+      cp_async16(sef + (e >> 4) * LY::kSL + 4 * (e & 15), send_ + 4 * e);
     }
     if (FM) {  // the four matrices in this kernel's operand layout (rows of kLD32 elements), as stored
       const unsigned char* msrc = mats + ((size_t)bh_ * nchunks + ci_) * xck_stride * 4;
@@ -312,27 +313,44 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   }
   cp_async_wait<0>();  // S0, G, S_e
   __syncthreads();
-  if (tid < 256) {  // colsum(G o S_e) partials: 4 row blocks of 16 per column
-    const float* gf = reinterpret_cast<const float*>(sm + LY::oGf);
-    const float* sef = reinterpret_cast<const float*>(sm + LY::oSef);
-    const int j = tid & 63, part = tid >> 6;
-    float z = 0.f;
-#pragma unroll
-    for (int i = part * 16; i < part * 16 + 16; ++i) z = fmaf(gf[acc_order(i, j)], sef[i * kD + j], z);
-    if (WKV7_IN(part, 4, dbg::kColmat)) ZP[part * 64 + j] = z;
-  }
-  // S0 and Xb = G diag(gamma_{n-1}) (rows i, columns j)
+  // Xb = G diag(gamma_{n-1}) and colsum(G o S_e): warp w takes G's accumulator tiles (m-tile 0-3, n-tile w) in
+  // their stored order, one float4 per lane -- (i, j), (i, j + 1), (i + 8, j), (i + 8, j + 1) -- and sums its
+  // column pair over the rows by shuffles
+  static_assert(kNW == 8, "one n-tile of G per warp");
   {
+    const float4* gf4 = reinterpret_cast<const float4*>(sm + LY::oGf);
+    const float* sef = reinterpret_cast<const float*>(sm + LY::oSef);
+    const int j = warp * 8 + 2 * q;
+    const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int i = mt * 16 + g;
+      const float4 x = gf4[(mt * 8 + warp) * 32 + lane];
+      rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
+      rm_store(Xb, i + 8, j, x.z * gl.x, x.w * gl.y);
+      const float2 e0 = *reinterpret_cast<const float2*>(sef + i * LY::kSL + j);
+      const float2 e8 = *reinterpret_cast<const float2*>(sef + (i + 8) * LY::kSL + j);
+      z0 = fmaf(x.x, e0.x, fmaf(x.z, e8.x, z0));
+      z1 = fmaf(x.y, e0.y, fmaf(x.w, e8.y, z1));
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      z0 += __shfl_xor_sync(0xffffffffu, z0, o);
+      z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+    }
+    if (g == 0 && WKV7_IN(j + 1, kD, dbg::kColmat)) {
+      ZP[j] = z0;
+      ZP[j + 1] = z1;
+    }
+  }
+  {  // S0 (rows i, columns j)
     const float* s0f = reinterpret_cast<const float*>(sm + LY::oS0f);
-    const float* gf = reinterpret_cast<const float*>(sm + LY::oGf);
 #pragma unroll 4
     for (int e = tid; e < kD * (kD / 2); e += kNT) {
       const int i = e >> 5, j = 2 * (e & 31);
       const float2 s = s0 != nullptr ? *reinterpret_cast<const float2*>(s0f + i * kD + j) : make_float2(0.f, 0.f);
       rm_store(S0, i, j, s.x, s.y);
-      const float2 x = *reinterpret_cast<const float2*>(gf + acc_order(i, j));  // (i, j), (i, j + 1)
-      const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
-      rm_store(Xb, i, j, x.x * gl.x, x.y * gl.y);
     }
   }
   __syncthreads();
@@ -699,7 +717,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     if (act) {
     float later = 0.f;
     for (int q2 = blk + 1; q2 < 4; ++q2) later += BT[q2 * 64 + j];
-    const float zn = ZP[j] + ZP[64 + j] + ZP[128 + j] + ZP[192 + j] + sRDR[(n - 1) * TL + j];
+    const float zn = ZP[j] + sRDR[(n - 1) * TL + j];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int t = 8 * blk + u;
