@@ -58,9 +58,11 @@ __host__ __device__ constexpr int rm_bytes(int rows, int ld) { return 2 * rows *
 template <typename Tin>
 struct Lay {
   // ---- long-lived
-  static constexpr int oG = 0;                                  // float [32][64] gamma
-  static constexpr int oZP = oG + 32 * 64 * 4;                  // float [64] colsum(G o S_e) (room for 256)
-  static constexpr int oBT = oZP + 4 * 64 * 4;                  // float [4][64] block totals of the scans
+  static constexpr int kGL = 64 + 8;                            // gamma row stride (floats): padded so that a
+                                                                // warp's reads of eight rows hit distinct banks
+  static constexpr int oG = 0;                                  // float [32][kGL] gamma
+  static constexpr int oZP = oG + 32 * kGL * 4;                 // float [64] colsum(G o S_e)
+  static constexpr int oBT = oZP + 64 * 4;                      // float [4][64] block totals of the scans
   static constexpr int oMeta = oBT + 4 * 64 * 4;                // int [8]
   static constexpr int oWc = oMeta + 256;                       // float [32][64] w (1 past n)
   static constexpr int oAh = oWc + 32 * 64 * 4;
@@ -254,7 +256,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       float pre = 1.f;
       for (int q2 = 0; q2 < blk; ++q2) pre *= BT[q2 * 64 + j];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) G[(8 * blk + u) * kD + j] = pre * loc[u];
+      for (int u = 0; u < 8; ++u) G[(8 * blk + u) * LY::kGL + j] = pre * loc[u];
       if (blk == 3) {
         const float gm = pre * p;
         bad |= !(gm >= kMinGamma) || !(gm <= 3.0e38f);
@@ -280,9 +282,9 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     const int t = tid >> 3, c0 = (tid & 7) * 8;
     const bool ok = t < n;
     float gt[8], gp[8], av[8], rv8[8], kv[8], bv[8], vv[8], dv8[8];
-    raw8(G + t * kD + c0, gt);
+    raw8(G + t * LY::kGL + c0, gt);
     if (t > 0) {
-      raw8(G + (t - 1) * kD + c0, gp);
+      raw8(G + (t - 1) * LY::kGL + c0, gp);
     } else {
 #pragma unroll
       for (int u = 0; u < 8; ++u) gp[u] = 1.f;
@@ -321,7 +323,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     const float4* gf4 = reinterpret_cast<const float4*>(sm + LY::oGf);
     const float* sef = reinterpret_cast<const float*>(sm + LY::oSef);
     const int j = warp * 8 + 2 * q;
-    const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * kD + j);
+    const float2 gl = *reinterpret_cast<const float2*>(G + (n - 1) * LY::kGL + j);
     float z0 = 0.f, z1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
@@ -611,11 +613,11 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
           const int t = mt * 16 + g + 8 * hr;
           float2 sc = make_float2(1.f, 1.f);
           if (prod == 0) {
-            sc = *reinterpret_cast<const float2*>(G + t * kD + j);
+            sc = *reinterpret_cast<const float2*>(G + t * LY::kGL + j);
           } else if (prod == 1) {
-            if (t > 0) sc = *reinterpret_cast<const float2*>(G + (t - 1) * kD + j);
+            if (t > 0) sc = *reinterpret_cast<const float2*>(G + (t - 1) * LY::kGL + j);
           } else {
-            const float2 gt = *reinterpret_cast<const float2*>(G + t * kD + j);
+            const float2 gt = *reinterpret_cast<const float2*>(G + t * LY::kGL + j);
             sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
           }
           res[rep][x][2 * hr] *= sc.x;
