@@ -96,18 +96,13 @@ struct Lay {
   static constexpr int oL = oU;                                 // L1..L4 (32 x 32 each)
   static_assert(oL + 4 * rm_bytes(32, kLD32) <= oTI, "L1..L4 fit over U, W and M_ab");
   static constexpr int kMain = (kRawEnd > kPhaseEnd ? kRawEnd : kPhaseEnd);
-  // ---- fp32 S0 and G [64][64] staged by cp.async (through P1b); then r, a, k, b [32][64] (Tin) for the
-  // output stage.  S_e [64][64] fp32 is staged over SA and DSA (first written in P5).
+  // ---- fp32 S0 and G [64][64] staged by cp.async (through P1b).  S_e [64][kSL] fp32 is staged over SA and
+  // DSA (first written in P5).
   static constexpr int oS0f = (kMain + 127) / 128 * 128;
   static constexpr int oGf = oS0f + kD * kD * 4;
-  static constexpr int oIn = oS0f;
-  // row stride (elements) of r, a, k, b there: padded for bf16 so that the rows of a warp's reads fall
-  // in distinct banks (fp32 rows fill the staging unpadded)
-  static constexpr int kIL = sizeof(Tin) == 2 ? kD + 8 : kD;
   static constexpr int oSef = oSA;
   static constexpr int kSL = kD + 8;  // S_e row stride (floats): padded so a warp's rows fall in distinct banks
   static_assert(oSef + kD * kSL * 4 <= oB, "S_e fits over SA and DSA");
-  static_assert(4 * kL * kIL * (int)sizeof(Tin) <= 2 * kD * kD * 4, "r, a, k, b fit over the S0 and G staging");
   static constexpr int kBytes = oGf + kD * kD * 4;
   // ---- (matrices from the forward) M_ak, M_rb, M_rk, T, loaded with S0, G and S_e
   static constexpr int oM = kBytes;
@@ -356,19 +351,6 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     }
   }
   __syncthreads();
-  {  // r, a, k, b again (for the dw recurrence at the end) over the dead S0 / G staging
-    constexpr int CPR = kD * (int)sizeof(Tin) / 16;
-    constexpr int EPC = 16 / (int)sizeof(Tin);
-    Tin* in4 = reinterpret_cast<Tin*>(sm + LY::oIn);
-    const Tin* srcs[4] = {r, a, k, b};
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4)
-      for (int e = tid; e < n * CPR; e += kNT) {
-        const int tt = e / CPR, pc = e % CPR;
-        cp_async16(in4 + (s4 * kL + tt) * LY::kIL + pc * EPC, srcs[s4] + base + (size_t)(t0 + tt) * tstride + pc * EPC);
-      }
-    cp_async_commit();
-  }
 
   if constexpr (!FM) {  // (from the forward: loaded instead)
   // ---- P2: M_ab = tril(A^ B~^T, -1) (fp32), M_ak = tril(A^ K~^T, -1), M_rb = tril(R^ B~^T),
@@ -551,8 +533,10 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   // operands -- warps 0-3: DR and DA (S0, then [K~; B~]), warps 4-7: DK and DB (Xb, then [A^; R^]) -- each a
   // K = 64 product plus the masked products, the two accumulator sets pass-major; then DV (rows t, columns
   // i) at (m-tile, 2 n-tiles), one per warp, so that every warp forms the same number of products.  Each
-  // gradient (dr, da, dk, db scaled by Gamma, Gamma_-, 1 / Gamma) is written as soon as formed, so that the
-  // stores drain during the warp's later products; the scaled values stay in registers for the dw terms.
+  // gradient (dr, da, dk, db: the products scaled by Gamma, Gamma_-, 1 / Gamma) is written as soon as
+  // formed, so that the stores drain during the warp's later products.  The dw terms r o dr, a o da, k o dk,
+  // b o db are the unscaled products times R^, A^, K~, B~ (the same scalings), formed here and kept in
+  // registers.
   static_assert(kNW == 8, "P7 job split assumes 8 warps");
   float res[2][4][4];  // the pair's products 2 pg and 2 pg + 1 (0 dr, 1 da, 2 dk, 3 db)
   const int pg = warp >> 2;
@@ -620,11 +604,12 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
             const float2 gt = *reinterpret_cast<const float2*>(G + t * LY::kGL + j);
             sc = make_float2(__fdividef(1.f, gt.x), __fdividef(1.f, gt.y));
           }
-          res[rep][x][2 * hr] *= sc.x;
-          res[rep][x][2 * hr + 1] *= sc.y;
+          const float2 sop = rm_get2(prod == 0 ? Rh : (prod == 1 ? Ah : (prod == 2 ? Kt : Bt)), t, j);
+          const float u0 = res[rep][x][2 * hr], u1 = res[rep][x][2 * hr + 1];
+          res[rep][x][2 * hr] = u0 * sop.x;  // the dw term (zero past the chunk: the operand rows are)
+          res[rep][x][2 * hr + 1] = u1 * sop.y;
           if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat) && WKV7_IN(j + 1, kD, dbg::kColmat))
-            *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) =
-                make_float2(res[rep][x][2 * hr], res[rep][x][2 * hr + 1]);
+            *reinterpret_cast<float2*>(outp + base + (size_t)(t0 + t) * tstride + j) = make_float2(u0 * sc.x, u1 * sc.y);
         }
       }
     }
@@ -664,27 +649,17 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   __syncthreads();  // every operand has been read: stage over A^ .. Xb
   // ---- r o dr, a o da, k o dk, b o db into shared memory (over A^ ..) for dw
   float* terms = reinterpret_cast<float*>(sm + LY::oStage);
-  const Tin* in4 = reinterpret_cast<const Tin*>(sm + LY::oIn);
 #pragma unroll
   for (int rep = 0; rep < 2; ++rep) {
     const int prod = 2 * pg + rep, mt = (warp >> 1) & 1, nh = warp & 1;
     float* sp = terms + prod * kL * LY::kTL;
-    const Tin* inp = in4 + prod * kL * LY::kIL;  // r, a, k, b
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int j = (4 * nh + x) * 8 + 2 * q;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int t = mt * 16 + g + 8 * hr;
-        float2 in = make_float2(0.f, 0.f);
-        if (t < n) {
-          if constexpr (sizeof(Tin) == 2)
-            in = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(inp + t * LY::kIL + j));
-          else
-            in = *reinterpret_cast<const float2*>(inp + t * LY::kIL + j);
-        }
-        *reinterpret_cast<float2*>(sp + t * LY::kTL + j) =
-            make_float2(res[rep][x][2 * hr] * in.x, res[rep][x][2 * hr + 1] * in.y);
+        *reinterpret_cast<float2*>(sp + t * LY::kTL + j) = make_float2(res[rep][x][2 * hr], res[rep][x][2 * hr + 1]);
       }
     }
   }
