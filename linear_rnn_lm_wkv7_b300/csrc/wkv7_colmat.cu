@@ -26,9 +26,9 @@
 // from Z_t = colsum(X_t o S_t): Z_{n-1} = colsum(G o S_e) + r_{n-1} o dr_{n-1}, w_t o dw_t = Z_t - k_t o dk_t - b_t o db_t,
 // Z_{t-1} = w_t o dw_t + a_t o da_t + r_{t-1} o dr_{t-1}.  No state is divided by w.
 //
-// A chunk whose gamma_31 falls below 1e-20 in some column (or is not finite), or that has some w_t
-// below 1/32 (where dividing w_t o dw_t by w_t would cost digits), takes the exact token-by-token
-// column passes instead (sa, dsa and dv by their own recurrences, then wkv7_colpass.cuh).
+// A chunk whose gamma_31 falls below 1e-20 in some column (or above 1e37, or is not finite), or that
+// has some w_t below 1/32 (where dividing w_t o dw_t by w_t would cost digits), takes the exact
+// token-by-token column passes instead (sa, dsa and dv by their own recurrences, then wkv7_colpass.cuh).
 //
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation; operands are stored once, row-major, split into bf16 hi and lo, and read with
@@ -51,6 +51,7 @@ constexpr int kNW = kNT / 32;
 constexpr int kLD64 = 72;  // row stride (bf16 elements) of 64-wide operands
 constexpr int kLD32 = 40;  // of 32-wide operands
 constexpr float kMinGamma = 1e-20f;
+constexpr float kMaxGamma = 1e37f;  // (1 / gamma by __fdividef, exact to a few ulp below 2^126)
 constexpr float kWMin = 0.03125f;
 
 __host__ __device__ constexpr int rm_bytes(int rows, int ld) { return 2 * rows * ld * 2; }  // hi + lo
@@ -116,7 +117,7 @@ struct Lay {
 
 // FM: M_ak, M_rb, M_rk and T come from the forward's operator blocks (`mats`, at the blocks' stride of
 // xck_stride floats) instead of being formed here (no M_ab, no inverse).  The forward formed them in
-// closed form for every chunk whose gamma_31 passes the same test as here (>= 1e-20 and finite), a
+// closed form for every chunk whose gamma_31 passes the same test as here (in [1e-20, 1e37]), a
 // superset of the chunks this kernel takes in matrix form.
 template <typename Tin, bool FM>
 __global__ void __launch_bounds__(kNT, 1)
@@ -254,7 +255,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       for (int u = 0; u < 8; ++u) G[(8 * blk + u) * LY::kGL + j] = pre * loc[u];
       if (blk == 3) {
         const float gm = pre * p;
-        bad |= !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+        bad |= !(gm >= kMinGamma) || !(gm <= kMaxGamma);
       }
     }
     const unsigned any = __ballot_sync(0xffffffffu, bad);
@@ -293,7 +294,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     float oa[8], orr[8], ok8[8], ob[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const float ig = __frcp_rn(gt[u]);
+      const float ig = __fdividef(1.f, gt[u]);  // (the forward's operator kernel forms K~, B~ the same way)
       oa[u] = ok ? av[u] * gp[u] : 0.f;
       orr[u] = ok ? rv8[u] * gt[u] : 0.f;
       ok8[u] = ok ? kv[u] * ig : 0.f;

@@ -19,9 +19,9 @@
 //     K' = K~ diag(gamma_L) + M_ak^T B',  P = M_rk + C M_ak,
 //     A_c = diag(gamma_L) + A^^T B',  U_c = V^T K',  Q_c = (R^ + C A^)^T,  Y_intra = P V.
 // (Unrolled over the chunk, sa is coupled through the unit lower-triangular system I - M_ab; T
-// eliminates it.)  A chunk whose gamma_L falls below 1e-20 in some column, or is not finite, forms the
-// same operators token by token instead (rows of A_c and U_c run the recurrence from I and 0), which
-// divides by nothing.
+// eliminates it.)  A chunk whose gamma_L falls below 1e-20 in some column, or above 1e37 (only decays
+// w > 1 reach that) or is not finite, forms the same operators token by token instead (rows of A_c and
+// U_c run the recurrence from I and 0), which divides by nothing.
 //
 // xop_prep_kernel: all chunks at once, two CTAs per SM each looping over chunks (the next chunk's inputs
 // loaded during the current one's last products); writes A_c, Q_c (bf16 hi + lo), and U_c (forward;
@@ -47,6 +47,7 @@ constexpr int kL = 32;
 constexpr int kLD64 = 72;
 constexpr int kLD32 = 40;
 constexpr float kMinGamma = 1e-20f;
+constexpr float kMaxGamma = 1e37f;  // (1 / gamma by __fdividef, exact to a few ulp below 2^126)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
 
 // ---- per-chunk operator block (bytes).  A_c and Q_c: bf16 hi array then lo array, rows unpadded, the
@@ -241,7 +242,7 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
     if (blk == 3) {
       const float gm = pre * p;
       GL[j] = gm;
-      bad = !(gm >= kMinGamma) || !(gm <= 3.0e38f);
+      bad = !(gm >= kMinGamma) || !(gm <= kMaxGamma);
     }
     const unsigned any = __ballot_sync(0xffffffffu, bad);
     if (lane == 0) meta[warp] = any != 0u;
