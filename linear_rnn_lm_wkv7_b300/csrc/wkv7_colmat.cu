@@ -400,8 +400,56 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
   // ---- P3 || P4: warp 0 solves the diagonal blocks of T = (I - M_ab)^-1 (forward substitution, one column
   // per lane: lanes 0-15 T11, lanes 16-31 T22); the other warps form U = A^ S0^T + M_ak V and
   // W = B~ Xb^T + M_rb^T DY (rows t, columns i): 16 jobs of (product, m-tile, 4 n-tiles)
-  // (from the forward: T is loaded, and all eight warps form U and W)
-  if (!FM && warp == 0) {
+  // (from the forward: T is loaded, and all eight warps form U and W, each warp both m-tiles of one pair of
+  // n-tiles so that the two share their right operands: warps 0-3 U, 4-7 W)
+  if constexpr (FM) {
+    const int pg = warp >> 2, nq = warp & 3;  // n-tiles 2nq, 2nq + 1
+    float acc[2][2][4] = {};                 // [m-tile][n-tile]
+    const RM& A1 = pg == 0 ? Ah : Bt;
+    const RM& B1 = pg == 0 ? S0 : Xb;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      FragB fb[2];
+      rm_b2(B1, 2 * nq, kk, lane, fb[0], fb[1]);
+      const FragA fa0 = rm_a(A1, 0, kk, lane), fa1 = rm_a(A1, 1, kk, lane);
+      mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
+    }
+    // U: M_ak V (V is B[k = u][n = i] = V[u][i]); W: M_rb^T DY.  Blocks above the diagonal are zero:
+    // M_ak rows 0-15 at columns 16-31 (m-tile 0, k-tile 1), M_rb^T rows 16-31 at 0-15 (m-tile 1, k-tile 0)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const bool on0 = pg == 0 ? kk == 0 : true, on1 = pg == 0 ? true : kk == 1;
+      FragB fb[2];
+      FragA fa0, fa1;
+      if (pg == 0) {
+        rm_bt2(Vm, 2 * nq, kk, lane, fb[0], fb[1], !kVExact);
+        fa0 = rm_a(Mak, 0, kk, lane);
+        fa1 = rm_a(Mak, 1, kk, lane);
+      } else {
+        rm_bt2(DY, 2 * nq, kk, lane, fb[0], fb[1]);
+        fa0 = rm_at(Mrb, 0, kk, lane);
+        fa1 = rm_at(Mrb, 1, kk, lane);
+      }
+      if (pg == 0 && kVExact) {
+        if (on0) {
+          mma2b(acc[0][0], fa0, fb[0]);
+          mma2b(acc[0][1], fa0, fb[1]);
+        }
+        mma2b(acc[1][0], fa1, fb[0]);
+        mma2b(acc[1][1], fa1, fb[1]);
+      } else if (on0 && on1) {
+        mma3n_two<2>(acc[0], fa0, fb, acc[1], fa1, fb);
+      } else if (on0) {
+        mma3n<2>(acc[0], fa0, fb);
+      } else {
+        mma3n<2>(acc[1], fa1, fb);
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) rm_store_acc(pg == 0 ? U : W, mt, 2 * nq + h, lane, acc[mt][h]);
+  } else if (warp == 0) {
     const int off = lane < 16 ? 0 : 16;
     const int c = lane & 15;
     float x[16];
@@ -417,7 +465,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
     __syncwarp();
     tri_inverse_t21(Mab, TI, SM, lane);  // T21 = T22 A21 T11 (A21 = M_ab[16..31][0..15])
   } else {
-    for (int job = FM ? warp : warp - 1; job < 16; job += FM ? kNW : kNW - 1) {
+    for (int job = warp - 1; job < 16; job += kNW - 1) {
       const int prod = job >> 3, mt = (job >> 2) & 1, nq = job & 3;  // n-tiles 2nq, 2nq + 1
       float acc[2][4] = {};
 #pragma unroll
@@ -701,7 +749,7 @@ colmat_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r, c
       const int t = 8 * blk + u;
       if (t < n && WKV7_IN(t0 + t, T, dbg::kColmat)) {
         const float wdw = zn + later + dsum[u] - sKDK[t * TL + j] - sBDB[t * TL + j];
-        dw[base + (size_t)(t0 + t) * tstride + j] = wdw / Wc[t * kD + j];
+        dw[base + (size_t)(t0 + t) * tstride + j] = __fdividef(wdw, Wc[t * kD + j]);  // (w >= 1/32 here)
       }
     }
     }
