@@ -771,7 +771,8 @@ __device__ __forceinline__ void ld_q_fwd(const __nv_bfloat16* sQ, int nt, int kk
   b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
 }
 
-constexpr int kNS = 3;  // stages in flight
+constexpr int kMaxStages = 5;     // stages in flight: as many as fit one CTA's shared memory, 3 to 5
+constexpr int kSmemCap = 232448;  // shared memory per CTA (bytes)
 
 // One chain CTA holds R state rows of a head: R / 16 row blocks of 16 rows, each split by columns between
 // two warps (column half 0: columns 0-31, half 1: 32-63) so that a CTA keeps every SM sub-partition's
@@ -790,11 +791,16 @@ struct Stage {
   static constexpr int oY = oX + kX;                             // forward: this CTA's rows of Y_intra^T
   static constexpr int kY = WALK ? 0 : kRB * 2048;
   static constexpr int kBytes = oY + kY;
-  static constexpr int oFlag = 64;                               // int [2][kNW] after the mbarriers
-  static constexpr int oXch = 128 + kNS * kBytes;                // uint4 [2][kNW][4][32]
-  static constexpr int kSmem = oXch + 2 * kNW * 4 * 32 * 16;
+  static constexpr int kHead = 256;                              // full[kNS], empty[kNS] mbarriers, flags
+  static constexpr int oFlag = 128;                              // int [2][kNW] after the mbarriers
+  static constexpr int kXch = 2 * kNW * 4 * 32 * 16;             // uint4 [2][kNW][4][32]
+  static constexpr int kFit = (kSmemCap - kHead - kXch) / kBytes;
+  static constexpr int kNS = kFit > kMaxStages ? kMaxStages : kFit;
+  static constexpr int oXch = kHead + kNS * kBytes;
+  static constexpr int kSmem = oXch + kXch;
   static_assert(kBytes % 128 == 0, "stage alignment");
-  static_assert(2 * kNS * 8 <= oFlag && oFlag + 2 * kNW * 4 <= 128, "barriers and flags fit the header");
+  static_assert(kNS >= 3, "at least three stages");
+  static_assert(2 * kNS * 8 <= oFlag && oFlag + 2 * kNW * 4 <= kHead, "barriers and flags fit the header");
 };
 
 template <int R, bool WALK>
@@ -811,10 +817,11 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
   extern __shared__ float4 smem4[];
   unsigned char* smc = reinterpret_cast<unsigned char*>(smem4);
   uint64_t* full = reinterpret_cast<uint64_t*>(smc);
-  uint64_t* empty = full + kNS;
+  uint64_t* empty = full + ST::kNS;
   int* okf = reinterpret_cast<int*>(smc + ST::oFlag);
   uint4* xch = reinterpret_cast<uint4*>(smc + ST::oXch);
-  auto stage = [&](int s) { return smc + 128 + s * ST::kBytes; };
+  constexpr int kNS = ST::kNS;
+  auto stage = [&](int s) { return smc + ST::kHead + s * ST::kBytes; };
   const int bh = blockIdx.x / NB, rb = blockIdx.x - (blockIdx.x / NB) * NB;
   const int bi = bh / H, hi = bh - bi * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
