@@ -75,15 +75,16 @@ cudaError_t launch_gwalk_chunked(const BwdArgs& a, float* dsa_ws, float* xck_ws,
 cudaError_t launch_forward_transition(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_gwalk_transition(const BwdArgs& a, float* xck_ws, cudaStream_t stream);
 // the chunk operators (wkv7_xop.cu): a workspace of xop_workspace_bytes() bytes, 256-byte aligned (a status
-// word, then one operator block per (head, chunk): 64 KB in the forward's, 40 KB in a backward's own).  The forward: operators, then the chain writing y,
-// h_ckpt and hT.  The walk: operators, then the chain writing G (the gradient w.r.t. the state after each
-// chunk from every later token) over the blocks (returned as g_ends with a stride of g_stride floats per
-// chunk) and dh0.  rows = state rows per chain CTA (16, 32 or 64; 0 picks by the head count).
+// word, then one operator block per (head, chunk): 68 KB in the forward's, 40 KB in a backward's own).
+// The forward: operators, then the chain writing y, h_ckpt and hT.  The walk: operators (or, on the
+// forward's workspace, E_c beside them), then the chain writing G (the gradient w.r.t. the state after
+// each chunk from every later token) over the blocks (returned in ChunkEnds) and dh0.  rows = state rows
+// per chain CTA (16, 32 or 64; 0 picks by the head count).
 size_t xop_workspace_bytes(int B, int T, int H, bool forward);
 cudaError_t launch_xop_forward(const FwdArgs& a, void* workspace, int rows, cudaStream_t stream);
 // what the walk leaves per chunk c of head bh (at (bh * C + c) * stride floats from each pointer): G, one
 // int of scratch for the column kernels, and (a walk on the forward's workspace; else null) the forward's
-// M_ak, M_rb, M_rk and T (bf16 hi rows then lo rows, 4 KB each)
+// M_ak, M_rb, M_rk and T (bf16 hi rows then lo rows of 40 elements, 5 KB each)
 struct ChunkEnds {
   const float* g;
   int* flags;

@@ -24,12 +24,13 @@
 // U_c run the recurrence from I and 0), which divides by nothing.
 //
 // xop_prep_kernel: all chunks at once, two CTAs per SM each looping over chunks (the next chunk's inputs
-// loaded during the current one's last products); writes A_c, Q_c (bf16 hi + lo), and U_c (forward;
-// Y_intra into y) or E_c (backward), per chunk, into an operator block.
+// loaded during the current one's last products); writes A_c, Q_c (bf16 hi + lo), and U_c, Y_intra^T and
+// the coupling matrices (forward) or E_c (backward), per chunk, into an operator block.
+// xop_e_kernel: E_c from the Q_c a forward left in its blocks (the backward on the forward's operators).
 // xop_chain_kernel: one CTA per (head, block of R state rows); a producer warp streams the chunks'
 // operator blocks into a ring of shared-memory stages with cp.async.bulk (one mbarrier per stage and
-// direction); R / 16 chain warps hold 16 state rows each as mma accumulators and apply
-//     forward: y_c += S Q_c;  S = S A_c + U_c  (checkpoint after every chunk)
+// direction); 2 R / 16 chain warps hold 16 state rows by 32 columns each as mma accumulators and apply
+//     forward: y_c = S Q_c + Y_intra;  S = S A_c + U_c  (checkpoint after every chunk)
 //     walk:    G_c written;   G = G A_c^T + E_c (G_c over E_c's block, accumulator order; dh0 at the end).
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation (wkv7_mma.cuh).  Waits are bounded in time: past the limit a kernel sets the status
@@ -639,7 +640,7 @@ xop_prep_kernel(int T, int H, int nchunks, int total, const Tin* __restrict__ r,
 
   // U_c = V^T K' (forward) or E_c = DY^T Q_c^T (backward), rows i in mma accumulator order: warp w forms
   // m-tiles w >> 2 and (w >> 2) + 2 at n-tiles 2 (w & 3) + 0, 1 (sharing K' or Q_c); the forward then forms
-  // Y_intra = P V at m-tile w >> 2, n-tiles 2 (w & 3) + 0, 1 into y
+  // Y_intra^T = V^T P^T into the block
   {
     const int mt0 = warp >> 2, p = warp & 3;
     float acc[2][2][4] = {};
