@@ -374,8 +374,9 @@ def test_backward_from_forward_equals_backward(wkv7, decay):
 TOL_Y_BF16 = 2.0 ** -8  # bf16 keeps 8 significant bits: one rounding is at most 2^-9 relative per element
 
 
-@pytest.mark.parametrize("name,shape", [("debug_b12_t1024_h6", None), ("ragged", (2, 33, 3)), ("m100_b4_t512_h12", None)])
-def test_forward_bf16_y(wkv7, name, shape):
+@pytest.mark.parametrize("name,shape,dtype", [("debug_b12_t1024_h6", None, "bf16"), ("ragged", (2, 33, 3), "bf16"),
+                                              ("ragged_f32", (2, 33, 3), "f32"), ("m100_b4_t512_h12", None, "bf16")])
+def test_forward_bf16_y(wkv7, name, shape, dtype):
     """wkv7_forward_bf16_y: y is the fp32 forward's y rounded to bf16 (bit for bit), within the bf16 rounding of
     the oracle (whole tensor and per row); checkpoints, hT and the operators left for the backward are the
     fp32 forward's, so the backward on them gives the same gradients bit for bit."""
@@ -384,9 +385,9 @@ def test_forward_bf16_y(wkv7, name, shape):
         x, ref = workload_ref(name)
     else:
         B, T, H = shape
-        x = gen.random_small(31, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype="bf16")
+        x = gen.random_small(31, B=B, T=T, H=H, D=64, h0_std=0.2, dhT_std=1.0, dtype=dtype)
         ref = oracle_ref(x, 32)
-    ins = [dev(x[n], "bf16") for n in "rwkvab"]
+    ins = [dev(x[n], dtype) for n in "rwkvab"]
     h0 = dev32(x.get("h0"))
     B, T, H, _ = ins[0].shape
     ws1 = torch.empty(wkv7.forward_workspace_size(B, T, H), dtype=torch.uint8, device="cuda")
@@ -470,6 +471,8 @@ def test_zero_tokens(wkv7):
     ws = torch.empty(wkv7.forward_workspace_size(B, 0, H), dtype=torch.uint8, device="cuda")
     grads = wkv7.backward_from_forward(e, e, e, e, e, e, h0, ck, e, dhT, workspace=ws)
     assert torch.equal(grads[6], dhT)
+    y16, ck16, hT16 = wkv7.forward(e, e, e, e, e, e, h0, y_bf16=True)
+    assert y16.dtype == torch.bfloat16 and y16.numel() == 0 and torch.equal(hT16, h0)
 
 
 # ---------------------------------------------------------------------------------- decode
