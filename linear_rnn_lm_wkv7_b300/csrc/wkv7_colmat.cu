@@ -32,7 +32,8 @@
 //
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation; operands are stored once, row-major, split into bf16 hi and lo, and read with
-// ldmatrix (.trans for the transposed uses).  Mapping: one CTA of 16 warps per (head, chunk).
+// ldmatrix (.trans for the transposed uses).  Mapping: one CTA of 8 warps per SM (its shared memory),
+// looping over the (head, chunk) jobs; the next chunk's loads are in flight during the current one's dw.
 #include <type_traits>
 
 #include "wkv7_colpass.cuh"
