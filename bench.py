@@ -433,10 +433,13 @@ def run_decode(args, rank, world, local_rank):
 PATHS = {
     # forward call, backward call and the kernels each launches (counted per step for gpu_launches)
     "operators": {"forward": "wkv7_forward with a workspace, no sa: chunk-operator prep + chain",
-                  "backward": "wkv7_backward_from_forward on the forward's workspace: E_c kernel + walk + matrix "
-                              "column kernel + token-by-token companion (exits at once without flagged chunks)",
+                  "backward": "wkv7_backward_from_forward on the forward's workspace: E_c kernel + walk (with "
+                              "whole-head chain CTAs, past 74 heads on 148 SMs: the walk forming E_c itself, no E_c "
+                              "kernel) + matrix column kernel + token-by-token companion (exits at once without "
+                              "flagged chunks)",
                   "backward_call": "wkv7_backward_from_forward",
-                  "launches": 2 + 4},
+                  # two 32-row chain CTAs per head while 2 x heads fit the SMs, else whole heads
+                  "launches": lambda heads, sms: 2 + (4 if 2 * heads <= sms else 3)},
     "operators-reform": {"forward": "wkv7_forward with a workspace, no sa: chunk-operator prep + chain",
                          "backward": "wkv7_backward with a workspace, no sa: operator prep + walk + matrix column "
                                      "kernel + token-by-token companion",
@@ -771,7 +774,7 @@ def run_ours(args, rank, world, local_rank):
                                   "roofline_ms": roof_d * 1e3, "frac": roof_d / step_s},
         "calls_ms": {"wkv7_forward": f_ms, bwd_call: b_ms, "timing": calls_timing},
         "clocks": clocks,
-        "gpu_launches": pth["launches"] * args.steps,
+        "gpu_launches": launches_per_step(pth, wl, sms) * args.steps,
         "e2e": e2e,
     }
     if world == 1 and not args.no_other_configs:
@@ -779,6 +782,12 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def launches_per_step(pth: dict, wl, sms: int) -> int:
+    """This library's kernel launches in one step of a path at a workload."""
+    n = pth["launches"]
+    return n(wl.B * wl.H, sms) if callable(n) else n
 
 
 def fp32_peak_tflops(peaks: dict, sms: int) -> float:

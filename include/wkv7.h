@@ -201,14 +201,16 @@ int wkv7_backward_workspace_size(int B, int T, int H, int D, int chunk, size_t *
  *           the workspace of the wkv7_forward call (chunk 32, no sa, with a workspace) that wrote
  *           h_ckpt from these same r..b and h0, untouched since; at least
  *           wkv7_forward_workspace_size() bytes, 256-byte aligned.  Required (WKV7_ERR_ARG if NULL).
- *           It is this call's only scratch and is consumed: E_c, then G, replace the forward's U_c,
- *           and flags replace Q_c, so a second backward needs the forward run again.  A workspace that
+ *           It is this call's only scratch and is consumed: E_c and G replace the forward's U_c and
+ *           flags replace Q_c, so a second backward needs the forward run again.  A workspace that
  *           holds anything else gives meaningless gradients (nothing on the device can tell).
  *   Every other argument, layout and result as wkv7_backward with a workspace and no sa; chunk must
- *   be 32 (WKV7_ERR_SHAPE otherwise).  The first kernel only forms E_c (one product per chunk) where
- *   wkv7_backward forms A_c, Q_c and E_c; the walk is the same kernel, and the column gradients skip
- *   forming the coupling matrices.  The walk sees the same A_c and E_c as wkv7_backward's on chunks in
- *   closed form (bit for bit); the matrices the forward formed differ from the column kernel's own in
+ *   be 32 (WKV7_ERR_SHAPE otherwise).  The walk reads A_c and Q_c from the forward's blocks and only
+ *   E_c = DY^T Q_c^T is formed (by a first kernel, or, past 74 heads on 148 SMs, inside the walk itself)
+ *   where wkv7_backward's first kernel forms A_c, Q_c and E_c; the column gradients skip forming the
+ *   coupling matrices.  The walk sees the same
+ *   A_c and E_c as wkv7_backward's on chunks in closed form (bit for bit); the matrices the forward
+ *   formed differ from the column kernel's own in
  *   rounding only, so the gradients agree with wkv7_backward's to ~1e-6 relative.  The workspace
  *   header's status word is as in wkv7_forward.
  * Source: Backward listing of "Metal kernel architecture" (see top of file).

@@ -76,10 +76,11 @@ cudaError_t launch_forward_transition(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_gwalk_transition(const BwdArgs& a, float* xck_ws, cudaStream_t stream);
 // the chunk operators (wkv7_xop.cu): a workspace of xop_workspace_bytes() bytes, 256-byte aligned (a status
 // word, then one operator block per (head, chunk): 68 KB in the forward's, 40 KB in a backward's own).
-// The forward: operators, then the chain writing y, h_ckpt and hT.  The walk: operators (or, on the
-// forward's workspace, E_c beside them), then the chain writing G (the gradient w.r.t. the state after
-// each chunk from every later token) over the blocks (returned in ChunkEnds) and dh0.  rows = state rows
-// per chain CTA (16, 32 or 64; 0 picks by the head count).
+// The forward: operators, then the chain writing y, h_ckpt and hT.  The walk: operators (on the forward's
+// workspace only E_c, by its own kernel, or, with whole-head chain CTAs, inside the chain from Q_c and dy),
+// then the chain writing G (the gradient w.r.t. the state after each chunk from every later token) over
+// the blocks (returned in ChunkEnds) and dh0.  rows = state rows per chain CTA (16, 32 or 64; 0 picks by
+// the head count).
 size_t xop_workspace_bytes(int B, int T, int H, bool forward);
 cudaError_t launch_xop_forward(const FwdArgs& a, void* workspace, int rows, cudaStream_t stream);
 // what the walk leaves per chunk c of head bh (at (bh * C + c) * stride floats from each pointer): G, one
@@ -97,8 +98,8 @@ cudaError_t launch_xop_walk(const BwdArgs& a, void* workspace, bool from_forward
 // the column gradients dr, dw, dk, dv, da, db of every 32-token chunk in matrix form, from G at the chunk
 // ends, the checkpoints and the inputs (no saved sa); chunks with tiny decays token by token
 cudaError_t launch_colgrad_matrix(const BwdArgs& a, const ChunkEnds& ends, cudaStream_t stream);
-// the backward without a saved sa at chunk 32: operators (or, from_forward, E_c beside the forward's
-// operators), walk, matrix column gradients
+// the backward without a saved sa at chunk 32: operators (or, from_forward, only E_c), walk, matrix column
+// gradients
 cudaError_t launch_backward_transition(const BwdArgs& a, void* workspace, bool from_forward, cudaStream_t stream);
 // bytes of the forward's workspace (the transition operands)
 size_t forward_workspace_bytes(int B, int T, int H, int chunk);

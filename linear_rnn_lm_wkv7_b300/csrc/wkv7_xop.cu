@@ -24,14 +24,17 @@
 // U_c run the recurrence from I and 0), which divides by nothing.
 //
 // xop_prep_kernel: all chunks at once, two CTAs per SM each looping over chunks (the next chunk's inputs
-// loaded during the current one's last products); writes A_c, Q_c (bf16 hi + lo), and U_c, Y_intra^T and
-// the coupling matrices (forward) or E_c (backward), per chunk, into an operator block.
-// xop_e_kernel: E_c from the Q_c a forward left in its blocks (the backward on the forward's operators).
+// loaded during the current one's last products); writes A_c (bf16 hi + lo) and, forward, Q_c (bf16 hi +
+// lo), U_c, Y_intra^T and the coupling matrices, or, backward, E_c, per chunk, into an operator block.
 // xop_chain_kernel: one CTA per (head, block of R state rows); a producer warp streams the chunks'
 // operator blocks into a ring of shared-memory stages with cp.async.bulk (one mbarrier per stage and
 // direction); 2 R / 16 chain warps hold 16 state rows by 32 columns each as mma accumulators and apply
 //     forward: y_c = S Q_c + Y_intra;  S = S A_c + U_c  (checkpoint after every chunk)
 //     walk:    G_c written;   G = G A_c^T + E_c (G_c over E_c's block, accumulator order; dh0 at the end).
+// xop_e_kernel: E_c from the Q_c a forward left in its blocks (the backward on the forward's operators).
+// The walk on a forward's blocks with whole-head CTAs instead copies the chunk's dy rows beside A_c and Q_c,
+// and the chain warps form E_c = DY^T Q_c^T at their own rows and columns, one chunk ahead (G_c then goes
+// over U_c's block).
 // Precision: products of fp32 operands as three bf16 products (hi hi + hi lo + lo hi, ~2^-17 each),
 // fp32 accumulation (wkv7_mma.cuh).  Waits are bounded in time: past the limit a kernel sets the status
 // word and returns.
@@ -740,7 +743,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-
 // B fragments (n-tiles nt, nt + 1; k-tile kk) of A_c for S A_c: B[k = j][n = j'] = A_c[j][j']
 __device__ __forceinline__ void ld_a_fwd(const __nv_bfloat16* sA, int nt, int kk, int lane, FragB& b0, FragB& b1) {
   const int j = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -772,6 +774,20 @@ __device__ __forceinline__ void ld_q_fwd(const __nv_bfloat16* sQ, int nt, int kk
   b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
 }
 
+// B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = Q_c[n][k] (rows j, tokens t) from an
+// operator block's Q_c copied as is (hi then lo, pieces permuted as swz_q)
+__device__ __forceinline__ void q_b2(const __nv_bfloat16* sq, int nt, int kk, int lane, FragB& b0, FragB& b1) {
+  const int j = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
+  const int t = kk * 16 + ((lane >> 3) & 1) * 8;
+  const int off = swz_q(j, t);
+  uint32_t h[4], l[4];
+  ldsm4<false>(h, sq + off);
+  ldsm4<false>(l, sq + 2048 + off);
+  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
+  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
+}
+
+
 constexpr int kMaxStages = 5;     // stages in flight: as many as fit one CTA's shared memory, 3 to 5
 constexpr int kSmemCap = 232448;  // shared memory per CTA (bytes)
 
@@ -781,14 +797,24 @@ constexpr int kSmemCap = 232448;  // shared memory per CTA (bytes)
 // operand: each warp forms the fragments of its own half from its accumulators and trades them with its
 // partner once per chunk through shared memory (double-buffered by chunk parity, one named barrier per
 // pair and chunk).
-template <int R, bool WALK>
+// EQ (the walk on the forward's operator blocks, which hold Q_c but no E_c): a stage holds A_c, Q_c and
+// this CTA's rows of the chunk's dy (fp32, one row of R values per token, rows padded to R + 4 floats so
+// that a warp's fragment loads fall in distinct banks), and each chain warp forms its own part of
+// E_c = DY^T Q_c^T, one chunk ahead.  A_c and Q_c come in one bulk copy, dy in 16-byte cp.async pieces
+// spread over the producer's lanes (small rows: one bulk copy per row would queue 32 short copies per
+// stage); the stage's barrier expects lane 0's arrival with the bulk bytes plus one arrival per lane, made
+// once the lane's pieces have landed (cp.async.wait_group, one stage behind the copies being issued) so that
+// the arrival's release ordering covers them.
+template <int R, bool WALK, bool EQ>
 struct Stage {
+  static_assert(WALK || !EQ, "E_c from Q_c in the walk only");
   static constexpr int kRB = R / 16;                             // row blocks
   static constexpr int kNW = 2 * kRB;                            // chain warps
-  static constexpr int oA = 0;                                   // A_c (16 KB), then Q_c (forward, 8 KB)
-  static constexpr int kAQ = WALK ? 16384 : 24576;
-  static constexpr int oX = kAQ;                                 // this CTA's rows of U_c / E_c
-  static constexpr int kX = kRB * 4096;
+  static constexpr int oA = 0;                                   // A_c (16 KB), then Q_c (forward, EQ: 8 KB)
+  static constexpr int kAQ = (WALK && !EQ) ? 16384 : 24576;
+  static constexpr int oX = kAQ;                                 // this CTA's rows of U_c / E_c, or of dy (EQ)
+  static constexpr int kDyLd = R + 4;                            // EQ: dy row stride (floats)
+  static constexpr int kX = EQ ? kL * kDyLd * 4 : kRB * 4096;
   static constexpr int oY = oX + kX;                             // forward: this CTA's rows of Y_intra^T
   static constexpr int kY = WALK ? 0 : kRB * 2048;
   static constexpr int kBytes = oY + kY;
@@ -804,15 +830,15 @@ struct Stage {
   static_assert(2 * kNS * 8 <= oFlag && oFlag + 2 * kNW * 4 <= kHead, "barriers and flags fit the header");
 };
 
-template <int R, bool WALK>
+template <int R, bool WALK, bool EQ>
 __global__ void __launch_bounds__((2 * R / 16 + 1) * 32)
 xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ ops, size_t bstride,
                  const float* __restrict__ s0, void* __restrict__ y, bool ybf, float* __restrict__ ck,
-                 size_t ck_stride, float* __restrict__ sT, unsigned* __restrict__ status) {
+                 size_t ck_stride, float* __restrict__ sT, const float* __restrict__ dy, unsigned* __restrict__ status) {
   // forward: s0 = h0 (or null), y out (fp32, or bf16 rounded to nearest when ybf), ck = h_ckpt (or null;
   // ck_stride = 4096 floats), sT = hT.  walk: s0 = dhT (or null), y unused, ck = G over each block's X in accumulator order
-  // (ck_stride = bstride / 4), sT = dh0.  bstride: bytes between operator blocks.
-  using ST = Stage<R, WALK>;
+  // (ck_stride = bstride / 4), sT = dh0; dy (EQ only): (B, T, H, 64) fp32.  bstride: bytes between operator blocks.
+  using ST = Stage<R, WALK, EQ>;
   constexpr int NW = ST::kNW;
   constexpr int NB = 64 / R;
   extern __shared__ float4 smem4[];
@@ -832,7 +858,7 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], EQ ? 33 : 1);
       mbar_init(&empty[s], NW);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -854,7 +880,27 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
       const int nm = min(kL, T - c * kL);
       unsigned char* st = stage(s);
       const unsigned char* src = hops + (size_t)c * bstride;
-      if (lane == 0) {
+      if (EQ) {
+        // A_c and Q_c in one bulk copy; the chunk's dy rows (this CTA's R values of each token) in 16-byte
+        // pieces over the lanes, one cp.async group per chunk.  Rows past the chunk are not copied.  Then the
+        // previous chunk's pieces of this lane have landed: its arrival releases them.
+        if (lane == 0) {
+          mbar_expect_tx(&full[s], ST::kAQ);
+          bulk_g2s(st + ST::oA, src + kXA, ST::kAQ, &full[s]);
+        }
+        constexpr int kPPR = R / 4;  // 16-byte pieces per row
+        for (int e = lane; e < nm * kPPR; e += 32) {
+          const int t = e / kPPR, pc = e - t * kPPR;
+          if (WKV7_IN(c * kL + t, T, dbg::kXopChain))
+            cp_async16(st + ST::oX + (t * ST::kDyLd + pc * 4) * 4,
+                       dy + base + (size_t)(c * kL + t) * tstride + rb * R + pc * 4);
+        }
+        cp_async_commit();
+        if (n > 0) {
+          cp_async_wait<1>();
+          mbar_arrive(&full[(n - 1) % kNS]);
+        }
+      } else if (lane == 0) {
         mbar_expect_tx(&full[s], ST::kAQ + ST::kX + ST::kY);
         bulk_g2s(st + ST::oA, src + kXA, ST::kAQ, &full[s]);
         bulk_g2s(st + ST::oX, src + kXX + rb * ST::kX, ST::kX, &full[s]);
@@ -862,6 +908,10 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
       }
       __syncwarp();
       issued = n + 1;
+    }
+    if (EQ && issued > 0) {  // the last issued chunk's pieces
+      cp_async_wait<0>();
+      mbar_arrive(&full[(issued - 1) % kNS]);
     }
     if (!ok) {
       if (lane == 0) atomicOr(status, 1u);
@@ -898,6 +948,38 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
       *reinterpret_cast<float2*>(dst + (size_t)(row + 8) * kD + col) = make_float2(S[nj][2], S[nj][3]);
     }
   };
+  // EQ: E_c at this warp's rows and columns for the m-th chunk taken, into en: DY^T (rows i, tokens t; split
+  // into bf16 hi + lo, zero past the chunk) times Q_c^T, the passes in the same order as the backward's
+  // operator kernel forms E_c.  Formed one chunk ahead (chunk 0's before the loop), after the current
+  // chunk's products, so that it stays off the chain's dependent path.
+  float en[4][4];
+  auto form_e = [&](int m) {
+    const int cm = nchunks - 1 - m;
+    const int nmm = min(kL, T - cm * kL);
+    const unsigned char* stm = stage(m % kNS);
+    const float* sdy = reinterpret_cast<const float*>(stm + ST::oX);
+    const __nv_bfloat16* sqm = reinterpret_cast<const __nv_bfloat16*>(stm + kXQ);
+    auto dyv = [&](int t, int i) { return t < nmm ? sdy[t * ST::kDyLd + i] : 0.f; };
+#pragma unroll
+    for (int nj = 0; nj < 4; ++nj) en[nj][0] = en[nj][1] = en[nj][2] = en[nj][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int t = kk * 16 + 2 * q;
+      FragA fa;
+      split2(dyv(t, lrow), dyv(t + 1, lrow), fa.h[0], fa.l[0]);
+      split2(dyv(t, lrow + 8), dyv(t + 1, lrow + 8), fa.h[1], fa.l[1]);
+      split2(dyv(t + 8, lrow), dyv(t + 9, lrow), fa.h[2], fa.l[2]);
+      split2(dyv(t + 8, lrow + 8), dyv(t + 9, lrow + 8), fa.h[3], fa.l[3]);
+      FragB fb[4];
+      q_b2(sqm, 4 * half, kk, lane, fb[0], fb[1]);
+      q_b2(sqm, 4 * half + 2, kk, lane, fb[2], fb[3]);
+      mma3n<4>(en, fa, fb);
+    }
+  };
+  if (EQ && nchunks > 0) {
+    (void)mbar_wait(&full[0], 0);  // (a wait that gives up is met again, and acted on, in the loop)
+    form_e(0);
+  }
 
   for (int n = 0; n < nchunks; ++n) {
     const int c = WALK ? nchunks - 1 - n : n;
@@ -931,7 +1013,8 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     }
     const unsigned char* st = stage(s);
     const __nv_bfloat16* sA = reinterpret_cast<const __nv_bfloat16*>(st + ST::oA);
-    // the walk's G before this chunk, over its E block (already read into the stage), in accumulator order
+    // the walk's G before this chunk, in accumulator order, over the block's X (E_c, already read into the
+    // stage; or, EQ, the forward's U_c)
     if (WALK && ck != nullptr) {
       float4* dst = reinterpret_cast<float4*>(ck + ((size_t)bh * nchunks + c) * ck_stride) +
                     ((rb * ST::kRB + pair) * 8 + 4 * half) * 32 + lane;
@@ -945,11 +1028,18 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     const int nm = min(kL, T - c * kL);
     const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(st + kXQ);
     float acc[4][4], ya[2][4];
-    const float4* xs = reinterpret_cast<const float4*>(st + ST::oX) + (pair * 8 + 4 * half) * 32 + lane;
+    if (EQ) {
 #pragma unroll
-    for (int nj = 0; nj < 4; ++nj) {
-      const float4 u = xs[nj * 32];
-      acc[nj][0] = u.x; acc[nj][1] = u.y; acc[nj][2] = u.z; acc[nj][3] = u.w;
+      for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nj][e] = en[nj][e];
+    } else {
+      const float4* xs = reinterpret_cast<const float4*>(st + ST::oX) + (pair * 8 + 4 * half) * 32 + lane;
+#pragma unroll
+      for (int nj = 0; nj < 4; ++nj) {
+        const float4 u = xs[nj * 32];
+        acc[nj][0] = u.x; acc[nj][1] = u.y; acc[nj][2] = u.z; acc[nj][3] = u.w;
+      }
     }
     if (!WALK) {
       const float4* ys = reinterpret_cast<const float4*>(st + ST::oY) + (pair * 4 + 2 * half) * 32 + lane;
@@ -1016,6 +1106,10 @@ xop_chain_kernel(int T, int H, int nchunks, const unsigned char* __restrict__ op
     for (int nj = 0; nj < 4; ++nj)
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[nj][e] = acc[nj][e];
+    if (EQ && n + 1 < nchunks) {
+      (void)mbar_wait(&full[(n + 1) % kNS], ((n + 1) / kNS) & 1);  // (as above)
+      form_e(n + 1);
+    }
     if (!WALK && ck != nullptr) store_rows(ck + ((size_t)bh * nchunks + c) * ck_stride);
   }
   if (sT != nullptr) store_rows(sT + sbase);
@@ -1040,16 +1134,18 @@ cudaError_t launch_prep_t(const FwdArgs* fa, const BwdArgs* ba, unsigned char* o
   return cudaGetLastError();
 }
 
-template <int R, bool WALK>
+template <int R, bool WALK, bool EQ>
 cudaError_t launch_chain_t(int B, int T, int H, int C, const unsigned char* ops, size_t bstride, const float* s0, void* y,
-                           bool ybf, float* ck, size_t ck_stride, float* sT, unsigned* status, cudaStream_t stream) {
-  using ST = Stage<R, WALK>;
+                           bool ybf, float* ck, size_t ck_stride, float* sT, const float* dy, unsigned* status,
+                           cudaStream_t stream) {
+  using ST = Stage<R, WALK, EQ>;
   static_assert(ST::kSmem <= 232448, "shared memory per CTA");
-  auto kern = xop_chain_kernel<R, WALK>;
+  auto kern = xop_chain_kernel<R, WALK, EQ>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ST::kSmem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)B * H * (64 / R);
-  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status);
+  kern<<<grid, (ST::kNW + 1) * 32, ST::kSmem, stream>>>(T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, dy,
+                                                        status);
   return cudaGetLastError();
 }
 
@@ -1070,28 +1166,21 @@ cudaError_t launch_chain(int rows, int B, int T, int H, int C, const unsigned ch
                          void* y, bool ybf, float* ck, size_t ck_stride, float* sT, unsigned* status,
                          cudaStream_t stream) {
   switch (rows) {
-    case 64: return launch_chain_t<64, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
-    case 32: return launch_chain_t<32, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
-    default: return launch_chain_t<16, WALK>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, status, stream);
+    case 64:
+      return launch_chain_t<64, WALK, false>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, nullptr, status,
+                                             stream);
+    case 32:
+      return launch_chain_t<32, WALK, false>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, nullptr, status,
+                                             stream);
+    default:
+      return launch_chain_t<16, WALK, false>(B, T, H, C, ops, bstride, s0, y, ybf, ck, ck_stride, sT, nullptr, status,
+                                             stream);
   }
 }
 
 // ================================================================================ E_c from the forward
 
 constexpr int kNTE = 128;
-
-// B fragments of n-tiles nt, nt + 1 at k-tile kk for B[k][n] = Q_c[n][k] (rows j, tokens t) from an
-// operator block's Q_c copied as is (hi then lo, pieces permuted as swz_q)
-__device__ __forceinline__ void q_b2(const __nv_bfloat16* sq, int nt, int kk, int lane, FragB& b0, FragB& b1) {
-  const int j = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
-  const int t = kk * 16 + ((lane >> 3) & 1) * 8;
-  const int off = swz_q(j, t);
-  uint32_t h[4], l[4];
-  ldsm4<false>(h, sq + off);
-  ldsm4<false>(l, sq + 2048 + off);
-  b0.h[0] = h[0]; b0.h[1] = h[1]; b1.h[0] = h[2]; b1.h[1] = h[3];
-  b0.l[0] = l[0]; b0.l[1] = l[1]; b1.l[0] = l[2]; b1.l[1] = l[3];
-}
 
 // E_c = DY^T Q_c^T of every chunk from the Q_c that the forward left in the operator blocks: one CTA per
 // chunk, warp w forms rows 16 w .. 16 w + 15 (all 64 columns) and writes them over U_c in accumulator
@@ -1171,9 +1260,22 @@ cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward
   unsigned char* ops = static_cast<unsigned char*>(workspace) + kXHead;
   const size_t bstride = from_forward ? kXBytesFwd : kXBytesBwd;
   ends->g = reinterpret_cast<const float*>(ops + kXX);
-  ends->flags = reinterpret_cast<int*>(ops + kXQ);  // Q_c's slot: the walk does not use it
+  ends->flags = reinterpret_cast<int*>(ops + kXQ);  // Q_c's slot: free once the walk has run
   ends->stride = bstride / 4;
   ends->mats = from_forward ? ops + kXM : nullptr;
+  if (rows == 0) rows = chain_rows(p.B * p.H);
+  float* gck = reinterpret_cast<float*>(ops + kXX);
+  // The walk on a forward's blocks.  With whole-head CTAs (64 rows: two chain warps per SM sub-partition)
+  // the chain warps form E_c themselves, its products taking issue slots the dependent chain leaves idle
+  // (measured: B2 T4096 H64 backward 54 us shorter than with the E_c kernel); with 32-row CTAs (one chain
+  // warp per sub-partition) they lengthen the chain by about what the E_c kernel costs (B12 T1024 H6 1 us,
+  // B4 T512 H12 4 us longer), so E_c is formed by that kernel there.  Both give the same E_c bit for bit.
+  if (from_forward && rows == 64) {
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(unsigned), stream);
+    if (err != cudaSuccess) return err;
+    return launch_chain_t<64, true, true>(p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr, false, gck,
+                                          bstride / 4, p.dh0, p.dy, status, stream);
+  }
   if (p.nchunks > 0) {  // (no chunks: the chain only copies dhT to dh0)
     cudaError_t err;
     if (from_forward) {
@@ -1186,9 +1288,8 @@ cudaError_t launch_xop_walk(const BwdArgs& p, void* workspace, bool from_forward
     }
     if (err != cudaSuccess) return err;
   }
-  if (rows == 0) rows = chain_rows(p.B * p.H);
-  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr, false,
-                            reinterpret_cast<float*>(ops + kXX), bstride / 4, p.dh0, status, stream);
+  return launch_chain<true>(rows, p.B, p.T, p.H, p.nchunks, ops, bstride, p.dhT, nullptr, false, gck, bstride / 4,
+                            p.dh0, status, stream);
 }
 
 }  // namespace wkv7
