@@ -53,6 +53,19 @@ def test_single_process_passthrough():
     assert bench.job_tokens_per_s(100, 1, 1000.0) == pytest.approx(100.0)
 
 
+def test_launch_count_follows_chain_rows():
+    """gpu_launches per step of the default path: the backward on the forward's workspace runs an E_c kernel
+    while two 32-row chain CTAs per head fit the SMs (2 x heads <= SMs), and none with whole-head CTAs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    gen = bench.gen
+    pth = bench.PATHS["operators"]
+    assert bench.launches_per_step(pth, gen.WORKLOADS["debug_b12_t1024_h6"], 148) == 2 + 4      # 72 heads
+    assert bench.launches_per_step(pth, gen.WORKLOADS["m100_b4_t512_h12"], 148) == 2 + 4        # 48 heads
+    assert bench.launches_per_step(pth, gen.WORKLOADS["wide7b_b2_t4096_h64"], 148) == 2 + 3     # 128 heads
+    assert bench.launches_per_step(bench.PATHS["operators-reform"], gen.WORKLOADS["wide7b_b2_t4096_h64"], 148) == 6
+
+
 def test_reference_arm_only_rank0_prints():
     sys.path.insert(0, ROOT)
     import bench

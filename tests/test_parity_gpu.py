@@ -340,14 +340,19 @@ def test_backward_paths_agree(wkv7):
         assert rel(host(q_), host(p_).astype(np.float64)) <= 5e-5, name
 
 
-@pytest.mark.parametrize("decay", ["workload", "strong"])
+@pytest.mark.parametrize("decay", ["workload", "workload_whole_heads", "strong"])
 def test_backward_from_forward_equals_backward(wkv7, decay):
     """wkv7_backward_from_forward on the forward's operators against wkv7_backward forming them again: the
-    walk sees the same A_c and E_c on closed-form chunks (dh0 bit for bit); the column gradients use the
-    forward's coupling matrices, which differ from their own in rounding only (within 1e-5); with strong
-    decays (chunks taken token by token, whose E_c comes from the split Q_c) within 1e-5."""
+    walk sees the same A_c and E_c on closed-form chunks (dh0 bit for bit) -- with 32-row chain CTAs E_c
+    comes from its own kernel, with whole-head CTAs (more heads than half the SMs) the walk forms it, in
+    the same arithmetic; the column gradients use the forward's coupling matrices, which differ from their
+    own in rounding only (within 1e-5); with strong decays (chunks taken token by token, whose E_c comes
+    from the split Q_c) within 1e-5."""
     if decay == "workload":
         x = gen.random_small(12, B=3, T=200, H=4, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
+    elif decay == "workload_whole_heads":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        x = gen.random_small(5, B=1, T=300, H=sms // 2 + 6, D=64, h0_std=0.1, dhT_std=1.0, dtype="bf16")
     else:
         x = strong_decay(4245, "bf16", 0.005, 0.05)
     ins = [dev(x[n], "bf16") for n in "rwkvab"]
@@ -358,7 +363,7 @@ def test_backward_from_forward_equals_backward(wkv7, decay):
     g1 = wkv7.backward(*ins, h0, ck, dy, dhT, workspace="auto")
     g2 = wkv7.backward_from_forward(*ins, h0, ck, dy, dhT, workspace=ws)
     for name, p_, q_ in zip(("dr", "dw", "dk", "dv", "da", "db", "dh0"), g1, g2):
-        if decay == "workload" and name == "dh0":
+        if decay.startswith("workload") and name == "dh0":
             assert torch.equal(p_, q_), name
         else:
             assert rel(host(q_), host(p_)) <= 1e-5, name
